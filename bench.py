@@ -1,0 +1,339 @@
+"""Benchmark of the Dual-AR decode step on GB300.
+
+One step = one decode frame: a slow-decoder token through 36 layers, the
+tied semantic head, and 9 fast-decoder steps of 4 layers (10 codebook ids).
+Default workload: the full-size S2-Pro-shaped model with bf16 weights, batch
+1, prefill 128 prompt ids, then the 896 decode frames that fill the static
+KV cache of 1024 (the schedule of the tuna-fish README speed test
+"prefill 128, decode 896").
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  `value` is frames/s over all ranks with the
+weights already resident in HBM, timed with CUDA events on the library's
+stream; `e2e` is the same metric through the public C API with host
+buffers (prompt upload and every frame's download inside the timed region).
+Multi-GPU: independent replicas, one per rank, no collective on the data
+path (batch-1 decode is one serial dependency chain).
+`--impl reference` times the CPU oracle (float64 NumPy) on a bounded sample
+of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from synth import WORKLOADS, tensor_specs  # noqa: E402
+
+METRIC = "Dual-AR decode frames/s at batch 1; achieved HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+PAGE_LOAD_ELEMENTS = 7_377_351_168   # tuna-fish README, "Inference estimation"
+
+
+# ---------------------------------------------------------------- accounting
+def frame_bytes(d, weight_dtype: str, pos: int) -> dict:
+    """Algorithmic HBM bytes of one decode frame whose slow token sits at
+    position `pos`: every weight streamed once (slow pass + 9 fast passes),
+    the valid KV rows read, the new KV rows written, embedding rows read."""
+    eb = 1 if weight_dtype == "fp8" else 2
+    H, F = d.hidden, d.ffn
+    lin_rows = d.qkv_dim + H + 2 * F + H
+    lin = d.qkv_dim * H + H * d.q_dim + 2 * F * H + H * F
+    scales = lin_rows * 4 if eb == 1 else 0
+    layer = lin * eb + scales + 2 * H * 2
+    slow_w = d.slow_layers * layer + d.semantic_vocab * H * 2 + H * 2 + H * 2
+    fast_w = d.fast_layers * layer + d.codebook_size * H * eb + (d.codebook_size * 4 if eb == 1 else 0) \
+        + H * 2 + H * 2
+    kv_row = d.kv_dim * 2                          # one K or V row of one layer, bf16
+    kv_read = d.slow_layers * 2 * kv_row * (pos + 1)
+    kv_read += sum(d.fast_layers * 2 * kv_row * (j + 1) for j in range(1, d.n_codebooks))
+    kv_write = d.slow_layers * 2 * kv_row + d.fast_layers * 2 * kv_row * (d.n_codebooks)
+    weights = slow_w + (d.n_codebooks - 1) * fast_w
+    return {"weights": weights, "kv_read": kv_read, "kv_write": kv_write,
+            "total": weights + kv_read + kv_write}
+
+
+def schedule_bytes(d, weight_dtype, prefill, frames) -> float:
+    return float(np.mean([frame_bytes(d, weight_dtype, p)["total"]
+                          for p in range(prefill, prefill + frames)]))
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "source": "of measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "of fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- inputs
+def device_weights(d, seed: int, device):
+    """Seeded N(0, 0.02) bf16 weights drawn on the device (torch Philox),
+    norms 1.0; returns name -> torch tensor (bf16)."""
+    import torch
+    out = {}
+    for idx, (name, shape, kind) in enumerate(tensor_specs(d)):
+        if kind == "norm":
+            out[name] = torch.ones(shape, dtype=torch.bfloat16, device=device)
+            continue
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1_000_003 + idx)
+        out[name] = (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 0.02
+                     ).to(torch.bfloat16)
+    return out
+
+
+def host_bits(tensors) -> dict:
+    import torch
+    return {k: v.view(torch.int16).cpu().numpy().view(np.uint16) for k, v in tensors.items()}
+
+
+# ---------------------------------------------------------------- oracle leg
+def oracle_sample(wl, weights_bits, prompt, budget_s: float = 20.0) -> dict:
+    """Oracle frames/s on a bounded sample: prefill (untimed), then decode
+    frames until `budget_s` of CPU time has passed (at least one)."""
+    import oracle
+    ref = oracle.DualAROracle(wl.dims, weights_bits, wl.weight_dtype)
+    t0 = time.perf_counter()
+    ref.prefill(prompt)
+    t_prefill = time.perf_counter() - t0
+    n, t0 = 0, time.perf_counter()
+    while True:
+        ref.decode_frame()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 8:
+            break
+    return {"value": n / el, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{wl.name}: oracle prefill of {prompt.shape[1]} ids ({t_prefill:.1f} s, untimed) "
+                      f"then {n} decode frame(s) timed ({el:.1f} s); float64 NumPy, BLAS on all host cores"}
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=896)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--workload", default="full_bf16", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = WORKLOADS[args.workload]
+    d = wl.dims
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        return run_reference(args, wl, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    from dual_ar_decode_gb300 import Decoder
+    from synth import make_prompt
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    tensors = device_weights(d, args.seed, device)
+    prompt = make_prompt(d, wl.prefill, seed=args.seed + rank)
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
+    bits = host_bits(tensors) if want_cpu else None
+    dec = Decoder(d, wl.weight_dtype, device=local)
+    dec.load_weights(tensors)
+    del tensors
+    torch.cuda.empty_cache()
+    sampling = {"top_k": wl.top_k, "seed": 1234} if wl.top_k else None
+    stream = torch.cuda.ExternalStream(dec.stream(), device=device)
+
+    # warm-up: prefill + W frames (captures the frame graph)
+    dec.prefill(prompt, sampling)
+    dec.decode_frames(min(args.warmup, d.max_seq_len - wl.prefill), sampling)
+
+    cap = d.max_seq_len - wl.prefill
+    remaining, total_ms, segs = args.steps, 0.0, 0
+    clocks = ClockSampler(local)
+    positions = []
+    clocks.start()
+    while remaining > 0:
+        k = min(cap, remaining)
+        dec.prefill(prompt, sampling)                    # untimed: resets position to P
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dec.decode_frames(k, sampling)
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize(device)
+        total_ms += e0.elapsed_time(e1)
+        positions += list(range(wl.prefill, wl.prefill + k))
+        remaining -= k
+        segs += 1
+    clk = clocks.stop()
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    frames_all = args.steps * world
+    value = frames_all / (total_ms / 1e3)
+    info = dec.info()
+
+    # dominant kernel, live: the slow gate/up GEMV in its in-frame configuration
+    prof_ms, prof_bytes = dec.profile_kernel(0, 4 * d.slow_layers)
+    peaks = measured_peaks()
+    achieved = prof_bytes / (prof_ms / 1e3) / 1e9
+
+    # e2e through the public API with host buffers
+    e2e_frames = min(args.steps, cap)
+    torch.cuda.synchronize(device)
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    dec.prefill(prompt, sampling)
+    for _ in range(e2e_frames):
+        dec.decode_frame(sampling)
+    h1.record(stream)
+    h1.synchronize()
+    e2e_ms = h0.elapsed_time(h1)
+    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = e2e_frames * world / (float(e2e_t.item()) / 1e3)
+
+    bytes_avg = float(np.mean([frame_bytes(d, wl.weight_dtype, p)["total"] for p in positions]))
+    frame_gbs = bytes_avg * value / world / 1e9
+    page_gib = PAGE_LOAD_ELEMENTS * (1 if wl.weight_dtype == "fp8" else 2) / 2 ** 30
+    cpu = oracle_sample(wl, bits, prompt) if want_cpu else None
+    dec.close()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "frames/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.weight_dtype == "bf16" else "fp8-e4m3 weights, bf16 KV, f32 accumulate",
+            "data": "synthetic: seeded N(0, 0.02) random-init weights, uniform prompt ids",
+            "config": {"workload": wl.name, "batch": wl.batch, "prefill": wl.prefill,
+                       "decode_frames_timed": args.steps, "timed_segments": segs,
+                       "max_seq_len": d.max_seq_len, "weights": wl.weight_dtype,
+                       "sampling": "greedy argmax" if not wl.top_k else f"top-k {wl.top_k}",
+                       "l2": f"inputs larger than L2: {bytes_avg / 1e9:.2f} GB streamed per frame",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "tok_s": round(value, 3), "codebook_tok_s": round(10 * value, 3),
+            "frame_hbm": {"bytes_per_frame": round(bytes_avg), "achieved_gbs": round(frame_gbs, 1),
+                          "peak_gbs": peaks["hbm_gbs"], "frac": round(frame_gbs / peaks["hbm_gbs"], 4),
+                          "peak_source": peaks["source"],
+                          "page_convention_gib_s": round(value / world * page_gib, 1)},
+            "roofline": {"kernel": "k_gemv (slow gate/up, RMSNorm prologue, SwiGLU epilogue)",
+                         "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["source"], "bytes_per_launch": prof_bytes,
+                         "ms_per_launch": round(prof_ms, 5), "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "frames/s",
+                    "h2d_bytes_per_step": round((wl.prefill * 4 + 4 * (e2e_frames + 1)) / e2e_frames, 2),
+                    "d2h_bytes_per_step": 44,
+                    "note": "tf_prefill (host prompt) + one tf_decode_frame per frame (host frame out)"},
+            "gpu_launches": info["graph_nodes"] * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    from synth import make_prompt, make_weights
+    d = wl.dims
+    w = make_weights(d, args.seed)
+    prompt = make_prompt(d, wl.prefill, seed=args.seed)
+    per_step = []
+    for _ in range(args.warmup + args.steps if d.slow_layers <= 2 else 1):
+        s = oracle_sample(wl, w, prompt, budget_s=10.0)
+        per_step.append(s)
+    v = float(np.median([s["value"] for s in per_step]))
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "frames/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 / v, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch, "prefill": wl.prefill},
+            "cpu_baseline": per_step[-1] | {"value": round(v, 5)},
+            "e2e": {"value": round(v, 5), "unit": "frames/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) Dual-AR decode: thin Python binding over libtf_dualar.so.
+
+Every step of the decode path runs in the CUDA library; this package only
+marshals arguments through the C ABI declared in include/tf.h.  Importing it
+does not load the library; ``binding.lib()`` does, and raises if the library
+has not been built (there is no fallback).
+"""
+from .binding import (TF_OK, TfError, Decoder, config_from_dims, lib, library_path,
+                      op_gemv, op_quantize_fp8, op_select)
+
+__all__ = ["TF_OK", "TfError", "Decoder", "config_from_dims", "lib", "library_path",
+           "op_gemv", "op_quantize_fp8", "op_select"]

@@ -1,0 +1,91 @@
+// Epilogue helpers shared by the decode GEMV and the prompt GEMM.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tf {
+
+__device__ __forceinline__ int row_pos(const GemvParams& p, int m) {
+  return (p.pos_ptr ? __ldg(p.pos_ptr) : p.pos_fixed) + m;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// Dot product of one 16-byte weight chunk with the matching activations.
+template <int WT, int EPC>
+__device__ __forceinline__ float chunk_dot(const uint4 w, const float* a) {
+  float s = 0.f;
+  if constexpr (WT == 0) {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s = fmaf(bf16_lo(v[i]), a[2 * i], s);
+      s = fmaf(bf16_hi(v[i]), a[2 * i + 1], s);
+    }
+  } else {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(v[i] & 0xFFFFu));
+      float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(v[i] >> 16));
+      s = fmaf(lo.x, a[4 * i], s);
+      s = fmaf(lo.y, a[4 * i + 1], s);
+      s = fmaf(hi.x, a[4 * i + 2], s);
+      s = fmaf(hi.y, a[4 * i + 3], s);
+    }
+  }
+  return s;
+}
+
+__device__ __forceinline__ unsigned long long pack_key(float v, int idx) {
+  if (v == 0.f) v = 0.f;  // -0 and +0 tie, as equal floats do
+  return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+// Pair epilogue for RoPE-ordered q/k rows and plain v rows.
+__device__ __forceinline__ void epi_qkv_pair(const GemvParams& p, int m, int pair, float v0,
+                                             float v1) {
+  const int half = p.head_dim >> 1;
+  const int pos = row_pos(p, m);
+  if (pos < 0 || pos >= p.T) {
+    atomicOr(p.err, ERR_BAD_POS);
+    return;
+  }
+  const int qp = p.q_dim >> 1, kp = p.kv_dim >> 1;
+  if (pair < qp + kp) {
+    const bool isq = pair < qp;
+    const int pr = isq ? pair : pair - qp;
+    const int h = pr / half, i = pr - h * half;
+    const float2 cs = __ldg(&p.rope[(size_t)pos * half + i]);
+    const float r0 = v0 * cs.x - v1 * cs.y;
+    const float r1 = v1 * cs.x + v0 * cs.y;
+    if (isq) {
+      float* q = p.qout + (size_t)m * p.q_dim + h * p.head_dim;
+      q[i] = r0;
+      q[i + half] = r1;
+    } else {
+      uint16_t* k = p.Kc + ((size_t)h * p.T + pos) * p.head_dim;
+      k[i] = f32_to_bf16(r0);
+      k[i + half] = f32_to_bf16(r1);
+    }
+  } else {
+    const int d0 = 2 * (pair - qp - kp);
+    const int g = d0 / p.head_dim, d = d0 - g * p.head_dim;
+    uint16_t* v = p.Vc + ((size_t)g * p.T + pos) * p.head_dim + d;
+    v[0] = f32_to_bf16(v0);
+    v[1] = f32_to_bf16(v1);
+  }
+}
+
+}  // namespace tf

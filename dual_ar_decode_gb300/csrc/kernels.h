@@ -1,0 +1,179 @@
+// Internal launch interface of the decode kernels (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tf {
+
+// Error bits raised by kernels (the host maps them to tf_status).
+enum : uint32_t {
+  ERR_TIMEOUT = 1u << 0,   // a bounded wait expired
+  ERR_NAN = 1u << 1,       // NaN logit met by a selection
+  ERR_BAD_ID = 1u << 2,    // an id fed back was outside its table
+  ERR_BAD_POS = 1u << 3,   // a position outside the KV cache
+};
+
+// ----------------------------------------------------------------- GEMV
+// Prologue: how the activation vector a[m][k] is formed.
+enum Prologue : int32_t {
+  PRO_PLAIN = 0,   // a = x
+  PRO_NORM = 1,    // a = RMSNorm(x) * w   (w bf16 [K])
+};
+// Epilogue: what happens to y[m][r] = sum_k W[r][k] a[m][k].
+enum Epilogue : int32_t {
+  EPI_STORE = 0,   // out[m][r] = y
+  EPI_RESID = 1,   // out[m][r] += y (in-place residual add)
+  EPI_SWIGLU = 2,  // rows (2i, 2i+1) = (gate_i, up_i): out[m][i] = silu(g) * u
+  EPI_QKV = 3,     // rows in RoPE-pair order: rotate q, k; q -> qout, k, v -> KV cache
+  EPI_LOGITS = 4,  // out[r] = y (M = 1) and, if select, grid-wide argmax -> ids
+};
+
+struct GemvParams {
+  const uint8_t* W;      // [N][K] row-major, bf16 or e4m3 bytes
+  const float* scale;    // [N] per-row scale (fp8) or nullptr
+  int32_t N, K;
+  int32_t unit;          // rows per partition unit (2 for pair epilogues)
+  int32_t units;         // N / unit
+  int32_t rs;            // rows per pipeline stage
+  int32_t nst;           // stages in the shared-memory ring
+  int32_t stb;           // bytes per stage slot (multiple of 128)
+  // prologue
+  int32_t pro;
+  const float* x;        // [M][ldx]
+  int32_t ldx;
+  const uint16_t* nw;    // RMSNorm weight (bf16 bits) [K]
+  float eps;
+  // epilogue
+  int32_t epi;
+  float* out;            // [M][ldo]
+  int32_t ldo;
+  // EPI_QKV
+  int32_t q_dim, kv_dim, head_dim;
+  float* qout;           // [M][q_dim]
+  uint16_t* Kc;          // [Hkv][T][head_dim] bf16
+  uint16_t* Vc;
+  int32_t T;
+  const int32_t* pos_ptr;  // row m sits at position pos_ptr[0] + m, or
+  int32_t pos_fixed;       // pos_fixed + m when pos_ptr is null
+  const float2* rope;    // [T][head_dim/2] (cos, sin)
+  // EPI_LOGITS
+  int32_t select;        // 1: argmax -> sel[cb], fb[cb]
+  unsigned long long* best;
+  uint32_t* ticket;
+  int32_t* sel;          // selected id slot
+  int32_t* fb;           // fed-back id slot
+  const int32_t* forced;     // forced id slot (if *forced_on)
+  const int32_t* forced_on;
+  uint32_t* err;
+};
+
+// Shared memory bytes a launch with these params needs.
+size_t gemv_smem_bytes(const GemvParams& p, int M);
+// Fills unit/units/rs/nst/stb for a matrix of N x K elements of `eb` bytes.
+void gemv_plan(GemvParams& p, int eb, int num_sms);
+// Launch (weight type wt: 0 bf16, 1 fp8) on `grid` CTAs; pdl = allow
+// programmatic dependent launch on the previous kernel of the stream.
+cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl,
+                        cudaStream_t s);
+cudaError_t gemv_set_attributes();
+
+// ----------------------------------------------------------------- attention
+struct AttnParams {
+  const float* q;        // [M][Hq*D] rotated queries
+  const uint16_t* Kc;    // [Hkv][T][D]
+  const uint16_t* Vc;
+  int32_t T, Hq, Hkv, D;
+  const int32_t* pos_ptr;
+  int32_t pos_fixed;
+  int32_t S;             // splits over the key range (grid.x)
+  float* part;           // [M][Hq][S][D + 2] partial (m, l, acc)
+  uint32_t* counters;    // [M][Hkv], zero between launches
+  float* out;            // [M][Hq*D]
+  uint32_t* err;
+};
+cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t s);
+
+// ----------------------------------------------------------------- misc
+// Builds the input rows of a decoder pass.
+enum BuildMode : int32_t {
+  BUILD_SLOW = 0,    // x[0] = text_embed[sem_base + fb[0]]
+  BUILD_FAST1 = 1,   // x[0] = RMSNorm(xs) * w_final; x[1] = cb_embed[0][fb[0]]
+  BUILD_FASTJ = 2,   // x[0] = cb_embed[j-1][fb[j-1]]
+  BUILD_TOKENS = 3,  // x[m] = text_embed[tokens[m]]  (prefill)
+};
+struct BuildParams {
+  int32_t mode, j, H, M;
+  const uint16_t* table;   // embedding table base (text_embed or cb_embed[j-1])
+  int32_t table_rows;      // rows the id may address
+  int32_t row_base;        // added to the id (sem_base for BUILD_SLOW)
+  const int32_t* ids;      // id source (fb slot, or tokens for BUILD_TOKENS)
+  const float* xs;         // slow residual (BUILD_FAST1)
+  const uint16_t* nw;      // final slow norm (BUILD_FAST1)
+  float eps;
+  float* x;                // output rows [M][H]
+  uint32_t* err;
+};
+cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s);
+
+// Per-frame bookkeeping after the last codebook: pos += advance,
+// frame_index += 1, history[hist_idx++] = sel.
+struct FrameEndParams {
+  int32_t* pos;
+  int32_t advance;
+  int32_t* frame_index;
+  const int32_t* sel;
+  int32_t ncb;
+  int32_t* hist;         // [hist_cap][ncb]
+  int32_t* hist_idx;
+  int32_t hist_cap;
+};
+cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s);
+
+// Top-k / argmax selection of one row of logits per CTA.
+struct SelectParams {
+  const float* logits;   // [n][ld]
+  int32_t ld, vocab, n;
+  int32_t top_k;
+  float temperature;
+  uint32_t key0, key1;   // Philox key (seed low / high)
+  const int32_t* frame_ptr;  // frame index from device (or null -> frame)
+  int32_t frame;
+  int32_t codebook0;     // row i uses codebook0 + i
+  int32_t sequence;
+  int32_t* sel;          // [n]
+  int32_t* fb;           // [n] fed-back ids or null
+  const int32_t* forced;
+  const int32_t* forced_on;
+  uint32_t* err;
+};
+cudaError_t launch_select(const SelectParams& p, bool pdl, cudaStream_t s);
+
+// Weight re-layout and quantisation at load time.
+enum RowMap : int32_t {
+  MAP_IDENTITY = 0,
+  MAP_QKV = 1,       // dst row order: RoPE pairs of q heads, k heads; v as is
+  MAP_GATE = 2,      // src row i -> dst row 2i
+  MAP_UP = 3,        // src row i -> dst row 2i + 1
+};
+struct PackParams {
+  const uint8_t* src;    // [rows][cols] bf16 or e4m3
+  const float* src_scale;  // e4m3 input: [rows]
+  uint8_t* dst;          // packed destination (bf16 or e4m3)
+  float* dst_scale;      // fp8 destination: [dst rows]
+  int64_t rows, cols;
+  int32_t map;
+  int32_t q_dim, kv_dim, head_dim;
+  int32_t mode;          // 0 copy bf16, 1 quantise bf16 -> fp8, 2 copy fp8 + scale
+};
+cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- prefill
+// Row-block GEMM on CUDA cores for prompts: out = epi(A[M][K] * W[N][K]^T)
+// with the GEMV's prologue/epilogue semantics (positions: row m at pos m).
+cudaError_t launch_gemm_rows(const GemvParams& p, int wt, int M, cudaStream_t s);
+// a[m] = RMSNorm(x[m]) * w for M rows (prefill prologue).
+cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int M, int H,
+                                float eps, cudaStream_t s);
+
+}  // namespace tf

@@ -1,0 +1,341 @@
+// Weight-streaming GEMV for batch-1 decode (sm_103a).
+//
+// Every linear layer of the decode step is a matrix-vector product whose
+// cost is reading the weight once from HBM (tuna-fish README, "Inference
+// estimation": the decode step loads every parameter once per step).  The
+// kernel is built around that:
+//   * one CTA per SM; CTA c owns a contiguous, balanced range of rows, which
+//     is one contiguous block of the row-major weight;
+//   * a producer warp streams that block into a ring of shared-memory stages
+//     with bulk copies on the TMA engine (cp.async.bulk + mbarrier
+//     transaction counts), L2 evict-first; it starts before the previous
+//     kernel finishes (programmatic dependent launch) because weights never
+//     depend on activations;
+//   * 8 consumer warps hold the activation slice they need in registers
+//     (thread t owns 16-byte chunks t, t+256, ... of every row) and reduce
+//     each row with warp shuffles; per-warp row sums meet in shared memory
+//     in a fixed order, so results are bitwise deterministic;
+//   * fused prologue (RMSNorm) and epilogues (residual add, SwiGLU, RoPE +
+//     KV-cache append, logits + grid-wide argmax).
+// FP8 weights (e4m3 with a float32 scale per row, drbaph s2-pro-fp8 model
+// card, "Quantization Details") are decoded in registers and the row scale is
+// applied once to the finished dot product.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace tf {
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + producer warp
+constexpr int kRowBatch = 128;             // rows reduced per epilogue round
+constexpr int kStageTarget = 24 * 1024;
+constexpr int kRingBytes = 96 * 1024;
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+template <int WT, int M, int J>
+__global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int EPC = WT ? 16 : 8;  // elements per 16-byte chunk
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int u0 = (int)((long long)p.units * c / G);
+  const int u1 = (int)((long long)p.units * (c + 1) / G);
+  const int r0 = u0 * p.unit;
+  const int nrows = (u1 - u0) * p.unit;
+  const uint32_t rowbytes = static_cast<uint32_t>(p.K) * (WT ? 1u : 2u);
+  const int nch = static_cast<int>(rowbytes >> 4);
+
+  uint8_t* ring = smem;
+  float* red = reinterpret_cast<float*>(smem + (size_t)p.nst * p.stb);  // [kRowBatch][8][M]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + kRowBatch * kConsumerWarps * M);
+  uint64_t* empty = full + p.nst;
+  float* misc = reinterpret_cast<float*>(empty + p.nst);  // [8][M] + 8 keys
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(misc + 8 * M);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(keys + kConsumerWarps);
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < p.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int s = 0;
+      for (int b0 = 0; b0 < nrows && !*abort_flag; b0 += kRowBatch) {
+        const int nb = min(kRowBatch, nrows - b0);
+        for (int i0 = 0; i0 < nb; i0 += p.rs) {
+          const int n = min(p.rs, nb - i0);
+          const int slot = s % p.nst;
+          if (s >= p.nst && !mbar_wait(&empty[slot], ((s / p.nst) & 1) ^ 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          const uint32_t bytes = static_cast<uint32_t>(n) * rowbytes;
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          bulk_g2s(ring + (size_t)slot * p.stb, p.W + (size_t)(r0 + b0 + i0) * rowbytes, bytes,
+                   &full[slot], pol);
+          ++s;
+        }
+      }
+      // Drain: the last (up to nst) issued copies may still be in flight.
+      for (int t = max(0, s - p.nst); t < s; ++t)
+        mbar_wait(&full[t % p.nst], (t / p.nst) & 1, p.err);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  pdl_wait();  // activations come from the previous kernel
+
+  float a[M][J][EPC];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const float* xm = p.x + (size_t)m * p.ldx;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int ch = tid + j * kConsumers;
+      if (ch < nch) {
+        const float4* src = reinterpret_cast<const float4*>(xm + ch * EPC);
+#pragma unroll
+        for (int q = 0; q < EPC / 4; ++q) {
+          const float4 v = src[q];
+          a[m][j][4 * q] = v.x;
+          a[m][j][4 * q + 1] = v.y;
+          a[m][j][4 * q + 2] = v.z;
+          a[m][j][4 * q + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) a[m][j][e] = 0.f;
+      }
+    }
+  }
+  if (p.pro == PRO_NORM) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) ss = fmaf(a[m][j][e], a[m][j][e], ss);
+      ss = warp_sum(ss);
+      if (lane == 0) misc[warp * M + m] = ss;
+    }
+    consumer_sync();
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      float ss = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) ss += misc[w * M + m];
+      const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int ch = tid + j * kConsumers;
+        if (ch < nch) {
+#pragma unroll
+          for (int e = 0; e < EPC; ++e)
+            a[m][j][e] = a[m][j][e] * rstd * bf16_to_f32(__ldg(&p.nw[ch * EPC + e]));
+        }
+      }
+    }
+  }
+
+  unsigned long long best = 0ull;  // EPI_LOGITS: best (value, lowest index) key seen
+  int s = 0;
+  for (int b0 = 0; b0 < nrows; b0 += kRowBatch) {
+    const int nb = min(kRowBatch, nrows - b0);
+    for (int i0 = 0; i0 < nb; i0 += p.rs) {
+      const int n = min(p.rs, nb - i0);
+      const int slot = s % p.nst;
+      if (!*abort_flag && !mbar_wait(&full[slot], (s / p.nst) & 1, p.err)) *abort_flag = 1;
+      const uint8_t* st = ring + (size_t)slot * p.stb;
+      for (int i = 0; i < n; ++i) {
+        const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)i * rowbytes);
+        float acc[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m] = 0.f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int ch = tid + j * kConsumers;
+          if (ch < nch) {
+            const uint4 w = row[ch];
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] += chunk_dot<WT, EPC>(w, a[m][j]);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const float v = warp_sum(acc[m]);
+          if (lane == 0) red[((i0 + i) * kConsumerWarps + warp) * M + m] = v;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++s;
+    }
+    consumer_sync();
+
+    // ---------------------------------------------------------- epilogue
+    if (p.unit == 2) {
+      for (int pi = tid; pi < (nb >> 1); pi += kConsumers) {
+        const int rg = r0 + b0 + 2 * pi;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            v0 += red[((2 * pi) * kConsumerWarps + w) * M + m];
+            v1 += red[((2 * pi + 1) * kConsumerWarps + w) * M + m];
+          }
+          if (p.scale) {
+            v0 *= __ldg(&p.scale[rg]);
+            v1 *= __ldg(&p.scale[rg + 1]);
+          }
+          if (p.epi == EPI_SWIGLU) {
+            p.out[(size_t)m * p.ldo + (rg >> 1)] = silu(v0) * v1;
+          } else {  // EPI_QKV
+            epi_qkv_pair(p, m, rg >> 1, v0, v1);
+          }
+        }
+      }
+    } else {
+      for (int ri = tid; ri < nb; ri += kConsumers) {
+        const int rg = r0 + b0 + ri;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) v += red[(ri * kConsumerWarps + w) * M + m];
+          if (p.scale) v *= __ldg(&p.scale[rg]);
+          float* o = p.out + (size_t)m * p.ldo + rg;
+          if (p.epi == EPI_RESID) {
+            *o += v;
+          } else {
+            *o = v;
+            if (p.epi == EPI_LOGITS) {
+              if (v != v) atomicOr(p.err, ERR_NAN);
+              const unsigned long long k = pack_key(v, rg);
+              best = k > best ? k : best;
+            }
+          }
+        }
+      }
+    }
+    consumer_sync();
+  }
+
+  if (p.epi == EPI_LOGITS && p.select) {
+    best = warp_max_u64(best);
+    if (lane == 0) keys[warp] = best;
+    consumer_sync();
+    if (tid == 0) {
+      unsigned long long b = 0ull;
+      for (int w = 0; w < kConsumerWarps; ++w) b = keys[w] > b ? keys[w] : b;
+      if (b) atomicMax(p.best, b);
+      __threadfence();
+      const uint32_t t = atomicAdd(p.ticket, 1u);
+      if (t == static_cast<uint32_t>(G) - 1u) {
+        __threadfence();
+        const unsigned long long fin = atomicExch(p.best, 0ull);
+        const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(fin & 0xFFFFFFFFull));
+        *p.sel = idx;
+        *p.fb = (p.forced_on && *p.forced_on) ? *p.forced : idx;
+        *p.ticket = 0u;
+      }
+    }
+  }
+}
+
+template <int WT, int M, int J>
+cudaError_t launch_t(const GemvParams& p, int grid, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = gemv_smem_bytes(p, M);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_gemv<WT, M, J>, p);
+}
+
+template <int WT, int M>
+cudaError_t launch_j(const GemvParams& p, int J, int grid, bool pdl, cudaStream_t s) {
+  switch (J) {
+    case 1: return launch_t<WT, M, 1>(p, grid, pdl, s);
+    case 2: return launch_t<WT, M, 2>(p, grid, pdl, s);
+    case 3: return launch_t<WT, M, 3>(p, grid, pdl, s);
+    case 4:
+    case 5: return launch_t<WT, M, 5>(p, grid, pdl, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int WT, int M>
+cudaError_t set_attr_m() {
+  const int bytes = 200 * 1024;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_gemv<WT, M, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemv<WT, M, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  if ((e = cudaFuncSetAttribute(k_gemv<WT, M, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
+  return cudaFuncSetAttribute(k_gemv<WT, M, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+size_t gemv_smem_bytes(const GemvParams& p, int M) {
+  size_t b = (size_t)p.nst * p.stb;
+  b += (size_t)kRowBatch * kConsumerWarps * M * sizeof(float);
+  b += 2 * (size_t)p.nst * sizeof(uint64_t);
+  b += (8 * M + 1) * sizeof(float) + kConsumerWarps * sizeof(unsigned long long) + 16;
+  return b;
+}
+
+void gemv_plan(GemvParams& p, int eb, int num_sms) {
+  (void)num_sms;
+  p.unit = (p.epi == EPI_SWIGLU || p.epi == EPI_QKV) ? 2 : 1;
+  p.units = p.N / p.unit;
+  const int rowbytes = p.K * eb;
+  p.rs = rowbytes >= kStageTarget ? 1 : kStageTarget / rowbytes;
+  p.stb = ((p.rs * rowbytes + 127) / 128) * 128;
+  p.nst = kRingBytes / p.stb;
+  if (p.nst < 2) p.nst = 2;
+  if (p.nst > 8) p.nst = 8;
+}
+
+cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, cudaStream_t s) {
+  const int nch = p.K * (wt ? 1 : 2) / 16;
+  const int J = (nch + kConsumers - 1) / kConsumers;
+  if (J < 1 || J > 5 || M < 1 || M > 2) return cudaErrorInvalidValue;
+  if (wt == 0) return M == 1 ? launch_j<0, 1>(p, J, grid, pdl, s) : launch_j<0, 2>(p, J, grid, pdl, s);
+  return M == 1 ? launch_j<1, 1>(p, J, grid, pdl, s) : launch_j<1, 2>(p, J, grid, pdl, s);
+}
+
+cudaError_t gemv_set_attributes() {
+  cudaError_t e;
+  if ((e = set_attr_m<0, 1>())) return e;
+  if ((e = set_attr_m<0, 2>())) return e;
+  if ((e = set_attr_m<1, 1>())) return e;
+  return set_attr_m<1, 2>();
+}
+
+}  // namespace tf

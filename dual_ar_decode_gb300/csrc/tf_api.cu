@@ -1,0 +1,1081 @@
+// C ABI of the Dual-AR decode library: context, weights, prefill and the
+// decode frame (declared in include/tf.h).
+//
+// One decode frame (fish-s2-pro-mlx-local-deploy README, architecture
+// paragraph; tuna-fish README, "Inference estimation"):
+//   slow:  x = text_embed[sem_base + c0(prev)]; 36 x layer; semantic head
+//          (tied text-embedding slice) -> c0
+//   fast:  step 1 rows [RMSNorm(x_slow), cb_embed[0][c0]] at positions 0, 1;
+//          step j = 2..9 row cb_embed[j-1][c_{j-1}] at position j;
+//          4 x layer each; fast head -> c_j
+//   layer: QKV GEMV (RMSNorm prologue, RoPE + KV append epilogue) ->
+//          attention -> O GEMV (+residual) -> gate/up GEMV (RMSNorm prologue,
+//          SwiGLU epilogue) -> down GEMV (+residual)
+// The whole frame is captured once as a CUDA graph whose kernels are chained
+// with programmatic dependent launch, and replayed per decode call; all
+// frame-varying state (position, fed-back ids, forced ids, frame index)
+// lives in device memory.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/tf.h"
+#include "kernels.h"
+
+using namespace tf;
+
+namespace {
+
+constexpr int kAlign = 256;
+thread_local std::string g_create_error;
+
+struct Lin {
+  uint8_t* w = nullptr;
+  float* s = nullptr;  // per-row scales (fp8)
+  int N = 0, K = 0;
+};
+
+struct Layer {
+  Lin qkv, o, w13, w2;
+  uint16_t* attn_norm = nullptr;
+  uint16_t* ffn_norm = nullptr;
+  uint16_t* K = nullptr;  // [Hkv][T][D]
+  uint16_t* V = nullptr;
+};
+
+// Device-resident frame state (one sequence).
+struct DevState {
+  int32_t pos;
+  int32_t frame_index;
+  int32_t forced_on;
+  int32_t hist_idx;
+  uint32_t err;
+  uint32_t samp[3];       // Philox key low, high; temperature bits
+  int32_t forced[16];
+  int32_t sel[16];
+  int32_t fb[16];
+  unsigned long long best[16];
+  uint32_t ticket[16];
+};
+
+}  // namespace
+
+struct tf_ctx {
+  tf_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int eb = 2;        // bytes per linear weight element
+  bool fp8 = false;
+  cudaStream_t own_stream = nullptr;
+  cudaStream_t stream = nullptr;
+  std::string err;
+  bool poisoned = false;
+
+  // sizes
+  int H = 0, Q = 0, KV = 0, QKV = 0, F = 0, D = 0, Hq = 0, Hkv = 0, T = 0;
+  int Vt = 0, Vs = 0, Vc = 0, NCB = 0, Vmax = 0, sem_base = 0;
+
+  // device memory
+  std::vector<void*> allocs;
+  size_t device_bytes = 0;
+  size_t weight_bytes = 0;
+  uint8_t* wbuf = nullptr;
+  std::vector<Layer> slow, fast;
+  uint16_t* text_embed = nullptr;
+  uint16_t* slow_norm = nullptr;
+  uint16_t* fast_norm = nullptr;
+  Lin fast_head;
+  uint16_t* cb_embed = nullptr;
+  std::vector<std::string> loaded;
+  float2* rope = nullptr;
+  uint8_t* staging = nullptr;
+  size_t staging_bytes = 0;
+  float* staging_scale = nullptr;
+
+  float *xs = nullptr, *xf = nullptr, *qbuf = nullptr, *obuf = nullptr, *ubuf = nullptr;
+  float* logits = nullptr;
+  float* part = nullptr;
+  uint32_t* counters = nullptr;
+  float *px = nullptr, *pa = nullptr, *pq = nullptr, *po = nullptr, *pu = nullptr;
+  int32_t* tokens = nullptr;
+  int32_t* hist = nullptr;
+  DevState* st = nullptr;
+  int S_slow = 1;
+
+  // host mirrors
+  int pos_host = 0;
+  int frame_host = 0;
+  bool prefilled = false;
+
+  cudaGraphExec_t graph[2] = {nullptr, nullptr};  // [0] greedy, [1] top-k
+  int graph_nodes = 0;
+  tf_sampling graph_samp{};
+};
+
+namespace {
+
+tf_status fail(tf_ctx* c, tf_status s, const std::string& msg) {
+  c->err = msg;
+  return s;
+}
+
+tf_status cuda_fail(tf_ctx* c, cudaError_t e, const char* where) {
+  c->err = std::string(where) + ": " + cudaGetErrorString(e);
+  c->poisoned = true;
+  return TF_E_CUDA;
+}
+
+#define CK(expr)                                          \
+  do {                                                    \
+    cudaError_t e_ = (expr);                              \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, #expr); \
+  } while (0)
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+tf_status dev_alloc(tf_ctx* c, void** p, size_t bytes) {
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    *p = nullptr;
+    return fail(c, TF_E_NOMEM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+  }
+  c->allocs.push_back(*p);
+  c->device_bytes += bytes;
+  return TF_OK;
+}
+
+template <typename T>
+tf_status dev_alloc_t(tf_ctx* c, T** p, size_t count) {
+  return dev_alloc(c, reinterpret_cast<void**>(p), align_up(count * sizeof(T)));
+}
+
+bool valid_config(const tf_config* cfg, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return false;
+  };
+  if (!cfg) return bad("cfg is NULL");
+  if (cfg->slow_layers < 1 || cfg->fast_layers < 1) return bad("layers must be >= 1");
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (cfg->n_kv_heads < 1 || cfg->n_heads < cfg->n_kv_heads || cfg->n_heads % cfg->n_kv_heads)
+    return bad("n_heads must be a multiple of n_kv_heads");
+  const int g = cfg->n_heads / cfg->n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return bad("n_heads / n_kv_heads must be 1, 2, 4 or 8");
+  if (cfg->hidden < 16 || cfg->hidden % 32) return bad("hidden must be a positive multiple of 32");
+  if (cfg->ffn < 16 || cfg->ffn % 32) return bad("ffn must be a positive multiple of 32");
+  if ((cfg->n_heads * cfg->head_dim) % 32) return bad("n_heads*head_dim must be a multiple of 32");
+  // GEMV activations live in registers: K * bytes / 16 chunks over 256 threads <= 5 each.
+  const int eb = cfg->weight_dtype == TF_WEIGHT_FP8 ? 1 : 2;
+  const int kmax = std::max(std::max(cfg->hidden, cfg->ffn), cfg->n_heads * cfg->head_dim);
+  if (kmax * eb / 16 > 5 * 256) return bad("hidden/ffn too large for the decode GEMV");
+  if (cfg->hidden > 16384) return bad("hidden too large");
+  if (cfg->n_codebooks != 10) return bad("n_codebooks must be 10");
+  if (cfg->semantic_vocab < 1 || cfg->semantic_vocab > cfg->text_vocab)
+    return bad("semantic_vocab must be in [1, text_vocab]");
+  if (cfg->semantic_vocab > 8192 || cfg->codebook_size > 8192 || cfg->codebook_size < 1)
+    return bad("semantic_vocab and codebook_size must be in [1, 8192]");
+  if (cfg->max_seq_len < 10 || cfg->max_seq_len > 65536) return bad("max_seq_len must be in [10, 65536]");
+  if (cfg->max_batch != 1) return bad("max_batch must be 1 (batched decode is not built)");
+  if (!(cfg->rms_eps > 0.f) || !(cfg->rope_theta > 1.f)) return bad("rms_eps > 0 and rope_theta > 1 required");
+  if (cfg->weight_dtype != TF_WEIGHT_BF16 && cfg->weight_dtype != TF_WEIGHT_FP8)
+    return bad("weight_dtype must be TF_WEIGHT_BF16 or TF_WEIGHT_FP8");
+  return true;
+}
+
+tf_status check_kernel_errors(tf_ctx* c) {
+  uint32_t e = 0;
+  CK(cudaMemcpyAsync(&e, &c->st->err, sizeof(e), cudaMemcpyDeviceToHost, c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  if (!e) return TF_OK;
+  if (e & ERR_TIMEOUT) {
+    c->poisoned = true;
+    return fail(c, TF_E_TIMEOUT, "a bounded device wait expired");
+  }
+  CK(cudaMemsetAsync(&c->st->err, 0, sizeof(uint32_t), c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  if (e & ERR_NAN) return fail(c, TF_E_NUMERIC, "NaN logit met during selection");
+  c->poisoned = true;
+  return fail(c, TF_E_STATE, "device reported an id or position out of range");
+}
+
+// ------------------------------------------------------------------ launches
+cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_t* nw, int epi,
+                 float* out, int ldo, int M, bool pdl, const Layer* layer = nullptr,
+                 const int32_t* pos_ptr = nullptr, int pos_fixed = 0, int cb = -1,
+                 bool select = false) {
+  GemvParams p = {};
+  p.W = L.w;
+  p.scale = L.s;
+  p.N = L.N;
+  p.K = L.K;
+  p.pro = pro;
+  p.x = x;
+  p.ldx = L.K;
+  p.nw = nw;
+  p.eps = c->cfg.rms_eps;
+  p.epi = epi;
+  p.out = out;
+  p.ldo = ldo;
+  p.q_dim = c->Q;
+  p.kv_dim = c->KV;
+  p.head_dim = c->D;
+  p.qout = c->qbuf;
+  if (layer) {
+    p.Kc = layer->K;
+    p.Vc = layer->V;
+  }
+  p.T = c->T;
+  p.pos_ptr = pos_ptr;
+  p.pos_fixed = pos_fixed;
+  p.rope = c->rope;
+  p.err = &c->st->err;
+  if (cb >= 0) {
+    p.select = select ? 1 : 0;
+    p.best = &c->st->best[cb];
+    p.ticket = &c->st->ticket[cb];
+    p.sel = &c->st->sel[cb];
+    p.fb = &c->st->fb[cb];
+    p.forced = &c->st->forced[cb];
+    p.forced_on = &c->st->forced_on;
+  }
+  const int eb = (L.s != nullptr) ? 1 : 2;
+  gemv_plan(p, eb, c->num_sms);
+  const int grid = std::min(c->num_sms, p.units);
+  return launch_gemv(p, eb == 1 ? 1 : 0, M, grid, pdl, c->stream);
+}
+
+cudaError_t layer_decode(tf_ctx* c, const Layer& L, float* x, int M, const int32_t* pos_ptr,
+                         int pos_fixed, int S, bool pdl_first) {
+  cudaError_t e;
+  if ((e = gemv(c, L.qkv, PRO_NORM, x, L.attn_norm, EPI_QKV, nullptr, 0, M, pdl_first, &L, pos_ptr,
+                pos_fixed)))
+    return e;
+  AttnParams a = {};
+  a.q = c->qbuf;
+  a.Kc = L.K;
+  a.Vc = L.V;
+  a.T = c->T;
+  a.Hq = c->Hq;
+  a.Hkv = c->Hkv;
+  a.D = c->D;
+  a.pos_ptr = pos_ptr;
+  a.pos_fixed = pos_fixed;
+  a.S = S;
+  a.part = c->part;
+  a.counters = c->counters;
+  a.out = c->obuf;
+  a.err = &c->st->err;
+  if ((e = launch_attention(a, M, true, c->stream))) return e;
+  if ((e = gemv(c, L.o, PRO_PLAIN, c->obuf, nullptr, EPI_RESID, x, c->H, M, true))) return e;
+  if ((e = gemv(c, L.w13, PRO_NORM, x, L.ffn_norm, EPI_SWIGLU, c->ubuf, c->F, M, true))) return e;
+  return gemv(c, L.w2, PRO_PLAIN, c->ubuf, nullptr, EPI_RESID, x, c->H, M, true);
+}
+
+cudaError_t enqueue_select(tf_ctx* c, int cb, const tf_sampling* s) {
+  SelectParams q = {};
+  q.logits = c->logits + (size_t)cb * c->Vmax;
+  q.ld = c->Vmax;
+  q.vocab = cb == 0 ? c->Vs : c->Vc;
+  q.n = 1;
+  q.top_k = s->top_k;
+  q.temperature = s->temperature;
+  q.key0 = static_cast<uint32_t>(s->seed & 0xFFFFFFFFull);
+  q.key1 = static_cast<uint32_t>(s->seed >> 32);
+  q.frame_ptr = &c->st->frame_index;
+  q.codebook0 = cb;
+  q.sequence = 0;
+  q.sel = &c->st->sel[cb];
+  q.fb = &c->st->fb[cb];
+  q.forced = &c->st->forced[cb];
+  q.forced_on = &c->st->forced_on;
+  q.err = &c->st->err;
+  return launch_select(q, true, c->stream);
+}
+
+// Semantic head + fast loop + bookkeeping, from the slow residual xs.
+cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_first) {
+  cudaError_t e;
+  const bool topk = s->top_k > 0;
+  Lin sem;
+  sem.w = reinterpret_cast<uint8_t*>(c->text_embed + (size_t)c->sem_base * c->H);
+  sem.N = c->Vs;
+  sem.K = c->H;
+  if ((e = gemv(c, sem, PRO_NORM, c->xs, c->slow_norm, EPI_LOGITS, c->logits, 0, 1, pdl_first,
+                nullptr, nullptr, 0, 0, !topk)))
+    return e;
+  if (topk && (e = enqueue_select(c, 0, s))) return e;
+  for (int j = 1; j < c->NCB; ++j) {
+    BuildParams b = {};
+    b.mode = j == 1 ? BUILD_FAST1 : BUILD_FASTJ;
+    b.j = j;
+    b.H = c->H;
+    b.M = j == 1 ? 2 : 1;
+    b.table = c->cb_embed + (size_t)(j - 1) * c->Vc * c->H;
+    b.table_rows = c->Vc;
+    b.row_base = 0;
+    b.ids = &c->st->fb[j - 1];
+    b.xs = c->xs;
+    b.nw = c->slow_norm;
+    b.eps = c->cfg.rms_eps;
+    b.x = c->xf;
+    b.err = &c->st->err;
+    if ((e = launch_build(b, true, c->stream))) return e;
+    const int M = b.M;
+    for (const Layer& L : c->fast)
+      if ((e = layer_decode(c, L, c->xf, M, nullptr, j == 1 ? 0 : j, 1, true))) return e;
+    if ((e = gemv(c, c->fast_head, PRO_NORM, c->xf + (size_t)(M - 1) * c->H, c->fast_norm,
+                  EPI_LOGITS, c->logits + (size_t)j * c->Vmax, 0, 1, true, nullptr, nullptr, 0, j,
+                  !topk)))
+      return e;
+    if (topk && (e = enqueue_select(c, j, s))) return e;
+  }
+  FrameEndParams f = {};
+  f.pos = &c->st->pos;
+  f.advance = advance;
+  f.frame_index = &c->st->frame_index;
+  f.sel = c->st->sel;
+  f.ncb = c->NCB;
+  f.hist = c->hist;
+  f.hist_idx = &c->st->hist_idx;
+  f.hist_cap = c->T;
+  return launch_frame_end(f, true, c->stream);
+}
+
+cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
+  cudaError_t e;
+  BuildParams b = {};
+  b.mode = BUILD_SLOW;
+  b.H = c->H;
+  b.M = 1;
+  b.table = c->text_embed;
+  b.table_rows = c->Vs;
+  b.row_base = c->sem_base;
+  b.ids = &c->st->fb[0];
+  b.x = c->xs;
+  b.err = &c->st->err;
+  if ((e = launch_build(b, false, c->stream))) return e;
+  for (const Layer& L : c->slow)
+    if ((e = layer_decode(c, L, c->xs, 1, &c->st->pos, 0, c->S_slow, true))) return e;
+  return enqueue_tail(c, s, 1, true);
+}
+
+bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
+  return a.top_k == b.top_k && a.temperature == b.temperature && a.seed == b.seed;
+}
+
+tf_status get_graph(tf_ctx* c, const tf_sampling* s, cudaGraphExec_t* out) {
+  const int gi = s->top_k > 0 ? 1 : 0;
+  if (c->graph[gi] && (gi == 0 || same_sampling(c->graph_samp, *s))) {
+    *out = c->graph[gi];
+    return TF_OK;
+  }
+  if (c->graph[gi]) {
+    cudaGraphExecDestroy(c->graph[gi]);
+    c->graph[gi] = nullptr;
+  }
+  cudaGraph_t g = nullptr;
+  CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+  cudaError_t e = enqueue_decode_frame(c, s);
+  cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return cuda_fail(c, e, "capture of the decode frame");
+  }
+  if (e2 != cudaSuccess) return cuda_fail(c, e2, "cudaStreamEndCapture");
+  size_t n = 0;
+  cudaGraphGetNodes(g, nullptr, &n);
+  c->graph_nodes = static_cast<int>(n);
+  cudaError_t e3 = cudaGraphInstantiate(&c->graph[gi], g, 0);
+  cudaGraphDestroy(g);
+  if (e3 != cudaSuccess) return cuda_fail(c, e3, "cudaGraphInstantiate");
+  if (gi == 1) c->graph_samp = *s;
+  *out = c->graph[gi];
+  return TF_OK;
+}
+
+tf_status check_sampling(tf_ctx* c, const tf_sampling* s, tf_sampling* out) {
+  tf_sampling d = {0, 1.0f, 0};
+  if (s) d = *s;
+  if (d.top_k < 0 || d.top_k > 256) return fail(c, TF_E_INVAL, "top_k must be in [0, 256]");
+  if (!(d.temperature > 0.f) || !std::isfinite(d.temperature))
+    return fail(c, TF_E_INVAL, "temperature must be finite and > 0");
+  if (d.top_k == 1) d.top_k = 0;  // one candidate: the argmax
+  if (d.top_k == 0) {
+    d.temperature = 1.0f;
+    d.seed = 0;
+  }
+  *out = d;
+  return TF_OK;
+}
+
+tf_status set_forced(tf_ctx* c, const int32_t* forced) {
+  int32_t on = forced ? 1 : 0;
+  if (forced) {
+    for (int j = 0; j < c->NCB; ++j) {
+      const int lim = j == 0 ? c->Vs : c->Vc;
+      if (forced[j] < 0 || forced[j] >= lim)
+        return fail(c, TF_E_INVAL, "forced id out of range at codebook " + std::to_string(j));
+    }
+    CK(cudaMemcpyAsync(c->st->forced, forced, sizeof(int32_t) * c->NCB, cudaMemcpyHostToDevice,
+                       c->stream));
+  }
+  CK(cudaMemcpyAsync(&c->st->forced_on, &on, sizeof(on), cudaMemcpyHostToDevice, c->stream));
+  return TF_OK;
+}
+
+tf_status read_frame(tf_ctx* c, int32_t* frame, float* logits) {
+  if (frame)
+    CK(cudaMemcpyAsync(frame, c->st->sel, sizeof(int32_t) * c->NCB, cudaMemcpyDeviceToHost,
+                       c->stream));
+  if (logits)
+    CK(cudaMemcpyAsync(logits, c->logits, sizeof(float) * c->NCB * c->Vmax, cudaMemcpyDeviceToHost,
+                       c->stream));
+  return check_kernel_errors(c);
+}
+
+bool all_loaded(tf_ctx* c, std::string* missing);
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
+  if (!out) {
+    g_create_error = "out is NULL";
+    return TF_E_INVAL;
+  }
+  *out = nullptr;
+  std::string why;
+  if (!valid_config(cfg, &why)) {
+    g_create_error = why;
+    return TF_E_INVAL;
+  }
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    (void)cudaGetLastError();
+    g_create_error = "no such CUDA device";
+    return TF_E_INVAL;
+  }
+  tf_ctx* c = new (std::nothrow) tf_ctx();
+  if (!c) {
+    g_create_error = "host allocation failed";
+    return TF_E_NOMEM;
+  }
+  c->cfg = *cfg;
+  c->device = device;
+  auto bail = [&](tf_status s) {
+    g_create_error = c->err;
+    tf_destroy(c);
+    return s;
+  };
+  if (cudaSetDevice(device) != cudaSuccess) {
+    c->err = "cudaSetDevice failed";
+    return bail(TF_E_CUDA);
+  }
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device);
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  if (major * 10 + minor != 103) {
+    c->err = "this library is built for sm_103 (GB300); device is sm_" + std::to_string(major * 10 + minor);
+    return bail(TF_E_INVAL);
+  }
+  if (cudaStreamCreateWithFlags(&c->own_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    c->err = "cudaStreamCreate failed";
+    return bail(TF_E_CUDA);
+  }
+  c->stream = c->own_stream;
+  if (gemv_set_attributes() != cudaSuccess) {
+    c->err = "cudaFuncSetAttribute failed";
+    return bail(TF_E_CUDA);
+  }
+
+  c->fp8 = cfg->weight_dtype == TF_WEIGHT_FP8;
+  c->eb = c->fp8 ? 1 : 2;
+  c->H = cfg->hidden;
+  c->D = cfg->head_dim;
+  c->Hq = cfg->n_heads;
+  c->Hkv = cfg->n_kv_heads;
+  c->Q = c->Hq * c->D;
+  c->KV = c->Hkv * c->D;
+  c->QKV = c->Q + 2 * c->KV;
+  c->F = cfg->ffn;
+  c->T = cfg->max_seq_len;
+  c->Vt = cfg->text_vocab;
+  c->Vs = cfg->semantic_vocab;
+  c->Vc = cfg->codebook_size;
+  c->NCB = cfg->n_codebooks;
+  c->Vmax = std::max(c->Vs, c->Vc);
+  c->sem_base = c->Vt - c->Vs;
+  c->S_slow = std::max(1, std::min(64, 2 * c->num_sms / c->Hkv));
+
+  // ---- weights: one allocation
+  const size_t eb = c->eb, H = c->H;
+  auto lin_bytes = [&](size_t n, size_t k) {
+    return align_up(n * k * eb) + (c->fp8 ? align_up(n * sizeof(float)) : 0);
+  };
+  const size_t layer_bytes = lin_bytes(c->QKV, H) + lin_bytes(H, c->Q) + lin_bytes(2 * c->F, H) +
+                             lin_bytes(H, c->F) + 2 * align_up(H * 2);
+  size_t wtotal = align_up((size_t)c->Vt * H * 2) + (cfg->slow_layers + cfg->fast_layers) * layer_bytes +
+                  2 * align_up(H * 2) + lin_bytes(c->Vc, H) +
+                  align_up((size_t)(c->NCB - 1) * c->Vc * H * 2);
+  if (dev_alloc(c, reinterpret_cast<void**>(&c->wbuf), wtotal) != TF_OK) return bail(TF_E_NOMEM);
+  c->weight_bytes = wtotal;
+  uint8_t* cur = c->wbuf;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = cur;
+    cur += align_up(bytes);
+    return p;
+  };
+  auto make_lin = [&](int n, int k) {
+    Lin L;
+    L.N = n;
+    L.K = k;
+    L.w = take((size_t)n * k * eb);
+    if (c->fp8) L.s = reinterpret_cast<float*>(take((size_t)n * sizeof(float)));
+    return L;
+  };
+  c->text_embed = reinterpret_cast<uint16_t*>(take((size_t)c->Vt * H * 2));
+  auto make_layers = [&](std::vector<Layer>& v, int n) {
+    v.resize(n);
+    for (Layer& L : v) {
+      L.qkv = make_lin(c->QKV, c->H);
+      L.o = make_lin(c->H, c->Q);
+      L.w13 = make_lin(2 * c->F, c->H);
+      L.w2 = make_lin(c->H, c->F);
+      L.attn_norm = reinterpret_cast<uint16_t*>(take(H * 2));
+      L.ffn_norm = reinterpret_cast<uint16_t*>(take(H * 2));
+    }
+  };
+  make_layers(c->slow, cfg->slow_layers);
+  make_layers(c->fast, cfg->fast_layers);
+  c->slow_norm = reinterpret_cast<uint16_t*>(take(H * 2));
+  c->fast_norm = reinterpret_cast<uint16_t*>(take(H * 2));
+  c->fast_head = make_lin(c->Vc, c->H);
+  c->cb_embed = reinterpret_cast<uint16_t*>(take((size_t)(c->NCB - 1) * c->Vc * H * 2));
+
+  // ---- KV caches
+  const size_t kv_elems = (size_t)c->Hkv * c->T * c->D;
+  for (Layer& L : c->slow) {
+    if (dev_alloc_t(c, &L.K, kv_elems) || dev_alloc_t(c, &L.V, kv_elems)) return bail(TF_E_NOMEM);
+  }
+  const size_t fkv = (size_t)c->Hkv * c->T * c->D;  // fast uses positions 0..9 of a T-slot cache
+  for (Layer& L : c->fast) {
+    if (dev_alloc_t(c, &L.K, fkv) || dev_alloc_t(c, &L.V, fkv)) return bail(TF_E_NOMEM);
+  }
+
+  // ---- staging for weight loads (largest linear tensor, bf16)
+  size_t st = std::max({(size_t)c->QKV * H, (size_t)H * c->Q, (size_t)c->F * H, (size_t)c->Vc * H}) * 2;
+  c->staging_bytes = st;
+  if (dev_alloc(c, reinterpret_cast<void**>(&c->staging), st)) return bail(TF_E_NOMEM);
+  if (dev_alloc_t(c, &c->staging_scale, std::max({c->QKV, c->H, c->F, c->Vc}))) return bail(TF_E_NOMEM);
+
+  // ---- activations and state
+  const int T = c->T;
+  if (dev_alloc_t(c, &c->xs, H) || dev_alloc_t(c, &c->xf, 2 * H) || dev_alloc_t(c, &c->qbuf, 2 * c->Q) ||
+      dev_alloc_t(c, &c->obuf, 2 * c->Q) || dev_alloc_t(c, &c->ubuf, 2 * c->F) ||
+      dev_alloc_t(c, &c->logits, (size_t)c->NCB * c->Vmax) ||
+      dev_alloc_t(c, &c->part, (size_t)2 * c->Hq * c->S_slow * (c->D + 2)) ||
+      dev_alloc_t(c, &c->counters, (size_t)2 * c->Hkv) ||
+      dev_alloc_t(c, &c->px, (size_t)T * H) || dev_alloc_t(c, &c->pa, (size_t)T * H) ||
+      dev_alloc_t(c, &c->pq, (size_t)T * c->Q) || dev_alloc_t(c, &c->po, (size_t)T * c->Q) ||
+      dev_alloc_t(c, &c->pu, (size_t)T * c->F) || dev_alloc_t(c, &c->tokens, (size_t)T) ||
+      dev_alloc_t(c, &c->hist, (size_t)T * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
+      dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)))
+    return bail(TF_E_NOMEM);
+
+  // RoPE table: angle pos * theta^(-2i/D) evaluated in double, stored as float.
+  {
+    std::vector<float2> tab((size_t)T * (c->D / 2));
+    for (int p = 0; p < T; ++p)
+      for (int i = 0; i < c->D / 2; ++i) {
+        const double inv = std::pow((double)cfg->rope_theta, -2.0 * i / c->D);
+        const double a = p * inv;
+        tab[(size_t)p * (c->D / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    if (cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice)) {
+      c->err = "rope table upload failed";
+      return bail(TF_E_CUDA);
+    }
+  }
+  if (cudaMemset(c->st, 0, sizeof(DevState)) || cudaMemset(c->counters, 0, 2 * c->Hkv * 4)) {
+    c->err = "state init failed";
+    return bail(TF_E_CUDA);
+  }
+  for (const Layer& L : c->fast) {
+    cudaMemset(L.K, 0, fkv * 2);
+    cudaMemset(L.V, 0, fkv * 2);
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    c->err = "device sync failed";
+    return bail(TF_E_CUDA);
+  }
+  *out = c;
+  return TF_OK;
+}
+
+void tf_destroy(tf_ctx* c) {
+  if (!c) return;
+  for (auto& g : c->graph)
+    if (g) cudaGraphExecDestroy(g);
+  if (c->own_stream) cudaStreamSynchronize(c->own_stream);
+  for (void* p : c->allocs) cudaFree(p);
+  if (c->own_stream) cudaStreamDestroy(c->own_stream);
+  delete c;
+}
+
+const char* tf_last_error(const tf_ctx* c) {
+  if (!c) return g_create_error.c_str();
+  return c->err.c_str();
+}
+
+tf_status tf_set_stream(tf_ctx* c, void* stream) {
+  if (!c) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  CK(cudaStreamSynchronize(c->stream));
+  c->stream = stream ? static_cast<cudaStream_t>(stream) : c->own_stream;
+  return TF_OK;
+}
+
+void* tf_get_stream(const tf_ctx* c) { return c ? static_cast<void*>(c->stream) : nullptr; }
+
+tf_status tf_get_info(const tf_ctx* c, tf_info* info) {
+  if (!c || !info) return TF_E_INVAL;
+  info->position = c->pos_host;
+  info->frame_index = c->frame_host;
+  info->num_sms = c->num_sms;
+  info->graph_nodes = c->graph_nodes;
+  info->weight_bytes = static_cast<int64_t>(c->weight_bytes);
+  int64_t lin = (int64_t)c->QKV * c->H + (int64_t)c->H * c->Q + 2LL * c->F * c->H + (int64_t)c->H * c->F;
+  int64_t norms = 2LL * c->H * 2;
+  int64_t slow = c->slow.size() * (lin * c->eb + norms) + (int64_t)c->Vs * c->H * 2 + c->H * 2 + c->H * 2;
+  int64_t fast = c->fast.size() * (lin * c->eb + norms) + (int64_t)c->Vc * c->H * c->eb + c->H * 2 + c->H * 2;
+  if (c->fp8) {
+    slow += c->slow.size() * (int64_t)(c->QKV + c->H + 2 * c->F + c->H) * 4;
+    fast += c->fast.size() * (int64_t)(c->QKV + c->H + 2 * c->F + c->H) * 4 + (int64_t)c->Vc * 4;
+  }
+  info->frame_weight_bytes = slow + (c->NCB - 1) * fast;
+  info->device_bytes = static_cast<int64_t>(c->device_bytes);
+  return TF_OK;
+}
+
+tf_status tf_load_weights(tf_ctx* c, const tf_tensor* t, int32_t n) {
+  if (!c || (!t && n) || n < 0) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  CK(cudaSetDevice(c->device));
+  for (int32_t i = 0; i < n; ++i) {
+    const tf_tensor& x = t[i];
+    if (!x.name || !x.data) return fail(c, TF_E_INVAL, "tensor without name or data");
+    const std::string name = x.name;
+    auto shape_is = [&](std::initializer_list<int64_t> s) {
+      if (x.ndim != (int)s.size()) return false;
+      int k = 0;
+      for (int64_t v : s)
+        if (x.shape[k++] != v) return false;
+      return true;
+    };
+    auto bad_shape = [&]() { return fail(c, TF_E_INVAL, "wrong shape for " + name); };
+    auto copy_raw = [&](void* dst, size_t bytes) -> tf_status {
+      if (x.dtype != TF_DTYPE_BF16) return fail(c, TF_E_INVAL, name + " must be bf16");
+      CK(cudaMemcpyAsync(dst, x.data, bytes, cudaMemcpyDefault, c->stream));
+      return TF_OK;
+    };
+    auto load_lin = [&](Lin& L, int rows, int cols, int map, size_t dst_row0) -> tf_status {
+      if (!shape_is({rows, cols})) return bad_shape();
+      PackParams p = {};
+      p.rows = rows;
+      p.cols = cols;
+      p.map = map;
+      p.q_dim = c->Q;
+      p.kv_dim = c->KV;
+      p.head_dim = c->D;
+      p.src = c->staging;
+      p.dst = L.w + dst_row0 * cols * c->eb;
+      p.dst_scale = L.s ? L.s + dst_row0 : nullptr;
+      if (x.dtype == TF_DTYPE_BF16) {
+        CK(cudaMemcpyAsync(c->staging, x.data, (size_t)rows * cols * 2, cudaMemcpyDefault, c->stream));
+        p.mode = c->fp8 ? 1 : 0;
+      } else if (x.dtype == TF_DTYPE_FP8_E4M3) {
+        if (!c->fp8) return fail(c, TF_E_INVAL, name + ": fp8 tensor in a bf16 context");
+        if (!x.row_scale) return fail(c, TF_E_INVAL, name + ": fp8 tensor without row_scale");
+        CK(cudaMemcpyAsync(c->staging, x.data, (size_t)rows * cols, cudaMemcpyDefault, c->stream));
+        CK(cudaMemcpyAsync(c->staging_scale, x.row_scale, (size_t)rows * 4, cudaMemcpyDefault, c->stream));
+        p.src_scale = c->staging_scale;
+        p.mode = 2;
+      } else {
+        return fail(c, TF_E_INVAL, name + ": unknown dtype");
+      }
+      CK(launch_pack(p, c->stream));
+      return TF_OK;
+    };
+    tf_status s = TF_OK;
+    const size_t H = c->H;
+    int li = -1;
+    char part[16] = {0}, field[32] = {0};
+    if (name == "text_embed") {
+      s = shape_is({c->Vt, c->H}) ? copy_raw(c->text_embed, (size_t)c->Vt * H * 2) : bad_shape();
+    } else if (name == "slow.norm" || name == "fast.norm") {
+      s = shape_is({c->H}) ? copy_raw(name[0] == 's' ? c->slow_norm : c->fast_norm, H * 2) : bad_shape();
+    } else if (name == "fast.head") {
+      s = load_lin(c->fast_head, c->Vc, c->H, MAP_IDENTITY, 0);
+    } else if (name == "fast.cb_embed") {
+      s = shape_is({c->NCB - 1, c->Vc, c->H}) ? copy_raw(c->cb_embed, (size_t)(c->NCB - 1) * c->Vc * H * 2)
+                                              : bad_shape();
+    } else if (std::sscanf(name.c_str(), "%15[a-z].%d.%31s", part, &li, field) == 3 &&
+               (std::string(part) == "slow" || std::string(part) == "fast")) {
+      std::vector<Layer>& v = std::string(part) == "slow" ? c->slow : c->fast;
+      if (li < 0 || li >= (int)v.size()) return fail(c, TF_E_INVAL, "layer index out of range: " + name);
+      Layer& L = v[li];
+      const std::string f = field;
+      if (f == "attn_norm" || f == "ffn_norm") {
+        s = shape_is({c->H}) ? copy_raw(f[0] == 'a' ? L.attn_norm : L.ffn_norm, H * 2) : bad_shape();
+      } else if (f == "wqkv") {
+        s = load_lin(L.qkv, c->QKV, c->H, MAP_QKV, 0);
+      } else if (f == "wo") {
+        s = load_lin(L.o, c->H, c->Q, MAP_IDENTITY, 0);
+      } else if (f == "w1") {
+        s = load_lin(L.w13, c->F, c->H, MAP_GATE, 0);
+      } else if (f == "w3") {
+        s = load_lin(L.w13, c->F, c->H, MAP_UP, 0);
+      } else if (f == "w2") {
+        s = load_lin(L.w2, c->H, c->F, MAP_IDENTITY, 0);
+      } else {
+        return fail(c, TF_E_INVAL, "unknown tensor " + name);
+      }
+    } else {
+      return fail(c, TF_E_INVAL, "unknown tensor " + name);
+    }
+    if (s != TF_OK) return s;
+    // The staging buffer is reused by the next tensor.
+    CK(cudaStreamSynchronize(c->stream));
+    bool seen = false;
+    for (auto& l : c->loaded) seen |= (l == name);
+    if (!seen) c->loaded.push_back(name);
+  }
+  CK(cudaStreamSynchronize(c->stream));
+  return TF_OK;
+}
+
+}  // extern "C"
+
+namespace {
+bool all_loaded(tf_ctx* c, std::string* missing) {
+  const size_t need = 1 + 7 * (c->slow.size() + c->fast.size()) + 4;
+  if (c->loaded.size() >= need) return true;
+  *missing = std::to_string(need - c->loaded.size()) + " tensor(s) not loaded";
+  return false;
+}
+}  // namespace
+
+extern "C" {
+
+tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
+                     const tf_sampling* sampling, const int32_t* forced, int32_t* frame0,
+                     float* logits) {
+  if (!c) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  if (!tokens || !frame0) return fail(c, TF_E_INVAL, "tokens and frame0 are required");
+  if (B != 1) return fail(c, TF_E_INVAL, "B must be 1");
+  if (P < 1 || P > c->T) return fail(c, TF_E_INVAL, "P must be in [1, max_seq_len]");
+  std::string missing;
+  if (!all_loaded(c, &missing)) return fail(c, TF_E_STATE, missing);
+  for (int i = 0; i < P; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c->Vt) return fail(c, TF_E_INVAL, "prompt id out of range");
+  tf_sampling s;
+  tf_status r = check_sampling(c, sampling, &s);
+  if (r) return r;
+  CK(cudaSetDevice(c->device));
+  if ((r = set_forced(c, forced))) return r;
+  CK(cudaMemcpyAsync(c->tokens, tokens, sizeof(int32_t) * P, cudaMemcpyHostToDevice, c->stream));
+  const int32_t zero4[4] = {0, 0, 0, 0};  // pos, frame_index, forced_on kept, hist_idx
+  CK(cudaMemcpyAsync(&c->st->pos, &zero4[0], 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(&c->st->frame_index, &zero4[1], 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(&c->st->hist_idx, &zero4[3], 4, cudaMemcpyHostToDevice, c->stream));
+  if (s.top_k > 0) {
+    const uint32_t samp[3] = {(uint32_t)(s.seed & 0xFFFFFFFFu), (uint32_t)(s.seed >> 32), 0};
+    CK(cudaMemcpyAsync(c->st->samp, samp, sizeof(samp), cudaMemcpyHostToDevice, c->stream));
+  }
+
+  // Slow decoder over the prompt: row m at position m.
+  BuildParams b = {};
+  b.mode = BUILD_TOKENS;
+  b.H = c->H;
+  b.M = P;
+  b.table = c->text_embed;
+  b.table_rows = c->Vt;
+  b.ids = c->tokens;
+  b.x = c->px;
+  b.err = &c->st->err;
+  CK(launch_build(b, false, c->stream));
+  const int wt = c->fp8 ? 1 : 0;
+  auto gemm = [&](const Lin& L, const float* A, int epi, float* out, int ldo, const Layer* layer) {
+    GemvParams p = {};
+    p.W = L.w;
+    p.scale = L.s;
+    p.N = L.N;
+    p.K = L.K;
+    p.x = A;
+    p.ldx = L.K;
+    p.epi = epi;
+    p.out = out;
+    p.ldo = ldo;
+    p.q_dim = c->Q;
+    p.kv_dim = c->KV;
+    p.head_dim = c->D;
+    p.qout = c->pq;
+    if (layer) {
+      p.Kc = layer->K;
+      p.Vc = layer->V;
+    }
+    p.T = c->T;
+    p.pos_fixed = 0;
+    p.rope = c->rope;
+    p.err = &c->st->err;
+    return launch_gemm_rows(p, wt, P, c->stream);
+  };
+  for (const Layer& L : c->slow) {
+    CK(launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
+    CK(gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L));
+    AttnParams a = {};
+    a.q = c->pq;
+    a.Kc = L.K;
+    a.Vc = L.V;
+    a.T = c->T;
+    a.Hq = c->Hq;
+    a.Hkv = c->Hkv;
+    a.D = c->D;
+    a.pos_fixed = 0;
+    a.S = 1;
+    a.part = c->part;
+    a.counters = c->counters;
+    a.out = c->po;
+    a.err = &c->st->err;
+    CK(launch_attention(a, P, false, c->stream));
+    CK(gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr));
+    CK(launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
+    CK(gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr));
+    CK(gemm(L.w2, c->pu, EPI_RESID, c->px, c->H, nullptr));
+  }
+  CK(cudaMemcpyAsync(c->xs, c->px + (size_t)(P - 1) * c->H, sizeof(float) * c->H,
+                     cudaMemcpyDeviceToDevice, c->stream));
+  const int32_t posP = P;
+  CK(cudaMemcpyAsync(&c->st->pos, &posP, 4, cudaMemcpyHostToDevice, c->stream));
+  CK(enqueue_tail(c, &s, 0, false));
+  c->pos_host = P;
+  c->frame_host = 1;
+  c->prefilled = true;
+  return read_frame(c, frame0, logits);
+}
+
+tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t* forced,
+                          int32_t* frame, float* logits) {
+  if (!c) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  if (!frame) return fail(c, TF_E_INVAL, "frame is required");
+  if (!c->prefilled) return fail(c, TF_E_STATE, "tf_prefill must come first");
+  if (c->pos_host >= c->T) return fail(c, TF_E_CAPACITY, "KV cache full");
+  tf_sampling s;
+  tf_status r = check_sampling(c, sampling, &s);
+  if (r) return r;
+  CK(cudaSetDevice(c->device));
+  if ((r = set_forced(c, forced))) return r;
+  cudaGraphExec_t g;
+  if ((r = get_graph(c, &s, &g))) return r;
+  CK(cudaGraphLaunch(g, c->stream));
+  c->pos_host += 1;
+  c->frame_host += 1;
+  return read_frame(c, frame, logits);
+}
+
+tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, int32_t* frames) {
+  if (!c) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  if (n < 0 || (n > 0 && !frames)) return fail(c, TF_E_INVAL, "bad n or frames");
+  if (!c->prefilled) return fail(c, TF_E_STATE, "tf_prefill must come first");
+  if (c->pos_host + n > c->T) return fail(c, TF_E_CAPACITY, "KV cache cannot hold n more frames");
+  if (n == 0) return TF_OK;
+  tf_sampling s;
+  tf_status r = check_sampling(c, sampling, &s);
+  if (r) return r;
+  CK(cudaSetDevice(c->device));
+  if ((r = set_forced(c, nullptr))) return r;
+  cudaGraphExec_t g;
+  if ((r = get_graph(c, &s, &g))) return r;
+  const int32_t zero = 0;
+  CK(cudaMemcpyAsync(&c->st->hist_idx, &zero, 4, cudaMemcpyHostToDevice, c->stream));
+  for (int i = 0; i < n; ++i) CK(cudaGraphLaunch(g, c->stream));
+  c->pos_host += n;
+  c->frame_host += n;
+  CK(cudaMemcpyAsync(frames, c->hist, sizeof(int32_t) * c->NCB * n, cudaMemcpyDeviceToHost, c->stream));
+  return check_kernel_errors(c);
+}
+
+tf_status tf_profile_kernel(tf_ctx* c, int32_t which, int32_t iters, float* ms_per_launch,
+                            int64_t* bytes_per_launch) {
+  if (!c || iters < 1 || which < 0 || which > 3) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  std::string missing;
+  if (!all_loaded(c, &missing)) return fail(c, TF_E_STATE, missing);
+  CK(cudaSetDevice(c->device));
+  const int Ls = static_cast<int>(c->slow.size());
+  // Scratch input rows: finite values in every activation buffer the kernel reads.
+  CK(cudaMemsetAsync(c->pa, 0, sizeof(float) * c->H, c->stream));
+  std::vector<float> ones(std::max({c->H, c->Q, c->F}), 0.01f);
+  CK(cudaMemcpyAsync(c->pa, ones.data(), sizeof(float) * c->H, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->po, ones.data(), sizeof(float) * c->Q, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->pu, ones.data(), sizeof(float) * c->F, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  const int32_t pos0 = 0;
+  auto launch = [&](int i, bool pdl) -> cudaError_t {
+    const Layer& L = c->slow[i % Ls];
+    switch (which) {
+      case 0: return gemv(c, L.w13, PRO_NORM, c->pa, L.ffn_norm, EPI_SWIGLU, c->pq, c->F, 1, pdl);
+      case 1: return gemv(c, L.qkv, PRO_NORM, c->pa, L.attn_norm, EPI_QKV, nullptr, 0, 1, pdl,
+                          &c->slow[(i + 1) % Ls], nullptr, pos0);
+      case 2: return gemv(c, L.o, PRO_PLAIN, c->po, nullptr, EPI_RESID, c->px, c->H, 1, pdl);
+      default: return gemv(c, L.w2, PRO_PLAIN, c->pu, nullptr, EPI_RESID, c->px, c->H, 1, pdl);
+    }
+  };
+  // Warm-up (one pass over the layers), then the timed launches.
+  for (int i = 0; i < Ls; ++i) CK(launch(i, i > 0));
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  CK(cudaEventRecord(e0, c->stream));
+  for (int i = 0; i < iters; ++i) CK(launch(i, i > 0));
+  CK(cudaEventRecord(e1, c->stream));
+  CK(cudaEventSynchronize(e1));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (ms_per_launch) *ms_per_launch = ms / iters;
+  const Layer& L0 = c->slow[0];
+  const Lin& lin = which == 0 ? L0.w13 : which == 1 ? L0.qkv : which == 2 ? L0.o : L0.w2;
+  int64_t bytes = (int64_t)lin.N * lin.K * c->eb + (c->fp8 ? (int64_t)lin.N * 4 : 0);
+  bytes += (int64_t)lin.K * 4;                        // activation row in
+  if (which == 0 || which == 1) bytes += (int64_t)lin.K * 2;  // RMSNorm weight
+  bytes += which == 0 ? (int64_t)c->F * 4 : which == 1 ? (int64_t)(c->Q * 4 + 2 * c->KV * 2)
+                                                       : (int64_t)c->H * 8;  // out (+ residual read)
+  if (bytes_per_launch) *bytes_per_launch = bytes;
+  return check_kernel_errors(c);
+}
+
+// ------------------------------------------------------------------ ops
+tf_status tf_op_quantize_fp8(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* codes,
+                             float* scale, void* stream) {
+  if (!w || !codes || !scale || rows < 1 || cols < 16 || cols % 16 || rows > (1 << 30))
+    return TF_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PackParams p = {};
+  p.src = reinterpret_cast<const uint8_t*>(w);
+  p.dst = codes;
+  p.dst_scale = scale;
+  p.rows = rows;
+  p.cols = cols;
+  p.map = MAP_IDENTITY;
+  p.mode = 1;
+  if (launch_pack(p, s) != cudaSuccess) return TF_E_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? TF_OK : TF_E_CUDA;
+}
+
+tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab, const tf_sampling* sampling,
+                       int32_t frame, int32_t codebook0, int32_t sequence, int32_t* ids,
+                       void* stream) {
+  if (!logits || !ids || !sampling || n < 1 || vocab < 1 || vocab > 8192) return TF_E_INVAL;
+  if (sampling->top_k < 0 || sampling->top_k > 256 || !(sampling->temperature > 0.f)) return TF_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* err = nullptr;
+  if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return TF_E_NOMEM;
+  cudaMemsetAsync(err, 0, 4, s);
+  SelectParams q = {};
+  q.logits = logits;
+  q.ld = vocab;
+  q.vocab = vocab;
+  q.n = n;
+  q.top_k = sampling->top_k;
+  q.temperature = sampling->temperature;
+  q.key0 = static_cast<uint32_t>(sampling->seed & 0xFFFFFFFFull);
+  q.key1 = static_cast<uint32_t>(sampling->seed >> 32);
+  q.frame = frame;
+  q.codebook0 = codebook0;
+  q.sequence = sequence;
+  q.sel = ids;
+  q.err = err;
+  tf_status r = TF_OK;
+  if (launch_select(q, false, s) != cudaSuccess) r = TF_E_CUDA;
+  uint32_t e = 0;
+  if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                     cudaStreamSynchronize(s) != cudaSuccess))
+    r = TF_E_CUDA;
+  cudaFree(err);
+  if (r == TF_OK && (e & ERR_NAN)) r = TF_E_NUMERIC;
+  return r;
+}
+
+tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64_t rows,
+                     int64_t cols, const float* x, float* y, int32_t repeat, float* ms,
+                     void* stream) {
+  if (!W || !x || !y || rows < 1 || cols < 16 || rows > (1 << 30) || repeat < 1) return TF_E_INVAL;
+  if (dtype != TF_DTYPE_BF16 && dtype != TF_DTYPE_FP8_E4M3) return TF_E_INVAL;
+  if (dtype == TF_DTYPE_FP8_E4M3 && !row_scale) return TF_E_INVAL;
+  const int eb = dtype == TF_DTYPE_FP8_E4M3 ? 1 : 2;
+  if ((cols * eb) % 16 || cols * eb / 16 > 5 * 256) return TF_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (gemv_set_attributes() != cudaSuccess) return TF_E_CUDA;
+  uint32_t* err = nullptr;
+  if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return TF_E_NOMEM;
+  cudaMemsetAsync(err, 0, 4, s);
+  GemvParams p = {};
+  p.N = static_cast<int32_t>(rows);
+  p.K = static_cast<int32_t>(cols);
+  p.pro = PRO_PLAIN;
+  p.x = x;
+  p.ldx = p.K;
+  p.epi = EPI_STORE;
+  p.out = y;
+  p.ldo = 0;
+  p.err = err;
+  gemv_plan(p, eb, sms);
+  const int grid = std::min(sms, p.units);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  tf_status r = TF_OK;
+  if (ms) {
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0, s);
+  }
+  for (int i = 0; i < repeat && r == TF_OK; ++i) {
+    p.W = static_cast<const uint8_t*>(W) + (size_t)i * rows * cols * eb;
+    p.scale = row_scale ? row_scale + (size_t)i * rows : nullptr;
+    if (launch_gemv(p, eb == 1 ? 1 : 0, 1, grid, i > 0, s) != cudaSuccess) r = TF_E_CUDA;
+  }
+  if (ms) cudaEventRecord(e1, s);
+  uint32_t e = 0;
+  if (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    r = TF_E_CUDA;
+  if (ms && r == TF_OK) {
+    float t = 0.f;
+    cudaEventElapsedTime(&t, e0, e1);
+    *ms = t / repeat;
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  cudaFree(err);
+  if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
+  return r;
+}
+
+}  // extern "C"

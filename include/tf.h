@@ -1,0 +1,228 @@
+/*
+ * tf.h - C ABI of the GB300 (sm_103a) Dual-AR decode library.
+ *
+ * The library runs the decode step of a Dual-AR (RQ-Transformer) text-to-
+ * speech model shaped like Fish-Speech S2-Pro: per frame, one token through a
+ * "slow" decoder along time (GQA attention with RoPE over a static KV cache,
+ * SwiGLU MLP, RMSNorm) whose tied semantic head picks codebook 0, then a loop
+ * of 9 steps through a "fast" decoder along depth that picks the residual
+ * codebooks 1..9.  One decode call emits one frame of 10 codebook ids.
+ *   - Dual-AR structure, 10 codebooks: fish-s2-pro-mlx-local-deploy README,
+ *     architecture paragraph ("Slow AR ... time axis ... primary semantic
+ *     codebook; Fast AR ... remaining 9 residual codebooks").
+ *   - Shapes, static KV cache, bytes per decode step: tuna-fish README,
+ *     "Inference estimation".
+ *   - Per-row FP8 weights: drbaph s2-pro-fp8 model card, "Quantization Details".
+ *
+ * Conventions for every call:
+ *   - The caller owns every pointer it passes; host buffers may be freed as
+ *     soon as the call returns.  The library owns all device memory it
+ *     allocates (tf_create) and frees it in tf_destroy.
+ *   - Calls are synchronous with respect to the host: outputs are valid on
+ *     return.  Work runs on the context's stream (tf_set_stream).
+ *   - A context is used by one host thread at a time.
+ *   - Errors: every call returns a tf_status; tf_last_error() gives a one-line
+ *     message.  After TF_E_CUDA or TF_E_TIMEOUT the context is poisoned and
+ *     every later call except tf_destroy returns TF_E_STATE.
+ *   - Device kernels never trap: a kernel that detects a bad id, a NaN logit or
+ *     an expired wait sets a flag that the call turns into TF_E_NUMERIC,
+ *     TF_E_INVAL or TF_E_TIMEOUT.
+ */
+#ifndef TF_H
+#define TF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tf_ctx tf_ctx;
+
+typedef enum {
+  TF_OK = 0,
+  TF_E_INVAL = 1,     /* bad argument, shape, name or id; nothing changed       */
+  TF_E_NOMEM = 2,     /* device allocation failed                               */
+  TF_E_CUDA = 3,      /* CUDA runtime error; context poisoned                   */
+  TF_E_STATE = 4,     /* call out of order (no weights, no prefill) or poisoned */
+  TF_E_CAPACITY = 5,  /* KV cache full (position == max_seq_len); state kept    */
+  TF_E_TIMEOUT = 6,   /* a bounded device wait expired; context poisoned        */
+  TF_E_NUMERIC = 7    /* NaN logit met during selection                          */
+} tf_status;
+
+/* Weight formats of the linear layers (tf_config.weight_dtype). */
+enum { TF_WEIGHT_BF16 = 0, TF_WEIGHT_FP8 = 1 };
+/* Element types of tensors handed to tf_load_weights (tf_tensor.dtype). */
+enum { TF_DTYPE_BF16 = 0, TF_DTYPE_FP8_E4M3 = 1 };
+
+/* Model shape.  All sizes are element counts.
+ * head_dim must be 64 or 128; n_heads a multiple of n_kv_heads with
+ * n_heads / n_kv_heads <= 8; hidden, ffn and n_heads*head_dim multiples of 16;
+ * semantic_vocab <= text_vocab; n_codebooks = 10 (codebook 0 semantic). */
+typedef struct {
+  int32_t slow_layers, fast_layers;
+  int32_t hidden, n_heads, n_kv_heads, head_dim, ffn;
+  int32_t text_vocab;       /* rows of the tied text embedding                  */
+  int32_t semantic_vocab;   /* slow head = text-embedding rows [text_vocab - semantic_vocab, text_vocab) */
+  int32_t n_codebooks;      /* ids per frame (10)                               */
+  int32_t codebook_size;    /* rows of the fast head and of each codebook table */
+  int32_t max_seq_len;      /* static slow KV length T                          */
+  int32_t max_batch;        /* sequences per context (this build: 1)            */
+  float rms_eps, rope_theta;
+  int32_t weight_dtype;     /* TF_WEIGHT_BF16 or TF_WEIGHT_FP8                  */
+} tf_config;
+
+/* One named host (or device) tensor for tf_load_weights.
+ * Names: "text_embed" [text_vocab][hidden];
+ *        "slow.{i}.attn_norm" / "slow.{i}.ffn_norm" [hidden];
+ *        "slow.{i}.wqkv" [n_heads*head_dim + 2*n_kv_heads*head_dim][hidden]
+ *            (rows: q heads, then k heads, then v heads);
+ *        "slow.{i}.wo" [hidden][n_heads*head_dim];
+ *        "slow.{i}.w1" (gate), "slow.{i}.w3" (up) [ffn][hidden];
+ *        "slow.{i}.w2" (down) [hidden][ffn];
+ *        "slow.norm" [hidden];  the same for "fast.{i}.*" and "fast.norm";
+ *        "fast.head" [codebook_size][hidden];
+ *        "fast.cb_embed" [n_codebooks-1][codebook_size][hidden].
+ * Linear weights are [out][in] row-major.  Embeddings and norms are bf16.
+ * In an FP8 context a linear weight is given either as bf16 (the library
+ * quantises it per row, exactly as tf_op_quantize_fp8) or as
+ * TF_DTYPE_FP8_E4M3 codes with row_scale[out] (float32). */
+typedef struct {
+  const char* name;
+  int32_t dtype;
+  int32_t ndim;
+  int64_t shape[3];
+  const void* data;         /* host or device pointer                          */
+  const float* row_scale;   /* FP8 codes only: [shape[0]] float32, else NULL   */
+} tf_tensor;
+
+/* Codebook-id selection.  top_k = 0: greedy argmax (lowest index on ties).
+ * top_k > 0: keep the top_k logits ordered by (logit desc, index asc),
+ * weights exp((z - z_max) / temperature) summed in that order in float32,
+ * u = (w0 >> 8) * 2^-24 from Philox4x32-10 with counter
+ * (frame index, codebook, sequence, 0) and key (seed low, seed high 32 bits);
+ * the pick is the first candidate whose running sum exceeds u * sum. */
+typedef struct {
+  int32_t top_k;
+  float temperature;
+  uint64_t seed;
+} tf_sampling;
+
+/* Read-only facts about a context. */
+typedef struct {
+  int32_t position;         /* next slow position of sequence 0                */
+  int32_t frame_index;      /* frames emitted since the last prefill           */
+  int32_t num_sms;          /* SMs of the device                                */
+  int32_t graph_nodes;      /* kernel launches in one captured decode frame     */
+  int64_t weight_bytes;     /* device bytes of all weights as stored            */
+  int64_t frame_weight_bytes; /* weight bytes one decode frame streams          */
+  int64_t device_bytes;     /* all device memory the context owns               */
+} tf_info;
+
+/* Creates a context on CUDA device `device`: validates cfg, allocates weights,
+ * KV caches and work buffers (all device memory is allocated here), creates
+ * the context's stream.  On failure *out is NULL.  Errors: TF_E_INVAL (bad
+ * shape), TF_E_NOMEM, TF_E_CUDA. */
+tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out);
+
+/* Copies n named tensors into the context (host->device or device->device),
+ * re-laying them out for the kernels and quantising bf16 linears in an FP8
+ * context.  May be called several times; a decode needs every tensor loaded.
+ * Errors: TF_E_INVAL (unknown name, wrong shape or dtype), TF_E_CUDA. */
+tf_status tf_load_weights(tf_ctx* ctx, const tf_tensor* t, int32_t n);
+
+/* Prompt in, frame 0 out.  tokens: host int32 [B][P], ids in [0, text_vocab).
+ * Resets every sequence to position 0, runs the slow decoder over the prompt
+ * (positions 0..P-1), then selects frame 0 from the last row.
+ * forced: NULL, or host int32 [B][n_codebooks] ids that replace the selected
+ *   ids wherever they are fed back (teacher forcing); frame0 still reports the
+ *   library's own selections.
+ * frame0: host int32 [B][n_codebooks].  logits: NULL or host float
+ *   [B][n_codebooks][max(semantic_vocab, codebook_size)] (row 0 semantic).
+ * Errors: TF_E_INVAL (B, P or an id out of range), TF_E_STATE (weights
+ * missing), TF_E_NUMERIC, TF_E_CUDA. */
+tf_status tf_prefill(tf_ctx* ctx, const int32_t* tokens, int32_t B, int32_t P,
+                     const tf_sampling* sampling, const int32_t* forced,
+                     int32_t* frame0, float* logits);
+
+/* One decode frame: feeds each sequence's last codebook-0 id at its next
+ * position, emits the next frame.  Arguments as tf_prefill.  At position ==
+ * max_seq_len returns TF_E_CAPACITY and changes nothing. */
+tf_status tf_decode_frame(tf_ctx* ctx, const tf_sampling* sampling,
+                          const int32_t* forced, int32_t* frame, float* logits);
+
+/* n decode frames back to back on the device (no host round trip between
+ * frames); frames: host int32 [n][B][n_codebooks].  Fails with TF_E_CAPACITY
+ * before running anything if the n frames do not fit. */
+tf_status tf_decode_frames(tf_ctx* ctx, const tf_sampling* sampling, int32_t n,
+                           int32_t* frames);
+
+/* Sets the CUDA stream (cudaStream_t) all later work of ctx runs on; NULL
+ * restores the context's own stream.  The caller keeps the stream alive. */
+tf_status tf_set_stream(tf_ctx* ctx, void* stream);
+/* The stream work is currently enqueued on. */
+void* tf_get_stream(const tf_ctx* ctx);
+
+tf_status tf_get_info(const tf_ctx* ctx, tf_info* info);
+
+/* One-line description of the last error of ctx (or of the last failed
+ * tf_create when ctx is NULL).  Never NULL; valid until the next call. */
+const char* tf_last_error(const tf_ctx* ctx);
+
+/* Frees everything the context owns.  NULL-safe. */
+void tf_destroy(tf_ctx* ctx);
+
+/* Times one kernel of the decode frame in its in-frame configuration
+ * (same parameters, prologue, epilogue and launch chaining) on the context's
+ * stream with CUDA events: `iters` back-to-back launches cycling through the
+ * slow decoder's layers, so every launch streams a distinct weight from HBM.
+ * which: 0 = gate/up GEMV (RMSNorm prologue, SwiGLU epilogue),
+ *        1 = QKV GEMV, 2 = O GEMV, 3 = down GEMV.
+ * Outputs the mean device time per launch and the algorithmic bytes one
+ * launch moves (weights + scales + activations in and out).  Touches only
+ * scratch activations; the decode state is unchanged.  Needs loaded weights.
+ * Errors: TF_E_INVAL, TF_E_STATE, TF_E_CUDA. */
+tf_status tf_profile_kernel(tf_ctx* ctx, int32_t which, int32_t iters,
+                            float* ms_per_launch, int64_t* bytes_per_launch);
+
+/* ---------------------------------------------------------------------------
+ * Single-operation entry points, for parity tests and profiling.  Each runs
+ * one kernel of the decode path on caller-provided DEVICE buffers on `stream`
+ * (cudaStream_t, NULL = legacy default stream) and synchronises it.
+ * ------------------------------------------------------------------------- */
+
+/* Per-row symmetric FP8 quantisation (drbaph s2-pro-fp8 model card,
+ * "Quantization Details"): w_bf16 [rows][cols] (bf16 bits) ->
+ * codes [rows][cols] float8_e4m3fn, scale [rows] float32 with
+ * scale = amax/448 (IEEE float32 division; 1 for an all-zero row) and
+ * code = e4m3 round-to-nearest-even of clamp(w / scale, -448, 448).
+ * cols must be a multiple of 16.  Errors: TF_E_INVAL, TF_E_CUDA. */
+tf_status tf_op_quantize_fp8(const uint16_t* w_bf16, int64_t rows, int64_t cols,
+                             uint8_t* codes, float* scale, void* stream);
+
+/* Codebook-id selection over float32 logits [n][vocab] (device); row i uses
+ * Philox counter (frame, codebook0 + i, sequence, 0).  Writes ids [n] (device,
+ * int32).  sampling as tf_sampling (top_k 0 = argmax).  vocab <= 8192.
+ * Errors: TF_E_INVAL, TF_E_NUMERIC (NaN logit), TF_E_CUDA. */
+tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab,
+                       const tf_sampling* sampling, int32_t frame,
+                       int32_t codebook0, int32_t sequence, int32_t* ids,
+                       void* stream);
+
+/* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
+ * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
+ * TF_DTYPE_BF16) or e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3);
+ * x, y float32 device vectors.  `repeat` > 1 launches it that many times
+ * back to back (each launch with weights W + i * rows * cols elements, so the
+ * caller can rotate through distinct matrices) and returns the mean device
+ * time per launch in *ms (CUDA events on `stream`), if ms is not NULL.
+ * Errors: TF_E_INVAL, TF_E_CUDA. */
+tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale,
+                     int64_t rows, int64_t cols, const float* x, float* y,
+                     int32_t repeat, float* ms, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TF_H */

@@ -91,7 +91,11 @@ class DualAROracle:
         self.fmt = weight_format
         self.batch = batch
         total = sum(int(np.prod(v.shape)) for v in weights.values())
+        # float64 copies are kept for small models; for large ones only the
+        # fast decoder's (used 9 times per frame) are kept, the rest are
+        # converted from bf16 on each use.
         self.cache_f64 = (total < 100_000_000) if cache_f64 is None else cache_f64
+        self.cache_fast = total >= 100_000_000
         self._cache = {}
         self.fp8 = {}
         if weight_format == "fp8":
@@ -109,7 +113,7 @@ class DualAROracle:
             w = fp8_dequant_rows(*self.fp8[name])
         else:
             w = bf16_bits_to_f64(self.raw[name])
-        if self.cache_f64:
+        if self.cache_f64 or (self.cache_fast and name.startswith("fast.")):
             self._cache[name] = w
         return w
 

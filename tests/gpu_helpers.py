@@ -1,0 +1,89 @@
+"""Shared helpers of the GPU parity tests (teacher-forced comparison)."""
+import numpy as np
+
+import oracle
+from dual_ar_decode_gb300 import Decoder
+from synth import make_prompt, make_weights
+
+BF16_TOL = 1e-2      # logits relative L2, bf16 weights
+FP8_TOL = 2e-2       # logits relative L2, fp8 per-row weights
+MARGIN = 5e-2        # ids must agree where the oracle's top-1 - top-2 gap exceeds this
+
+
+def vocab_of(d, j):
+    return d.semantic_vocab if j == 0 else d.codebook_size
+
+
+def rel_l2(g, o):
+    return float(np.linalg.norm(g - o) / np.linalg.norm(o))
+
+
+def margin(z):
+    s = np.sort(np.asarray(z, np.float64))
+    return s[-1] - s[-2]
+
+
+def topk_robust(z, k, tol_abs, seed, frame, codebook, sequence=0, temperature=1.0):
+    """True when the top-k draw from logits z cannot change under logit
+    perturbations of size tol_abs: the k-th / (k+1)-th gap is wide, and the
+    draw u*S sits away from every running-sum boundary by more than the
+    relative change such a perturbation can make to the weights."""
+    z32 = np.asarray(z, np.float32)
+    s = np.sort(z32.astype(np.float64))[::-1]
+    if len(s) > k and (s[k - 1] - s[k]) <= 4 * tol_abs:
+        return False
+    _, det = oracle.topk_sample(z32, k, seed, frame, codebook, sequence, temperature)
+    rel = 4 * tol_abs / temperature
+    gaps = np.abs(det["c"].astype(np.float64) - float(det["t"]))
+    return bool(np.min(gaps) > rel * float(det["S"]))
+
+
+class TeacherForced:
+    """Runs the oracle free (greedy or sampled) and the GPU with the
+    oracle's ids forced, frame by frame, keeping both sides' logits."""
+
+    def __init__(self, dims, fmt="bf16", seed=0, weights=None, dec=None):
+        self.d = dims
+        self.w = weights if weights is not None else make_weights(dims, seed)
+        self.ref = oracle.DualAROracle(dims, self.w, fmt)
+        self.dec = dec if dec is not None else Decoder(dims, fmt)
+        if dec is None:
+            self.dec.load_weights(self.w)
+        self.frames = []
+
+    def prefill(self, prompt, sampling=None):
+        rf, rz = self.ref.prefill(prompt, sampling)
+        gf, gz = self.dec.prefill(prompt, sampling, forced=rf, logits=True)
+        self.frames.append((rf[0], rz[0], gf[0], gz[0]))
+        return self.frames[-1]
+
+    def decode(self, sampling=None):
+        rf, rz = self.ref.decode_frame(sampling)
+        gf, gz = self.dec.decode_frame(sampling, forced=rf, logits=True)
+        self.frames.append((rf[0], rz[0], gf[0], gz[0]))
+        return self.frames[-1]
+
+    def check(self, tol, sampling=None):
+        """Asserts the parity gates on every frame; returns (worst rel-L2,
+        ids compared, ids skipped)."""
+        worst, compared, skipped = 0.0, 0, 0
+        k = int(sampling.get("top_k", 0)) if sampling else 0
+        for t, (rf, rz, gf, gz) in enumerate(self.frames):
+            for j in range(self.d.n_codebooks):
+                V = vocab_of(self.d, j)
+                o, g = rz[j, :V], gz[j, :V]
+                e = rel_l2(g, o)
+                worst = max(worst, e)
+                assert e <= tol, f"frame {t} codebook {j}: rel-L2 {e:.3e} > {tol}"
+                if k <= 1:
+                    robust = margin(o) > MARGIN
+                else:
+                    tol_abs = 3 * tol * np.sqrt(np.mean(o * o))
+                    robust = topk_robust(o, k, tol_abs, int(sampling.get("seed", 0)), t, j,
+                                         0, float(sampling.get("temperature", 1.0)))
+                if robust:
+                    compared += 1
+                    assert gf[j] == rf[j], f"frame {t} codebook {j}: id {gf[j]} != {rf[j]}"
+                else:
+                    skipped += 1
+        return worst, compared, skipped

@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Gates: logits relative L2 <= 1e-2 (bf16 weights) / 2e-2 (fp8 per-row
+weights) per codebook and frame under teacher forcing; greedy ids equal
+wherever the oracle's top-1 - top-2 margin exceeds 5e-2; fp8 quantisation
+and the selection kernel bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dual_ar_decode_gb300 import Decoder, TfError, op_gemv, op_quantize_fp8, op_select
+from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
+from synth import FULL, TINY, make_logits, make_prompt, make_weights, f32_to_bf16_bits
+
+from gpu_helpers import BF16_TOL, FP8_TOL, TeacherForced
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV)
+
+
+# ------------------------------------------------------------------ ops
+
+@pytest.mark.parametrize("rows,cols", [(37, 2560), (5, 16), (64, 9728), (3, 48)])
+def test_quantize_fp8_bit_exact(rows, cols):
+    rng = np.random.default_rng(rows * 7 + cols)
+    w = f32_to_bf16_bits(rng.standard_normal((rows, cols)).astype(np.float32) * 0.02)
+    w[0] = 0                                         # all-zero row
+    w[1, 3] = f32_to_bf16_bits(np.array([5.0], np.float32))[0]   # an outlier
+    wd = dev_u16(w)
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=DEV)
+    scale = torch.empty(rows, dtype=torch.float32, device=DEV)
+    op_quantize_fp8(wd.data_ptr(), rows, cols, codes.data_ptr(), scale.data_ptr())
+    rc, rs = oracle.fp8_quantize_rows(w)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scale.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("vocab", [64, 4096, 1000])
+@pytest.mark.parametrize("top_k,temp", [(0, 1.0), (1, 1.0), (2, 1.0), (30, 1.0), (30, 0.7), (256, 1.0)])
+@pytest.mark.parametrize("ties", [False, True])
+def test_select_bit_exact(vocab, top_k, temp, ties):
+    n = 48
+    z = make_logits(n, vocab, seed=vocab + top_k, scale=2.0, ties=ties)
+    zd = torch.from_numpy(z).to(DEV)
+    ids = torch.full((n,), -1, dtype=torch.int32, device=DEV)
+    seed = 0x1234_5678_9ABC
+    frame, cb0, seq = 17, 3, 0
+    op_select(zd.data_ptr(), n, vocab, {"top_k": top_k, "temperature": temp, "seed": seed},
+              frame, cb0, seq, ids.data_ptr())
+    got = ids.cpu().numpy()
+    for i in range(n):
+        if top_k <= 1:
+            want = oracle.argmax_lowest(z[i])
+        else:
+            want, _ = oracle.topk_sample(z[i], top_k, seed, frame, cb0 + i, seq, temp)
+        assert got[i] == want, (i, got[i], want)
+
+
+def test_select_flags_nan():
+    z = make_logits(2, 64, seed=1)
+    z[1, 5] = np.nan
+    zd = torch.from_numpy(z).to(DEV)
+    ids = torch.zeros(2, dtype=torch.int32, device=DEV)
+    with pytest.raises(TfError, match="NUMERIC"):
+        op_select(zd.data_ptr(), 2, 64, {"top_k": 0}, 0, 0, 0, ids.data_ptr())
+
+
+@pytest.mark.parametrize("rows,cols,fp8", [(6144, 2560, False), (2560, 9728, False),
+                                           (2560, 4096, False), (37, 256, False),
+                                           (6144, 2560, True), (2560, 9728, True),
+                                           (4097, 2560, True), (3, 16, False)])
+def test_gemv_matches_oracle_linear(rows, cols, fp8):
+    rng = np.random.default_rng(rows + cols)
+    w = f32_to_bf16_bits(rng.standard_normal((rows, cols)).astype(np.float32) * 0.02)
+    x = rng.standard_normal(cols).astype(np.float32)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.zeros(rows, dtype=torch.float32, device=DEV)
+    if fp8:
+        codes, scale = oracle.fp8_quantize_rows(w)
+        Wd = torch.from_numpy(codes).to(DEV)
+        sd = torch.from_numpy(scale).to(DEV)
+        op_gemv(Wd.data_ptr(), TF_DTYPE_FP8_E4M3, sd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr())
+        ref = oracle.linear(oracle.fp8_dequant_rows(codes, scale), x.astype(np.float64))
+    else:
+        Wd = dev_u16(w)
+        op_gemv(Wd.data_ptr(), TF_DTYPE_BF16, None, rows, cols, xd.data_ptr(), y.data_ptr())
+        ref = oracle.linear(oracle.bf16_bits_to_f64(w), x.astype(np.float64))
+    got = y.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref) / (np.abs(ref) + 1e-3 * np.sqrt(np.mean(ref ** 2)))
+    assert err.max() < 1e-4, err.max()
+
+
+# ------------------------------------------------------------------ model
+
+TINY_ODD = TINY.replace(hidden=192, ffn=320, n_heads=4, n_kv_heads=4, head_dim=64,
+                        text_vocab=300, semantic_vocab=40, codebook_size=48, max_seq_len=40)
+TINY_G8 = TINY.replace(hidden=256, ffn=512, n_heads=8, n_kv_heads=1, head_dim=128,
+                       max_seq_len=48)
+
+
+@pytest.mark.parametrize("dims,fmt,tol", [(TINY, "bf16", BF16_TOL), (TINY, "fp8", FP8_TOL),
+                                          (TINY_ODD, "bf16", BF16_TOL), (TINY_G8, "bf16", BF16_TOL)])
+def test_tiny_teacher_forced(dims, fmt, tol):
+    tf = TeacherForced(dims, fmt, seed=0)
+    tf.prefill(make_prompt(dims, 16, seed=0))
+    for _ in range(8):
+        tf.decode()
+    worst, compared, skipped = tf.check(tol)
+    assert compared > 0.8 * (compared + skipped)
+    tf.dec.close()
+
+
+def test_tiny_topk_teacher_forced():
+    s = {"top_k": 30, "seed": 1234}
+    tf = TeacherForced(TINY, "bf16", seed=0)
+    tf.prefill(make_prompt(TINY, 16, seed=0), s)
+    for _ in range(8):
+        tf.decode(s)
+    worst, compared, skipped = tf.check(BF16_TOL, s)
+    assert compared > 0.5 * (compared + skipped)
+    tf.dec.close()
+
+
+def test_prompt_edges_and_capacity():
+    d = TINY.replace(max_seq_len=20)
+    w = make_weights(d, seed=2)
+    # single-token prompt
+    tf = TeacherForced(d, "bf16", weights=w)
+    tf.prefill(make_prompt(d, 1, seed=3))
+    tf.decode()
+    tf.check(BF16_TOL)
+    # prompt filling T-2 positions, decode to the last slot, then capacity
+    tf2 = TeacherForced(d, "bf16", weights=w, dec=tf.dec)
+    tf2.prefill(make_prompt(d, 18, seed=4))
+    tf2.decode()
+    tf2.decode()
+    tf2.check(BF16_TOL)
+    with pytest.raises(TfError, match="CAPACITY"):
+        tf.dec.decode_frame()
+    tf.dec.close()
+
+
+def test_decode_frames_equals_single_calls_and_is_deterministic():
+    w = make_weights(TINY, seed=5)
+    prompt = make_prompt(TINY, 12, seed=5)
+    runs = []
+    for mode in ("single", "batched", "batched"):
+        dec = Decoder(TINY, "bf16")
+        dec.load_weights(w)
+        f0, _ = dec.prefill(prompt)
+        if mode == "single":
+            fr = np.stack([dec.decode_frame()[0] for _ in range(10)])
+        else:
+            fr = dec.decode_frames(10)
+        runs.append(np.concatenate([f0[None], fr]))
+        dec.close()
+    assert np.array_equal(runs[0], runs[1]) and np.array_equal(runs[1], runs[2])
+
+
+def test_api_errors_leave_context_usable():
+    w = make_weights(TINY, seed=6)
+    dec = Decoder(TINY, "bf16")
+    with pytest.raises(TfError, match="STATE"):      # weights missing
+        dec.prefill(make_prompt(TINY, 4))
+    dec.load_weights(w)
+    with pytest.raises(TfError, match="STATE"):      # decode before prefill
+        dec.decode_frame()
+    with pytest.raises(TfError, match="INVAL"):      # prompt id out of range
+        dec.prefill(np.array([[0, TINY.text_vocab]], np.int32))
+    with pytest.raises(TfError, match="INVAL"):      # prompt longer than the cache
+        dec.prefill(make_prompt(TINY, TINY.max_seq_len + 1))
+    dec.prefill(make_prompt(TINY, 4))
+    with pytest.raises(TfError, match="INVAL"):      # forced id out of range
+        dec.decode_frame(forced=np.full((1, 10), TINY.codebook_size, np.int32))
+    f, _ = dec.decode_frame()                        # still usable
+    assert f.shape == (1, 10) and (f >= 0).all()
+    dec.close()
+
+
+# ------------------------------------------------------------------ full size
+
+@pytest.fixture(scope="module")
+def full_weights():
+    return make_weights(FULL, seed=0)
+
+
+@pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL)])
+def test_full_size_teacher_forced_sampled_frames(full_weights, fmt, tol):
+    """Full-size model (36+4 layers, hidden 2560), prefill 128 then 2 decode
+    frames, in the launch configuration the benchmark times."""
+    tf = TeacherForced(FULL, fmt, weights=full_weights)
+    tf.prefill(make_prompt(FULL, 128, seed=0))
+    tf.decode()
+    tf.decode()
+    worst, compared, skipped = tf.check(tol)
+    assert compared >= 15
+    tf.dec.close()

@@ -22,7 +22,7 @@ Each function cites the passage of the source pages it follows:
 Where the pages leave a step open, the reading taken is stated in the
 docstring of the function that implements it.
 """
-from .numerics import (bf16_bits_to_f64, bf16_bits_to_f32, e4m3_decode,
+from .numerics import (bf16_bits_to_f64, bf16_bits_to_f32, round_to_bf16, e4m3_decode,
                        e4m3_encode_rne, fp8_quantize_rows, fp8_dequant_rows,
                        rmsnorm, rope_angles, apply_rope, attention_row,
                        silu, linear)
@@ -31,7 +31,7 @@ from .sampler import (philox4x32_10, exp_f32, argmax_lowest, topk_candidates,
 from .model import DualAROracle, load_formula
 
 __all__ = [
-    "bf16_bits_to_f64", "bf16_bits_to_f32", "e4m3_decode", "e4m3_encode_rne",
+    "bf16_bits_to_f64", "bf16_bits_to_f32", "round_to_bf16", "e4m3_decode", "e4m3_encode_rne",
     "fp8_quantize_rows", "fp8_dequant_rows", "rmsnorm", "rope_angles",
     "apply_rope", "attention_row", "silu", "linear", "philox4x32_10", "exp_f32",
     "argmax_lowest", "topk_candidates", "topk_sample", "uniform24",

@@ -25,12 +25,16 @@ Readings taken where the pages are open (each is tested):
       9 fast weight passes per frame, as the load formula counts.
   R14 prefill of P tokens fills positions 0..P-1 and emits frame 0 from the
       last row; decode call t feeds c0 of frame t-1 at position P + t - 1.
+  R16 the static KV cache holds bfloat16 values: the tuna-fish load formula
+      counts every KV element at 2 bytes ("bfloat16 memory"), so keys (after
+      RoPE) and values are rounded to bf16 when they are written to the cache;
+      everything else stays float64.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .numerics import (bf16_bits_to_f64, fp8_quantize_rows, fp8_dequant_rows,
+from .numerics import (bf16_bits_to_f64, round_to_bf16, fp8_quantize_rows, fp8_dequant_rows,
                        rmsnorm, apply_rope, attention_row, silu, linear)
 from .sampler import argmax_lowest, topk_sample
 
@@ -135,8 +139,9 @@ class DualAROracle:
         """Pre-norm decoder layer over rows x [M][H] at the given positions.
 
         Every row's key/value is written into K, V [Hkv][T][D] at its
-        position before attention, and row r attends to positions
-        0..positions[r] (causal); rows are in increasing position order.
+        position before attention (rounded to bf16, R16), and row r attends
+        to positions 0..positions[r] (causal); rows are in increasing
+        position order.
         """
         d = self.d
         a = rmsnorm(x, bf16_bits_to_f64(self.raw[f"{prefix}.attn_norm"]), d.rms_eps)
@@ -146,8 +151,8 @@ class DualAROracle:
         v = qkv[:, d.q_dim + d.kv_dim:].reshape(-1, d.n_kv_heads, d.head_dim)
         o = np.empty((x.shape[0], d.q_dim))
         for r, p in enumerate(positions):
-            K[:, p] = apply_rope(k[r], p, d.rope_theta)
-            V[:, p] = v[r]
+            K[:, p] = round_to_bf16(apply_rope(k[r], p, d.rope_theta))
+            V[:, p] = round_to_bf16(v[r])
         for r, p in enumerate(positions):
             qr = apply_rope(q[r], p, d.rope_theta)
             o[r] = attention_row(qr, K, V, p + 1).reshape(-1)

@@ -23,6 +23,20 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(bits).astype(np.float64)
 
 
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (ties to even), as float64.
+
+    Written from the format: keep the sign, 8 exponent bits and 7 fraction
+    bits.  x is first rounded to float32 (ties to even), whose spacing is a
+    divisor of bf16's, then the low 16 bits of the float32 are rounded away
+    with ties to even.  Finite inputs only.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return bf16_bits_to_f64(u.astype(np.uint16))
+
+
 def _e4m3_value(code: int) -> float:
     """Value of one float8_e4m3fn code (OCP 8-bit floating point, E4M3).
 

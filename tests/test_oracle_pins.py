@@ -36,6 +36,14 @@ def test_bf16_decode_matches_torch():
     assert np.array_equal(oracle.bf16_bits_to_f32(bits), t)
 
 
+def test_round_to_bf16_matches_torch_cast():
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.standard_normal(200000) * 10.0 ** rng.integers(-6, 6, 200000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 3.0e38]])
+    ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(oracle.round_to_bf16(x), ref)
+
+
 def test_bf16_rounding_of_inputs_matches_torch():
     x = np.random.default_rng(2).standard_normal(100000).astype(np.float32) * 0.02
     ours = f32_to_bf16_bits(x)
@@ -290,7 +298,9 @@ def _torch_decoder(prefix, x, W, d):
     k = qkv[:, d.q_dim: d.q_dim + d.kv_dim].view(S, d.n_kv_heads, d.head_dim)
     v = qkv[:, d.q_dim + d.kv_dim:].view(S, d.n_kv_heads, d.head_dim)
     q = _rope_complex(q, pos, d.rope_theta)
-    k = _rope_complex(k, pos, d.rope_theta)
+    # the static KV cache holds bfloat16 values
+    k = _rope_complex(k, pos, d.rope_theta).to(torch.bfloat16).double()
+    v = v.to(torch.bfloat16).double()
     o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], k.transpose(0, 1)[None],
                                        v.transpose(0, 1)[None], is_causal=True,
                                        enable_gqa=True)[0].transpose(0, 1).reshape(S, -1)
@@ -387,6 +397,9 @@ def test_fast_step_one_two_rows_equal_two_single_rows():
     a = o._layer("fast.0", rows[:1], [0], K2, V2)
     b = o._layer("fast.0", rows[1:], [1], K2, V2)
     assert np.allclose(both, np.concatenate([a, b]), rtol=1e-13, atol=1e-13)
+    # cached keys and values are bf16 values
+    assert np.array_equal(K2[:, :2], oracle.round_to_bf16(K2[:, :2]))
+    assert np.array_equal(V2[:, :2], oracle.round_to_bf16(V2[:, :2]))
 
 
 def test_fp8_model_uses_dequantised_weights():

@@ -44,14 +44,20 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not ptxas_info and up_to_date():
+def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False,
+          defines=(), out: str | None = None) -> str:
+    """Build the library.  `defines` (e.g. ["TF_GEMV_RING_BYTES=131072"]) and
+    `out` build a variant elsewhere, for tuning sweeps."""
+    lib_path = out or LIB
+    if not force and not ptxas_info and not defines and out is None and up_to_date():
         return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = BUILD_DIR if out is None else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra += [f"-D{d}" for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nvcc(), *NVCC_FLAGS, *extra, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,14 +70,14 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
         for _, err in results:
             sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp, *objs,
            "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -22,6 +22,8 @@
 // applied once to the finished dot product.
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -30,21 +32,88 @@ namespace tf {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + producer warp
-constexpr int kRowBatch = 128;             // rows reduced per epilogue round
-constexpr int kStageTarget = 24 * 1024;
-constexpr int kRingBytes = 96 * 1024;
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kRowBatch = 128;  // rows reduced per epilogue round
+#ifndef TF_GEMV_STAGE_BYTES
+#define TF_GEMV_STAGE_BYTES (24 * 1024)
+#endif
+#ifndef TF_GEMV_RING_BYTES
+#define TF_GEMV_RING_BYTES (96 * 1024)
+#endif
+constexpr int kStageTarget = TF_GEMV_STAGE_BYTES;  // bytes of whole rows per stage
+constexpr int kRingBytes = TF_GEMV_RING_BYTES;     // shared-memory ring per CTA
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// d = a * b + c on a pair of floats (one packed FMA, each lane rounded once).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t A, B, C, D;
+  A = *reinterpret_cast<uint64_t*>(&a);
+  B = *reinterpret_cast<uint64_t*>(&b);
+  C = *reinterpret_cast<uint64_t*>(&c);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(D) : "l"(A), "l"(B), "l"(C));
+  return *reinterpret_cast<float2*>(&D);
+}
+
+// Accumulates one 16-byte weight chunk times its activations into acc
+// (two interleaved partial sums).
+template <int WT, int EPC>
+__device__ __forceinline__ float2 chunk_fma(const uint4 w, const float* a, float2 acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  if constexpr (WT == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      acc = fma2(make_float2(bf16_lo(v[i]), bf16_hi(v[i])), make_float2(a[2 * i], a[2 * i + 1]), acc);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(v[i] & 0xFFFFu));
+      const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(v[i] >> 16));
+      acc = fma2(lo, make_float2(a[4 * i], a[4 * i + 1]), acc);
+      acc = fma2(hi, make_float2(a[4 * i + 2], a[4 * i + 3]), acc);
+    }
+  }
+  return acc;
+}
+
+// Sums V values over the 32 lanes of a warp with a transposing butterfly:
+// log2(V) halving exchanges, then 5 - log2(V) plain ones.  Afterwards lane l
+// holds the warp total of value l >> (5 - log2 V).
+template <int V>
+__device__ __forceinline__ float warp_reduce_many(float (&v)[V], int lane) {
+  int n = V;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const bool up = lane & off;
+      const int h = n >> 1;
+#pragma unroll
+      for (int k = 0; k < V / 2; ++k) {
+        if (k < h) {
+          const float send = up ? v[k] : v[k + h];
+          const float keep = up ? v[k + h] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], off);
+    }
+  }
+  return v[0];
 }
 
 template <int WT, int M, int J>
-__global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
+__global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int EPC = WT ? 16 : 8;  // elements per 16-byte chunk
+  constexpr int EPC = WT ? 16 : 8;      // elements per 16-byte chunk
+  constexpr int R = M == 1 ? 4 : 2;     // rows reduced together
+  constexpr int V = R * M;              // values per butterfly (4)
+  constexpr int LOGV = V == 4 ? 2 : (V == 2 ? 1 : 0);
+  const int NT = static_cast<int>(blockDim.x) - 32;  // consumer threads
+  const int NW = NT >> 5;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, c = blockIdx.x;
   const int u0 = (int)((long long)p.units * c / G);
@@ -55,25 +124,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
   const int nch = static_cast<int>(rowbytes >> 4);
 
   uint8_t* ring = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)p.nst * p.stb);  // [kRowBatch][8][M]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + kRowBatch * kConsumerWarps * M);
+  float* red = reinterpret_cast<float*>(smem + (size_t)p.nst * p.stb);  // [kRowBatch][NW][M]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + kRowBatch * kMaxConsumerWarps * M);
   uint64_t* empty = full + p.nst;
-  float* misc = reinterpret_cast<float*>(empty + p.nst);  // [8][M] + 8 keys
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(misc + 8 * M);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(keys + kConsumerWarps);
+  float* misc = reinterpret_cast<float*>(empty + p.nst);  // [16][M]
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(misc + kMaxConsumerWarps * M);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(keys + kMaxConsumerWarps);
 
   pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < p.nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], NW);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == NW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -110,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
     const float* xm = p.x + (size_t)m * p.ldx;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const int ch = tid + j * kConsumers;
+      const int ch = tid + j * NT;
       if (ch < nch) {
         const float4* src = reinterpret_cast<const float4*>(xm + ch * EPC);
 #pragma unroll
@@ -138,16 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
       ss = warp_sum(ss);
       if (lane == 0) misc[warp * M + m] = ss;
     }
-    consumer_sync();
+    consumer_sync(NT);
 #pragma unroll
     for (int m = 0; m < M; ++m) {
       float ss = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) ss += misc[w * M + m];
+      for (int w = 0; w < NW; ++w) ss += misc[w * M + m];
       const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        const int ch = tid + j * kConsumers;
+        const int ch = tid + j * NT;
         if (ch < nch) {
 #pragma unroll
           for (int e = 0; e < EPC; ++e)
@@ -166,43 +234,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
       const int slot = s % p.nst;
       if (!*abort_flag && !mbar_wait(&full[slot], (s / p.nst) & 1, p.err)) *abort_flag = 1;
       const uint8_t* st = ring + (size_t)slot * p.stb;
-      for (int i = 0; i < n; ++i) {
-        const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)i * rowbytes);
-        float acc[M];
+      for (int i = 0; i < n; i += R) {
+        float v[V];
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = 0.f;
+        for (int r = 0; r < R; ++r) {
+          float2 acc[M];
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int ch = tid + j * kConsumers;
-          if (ch < nch) {
-            const uint4 w = row[ch];
+          for (int m = 0; m < M; ++m) acc[m] = make_float2(0.f, 0.f);
+          if (i + r < n) {
+            const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)(i + r) * rowbytes);
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] += chunk_dot<WT, EPC>(w, a[m][j]);
+            for (int j = 0; j < J; ++j) {
+              const int ch = tid + j * NT;
+              if (ch < nch) {
+                const uint4 w = row[ch];
+#pragma unroll
+                for (int m = 0; m < M; ++m) acc[m] = chunk_fma<WT, EPC>(w, a[m][j], acc[m]);
+              }
+            }
           }
-        }
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          const float v = warp_sum(acc[m]);
-          if (lane == 0) red[((i0 + i) * kConsumerWarps + warp) * M + m] = v;
+          for (int m = 0; m < M; ++m) v[r * M + m] = acc[m].x + acc[m].y;
+        }
+        const float tot = warp_reduce_many<V>(v, lane);
+        if ((lane & ((32 >> LOGV) - 1)) == 0) {
+          const int idx = lane >> (5 - LOGV);
+          const int r = idx / M, m = idx - r * M;
+          if (i + r < n) red[((i0 + i + r) * NW + warp) * M + m] = tot;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       ++s;
     }
-    consumer_sync();
+    consumer_sync(NT);
 
     // ---------------------------------------------------------- epilogue
     if (p.unit == 2) {
-      for (int pi = tid; pi < (nb >> 1); pi += kConsumers) {
+      for (int pi = tid; pi < (nb >> 1); pi += NT) {
         const int rg = r0 + b0 + 2 * pi;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
           float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            v0 += red[((2 * pi) * kConsumerWarps + w) * M + m];
-            v1 += red[((2 * pi + 1) * kConsumerWarps + w) * M + m];
+          for (int w = 0; w < NW; ++w) {
+            v0 += red[((2 * pi) * NW + w) * M + m];
+            v1 += red[((2 * pi + 1) * NW + w) * M + m];
           }
           if (p.scale) {
             v0 *= __ldg(&p.scale[rg]);
@@ -216,13 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
         }
       }
     } else {
-      for (int ri = tid; ri < nb; ri += kConsumers) {
+      for (int ri = tid; ri < nb; ri += NT) {
         const int rg = r0 + b0 + ri;
 #pragma unroll
         for (int m = 0; m < M; ++m) {
           float v = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) v += red[(ri * kConsumerWarps + w) * M + m];
+          for (int w = 0; w < NW; ++w) v += red[(ri * NW + w) * M + m];
           if (p.scale) v *= __ldg(&p.scale[rg]);
           float* o = p.out + (size_t)m * p.ldo + rg;
           if (p.epi == EPI_RESID) {
@@ -238,16 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
         }
       }
     }
-    consumer_sync();
+    consumer_sync(NT);
   }
 
   if (p.epi == EPI_LOGITS && p.select) {
     best = warp_max_u64(best);
     if (lane == 0) keys[warp] = best;
-    consumer_sync();
+    consumer_sync(NT);
     if (tid == 0) {
       unsigned long long b = 0ull;
-      for (int w = 0; w < kConsumerWarps; ++w) b = keys[w] > b ? keys[w] : b;
+      for (int w = 0; w < NW; ++w) b = keys[w] > b ? keys[w] : b;
       if (b) atomicMax(p.best, b);
       __threadfence();
       const uint32_t t = atomicAdd(p.ticket, 1u);
@@ -263,11 +338,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const GemvParams p) {
   }
 }
 
+// Consumer threads for a row of nch 16-byte chunks: the multiple of 32 (up
+// to 512) that splits the chunks most evenly over at most 5 chunks per
+// thread; ties go to the count closest to 320 (enough warps to hide shared-
+// memory latency, few enough registers for two CTAs per SM).
+int choose_threads(int nch, int* J) {
+  int best_nt = 32, best_j = 5;
+  double best_eff = -1.0;
+  for (int w = 1; w <= kMaxConsumerWarps; ++w) {
+    const int nt = 32 * w;
+    const int j = (nch + nt - 1) / nt;
+    if (j > 5) continue;
+    const double eff = static_cast<double>(nch) / (static_cast<double>(nt) * j);
+    const bool better = eff > best_eff + 1e-9 ||
+                        (eff > best_eff - 1e-9 && std::abs(nt - 320) < std::abs(best_nt - 320));
+    if (better) {
+      best_eff = eff;
+      best_nt = nt;
+      best_j = j;
+    }
+  }
+  *J = best_j;
+  return best_nt;
+}
+
 template <int WT, int M, int J>
-cudaError_t launch_t(const GemvParams& p, int grid, bool pdl, cudaStream_t s) {
+cudaError_t launch_t(const GemvParams& p, int nt, int grid, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(nt + 32);
   cfg.dynamicSmemBytes = gemv_smem_bytes(p, M);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -279,34 +378,39 @@ cudaError_t launch_t(const GemvParams& p, int grid, bool pdl, cudaStream_t s) {
 }
 
 template <int WT, int M>
-cudaError_t launch_j(const GemvParams& p, int J, int grid, bool pdl, cudaStream_t s) {
+cudaError_t launch_j(const GemvParams& p, int J, int nt, int grid, bool pdl, cudaStream_t s) {
   switch (J) {
-    case 1: return launch_t<WT, M, 1>(p, grid, pdl, s);
-    case 2: return launch_t<WT, M, 2>(p, grid, pdl, s);
-    case 3: return launch_t<WT, M, 3>(p, grid, pdl, s);
-    case 4:
-    case 5: return launch_t<WT, M, 5>(p, grid, pdl, s);
+    case 1: return launch_t<WT, M, 1>(p, nt, grid, pdl, s);
+    case 2: return launch_t<WT, M, 2>(p, nt, grid, pdl, s);
+    case 3: return launch_t<WT, M, 3>(p, nt, grid, pdl, s);
+    case 4: return launch_t<WT, M, 4>(p, nt, grid, pdl, s);
+    case 5: return launch_t<WT, M, 5>(p, nt, grid, pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
+template <typename K>
+cudaError_t set_smem(K kernel) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
 template <int WT, int M>
 cudaError_t set_attr_m() {
-  const int bytes = 200 * 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gemv<WT, M, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemv<WT, M, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  if ((e = cudaFuncSetAttribute(k_gemv<WT, M, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))) return e;
-  return cudaFuncSetAttribute(k_gemv<WT, M, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if ((e = set_smem(k_gemv<WT, M, 1>))) return e;
+  if ((e = set_smem(k_gemv<WT, M, 2>))) return e;
+  if ((e = set_smem(k_gemv<WT, M, 3>))) return e;
+  if ((e = set_smem(k_gemv<WT, M, 4>))) return e;
+  return set_smem(k_gemv<WT, M, 5>);
 }
 
 }  // namespace
 
 size_t gemv_smem_bytes(const GemvParams& p, int M) {
   size_t b = (size_t)p.nst * p.stb;
-  b += (size_t)kRowBatch * kConsumerWarps * M * sizeof(float);
+  b += (size_t)kRowBatch * kMaxConsumerWarps * M * sizeof(float);
   b += 2 * (size_t)p.nst * sizeof(uint64_t);
-  b += (8 * M + 1) * sizeof(float) + kConsumerWarps * sizeof(unsigned long long) + 16;
+  b += (size_t)kMaxConsumerWarps * M * sizeof(float) + kMaxConsumerWarps * sizeof(unsigned long long) + 16;
   return b;
 }
 
@@ -319,15 +423,16 @@ void gemv_plan(GemvParams& p, int eb, int num_sms) {
   p.stb = ((p.rs * rowbytes + 127) / 128) * 128;
   p.nst = kRingBytes / p.stb;
   if (p.nst < 2) p.nst = 2;
-  if (p.nst > 8) p.nst = 8;
+  if (p.nst > 16) p.nst = 16;
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, cudaStream_t s) {
   const int nch = p.K * (wt ? 1 : 2) / 16;
-  const int J = (nch + kConsumers - 1) / kConsumers;
+  int J = 0;
+  const int nt = choose_threads(nch, &J);
   if (J < 1 || J > 5 || M < 1 || M > 2) return cudaErrorInvalidValue;
-  if (wt == 0) return M == 1 ? launch_j<0, 1>(p, J, grid, pdl, s) : launch_j<0, 2>(p, J, grid, pdl, s);
-  return M == 1 ? launch_j<1, 1>(p, J, grid, pdl, s) : launch_j<1, 2>(p, J, grid, pdl, s);
+  if (wt == 0) return M == 1 ? launch_j<0, 1>(p, J, nt, grid, pdl, s) : launch_j<0, 2>(p, J, nt, grid, pdl, s);
+  return M == 1 ? launch_j<1, 1>(p, J, nt, grid, pdl, s) : launch_j<1, 2>(p, J, nt, grid, pdl, s);
 }
 
 cudaError_t gemv_set_attributes() {

@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kUnroll = 4;
+constexpr int kMinKeys = 32;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
@@ -42,7 +43,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
     return;
   }
   const int n = pos + 1;
-  const int L = (n + p.S - 1) / p.S;
+  // At least kMinKeys keys per split: short contexts use fewer CTAs.
+  const int L = max((n + p.S - 1) / p.S, kMinKeys);
   const int sact = (n + L - 1) / L;
   if (s >= sact) return;
   const int k0 = s * L, k1 = min(n, k0 + L);
@@ -186,6 +188,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
 
 template <int D, int G>
 cudaError_t launch_dg(const AttnParams& p, int M, bool pdl, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+    if (e) return e;
+    attr_set = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, p.Hkv, M);
   cfg.blockDim = dim3(kWarps * 32);

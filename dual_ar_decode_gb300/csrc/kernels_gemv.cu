@@ -391,7 +391,12 @@ cudaError_t launch_j(const GemvParams& p, int J, int nt, int grid, bool pdl, cud
 
 template <typename K>
 cudaError_t set_smem(K kernel) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e) return e;
+  // Every decode kernel asks for the full shared-memory carveout, so that a
+  // CTA of the next kernel (launched early by PDL) can share the SM.
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
 }
 
 template <int WT, int M>

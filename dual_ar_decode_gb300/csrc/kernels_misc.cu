@@ -451,13 +451,26 @@ __global__ void __launch_bounds__(256) k_gemm_rows(const GemvParams p, int M) {
 
 }  // namespace
 
+// Full shared-memory carveout for the small decode kernels too (see the
+// GEMV): kernels with equal carveouts can share an SM under PDL.
+template <typename K>
+cudaError_t carveout(K kernel) {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  done = true;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s) {
+  if (cudaError_t e = carveout(k_build)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(p.M), dim3(256), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_build, p);
 }
 
 cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s) {
+  if (cudaError_t e = carveout(k_frame_end)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_frame_end, p);
@@ -466,6 +479,7 @@ cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s) 
 cudaError_t launch_select(const SelectParams& p, bool pdl, cudaStream_t s) {
   if (p.vocab < 1 || p.vocab > kSelMaxVocab || p.top_k > kSelMaxK || p.n < 1)
     return cudaErrorInvalidValue;
+  if (cudaError_t e = carveout(k_select)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(p.n), dim3(kSelThreads), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_select, p);

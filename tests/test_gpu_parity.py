@@ -21,6 +21,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+@pytest.fixture(params=["persistent", "graph"])
+def driver(request, monkeypatch):
+    """Decode driver: the persistent frame kernel (default) or one kernel per
+    op replayed as a CUDA graph."""
+    if request.param == "graph":
+        monkeypatch.setenv("TF_DECODE_DRIVER", "graph")
+    else:
+        monkeypatch.delenv("TF_DECODE_DRIVER", raising=False)
+    return request.param
+
+
 @pytest.fixture(scope="module", autouse=True)
 def built():
     import __graft_entry__
@@ -117,7 +128,7 @@ TINY_G8 = TINY.replace(hidden=256, ffn=512, n_heads=8, n_kv_heads=1, head_dim=12
 
 @pytest.mark.parametrize("dims,fmt,tol", [(TINY, "bf16", BF16_TOL), (TINY, "fp8", FP8_TOL),
                                           (TINY_ODD, "bf16", BF16_TOL), (TINY_G8, "bf16", BF16_TOL)])
-def test_tiny_teacher_forced(dims, fmt, tol):
+def test_tiny_teacher_forced(dims, fmt, tol, driver):
     tf = TeacherForced(dims, fmt, seed=0)
     tf.prefill(make_prompt(dims, 16, seed=0))
     for _ in range(8):
@@ -130,7 +141,7 @@ def test_tiny_teacher_forced(dims, fmt, tol):
 
 
 @pytest.mark.parametrize("k", [30, 4])
-def test_tiny_topk_teacher_forced(k):
+def test_tiny_topk_teacher_forced(k, driver):
     # With 64 codes and k = 30 most candidate boundaries sit within the
     # measured logit perturbation; those draws are only checked for validity.
     s = {"top_k": k, "seed": 1234}
@@ -162,7 +173,7 @@ def test_prompt_edges_and_capacity():
     tf.dec.close()
 
 
-def test_decode_frames_equals_single_calls_and_is_deterministic():
+def test_decode_frames_equals_single_calls_and_is_deterministic(driver):
     w = make_weights(TINY, seed=5)
     prompt = make_prompt(TINY, 12, seed=5)
     runs = []
@@ -207,7 +218,7 @@ def full_weights():
 
 
 @pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL)])
-def test_full_size_teacher_forced_sampled_frames(full_weights, fmt, tol):
+def test_full_size_teacher_forced_sampled_frames(full_weights, fmt, tol, driver):
     """Full-size model (36+4 layers, hidden 2560), prefill 128 then 2 decode
     frames, in the launch configuration the benchmark times."""
     tf = TeacherForced(FULL, fmt, weights=full_weights)

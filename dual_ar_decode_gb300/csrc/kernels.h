@@ -259,6 +259,9 @@ struct FrameParams {
   uint32_t* counters;     // attention tickets [M][Hkv]
   uint32_t* gbar;         // grid barrier counter, zero at launch
   uint32_t* err;
+  // optional trace: per op, for CTA 0 and the last CTA, %globaltimer at
+  // barrier-wait start, barrier-wait end and op end: [n_ops][2][3]
+  unsigned long long* trace;
 };
 
 constexpr int kFrameStage = 24 * 1024;

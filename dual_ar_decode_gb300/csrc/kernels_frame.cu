@@ -795,6 +795,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
     for (int i = 0; i < P.n_ops; ++i) {
       const FrameOp& op = P.ops[i];
       const uint32_t gi = static_cast<uint32_t>(f) * P.n_ops + i;
+      const int trace_slot = (P.trace && f == 0 && tid == 0)
+                                 ? (blockIdx.x == 0 ? 0 : (blockIdx.x == G - 1 ? 1 : -1))
+                                 : -1;
+      if (trace_slot >= 0) P.trace[(i * 2 + trace_slot) * 3 + 0] = globaltimer_ns();
       // grid barrier: every CTA has finished ops 0 .. gi-1
       if (gi > 0) {
         if (tid == 0 && !*S.abort_flag) {
@@ -813,6 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
         }
         csync();
       }
+      if (trace_slot >= 0) P.trace[(i * 2 + trace_slot) * 3 + 1] = globaltimer_ns();
       switch (op.kind) {
         case OPK_GEMV:
           if (op.wt == 0) {
@@ -845,6 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
           break;
       }
       csync();
+      if (trace_slot >= 0) P.trace[(i * 2 + trace_slot) * 3 + 2] = globaltimer_ns();
       if (tid == 0) {
         __threadfence();
         red_release_add(P.gbar, 1u);

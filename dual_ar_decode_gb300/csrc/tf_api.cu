@@ -125,6 +125,8 @@ struct tf_ctx {
   int frame_slots = 0, frame_union = 0;
   int S_frame = 1;
   uint32_t* gbar = nullptr;
+  unsigned long long* trace = nullptr;  // [kMaxOps][2][3]
+  bool tracing = false;
 };
 
 namespace {
@@ -546,6 +548,7 @@ tf_status run_frames(tf_ctx* c, bool decode, const tf_sampling* s, int n_frames)
   P.counters = c->counters;
   P.gbar = c->gbar;
   P.err = &c->st->err;
+  P.trace = c->tracing ? c->trace : nullptr;
   CK(cudaMemsetAsync(c->gbar, 0, sizeof(uint32_t), c->stream));
   CK(launch_frame(P, c->num_sms, c->stream));
   return TF_OK;
@@ -786,7 +789,8 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       dev_alloc_t(c, &c->pu, (size_t)T * c->F) || dev_alloc_t(c, &c->tokens, (size_t)T) ||
       dev_alloc_t(c, &c->hist, (size_t)T * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
       dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)) ||
-      dev_alloc_t(c, &c->d_ops, (size_t)4 * kMaxOps) || dev_alloc_t(c, &c->gbar, 1))
+      dev_alloc_t(c, &c->d_ops, (size_t)4 * kMaxOps) || dev_alloc_t(c, &c->gbar, 1) ||
+      dev_alloc_t(c, &c->trace, (size_t)kMaxOps * 6))
     return bail(TF_E_NOMEM);
 
   // RoPE table: angle pos * theta^(-2i/D) evaluated in double, stored as float.
@@ -1098,6 +1102,31 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
   c->pos_host += 1;
   c->frame_host += 1;
   return read_frame(c, frame, logits);
+}
+
+tf_status tf_decode_trace(tf_ctx* c, const tf_sampling* sampling, int64_t* stamps, int32_t* kinds,
+                          int32_t cap, int32_t* n_ops) {
+  if (!c || !stamps || !kinds || !n_ops || cap < 1) return TF_E_INVAL;
+  if (c->use_graph) return fail(c, TF_E_STATE, "tracing needs the persistent frame kernel");
+  int32_t frame[16];
+  c->tracing = true;
+  tf_status r = tf_decode_frame(c, sampling, nullptr, frame, nullptr);
+  c->tracing = false;
+  if (r) return r;
+  tf_sampling s;
+  check_sampling(c, sampling, &s);
+  const FrameOp* ops;
+  int n;
+  if ((r = get_program(c, true, s.top_k > 0, &ops, &n))) return r;
+  *n_ops = n;
+  const int k = std::min(n, cap);
+  std::vector<unsigned long long> buf((size_t)k * 6);
+  CK(cudaMemcpy(buf.data(), c->trace, buf.size() * 8, cudaMemcpyDeviceToHost));
+  for (size_t i = 0; i < buf.size(); ++i) stamps[i] = static_cast<int64_t>(buf[i]);
+  std::vector<FrameOp> host(k);
+  CK(cudaMemcpy(host.data(), ops, (size_t)k * sizeof(FrameOp), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < k; ++i) kinds[i] = host[i].kind;
+  return TF_OK;
 }
 
 tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, int32_t* frames) {

@@ -186,6 +186,16 @@ void tf_destroy(tf_ctx* ctx);
 tf_status tf_profile_kernel(tf_ctx* ctx, int32_t which, int32_t iters,
                             float* ms_per_launch, int64_t* bytes_per_launch);
 
+/* One decode frame, like tf_decode_frame, with per-op timing: the persistent
+ * frame kernel stamps %globaltimer (ns) for each op of its program, on CTA 0
+ * and on the last CTA: barrier-wait start, barrier-wait end, op end.
+ * stamps: host int64 [cap][2][3]; kinds: host int32 [cap] (0 GEMV,
+ * 1 attention, 2 selection, 3 bookkeeping); *n_ops receives the program
+ * length (stamps beyond cap are dropped).  Errors as tf_decode_frame;
+ * TF_E_STATE when the context uses the kernel-per-op driver. */
+tf_status tf_decode_trace(tf_ctx* ctx, const tf_sampling* sampling, int64_t* stamps,
+                          int32_t* kinds, int32_t cap, int32_t* n_ops);
+
 /* ---------------------------------------------------------------------------
  * Single-operation entry points, for parity tests and profiling.  Each runs
  * one kernel of the decode path on caller-provided DEVICE buffers on `stream`

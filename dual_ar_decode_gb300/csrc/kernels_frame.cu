@@ -159,10 +159,11 @@ __device__ __forceinline__ void qkv_pair(const FrameParams& P, const FrameOp& op
 }
 
 // ------------------------------------------------------------------ GEMV op
-template <int WT, int M>
+// JM = chunks per consumer thread, a compile-time count so that the hot loop
+// carries no predicated-off chunk slots.
+template <int WT, int M, int JM>
 __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int& s_ctr) {
   constexpr int EPC = WT ? 16 : 8;
-  constexpr int JM = WT ? 2 : 4;
   constexpr int R = M == 1 ? 4 : 2;
   constexpr int V = R * M;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -171,7 +172,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
   op_rows(op, blockIdx.x, G, &r0, &nrows);
   const uint32_t rowbytes = static_cast<uint32_t>(op.K) * (WT ? 1u : 2u);
   const int nch = static_cast<int>(rowbytes >> 4);
-  const int nt = op.nt, J = op.J;
+  const int nt = op.nt;
   const bool active = tid < nt;
 
   // ---- activation rows into registers
@@ -196,7 +197,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
       const int ch = tid + j * nt;
-      if (!active || j >= J || ch >= nch) continue;
+      if (!active || ch >= nch) continue;
       const bool from_table = (op.src == SRC_EMBED && m == 0) || (op.src == SRC_FAST1 && m == 1);
       if (from_table) {
         const uint16_t* row = op.table + (size_t)(op.row_base + id) * op.K + ch * EPC;
@@ -255,7 +256,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
       const int ch = tid + j * nt;
-      if (!active || j >= J || ch >= nch) continue;
+      if (!active || ch >= nch) continue;
 #pragma unroll
       for (int e = 0; e < EPC; ++e)
         a[0][j][e] = a[0][j][e] * rstd * bf16_to_f32(__ldg(&op.nw_src[ch * EPC + e]));
@@ -268,7 +269,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
 #pragma unroll
       for (int j = 0; j < JM; ++j) {
         const int ch = tid + j * nt;
-        if (!active || j >= J || ch >= nch) continue;
+        if (!active || ch >= nch) continue;
 #pragma unroll
         for (int e = 0; e < EPC; ++e) op.xres[(size_t)m * op.K + ch * EPC + e] = a[m][j][e];
       }
@@ -282,7 +283,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
 #pragma unroll
       for (int j = 0; j < JM; ++j) {
         const int ch = tid + j * nt;
-        if (!active || j >= J || ch >= nch) continue;
+        if (!active || ch >= nch) continue;
 #pragma unroll
         for (int e = 0; e < EPC; ++e)
           a[m][j][e] = a[m][j][e] * rstd * bf16_to_f32(__ldg(&op.nw[ch * EPC + e]));
@@ -312,7 +313,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
 #pragma unroll
             for (int j = 0; j < JM; ++j) {
               const int ch = tid + j * nt;
-              if (j < J && ch < nch) {
+              if (ch < nch) {
                 const uint4 w = row[ch];
 #pragma unroll
                 for (int m = 0; m < M; ++m) acc[m] = chunk_fma<WT>(w, a[m][j], acc[m]);
@@ -398,6 +399,33 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
         P.ticket[op.cb] = 0u;
       }
     }
+  }
+}
+
+template <int WT, int M>
+__device__ __forceinline__ void gemv_dispatch_j(const FrameParams& P, const FrameOp& op, Shared& S,
+                                                int& s_ctr) {
+  if constexpr (WT == 0) {
+    switch (op.J) {
+      case 1: gemv_op<0, M, 1>(P, op, S, s_ctr); break;
+      case 2: gemv_op<0, M, 2>(P, op, S, s_ctr); break;
+      case 3: gemv_op<0, M, 3>(P, op, S, s_ctr); break;
+      default: gemv_op<0, M, 4>(P, op, S, s_ctr); break;
+    }
+  } else {
+    if (op.J == 1) gemv_op<1, M, 1>(P, op, S, s_ctr);
+    else gemv_op<1, M, 2>(P, op, S, s_ctr);
+  }
+}
+
+__device__ __noinline__ void gemv_dispatch(const FrameParams& P, const FrameOp& op, Shared& S,
+                                           int& s_ctr) {
+  if (op.wt == 0) {
+    if (op.M == 1) gemv_dispatch_j<0, 1>(P, op, S, s_ctr);
+    else gemv_dispatch_j<0, 2>(P, op, S, s_ctr);
+  } else {
+    if (op.M == 1) gemv_dispatch_j<1, 1>(P, op, S, s_ctr);
+    else gemv_dispatch_j<1, 2>(P, op, S, s_ctr);
   }
 }
 
@@ -820,13 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
       if (trace_slot >= 0) P.trace[(i * 2 + trace_slot) * 3 + 1] = globaltimer_ns();
       switch (op.kind) {
         case OPK_GEMV:
-          if (op.wt == 0) {
-            if (op.M == 1) gemv_op<0, 1>(P, op, S, s_ctr);
-            else gemv_op<0, 2>(P, op, S, s_ctr);
-          } else {
-            if (op.M == 1) gemv_op<1, 1>(P, op, S, s_ctr);
-            else gemv_op<1, 2>(P, op, S, s_ctr);
-          }
+          gemv_dispatch(P, op, S, s_ctr);
           break;
         case OPK_ATTN:
           if (P.D == 128) attn_dispatch_g<128>(P, op, S);

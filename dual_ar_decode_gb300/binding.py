@@ -68,6 +68,9 @@ EXPORTS = {
     "tf_op_select": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(TfSampling), ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+    "tf_op_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_gemv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]),
@@ -244,6 +247,11 @@ def op_select(logits_dev, n, vocab, sampling, frame, codebook0, sequence, ids_de
     s = _sampling(sampling)
     _check(lib().tf_op_select(logits_dev, n, vocab, ctypes.byref(s), frame, codebook0, sequence,
                               ids_dev, stream))
+
+
+def op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev, stream=0):
+    _check(lib().tf_op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev,
+                                 stream))
 
 
 def op_gemv(W_dev, dtype, scale_dev, rows, cols, x_dev, y_dev, repeat=1, stream=0):

@@ -1259,6 +1259,58 @@ tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab, const tf_s
   return r;
 }
 
+tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
+                          int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
+                          int32_t splits, float* out, void* stream) {
+  if (!q || !K || !V || !out || T < 1 || Hq < 1 || Hkv < 1 || rows < 1 || pos0 < 0 ||
+      (int64_t)pos0 + rows > T || splits < 1 || splits > 64 || rows > 65535)
+    return TF_E_INVAL;
+  if ((D != 64 && D != 128) || Hq % Hkv) return TF_E_INVAL;
+  const int g = Hq / Hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return TF_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t part_bytes = (size_t)rows * Hq * splits * (D + 2) * sizeof(float);
+  const size_t cnt_bytes = (size_t)rows * Hkv * sizeof(uint32_t);
+  float* part = nullptr;
+  uint32_t* cnt = nullptr;
+  uint32_t* err = nullptr;
+  if (cudaMalloc(&part, part_bytes) != cudaSuccess || cudaMalloc(&cnt, cnt_bytes) != cudaSuccess ||
+      cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFree(part);
+    cudaFree(cnt);
+    cudaFree(err);
+    return TF_E_NOMEM;
+  }
+  tf_status r = TF_OK;
+  if (cudaMemsetAsync(cnt, 0, cnt_bytes, s) != cudaSuccess || cudaMemsetAsync(err, 0, 4, s) != cudaSuccess)
+    r = TF_E_CUDA;
+  AttnParams a = {};
+  a.q = q;
+  a.Kc = K;
+  a.Vc = V;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.pos_fixed = pos0;
+  a.S = splits;
+  a.part = part;
+  a.counters = cnt;
+  a.out = out;
+  a.err = err;
+  if (r == TF_OK && launch_attention(a, rows, false, s) != cudaSuccess) r = TF_E_CUDA;
+  uint32_t e = 0;
+  if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                     cudaStreamSynchronize(s) != cudaSuccess))
+    r = TF_E_CUDA;
+  cudaFree(part);
+  cudaFree(cnt);
+  cudaFree(err);
+  if (r == TF_OK && e) r = TF_E_INVAL;
+  return r;
+}
+
 tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64_t rows,
                      int64_t cols, const float* x, float* y, int32_t repeat, float* ms,
                      void* stream) {

@@ -220,6 +220,23 @@ tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab,
                        int32_t codebook0, int32_t sequence, int32_t* ids,
                        void* stream);
 
+/* Grouped-query decode attention ("Fish Speech" tour, "Why You Need This":
+ * rotary embeddings and grouped-query attention; tuna-fish README,
+ * "Inference estimation": static KV cache), the decode path's attention
+ * kernel on its own: query row m (m < rows) sits at position pos0 + m and
+ * attends to keys 0..pos0+m of its KV head (query head h reads KV head
+ * h / (Hq/Hkv)), scores scaled by 1/sqrt(D), softmax over the keys.
+ * q: float32 [rows][Hq*D] (already rotated); K, V: bf16 bits [Hkv][T][D];
+ * out: float32 [rows][Hq*D]; all device pointers.  `splits` (1..64) is the
+ * number of key slices per KV head (at least 32 keys each) whose partial
+ * softmax results are merged afterwards.  Allocates its scratch (partials,
+ * tickets, error word) with cudaMalloc and frees it before returning.
+ * D must be 64 or 128, Hq / Hkv one of 1, 2, 4, 8, pos0 + rows <= T.
+ * Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA. */
+tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
+                          int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
+                          int32_t splits, float* out, void* stream);
+
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
  * TF_DTYPE_BF16) or e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3);

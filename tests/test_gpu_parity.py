@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from dual_ar_decode_gb300 import Decoder, TfError, op_gemv, op_quantize_fp8, op_select
+from dual_ar_decode_gb300 import Decoder, TfError, op_attention, op_gemv, op_quantize_fp8, op_select
 from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
 from synth import FULL, TINY, make_logits, make_prompt, make_weights, f32_to_bf16_bits
 
@@ -116,6 +116,32 @@ def test_gemv_matches_oracle_linear(rows, cols, fp8):
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.max(np.abs(got - ref)) <= 1e-4 * rms
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-5
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,rows,pos0,splits", [
+    (32, 8, 128, 1, 1023, 38),   # full-size slow decode at the last position
+    (32, 8, 128, 2, 0, 1),       # fast step 1: two rows at positions 0, 1
+    (32, 8, 128, 1, 77, 38),     # short context: fewer splits than asked
+    (4, 2, 64, 3, 200, 7),       # tiny heads, ragged split sizes
+    (8, 1, 128, 1, 333, 5),      # 8 query heads per KV head
+])
+def test_attention_matches_oracle(Hq, Hkv, D, rows, pos0, splits):
+    T = pos0 + rows + 5
+    rng = np.random.default_rng(Hq * 1000 + pos0)
+    q = rng.standard_normal((rows, Hq * D)).astype(np.float32)
+    Kb = f32_to_bf16_bits(rng.standard_normal((Hkv, T, D)).astype(np.float32))
+    Vb = f32_to_bf16_bits(rng.standard_normal((Hkv, T, D)).astype(np.float32))
+    qd = torch.from_numpy(q).to(DEV)
+    Kd, Vd = dev_u16(Kb), dev_u16(Vb)      # keep both alive while the kernel runs
+    out = torch.full((rows, Hq * D), np.nan, dtype=torch.float32, device=DEV)
+    op_attention(qd.data_ptr(), Kd.data_ptr(), Vd.data_ptr(), T, Hq, Hkv, D, rows,
+                 pos0, splits, out.data_ptr())
+    K = oracle.bf16_bits_to_f64(Kb)
+    V = oracle.bf16_bits_to_f64(Vb)
+    got = out.cpu().numpy()
+    for m in range(rows):
+        ref = oracle.attention_row(q[m].reshape(Hq, D).astype(np.float64), K, V, pos0 + m + 1)
+        assert np.allclose(got[m].reshape(Hq, D), ref, rtol=1e-4, atol=1e-5)
 
 
 # ------------------------------------------------------------------ model

@@ -14,6 +14,9 @@
 // merge in shared memory.  The last CTA of each (g, m) to finish (ticket on
 // a global counter) merges the S partials in split order, so the result is
 // deterministic, and re-arms the counter.
+#include <mutex>
+
+#include "../../include/tf.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -227,4 +230,97 @@ cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t 
   return cudaErrorInvalidValue;
 }
 
+// ------------------------------------------------------------------------
+// Allocation-free attention entry point.
+//
+// Some callers cannot allocate device memory at the time they run attention:
+// code inside an allocator-free real-time loop, a host that has handed all
+// device memory to its own pool, or a plugin that must not touch the global
+// CUDA allocator.  tf_op_attention_noalloc runs the same kernel as
+// tf_op_attention but takes its scratch (split partials, tickets, error word)
+// from a fixed array compiled into this library instead of cudaMalloc.
+//
+// The array lives in device memory on every GPU that loads the library,
+// until the process exits.  Host code cannot use the array's name as a
+// device address (on the host it only stands for the symbol), so the device
+// address is looked up once per device with cudaGetSymbolAddress, with that
+// device current, on the first call on it; that first call should happen
+// before any stream capture.  All calls share the one array and it keeps
+// what the last call left: tickets and the error word are cleared on every
+// call, and calls that overlap on the GPU (different streams, or different
+// host threads) race on it.
+constexpr size_t kNoAllocPartFloats = 512 * 1024;  // 2 MiB of split partials
+constexpr size_t kNoAllocTickets = 1024;
+constexpr size_t kNoAllocBytes = kNoAllocPartFloats * 4 + kNoAllocTickets * 4 + 256;
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once).
+void* noalloc_scratch(int dev) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_attn_noalloc_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+}  // namespace
+
 }  // namespace tf
+
+extern "C" tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, const uint16_t* V,
+                                             int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                             int32_t rows, int32_t pos0, int32_t splits, float* out,
+                                             void* stream) {
+  using namespace tf;
+  if (!q || !K || !V || !out || T < 1 || Hq < 1 || Hkv < 1 || rows < 1 || pos0 < 0 ||
+      (int64_t)pos0 + rows > T || splits < 1 || splits > 64 || rows > 65535)
+    return TF_E_INVAL;
+  if ((D != 64 && D != 128) || Hq % Hkv) return TF_E_INVAL;
+  const int g = Hq / Hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return TF_E_INVAL;
+  // Sizes beyond the fixed scratch are refused.
+  if ((size_t)rows * Hq * splits * (D + 2) > kNoAllocPartFloats ||
+      (size_t)rows * Hkv > kNoAllocTickets)
+    return TF_E_INVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TF_E_CUDA;
+  unsigned char* base = static_cast<unsigned char*>(noalloc_scratch(dev));
+  if (!base) return TF_E_CUDA;
+  float* part = reinterpret_cast<float*>(base);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + kNoAllocPartFloats * 4);
+  uint32_t* err = cnt + kNoAllocTickets;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(cnt, 0, (size_t)rows * Hkv * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(err, 0, 4, s) != cudaSuccess)
+    return TF_E_CUDA;
+  AttnParams a = {};
+  a.q = q;
+  a.Kc = K;
+  a.Vc = V;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.pos_fixed = pos0;
+  a.S = splits;
+  a.part = part;
+  a.counters = cnt;
+  a.out = out;
+  a.err = err;
+  if (launch_attention(a, rows, false, s) != cudaSuccess) return TF_E_CUDA;
+  uint32_t e = 0;
+  if (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return TF_E_CUDA;
+  return e ? TF_E_INVAL : TF_OK;
+}

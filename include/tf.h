@@ -237,6 +237,21 @@ tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, 
                           int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
                           int32_t splits, float* out, void* stream);
 
+/* tf_op_attention without any device allocation.  The source pages have no
+ * counterpart to this call; it exists for callers that must not allocate
+ * device memory while they run (a real-time loop with no allocator calls, a
+ * host that gives all device memory to its own pool, a plugin kept off the
+ * global CUDA allocator).  Same arguments, results and errors as
+ * tf_op_attention, but the scratch comes from one fixed array built into the
+ * library (present on every GPU that loads it, until the process exits):
+ * calls need rows*Hq*splits*(D+2) <= 524288 and rows*Hkv <= 1024, else
+ * TF_E_INVAL.  The first call on a device looks up the array's device
+ * address (make it before any stream capture).  All calls share the array:
+ * calls that overlap on the GPU race on it. */
+tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
+                                  int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
+                                  int32_t splits, float* out, void* stream);
+
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
  * TF_DTYPE_BF16) or e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3);

@@ -38,6 +38,7 @@ struct GemvParams {
   int32_t rs;            // rows per pipeline stage
   int32_t nst;           // stages in the shared-memory ring
   int32_t stb;           // bytes per stage slot (multiple of 128)
+  int32_t ctas_per_sm;   // 1 or 2 (set by gemv_plan)
   // prologue
   int32_t pro;
   const float* x;        // [M][ldx]
@@ -70,8 +71,11 @@ struct GemvParams {
 
 // Shared memory bytes a launch with these params needs.
 size_t gemv_smem_bytes(const GemvParams& p, int M);
-// Fills unit/units/rs/nst/stb for a matrix of N x K elements of `eb` bytes.
-void gemv_plan(GemvParams& p, int eb, int num_sms);
+// Fills unit/units/rs/nst/stb/ctas_per_sm for a matrix of N x K elements of
+// `eb` bytes and M activation rows.
+void gemv_plan(GemvParams& p, int eb, int num_sms, int M);
+// CTAs to launch for a planned GEMV.
+int gemv_grid(const GemvParams& p, int num_sms);
 // Launch (weight type wt: 0 bf16, 1 fp8) on `grid` CTAs; pdl = allow
 // programmatic dependent launch on the previous kernel of the stream.
 cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl,

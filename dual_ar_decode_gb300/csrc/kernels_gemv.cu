@@ -35,13 +35,11 @@ namespace {
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kRowBatch = 128;  // rows reduced per epilogue round
 #ifndef TF_GEMV_STAGE_BYTES
-#define TF_GEMV_STAGE_BYTES (24 * 1024)
-#endif
-#ifndef TF_GEMV_RING_BYTES
-#define TF_GEMV_RING_BYTES (96 * 1024)
+#define TF_GEMV_STAGE_BYTES (40 * 1024)
 #endif
 constexpr int kStageTarget = TF_GEMV_STAGE_BYTES;  // bytes of whole rows per stage
-constexpr int kRingBytes = TF_GEMV_RING_BYTES;     // shared-memory ring per CTA
+constexpr int kRingTwo = 80 * 1024;   // ring per CTA when two CTAs share an SM
+constexpr int kRingOne = 160 * 1024;  // ring of a lone CTA
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -109,9 +107,9 @@ template <int WT, int M, int J>
 __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int EPC = WT ? 16 : 8;      // elements per 16-byte chunk
-  constexpr int R = M == 1 ? 4 : 2;     // rows reduced together
-  constexpr int V = R * M;              // values per butterfly (4)
-  constexpr int LOGV = V == 4 ? 2 : (V == 2 ? 1 : 0);
+  constexpr int R = M == 1 ? 8 : 4;     // rows reduced together
+  constexpr int V = R * M;              // values per butterfly (8)
+  constexpr int LOGV = 3;
   const int NT = static_cast<int>(blockDim.x) - 32;  // consumer threads
   const int NW = NT >> 5;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -419,16 +417,55 @@ size_t gemv_smem_bytes(const GemvParams& p, int M) {
   return b;
 }
 
-void gemv_plan(GemvParams& p, int eb, int num_sms) {
+namespace {
+
+const void* kernel_for(int wt, int M, int J) {
+  const void* t[2][2][5] = {
+      {{(const void*)k_gemv<0, 1, 1>, (const void*)k_gemv<0, 1, 2>, (const void*)k_gemv<0, 1, 3>,
+        (const void*)k_gemv<0, 1, 4>, (const void*)k_gemv<0, 1, 5>},
+       {(const void*)k_gemv<0, 2, 1>, (const void*)k_gemv<0, 2, 2>, (const void*)k_gemv<0, 2, 3>,
+        (const void*)k_gemv<0, 2, 4>, (const void*)k_gemv<0, 2, 5>}},
+      {{(const void*)k_gemv<1, 1, 1>, (const void*)k_gemv<1, 1, 2>, (const void*)k_gemv<1, 1, 3>,
+        (const void*)k_gemv<1, 1, 4>, (const void*)k_gemv<1, 1, 5>},
+       {(const void*)k_gemv<1, 2, 1>, (const void*)k_gemv<1, 2, 2>, (const void*)k_gemv<1, 2, 3>,
+        (const void*)k_gemv<1, 2, 4>, (const void*)k_gemv<1, 2, 5>}}};
+  return t[wt][M - 1][J - 1];
+}
+
+void set_ring(GemvParams& p, int rowbytes, int ring) {
+  p.rs = rowbytes >= kStageTarget ? 1 : kStageTarget / rowbytes;
+  p.stb = ((p.rs * rowbytes + 127) / 128) * 128;
+  p.nst = std::max(2, std::min(16, ring / p.stb));
+}
+
+}  // namespace
+
+int gemv_grid(const GemvParams& p, int num_sms) {
+  return std::min(num_sms * p.ctas_per_sm, p.units);
+}
+
+// Two CTAs per SM (20 consumer warps, 2 x 80 KB rings) where registers and
+// shared memory allow it, else one CTA with a 160 KB ring: with only ten
+// consumer warps per SM the row reductions are latency-bound.
+void gemv_plan(GemvParams& p, int eb, int num_sms, int M) {
   (void)num_sms;
   p.unit = (p.epi == EPI_SWIGLU || p.epi == EPI_QKV) ? 2 : 1;
   p.units = p.N / p.unit;
   const int rowbytes = p.K * eb;
-  p.rs = rowbytes >= kStageTarget ? 1 : kStageTarget / rowbytes;
-  p.stb = ((p.rs * rowbytes + 127) / 128) * 128;
-  p.nst = kRingBytes / p.stb;
-  if (p.nst < 2) p.nst = 2;
-  if (p.nst > 16) p.nst = 16;
+  int J = 0;
+  const int nt = choose_threads(rowbytes / 16, &J);
+  p.ctas_per_sm = 1;
+  set_ring(p, rowbytes, kRingTwo);
+  int n = 0;
+  if (J >= 1 && J <= 5 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_for(eb == 1 ? 1 : 0, M, J), nt + 32,
+                                                    gemv_smem_bytes(p, M)) == cudaSuccess &&
+      n >= 2) {
+    p.ctas_per_sm = 2;
+  } else {
+    (void)cudaGetLastError();
+    set_ring(p, rowbytes, kRingOne);
+  }
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, cudaStream_t s) {

@@ -119,7 +119,7 @@ struct tf_ctx {
   tf_sampling graph_samp{};
 
   // persistent frame kernel
-  bool use_graph = false;         // TF_DECODE_DRIVER=graph: one kernel per op in a CUDA graph
+  bool use_graph = true;          // false: persistent frame kernel (TF_DECODE_DRIVER=persistent)
   FrameOp* d_ops = nullptr;       // [4][kMaxOps]: decode/tail x greedy/top-k
   int n_ops[4] = {0, 0, 0, 0};
   int frame_slots = 0, frame_union = 0;
@@ -257,8 +257,8 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
     p.forced_on = &c->st->forced_on;
   }
   const int eb = (L.s != nullptr) ? 1 : 2;
-  gemv_plan(p, eb, c->num_sms);
-  const int grid = std::min(c->num_sms, p.units);
+  gemv_plan(p, eb, c->num_sms, M);
+  const int grid = gemv_grid(p, c->num_sms);
   return launch_gemv(p, eb == 1 ? 1 : 0, M, grid, pdl, c->stream);
 }
 
@@ -686,8 +686,10 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
     return bail(TF_E_CUDA);
   }
   {
+    // Default: one kernel per op replayed as a CUDA graph with PDL chaining;
+    // TF_DECODE_DRIVER=persistent selects the persistent frame kernel.
     const char* drv = std::getenv("TF_DECODE_DRIVER");
-    c->use_graph = drv && std::string(drv) == "graph";
+    c->use_graph = !(drv && std::string(drv) == "persistent");
   }
 
   c->fp8 = cfg->weight_dtype == TF_WEIGHT_FP8;
@@ -1337,8 +1339,8 @@ tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64
   p.out = y;
   p.ldo = 0;
   p.err = err;
-  gemv_plan(p, eb, sms);
-  const int grid = std::min(sms, p.units);
+  gemv_plan(p, eb, sms, 1);
+  const int grid = gemv_grid(p, sms);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   tf_status r = TF_OK;
   if (ms) {

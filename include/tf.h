@@ -192,7 +192,9 @@ tf_status tf_profile_kernel(tf_ctx* ctx, int32_t which, int32_t iters,
  * stamps: host int64 [cap][2][3]; kinds: host int32 [cap] (0 GEMV,
  * 1 attention, 2 selection, 3 bookkeeping); *n_ops receives the program
  * length (stamps beyond cap are dropped).  Errors as tf_decode_frame;
- * TF_E_STATE when the context uses the kernel-per-op driver. */
+ * TF_E_STATE when the context uses the kernel-per-op driver (the default;
+ * the persistent frame kernel is selected by TF_DECODE_DRIVER=persistent in
+ * the environment of tf_create). */
 tf_status tf_decode_trace(tf_ctx* ctx, const tf_sampling* sampling, int64_t* stamps,
                           int32_t* kinds, int32_t cap, int32_t* n_ops);
 

@@ -23,10 +23,10 @@ DEV = "cuda:0"
 
 @pytest.fixture(params=["persistent", "graph"])
 def driver(request, monkeypatch):
-    """Decode driver: the persistent frame kernel (default) or one kernel per
-    op replayed as a CUDA graph."""
-    if request.param == "graph":
-        monkeypatch.setenv("TF_DECODE_DRIVER", "graph")
+    """Decode driver: one kernel per op replayed as a CUDA graph (default) or
+    the persistent frame kernel."""
+    if request.param == "persistent":
+        monkeypatch.setenv("TF_DECODE_DRIVER", "persistent")
     else:
         monkeypatch.delenv("TF_DECODE_DRIVER", raising=False)
     return request.param

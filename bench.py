@@ -179,7 +179,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--op", default=None, choices=["gemv"],
+                    help="time one kernel on its own instead of the decode step")
+    ap.add_argument("--rows", type=int, default=19456)
+    ap.add_argument("--cols", type=int, default=2560)
+    ap.add_argument("--fp8", action="store_true")
     args = ap.parse_args()
+    if args.op == "gemv":
+        return run_gemv_case(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -310,6 +317,41 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_gemv_case(args):
+    """The decode GEMV alone (tf_op_gemv, no prologue or epilogue) on
+    `rows` x `cols` weights, bf16 or e4m3 + row scales: K launches chained
+    with PDL, each on a distinct copy of the matrix (about 2.5 GB in all, far
+    above L2), after W warm-up passes.  Prints one JSON line."""
+    import torch
+    from dual_ar_decode_gb300 import op_gemv
+    from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
+    dev = torch.device("cuda", 0)
+    eb = 1 if args.fp8 else 2
+    mat = args.rows * args.cols * eb
+    reps = max(args.steps, int(2.5e9 // mat))
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    W = torch.randint(0, 120, (reps * mat,), dtype=torch.uint8, device=dev, generator=g)
+    if eb == 2:
+        W = (W.view(torch.int16) & 0x3FFF).view(torch.uint8)   # finite bf16
+    S = torch.rand(reps * args.rows, device=dev, generator=g) if eb == 1 else None
+    x = torch.randn(args.cols, device=dev, generator=g)
+    y = torch.empty(args.rows, device=dev)
+    dt = TF_DTYPE_FP8_E4M3 if eb == 1 else TF_DTYPE_BF16
+    for _ in range(args.warmup):
+        op_gemv(W.data_ptr(), dt, S.data_ptr() if S is not None else None, args.rows, args.cols,
+                x.data_ptr(), y.data_ptr(), reps)
+    ms = op_gemv(W.data_ptr(), dt, S.data_ptr() if S is not None else None, args.rows, args.cols,
+                 x.data_ptr(), y.data_ptr(), reps)
+    nbytes = mat + (args.rows * 4 if eb == 1 else 0) + args.cols * 4 + args.rows * 4
+    peaks = measured_peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"op": "gemv", "rows": args.rows, "cols": args.cols,
+                      "weights": "fp8" if eb == 1 else "bf16", "launches": reps,
+                      "us_per_launch": round(ms * 1e3, 3), "achieved_gbs": round(gbs, 1),
+                      "peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+                      "peak_source": peaks["source"]}), flush=True)
 
 
 def run_reference(args, wl, world, rank):

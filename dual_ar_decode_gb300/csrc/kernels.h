@@ -39,6 +39,7 @@ struct GemvParams {
   int32_t nst;           // stages in the shared-memory ring
   int32_t stb;           // bytes per stage slot (multiple of 128)
   int32_t ctas_per_sm;   // 1 or 2 (set by gemv_plan)
+  int32_t nt, J;         // consumer threads and 16-byte chunks per thread (gemv_plan)
   // prologue
   int32_t pro;
   const float* x;        // [M][ldx]
@@ -243,7 +244,8 @@ struct FrameParams {
   int32_t T, Hq, Hkv, D, q_dim, kv_dim;
   const float2* rope;
   float eps;
-  int32_t slots;          // ring slots (each kFrameStage bytes)
+  int32_t slots;          // ring slots
+  int32_t stage;          // bytes per ring slot (multiple of 128)
   int32_t un_bytes;       // union scratch bytes
   int32_t* pos;
   int32_t* frame_index;
@@ -268,12 +270,14 @@ struct FrameParams {
   unsigned long long* trace;
 };
 
-constexpr int kFrameStage = 24 * 1024;
+constexpr int kFrameStage = 40 * 1024;     // largest ring slot
 constexpr int kFrameConsumerWarps = 10;
+constexpr int kFrameCtasPerSm = 2;         // two CTAs per SM: 20 consumer warps
+constexpr int kFrameSmemPerCta = 112 * 1024;
 // Plans a GEMV op's staging and thread split; returns false if it does not fit.
-bool frame_plan_gemv(FrameOp& op);
+bool frame_plan_gemv(FrameOp& op, int stage);
 // Shared memory the frame kernel needs for these params.
-size_t frame_smem_bytes(int slots, int un_bytes);
+size_t frame_smem_bytes(int slots, int stage, int un_bytes);
 // Union-scratch bytes for the given shapes.
 int frame_union_bytes(int G, int D, int max_vocab);
 cudaError_t frame_set_attributes();

@@ -162,10 +162,10 @@ __device__ __forceinline__ void qkv_pair(const FrameParams& P, const FrameOp& op
 // JM = chunks per consumer thread, a compile-time count so that the hot loop
 // carries no predicated-off chunk slots.
 template <int WT, int M, int JM>
-__device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int& s_ctr) {
+__device__ __noinline__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int& s_ctr) {
   constexpr int EPC = WT ? 16 : 8;
-  constexpr int R = M == 1 ? 4 : 2;
-  constexpr int V = R * M;
+  constexpr int R = M == 1 ? 8 : 4;
+  constexpr int V = R * M;  // 8 values per butterfly
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
   int r0, nrows;
@@ -300,7 +300,7 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
       const int n = min(op.rs, nb - i0);
       const int slot = s_ctr % S.slots;
       if (!*S.abort_flag && !mbar_wait(&S.full[slot], (s_ctr / S.slots) & 1, P.err)) *S.abort_flag = 1;
-      const uint8_t* st = S.ring + (size_t)slot * kFrameStage;
+      const uint8_t* st = S.ring + (size_t)slot * P.stage;
       for (int i = 0; i < n; i += R) {
         float v[V];
 #pragma unroll
@@ -324,8 +324,8 @@ __device__ void gemv_op(const FrameParams& P, const FrameOp& op, Shared& S, int&
           for (int m = 0; m < M; ++m) v[r * M + m] = acc[m].x + acc[m].y;
         }
         const float tot = warp_reduce_many<V>(v, lane);
-        if ((lane & 7) == 0) {  // V == 4: lane >> 3 selects the value
-          const int idx = lane >> 3;
+        if ((lane & 3) == 0) {  // V == 8: lane >> 2 selects the value
+          const int idx = lane >> 2;
           const int r = idx / M, m = idx - r * M;
           if (i + r < n) red[((i0 + i + r) * kCW + warp) * M + m] = tot;
         }
@@ -410,11 +410,15 @@ __device__ __forceinline__ void gemv_dispatch_j(const FrameParams& P, const Fram
       case 1: gemv_op<0, M, 1>(P, op, S, s_ctr); break;
       case 2: gemv_op<0, M, 2>(P, op, S, s_ctr); break;
       case 3: gemv_op<0, M, 3>(P, op, S, s_ctr); break;
-      default: gemv_op<0, M, 4>(P, op, S, s_ctr); break;
+      case 4: gemv_op<0, M, 4>(P, op, S, s_ctr); break;
+      default: gemv_op<0, M, 5>(P, op, S, s_ctr); break;
     }
   } else {
-    if (op.J == 1) gemv_op<1, M, 1>(P, op, S, s_ctr);
-    else gemv_op<1, M, 2>(P, op, S, s_ctr);
+    switch (op.J) {
+      case 1: gemv_op<1, M, 1>(P, op, S, s_ctr); break;
+      case 2: gemv_op<1, M, 2>(P, op, S, s_ctr); break;
+      default: gemv_op<1, M, 3>(P, op, S, s_ctr); break;
+    }
   }
 }
 
@@ -757,12 +761,12 @@ __device__ void select_op(const FrameParams& P, const FrameOp& op, Shared& S) {
 }
 
 // ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
+__global__ void __launch_bounds__(kThreads, kFrameCtasPerSm) k_frame(const FrameParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   Shared S;
   S.slots = P.slots;
   S.ring = smem;
-  S.un = smem + (size_t)P.slots * kFrameStage;
+  S.un = smem + (size_t)P.slots * P.stage;
   S.full = reinterpret_cast<uint64_t*>(S.un + P.un_bytes);
   S.empty = S.full + P.slots;
   S.misc = reinterpret_cast<float*>(S.empty + P.slots);
@@ -803,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
               }
               const uint32_t bytes = static_cast<uint32_t>(n) * rowbytes;
               mbar_arrive_expect_tx(&S.full[slot], bytes);
-              bulk_g2s(S.ring + (size_t)slot * kFrameStage, op.W + (size_t)(r0 + b0 + i0) * rowbytes,
+              bulk_g2s(S.ring + (size_t)slot * P.stage, op.W + (size_t)(r0 + b0 + i0) * rowbytes,
                        bytes, &S.full[slot], pol);
               ++s;
             }
@@ -883,16 +887,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_frame(const FrameParams P) {
 
 }  // namespace
 
-bool frame_plan_gemv(FrameOp& op) {
+bool frame_plan_gemv(FrameOp& op, int stage) {
   const int eb = op.wt ? 1 : 2;
   const int rowbytes = op.K * eb;
-  if (rowbytes % 16 || rowbytes > kFrameStage) return false;
+  if (rowbytes % 16 || rowbytes > stage) return false;
   const int nch = rowbytes / 16;
-  const int jmax = op.wt ? 2 : 4;
-  op.J = (nch + kCT - 1) / kCT;
-  if (op.J > jmax) return false;
-  op.nt = (nch + op.J - 1) / op.J;
-  op.rs = std::max(1, kFrameStage / rowbytes);
+  // Most even split of the row's chunks over at most kCT threads (multiples
+  // of 32), at most 5 (bf16) or 3 (fp8) chunks per thread; ties go to more
+  // threads.
+  const int jmax = op.wt ? 3 : 5;
+  double best = -1.0;
+  op.J = 0;
+  for (int w = kCW; w >= 1; --w) {
+    const int nt = 32 * w, J = (nch + nt - 1) / nt;
+    if (J > jmax) continue;
+    const double eff = static_cast<double>(nch) / (static_cast<double>(nt) * J);
+    if (eff > best + 1e-9) {
+      best = eff;
+      op.J = J;
+      op.nt = nt;
+    }
+  }
+  if (op.J == 0) return false;
+  op.rs = std::max(1, stage / rowbytes);
   op.rs = std::min(op.rs, kRowBatch);
   op.unit = (op.epi == EPI_SWIGLU || op.epi == EPI_QKV) ? 2 : 1;
   return op.N % op.unit == 0;
@@ -905,8 +922,8 @@ int frame_union_bytes(int G, int D, int max_vocab) {
   return ((std::max({red, attn, sel}) + 127) / 128) * 128;
 }
 
-size_t frame_smem_bytes(int slots, int un_bytes) {
-  return (size_t)slots * kFrameStage + un_bytes + 2 * (size_t)slots * 8 + 32 * 4 + 16 * 8 + 16;
+size_t frame_smem_bytes(int slots, int stage, int un_bytes) {
+  return (size_t)slots * stage + un_bytes + 2 * (size_t)slots * 8 + 32 * 4 + 16 * 8 + 16;
 }
 
 cudaError_t frame_set_attributes() {
@@ -920,7 +937,7 @@ cudaError_t launch_frame(const FrameParams& p, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = frame_smem_bytes(p.slots, p.un_bytes);
+  cfg.dynamicSmemBytes = frame_smem_bytes(p.slots, p.stage, p.un_bytes);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -22,6 +22,7 @@
 // applied once to the finished dot product.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdlib>
 
 #include "common.cuh"
@@ -336,30 +337,6 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
   }
 }
 
-// Consumer threads for a row of nch 16-byte chunks: the multiple of 32 (up
-// to 512) that splits the chunks most evenly over at most 5 chunks per
-// thread; ties go to the count closest to 320 (enough warps to hide shared-
-// memory latency, few enough registers for two CTAs per SM).
-int choose_threads(int nch, int* J) {
-  int best_nt = 32, best_j = 5;
-  double best_eff = -1.0;
-  for (int w = 1; w <= kMaxConsumerWarps; ++w) {
-    const int nt = 32 * w;
-    const int j = (nch + nt - 1) / nt;
-    if (j > 5) continue;
-    const double eff = static_cast<double>(nch) / (static_cast<double>(nt) * j);
-    const bool better = eff > best_eff + 1e-9 ||
-                        (eff > best_eff - 1e-9 && std::abs(nt - 320) < std::abs(best_nt - 320));
-    if (better) {
-      best_eff = eff;
-      best_nt = nt;
-      best_j = j;
-    }
-  }
-  *J = best_j;
-  return best_nt;
-}
-
 template <int WT, int M, int J>
 cudaError_t launch_t(const GemvParams& p, int nt, int grid, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -444,34 +421,56 @@ int gemv_grid(const GemvParams& p, int num_sms) {
   return std::min(num_sms * p.ctas_per_sm, p.units);
 }
 
-// Two CTAs per SM (20 consumer warps, 2 x 80 KB rings) where registers and
-// shared memory allow it, else one CTA with a 160 KB ring: with only ten
-// consumer warps per SM the row reductions are latency-bound.
+// Splits of a row's chunks over consumer threads, most even first (multiples
+// of 32 threads, at most 5 chunks each); the plan takes the first split that
+// lets two CTAs share an SM (registers and shared memory), else the most even
+// one with a single CTA: with only one CTA's consumer warps per SM the row
+// reductions are latency-bound.
 void gemv_plan(GemvParams& p, int eb, int num_sms, int M) {
   (void)num_sms;
   p.unit = (p.epi == EPI_SWIGLU || p.epi == EPI_QKV) ? 2 : 1;
   p.units = p.N / p.unit;
   const int rowbytes = p.K * eb;
-  int J = 0;
-  const int nt = choose_threads(rowbytes / 16, &J);
-  p.ctas_per_sm = 1;
-  set_ring(p, rowbytes, kRingTwo);
-  int n = 0;
-  if (J >= 1 && J <= 5 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel_for(eb == 1 ? 1 : 0, M, J), nt + 32,
-                                                    gemv_smem_bytes(p, M)) == cudaSuccess &&
-      n >= 2) {
-    p.ctas_per_sm = 2;
-  } else {
-    (void)cudaGetLastError();
-    set_ring(p, rowbytes, kRingOne);
+  const int nch = rowbytes / 16;
+  struct Split {
+    int nt, J;
+    double eff;
+  };
+  Split cand[kMaxConsumerWarps];
+  int nc = 0;
+  for (int w = 1; w <= kMaxConsumerWarps; ++w) {
+    const int nt = 32 * w, J = (nch + nt - 1) / nt;
+    if (J > 5) continue;
+    cand[nc++] = {nt, J, static_cast<double>(nch) / (static_cast<double>(nt) * J)};
   }
+  std::stable_sort(cand, cand + nc, [](const Split& a, const Split& b) {
+    if (a.eff > b.eff + 1e-9) return true;
+    if (b.eff > a.eff + 1e-9) return false;
+    return std::abs(a.nt - 320) < std::abs(b.nt - 320);
+  });
+  set_ring(p, rowbytes, kRingTwo);
+  for (int i = 0; i < nc; ++i) {
+    if (cand[i].eff < 0.9) break;  // not worth a second CTA
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, kernel_for(eb == 1 ? 1 : 0, M, cand[i].J), cand[i].nt + 32, gemv_smem_bytes(p, M)) ==
+            cudaSuccess &&
+        n >= 2) {
+      p.ctas_per_sm = 2;
+      p.nt = cand[i].nt;
+      p.J = cand[i].J;
+      return;
+    }
+    (void)cudaGetLastError();
+  }
+  p.ctas_per_sm = 1;
+  p.nt = nc ? cand[0].nt : 32;
+  p.J = nc ? cand[0].J : 5;
+  set_ring(p, rowbytes, kRingOne);
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, cudaStream_t s) {
-  const int nch = p.K * (wt ? 1 : 2) / 16;
-  int J = 0;
-  const int nt = choose_threads(nch, &J);
+  const int J = p.J, nt = p.nt;
   if (J < 1 || J > 5 || M < 1 || M > 2) return cudaErrorInvalidValue;
   if (wt == 0) return M == 1 ? launch_j<0, 1>(p, J, nt, grid, pdl, s) : launch_j<0, 2>(p, J, nt, grid, pdl, s);
   return M == 1 ? launch_j<1, 1>(p, J, nt, grid, pdl, s) : launch_j<1, 2>(p, J, nt, grid, pdl, s);

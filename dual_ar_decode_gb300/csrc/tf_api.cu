@@ -122,7 +122,7 @@ struct tf_ctx {
   bool use_graph = true;          // false: persistent frame kernel (TF_DECODE_DRIVER=persistent)
   FrameOp* d_ops = nullptr;       // [4][kMaxOps]: decode/tail x greedy/top-k
   int n_ops[4] = {0, 0, 0, 0};
-  int frame_slots = 0, frame_union = 0;
+  int frame_slots = 0, frame_union = 0, frame_stage = 0;
   int S_frame = 1;
   uint32_t* gbar = nullptr;
   unsigned long long* trace = nullptr;  // [kMaxOps][2][3]
@@ -488,7 +488,7 @@ tf_status build_program(tf_ctx* c, bool decode, bool topk, std::vector<FrameOp>*
   end.advance = decode ? 1 : 0;
   ops.push_back(end);
   for (FrameOp& op : ops)
-    if (op.kind == OPK_GEMV && !frame_plan_gemv(op))
+    if (op.kind == OPK_GEMV && !frame_plan_gemv(op, c->frame_stage))
       return fail(c, TF_E_INVAL, "a GEMV shape does not fit the frame kernel");
   if ((int)ops.size() > kMaxOps) return fail(c, TF_E_INVAL, "op program too long");
   return TF_OK;
@@ -527,6 +527,7 @@ tf_status run_frames(tf_ctx* c, bool decode, const tf_sampling* s, int n_frames)
   P.rope = c->rope;
   P.eps = c->cfg.rms_eps;
   P.slots = c->frame_slots;
+  P.stage = c->frame_stage;
   P.un_bytes = c->frame_union;
   P.pos = &c->st->pos;
   P.frame_index = &c->st->frame_index;
@@ -550,7 +551,7 @@ tf_status run_frames(tf_ctx* c, bool decode, const tf_sampling* s, int n_frames)
   P.err = &c->st->err;
   P.trace = c->tracing ? c->trace : nullptr;
   CK(cudaMemsetAsync(c->gbar, 0, sizeof(uint32_t), c->stream));
-  CK(launch_frame(P, c->num_sms, c->stream));
+  CK(launch_frame(P, kFrameCtasPerSm * c->num_sms, c->stream));
   return TF_OK;
 }
 
@@ -710,10 +711,13 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   c->Vmax = std::max(c->Vs, c->Vc);
   c->sem_base = c->Vt - c->Vs;
   c->S_slow = std::max(1, std::min(64, 2 * c->num_sms / c->Hkv));
-  c->S_frame = std::max(1, std::min(c->S_slow, c->num_sms / c->Hkv));
+  c->S_frame = std::max(1, std::min(c->S_slow, kFrameCtasPerSm * c->num_sms / c->Hkv));
   c->frame_union = frame_union_bytes(c->Hq / c->Hkv, c->D, c->Vmax);
-  c->frame_slots = std::min(8, (int)((227 * 1024 - c->frame_union - 1024) / kFrameStage));
-  if (c->frame_slots < 2) {
+  // Two ring slots of up to 40 KB in what the union scratch leaves of a
+  // CTA's share; a slot must hold one whole weight row.
+  c->frame_slots = 2;
+  c->frame_stage = std::min(kFrameStage, ((kFrameSmemPerCta - c->frame_union - 1024) / 2) / 128 * 128);
+  if (c->frame_stage < std::max(c->H, std::max(c->Q, c->F)) * c->eb) {
     c->err = "frame kernel shared memory does not fit";
     return bail(TF_E_INVAL);
   }

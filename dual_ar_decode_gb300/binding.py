@@ -75,6 +75,8 @@ EXPORTS = {
                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+    "tf_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_gemv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]),
@@ -256,6 +258,10 @@ def op_select(logits_dev, n, vocab, sampling, frame, codebook0, sequence, ids_de
 def op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev, stream=0):
     _check(lib().tf_op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev,
                                  stream))
+
+
+def op_gemm(A_dev, W_dev, M, N, K, C_dev, stream=0):
+    _check(lib().tf_op_gemm(A_dev, W_dev, M, N, K, C_dev, stream))
 
 
 def op_gemv(W_dev, dtype, scale_dev, rows, cols, x_dev, y_dev, repeat=1, stream=0):

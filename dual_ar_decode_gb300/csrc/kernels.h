@@ -177,6 +177,14 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
 // Row-block GEMM on CUDA cores for prompts: out = epi(A[M][K] * W[N][K]^T)
 // with the GEMV's prologue/epilogue semantics (positions: row m at pos m).
 cudaError_t launch_gemm_rows(const GemvParams& p, int wt, int M, cudaStream_t s);
+// Tensor-core (tcgen05) GEMM for prompts, bf16 weights:
+// out = epi(A[M][K] * W[N][K]^T) with A given as bf16 hi/lo parts [M][K].
+bool gemm_tc_supported(int N, int K);
+size_t gemm_tc_smem_bytes();
+cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
+                           cudaStream_t s);
+// hi = bf16(a), lo = bf16(a - hi) elementwise.
+cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s);
 // a[m] = RMSNorm(x[m]) * w for M rows (prefill prologue).
 cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int M, int H,
                                 float eps, cudaStream_t s);

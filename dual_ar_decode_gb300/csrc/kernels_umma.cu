@@ -1,0 +1,302 @@
+// Tensor-core (tcgen05 / TMEM) GEMM for the prompt (sm_103a).
+//
+// Prefill runs every prompt token through the slow decoder (tuna-fish README,
+// "Inference speedtest": prefill is reported separately in tokens/s); its
+// linear layers are dense contractions C[m][n] = sum_k A[m][k] W[n][k] with
+// m over prompt tokens, so they belong on the 5th-generation tensor cores:
+//   * one CTA per 128 x 128 output tile; warp 0 streams 64-wide K slices of
+//     the activation tile and the weight tile into a 4-stage shared-memory
+//     ring with TMA tensor copies (128-byte swizzle), completion counted on
+//     mbarriers;
+//   * warp 1 owns 128 TMEM columns (the fp32 accumulator) and issues
+//     tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), four K=16 steps per slice;
+//     tcgen05.commit frees a stage once the MMAs reading it are done;
+//   * the activations enter as two bf16 parts (hi = bf16(a), lo = bf16(a -
+//     hi)) multiplied by the same weight slice, so the products keep about 16
+//     significant bits of the fp32 activations instead of 8;
+//   * warps 2-5 wait for the final commit, read the accumulator with
+//     tcgen05.ld (each warp its 32-lane quarter, one row per thread) and run
+//     the decode path's fused epilogues (RoPE + KV append, residual add,
+//     SwiGLU, store).
+// Every wait is bounded; the TMEM columns are always released.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace tf {
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int kStages = 4;
+constexpr int kTileA = BM * BK * 2;             // 16 KB (one bf16 part)
+constexpr int kTileW = BN * BK * 2;             // 16 KB
+constexpr int kStageBytes = 2 * kTileA + kTileW;  // A hi, A lo, W
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kTmemCols = 128;
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand tile in the 128-byte
+// swizzle layout that TMA writes (8-row groups of 128-byte rows, 1024 bytes
+// apart).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                // leading offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;        // stride between 8-row groups
+  d |= static_cast<uint64_t>(1) << 46;                // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
+// K-major, M = 128, N = BN.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_umma_gemm(const __grid_constant__ CUtensorMap map_ahi,
+                const __grid_constant__ CUtensorMap map_alo,
+                const __grid_constant__ CUtensorMap map_w, const GemvParams p, int M) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int nk = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % kStages;
+        if (k >= kStages && !mbar_wait(&empty[s], ((k / kStages) & 1) ^ 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tma_load_2d(st, &map_ahi, k * BK, m0, &full[s]);
+        tma_load_2d(st + kTileA, &map_alo, k * BK, m0, &full[s]);
+        tma_load_2d(st + 2 * kTileA, &map_w, k * BK, n0, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % kStages;
+        if (*abort_flag || !mbar_wait(&full[s], (k / kStages) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t st = smem_u32(smem + s * kStageBytes);
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t a_base = st + part * kTileA;
+          const uint32_t w_base = st + 2 * kTileA;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            mma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(w_base + kk * 32),
+                     (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&empty[s]);  // frees the stage when these MMAs are done
+      }
+      mma_commit(done);         // accumulator complete (or abandoned)
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const int m = m0 + row;
+    const bool ok = mbar_wait(done, 0, p.err);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok && !*abort_flag) {
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+        if (m >= M) continue;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const int n = n0 + c + i;
+          float v0 = v[i], v1 = v[i + 1];
+          if (p.scale) {
+            v0 *= __ldg(&p.scale[n]);
+            v1 *= __ldg(&p.scale[n + 1]);
+          }
+          if (p.epi == EPI_QKV) {
+            epi_qkv_pair(p, m, n >> 1, v0, v1);
+          } else if (p.epi == EPI_SWIGLU) {
+            p.out[(size_t)m * p.ldo + (n >> 1)] = silu(v0) * v1;
+          } else if (p.epi == EPI_RESID) {
+            p.out[(size_t)m * p.ldo + n] += v0;
+            p.out[(size_t)m * p.ldo + n + 1] += v1;
+          } else {
+            p.out[(size_t)m * p.ldo + n] = v0;
+            p.out[(size_t)m * p.ldo + n + 1] = v1;
+          }
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// Splits fp32 rows into bf16 hi and lo parts: hi = bf16(a), lo = bf16(a - hi).
+__global__ void k_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float x = a[i];
+    const uint16_t h = f32_to_bf16(x);
+    hi[i] = h;
+    lo[i] = f32_to_bf16(x - bf16_to_f32(h));
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(f);
+    else
+      (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// bf16 [rows][cols] row-major, box of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && encode_fn() != nullptr; }
+
+size_t gemm_tc_smem_bytes() { return 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 16; }
+
+cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s) {
+  const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
+  k_split_bf16<<<grid, 256, 0, s>>>(a, hi, lo, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
+                           cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_umma_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)gemm_tc_smem_bytes());
+    if (e) return e;
+    attr = true;
+  }
+  if (!gemm_tc_supported(p.N, p.K) || M < 1) return cudaErrorInvalidValue;
+  CUtensorMap ma_hi, ma_lo, mw;
+  if (!make_map(&ma_hi, a_hi, M, p.K, BM) || !make_map(&ma_lo, a_lo, M, p.K, BM) ||
+      !make_map(&mw, p.W, p.N, p.K, BN))
+    return cudaErrorInvalidValue;
+  dim3 grid((M + BM - 1) / BM, p.N / BN);
+  k_umma_gemm<<<grid, kThreads, gemm_tc_smem_bytes(), s>>>(ma_hi, ma_lo, mw, p, M);
+  return cudaGetLastError();
+}
+
+}  // namespace tf

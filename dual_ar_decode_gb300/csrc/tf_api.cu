@@ -105,6 +105,8 @@ struct tf_ctx {
   uint32_t* counters = nullptr;
   float *px = nullptr, *pa = nullptr, *pq = nullptr, *po = nullptr, *pu = nullptr;
   int32_t* tokens = nullptr;
+  uint16_t *a_hi = nullptr, *a_lo = nullptr;  // prompt GEMM inputs as bf16 hi / lo parts
+  bool prefill_tc = false;
   int32_t* hist = nullptr;
   DevState* st = nullptr;
   int S_slow = 1;
@@ -798,6 +800,13 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       dev_alloc_t(c, &c->d_ops, (size_t)4 * kMaxOps) || dev_alloc_t(c, &c->gbar, 1) ||
       dev_alloc_t(c, &c->trace, (size_t)kMaxOps * 6))
     return bail(TF_E_NOMEM);
+  // Tensor-core prompt GEMMs for bf16 weights whenever every shape tiles.
+  c->prefill_tc = !c->fp8 && gemm_tc_supported(c->QKV, c->H) && gemm_tc_supported(c->H, c->Q) &&
+                  gemm_tc_supported(2 * c->F, c->H) && gemm_tc_supported(c->H, c->F);
+  if (c->prefill_tc &&
+      (dev_alloc_t(c, &c->a_hi, (size_t)T * std::max({c->H, c->Q, c->F})) ||
+       dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F}))))
+    return bail(TF_E_NOMEM);
 
   // RoPE table: angle pos * theta^(-2i/D) evaluated in double, stored as float.
   {
@@ -1046,6 +1055,11 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
     p.pos_fixed = 0;
     p.rope = c->rope;
     p.err = &c->st->err;
+    if (c->prefill_tc) {
+      cudaError_t e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream);
+      if (e) return e;
+      return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
+    }
     return launch_gemm_rows(p, wt, P, c->stream);
   };
   for (const Layer& L : c->slow) {
@@ -1314,6 +1328,44 @@ tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, 
   cudaFree(cnt);
   cudaFree(err);
   if (r == TF_OK && e) r = TF_E_INVAL;
+  return r;
+}
+
+tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
+                     void* stream) {
+  if (!A || !W || !C || M < 1 || N < 1 || K < 1 || !gemm_tc_supported(N, K)) return TF_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t *hi = nullptr, *lo = nullptr;
+  uint32_t* err = nullptr;
+  const size_t n = (size_t)M * K;
+  if (cudaMalloc(&hi, n * 2) != cudaSuccess || cudaMalloc(&lo, n * 2) != cudaSuccess ||
+      cudaMalloc(&err, 4) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFree(hi);
+    cudaFree(lo);
+    cudaFree(err);
+    return TF_E_NOMEM;
+  }
+  tf_status r = TF_OK;
+  GemvParams p = {};
+  p.W = reinterpret_cast<const uint8_t*>(W);
+  p.N = N;
+  p.K = K;
+  p.epi = EPI_STORE;
+  p.out = C;
+  p.ldo = N;
+  p.err = err;
+  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || launch_split_bf16(A, hi, lo, n, s) != cudaSuccess ||
+      launch_gemm_tc(p, hi, lo, M, s) != cudaSuccess)
+    r = TF_E_CUDA;
+  uint32_t e = 0;
+  if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                     cudaStreamSynchronize(s) != cudaSuccess))
+    r = TF_E_CUDA;
+  cudaFree(hi);
+  cudaFree(lo);
+  cudaFree(err);
+  if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
   return r;
 }
 

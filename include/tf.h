@@ -254,6 +254,16 @@ tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, const uint1
                                   int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
                                   int32_t splits, float* out, void* stream);
 
+/* Prompt GEMM on the tensor cores (tcgen05, fp32 accumulation in TMEM), the
+ * prefill's matrix kernel: C[m][n] = sum_k A[m][k] W[n][k] for the prompt
+ * rows m.  A: float32 [M][K] device; W: bf16 bits [N][K] device; C: float32
+ * [M][N] device.  A is split into bf16 hi and lo parts that are both
+ * multiplied with W, so the result carries about 16 significant bits of A.
+ * N must be a multiple of 128 and K of 64.  Allocates and frees its scratch.
+ * Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA. */
+tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
+                     void* stream);
+
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
  * TF_DTYPE_BF16) or e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3);

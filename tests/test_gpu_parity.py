@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import oracle
-from dual_ar_decode_gb300 import Decoder, TfError, op_attention, op_gemv, op_quantize_fp8, op_select
+from dual_ar_decode_gb300 import (Decoder, TfError, op_attention, op_gemm, op_gemv,
+                                  op_quantize_fp8, op_select)
 from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
 from synth import FULL, TINY, make_logits, make_prompt, make_weights, f32_to_bf16_bits
 
@@ -142,6 +143,27 @@ def test_attention_matches_oracle(Hq, Hkv, D, rows, pos0, splits):
     for m in range(rows):
         ref = oracle.attention_row(q[m].reshape(Hq, D).astype(np.float64), K, V, pos0 + m + 1)
         assert np.allclose(got[m].reshape(Hq, D), ref, rtol=1e-4, atol=1e-5)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (200, 6144, 2560), (77, 2560, 9728),
+                                   (1, 256, 128), (300, 19456, 2560), (129, 2560, 4096)])
+def test_tensor_core_gemm_matches_oracle(M, N, K):
+    """The prompt GEMM (tcgen05 / TMEM) against A @ W^T in float64."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    Wb = f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32) * 0.02)
+    Ad = torch.from_numpy(A).to(DEV)
+    Wd = dev_u16(Wb)
+    C = torch.full((M, N), np.nan, dtype=torch.float32, device=DEV)
+    op_gemm(Ad.data_ptr(), Wd.data_ptr(), M, N, K, C.data_ptr())
+    ref = oracle.linear(oracle.bf16_bits_to_f64(Wb), A.astype(np.float64))
+    got = C.cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.isfinite(got).all()
+    # hi + lo bf16 parts carry A to ~2^-17 relative; fp32 tensor-core
+    # accumulation over up to 9728 terms adds about as much again
+    assert np.max(np.abs(got - ref)) <= 2e-4 * rms
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-5
 
 
 # ------------------------------------------------------------------ model

@@ -75,8 +75,18 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             j = json.load(f)
-        return {"hbm_gbs": float(j["hbm_gbs"]), "source": "of measured"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "of fallback"}
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j.get("bf16_tflops", 1900.0)),
+                "source": "of measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0, "source": "of fallback"}
+
+
+def prefill_flops(d, P: int) -> float:
+    """Algorithmic flops of a P-token prefill through the slow decoder:
+    2 * P * (linear weights of the 36 layers) + causal attention
+    (scores and weighted values, 2 * 2 * D per query-key pair and head)."""
+    lin = d.qkv_dim * d.hidden + d.hidden * d.q_dim + 3 * d.hidden * d.ffn
+    attn = 2 * 2 * d.n_heads * d.head_dim * P * (P + 1) / 2
+    return d.slow_layers * (2.0 * P * lin + attn)
 
 
 # ---------------------------------------------------------------- clocks
@@ -276,6 +286,20 @@ def main():
         dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
     e2e_value = e2e_frames * world / (float(e2e_t.item()) / 1e3)
 
+    # prefill throughput (prompt ids uploaded from the host, frame 0 returned)
+    pre_ms = []
+    for _ in range(3):
+        torch.cuda.synchronize(device)
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        dec.prefill(prompt, sampling)
+        p1.record(stream)
+        p1.synchronize()
+        pre_ms.append(p0.elapsed_time(p1))
+    pre = float(np.median(pre_ms))
+    pre_tflops = prefill_flops(d, wl.prefill) / (pre / 1e3) / 1e12
+
     bytes_avg = float(np.mean([frame_bytes(d, wl.weight_dtype, p)["total"] for p in positions]))
     frame_gbs = bytes_avg * value / world / 1e9
     page_gib = PAGE_LOAD_ELEMENTS * (1 if wl.weight_dtype == "fp8" else 2) / 2 ** 30
@@ -297,6 +321,12 @@ def main():
                        "l2": f"inputs larger than L2: {bytes_avg / 1e9:.2f} GB streamed per frame",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "tok_s": round(value, 3), "codebook_tok_s": round(10 * value, 3),
+            "prefill": {"tokens": wl.prefill, "ms": round(pre, 3),
+                        "tok_s": round(wl.prefill / (pre / 1e3), 1),
+                        "tflops": round(pre_tflops, 2), "bf16_peak_tflops": peaks["bf16_tflops"],
+                        "frac": round(pre_tflops / peaks["bf16_tflops"], 4),
+                        "note": "tcgen05 GEMMs (activations as bf16 hi+lo: tensor work is 2x the "
+                                "algorithmic flops) + attention + frame-0 tail"},
             "frame_hbm": {"bytes_per_frame": round(bytes_avg), "achieved_gbs": round(frame_gbs, 1),
                           "peak_gbs": peaks["hbm_gbs"], "frac": round(frame_gbs / peaks["hbm_gbs"], 4),
                           "peak_source": peaks["source"],

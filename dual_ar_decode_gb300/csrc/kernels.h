@@ -183,6 +183,8 @@ bool gemm_tc_supported(int N, int K);
 size_t gemm_tc_smem_bytes();
 cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
                            cudaStream_t s);
+// e4m3 codes -> bf16 bits of the same values (n even).
+cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaStream_t s);
 // hi = bf16(a), lo = bf16(a - hi) elementwise.
 cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s);
 // a[m] = RMSNorm(x[m]) * w for M rows (prefill prologue).

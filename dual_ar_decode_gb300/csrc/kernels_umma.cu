@@ -223,6 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// e4m3 codes -> bf16 bits of the same values (exact: every e4m3 value is a
+// bf16 value); the per-row scale is applied later, in the GEMM epilogue.
+__global__ void k_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n2) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n2;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const uint16_t v = reinterpret_cast<const uint16_t*>(q)[i];
+    const float2 f = e4m3x2_to_f32x2(v);
+    reinterpret_cast<uint32_t*>(out)[i] =
+        static_cast<uint32_t>(f32_to_bf16(f.x)) | (static_cast<uint32_t>(f32_to_bf16(f.y)) << 16);
+  }
+}
+
 // Splits fp32 rows into bf16 hi and lo parts: hi = bf16(a), lo = bf16(a - hi).
 __global__ void k_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -277,6 +289,12 @@ size_t gemm_tc_smem_bytes() { return 1024 + kStages * kStageBytes + (2 * kStages
 cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s) {
   const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
   k_split_bf16<<<grid, 256, 0, s>>>(a, hi, lo, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaStream_t s) {
+  const int grid = static_cast<int>(std::min<size_t>((n / 2 + 255) / 256, 8192));
+  k_e4m3_to_bf16<<<grid, 256, 0, s>>>(q, out, n / 2);
   return cudaGetLastError();
 }
 

@@ -106,6 +106,7 @@ struct tf_ctx {
   float *px = nullptr, *pa = nullptr, *pq = nullptr, *po = nullptr, *pu = nullptr;
   int32_t* tokens = nullptr;
   uint16_t *a_hi = nullptr, *a_lo = nullptr;  // prompt GEMM inputs as bf16 hi / lo parts
+  uint16_t* wconv = nullptr;  // fp8 weight converted to bf16 for one prompt GEMM
   bool prefill_tc = false;
   int32_t* hist = nullptr;
   DevState* st = nullptr;
@@ -801,11 +802,14 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       dev_alloc_t(c, &c->trace, (size_t)kMaxOps * 6))
     return bail(TF_E_NOMEM);
   // Tensor-core prompt GEMMs for bf16 weights whenever every shape tiles.
-  c->prefill_tc = !c->fp8 && gemm_tc_supported(c->QKV, c->H) && gemm_tc_supported(c->H, c->Q) &&
+  c->prefill_tc = gemm_tc_supported(c->QKV, c->H) && gemm_tc_supported(c->H, c->Q) &&
                   gemm_tc_supported(2 * c->F, c->H) && gemm_tc_supported(c->H, c->F);
   if (c->prefill_tc &&
       (dev_alloc_t(c, &c->a_hi, (size_t)T * std::max({c->H, c->Q, c->F})) ||
-       dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F}))))
+       dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F})) ||
+       (c->fp8 && dev_alloc_t(c, &c->wconv,
+                              std::max({(size_t)c->QKV * H, (size_t)H * c->Q, (size_t)2 * c->F * H,
+                                        (size_t)H * c->F})))))
     return bail(TF_E_NOMEM);
 
   // RoPE table: angle pos * theta^(-2i/D) evaluated in double, stored as float.
@@ -1058,6 +1062,10 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
     if (c->prefill_tc) {
       cudaError_t e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream);
       if (e) return e;
+      if (c->fp8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
+        if ((e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e;
+        p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+      }
       return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
     }
     return launch_gemm_rows(p, wt, P, c->stream);

@@ -189,14 +189,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--op", default=None, choices=["gemv"],
+    ap.add_argument("--op", default=None, choices=["gemv", "gemm"],
                     help="time one kernel on its own instead of the decode step")
     ap.add_argument("--rows", type=int, default=19456)
     ap.add_argument("--cols", type=int, default=2560)
     ap.add_argument("--fp8", action="store_true")
+    ap.add_argument("--m", type=int, default=1024, help="--op gemm: prompt rows")
     args = ap.parse_args()
     if args.op == "gemv":
         return run_gemv_case(args)
+    if args.op == "gemm":
+        return run_gemm_case(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -382,6 +385,39 @@ def run_gemv_case(args):
                       "us_per_launch": round(ms * 1e3, 3), "achieved_gbs": round(gbs, 1),
                       "peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
                       "peak_source": peaks["source"]}), flush=True)
+
+
+def run_gemm_case(args):
+    """The prompt GEMM alone (tf_op_gemm: tcgen05 tensor cores, activations
+    as bf16 hi + lo parts): C[m][rows] = A[m][cols] W[rows][cols]^T, W
+    steps times after W warm-up calls.  Prints one JSON line; tflops count
+    the algorithmic 2*m*rows*cols once."""
+    import torch
+    from dual_ar_decode_gb300 import op_gemm
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    A = torch.randn(args.m, args.cols, device=dev, generator=g)
+    W = (torch.randn(args.rows, args.cols, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    C = torch.empty(args.m, args.rows, device=dev)
+    for _ in range(args.warmup):
+        op_gemm(A.data_ptr(), W.data_ptr(), args.m, args.rows, args.cols, C.data_ptr())
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        op_gemm(A.data_ptr(), W.data_ptr(), args.m, args.rows, args.cols, C.data_ptr())
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    tflops = 2.0 * args.m * args.rows * args.cols / (ms / 1e3) / 1e12
+    peaks = measured_peaks()
+    print(json.dumps({"op": "gemm", "m": args.m, "rows": args.rows, "cols": args.cols,
+                      "ms_per_call": round(ms, 4), "tflops": round(tflops, 2),
+                      "bf16_peak_tflops": peaks["bf16_tflops"],
+                      "frac": round(tflops / peaks["bf16_tflops"], 4),
+                      "note": "per call: hi/lo split + GEMM; tensor work is 2x the algorithmic flops"}),
+          flush=True)
 
 
 def run_reference(args, wl, world, rank):

@@ -40,6 +40,7 @@ from synth import WORKLOADS, tensor_specs  # noqa: E402
 METRIC = "Dual-AR decode frames/s at batch 1; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 PAGE_LOAD_ELEMENTS = 7_377_351_168   # tuna-fish README, "Inference estimation"
+GATE_UP_TRAFFIC = 99_663_872 + 2_707_712  # ncu DRAM bytes per launch, gate/up-shaped k_gemv
 
 
 # ---------------------------------------------------------------- accounting
@@ -338,7 +339,10 @@ def main():
                          "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "peak_source": peaks["source"], "bytes_per_launch": prof_bytes,
-                         "ms_per_launch": round(prof_ms, 5), "traffic": None},
+                         "ms_per_launch": round(prof_ms, 5),
+                         # dram__bytes_read.sum + dram__bytes_write.sum of k_gemv<bf16,1,1> on the
+                         # 19456x2560 case (profiles/gemv_gate_up_19456x2560_bf16.md)
+                         "traffic": GATE_UP_TRAFFIC if wl.weight_dtype == "bf16" else None},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "frames/s",
                     "h2d_bytes_per_step": round((wl.prefill * 4 + 4 * (e2e_frames + 1)) / e2e_frames, 2),

@@ -44,10 +44,11 @@ GATE_UP_TRAFFIC = 99_663_872 + 2_707_712  # ncu DRAM bytes per launch, gate/up-s
 
 
 # ---------------------------------------------------------------- accounting
-def frame_bytes(d, weight_dtype: str, pos: int) -> dict:
-    """Algorithmic HBM bytes of one decode frame whose slow token sits at
+def frame_bytes(d, weight_dtype: str, pos: int, batch: int = 1) -> dict:
+    """Algorithmic HBM bytes of one decode step whose slow tokens sit at
     position `pos`: every weight streamed once (slow pass + 9 fast passes),
-    the valid KV rows read, the new KV rows written, embedding rows read."""
+    and for each of the `batch` sequences the valid KV rows read and the new
+    KV rows written (embedding rows are part of the weights)."""
     eb = 1 if weight_dtype == "fp8" else 2
     H, F = d.hidden, d.ffn
     lin_rows = d.qkv_dim + H + 2 * F + H
@@ -62,6 +63,7 @@ def frame_bytes(d, weight_dtype: str, pos: int) -> dict:
     kv_read += sum(d.fast_layers * 2 * kv_row * (j + 1) for j in range(1, d.n_codebooks))
     kv_write = d.slow_layers * 2 * kv_row + d.fast_layers * 2 * kv_row * (d.n_codebooks)
     weights = slow_w + (d.n_codebooks - 1) * fast_w
+    kv_read, kv_write = batch * kv_read, batch * kv_write
     return {"weights": weights, "kv_read": kv_read, "kv_write": kv_write,
             "total": weights + kv_read + kv_write}
 
@@ -162,9 +164,13 @@ def host_bits(tensors) -> dict:
 # ---------------------------------------------------------------- oracle leg
 def oracle_sample(wl, weights_bits, prompt, budget_s: float = 20.0) -> dict:
     """Oracle frames/s on a bounded sample: prefill (untimed), then decode
-    frames until `budget_s` of CPU time has passed (at least one)."""
+    frames until `budget_s` of CPU time has passed (at least one).  Batched
+    workloads: one sequence (the oracle has no batching; per-sequence frames
+    are the unit) with its prompt cut to 64 ids to bound the untimed part."""
     import oracle
     ref = oracle.DualAROracle(wl.dims, weights_bits, wl.weight_dtype)
+    if wl.batch > 1:
+        prompt = prompt[:1, :64]
     t0 = time.perf_counter()
     ref.prefill(prompt)
     t_prefill = time.perf_counter() - t0
@@ -223,10 +229,11 @@ def main():
         dist.init_process_group("nccl", device_id=device)
 
     tensors = device_weights(d, args.seed, device)
-    prompt = make_prompt(d, wl.prefill, seed=args.seed + rank)
+    B = wl.batch
+    prompt = make_prompt(d, wl.prefill, seed=args.seed + rank * B, batch=B)
     want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
     bits = host_bits(tensors) if want_cpu else None
-    dec = Decoder(d, wl.weight_dtype, device=local)
+    dec = Decoder(d, wl.weight_dtype, device=local, max_batch=B)
     dec.load_weights(tensors)
     del tensors
     torch.cuda.empty_cache()
@@ -264,12 +271,13 @@ def main():
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms = float(t.item())
-    frames_all = args.steps * world
+    frames_all = args.steps * world * B          # sequence-frames
     value = frames_all / (total_ms / 1e3)
     info = dec.info()
 
-    # dominant kernel, live: the slow gate/up GEMV in its in-frame configuration
-    prof_ms, prof_bytes = dec.profile_kernel(0, 4 * d.slow_layers)
+    # dominant kernel, live: the slow gate/up GEMV (batch 1) or skinny
+    # tensor-core GEMM (batch > 1) in its in-frame configuration
+    prof_ms, prof_bytes = dec.profile_kernel(0 if B == 1 else 4, 4 * d.slow_layers)
     peaks = measured_peaks()
     achieved = prof_bytes / (prof_ms / 1e3) / 1e9
 
@@ -288,7 +296,7 @@ def main():
     e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
     if world > 1:
         dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = e2e_frames * world / (float(e2e_t.item()) / 1e3)
+    e2e_value = e2e_frames * world * B / (float(e2e_t.item()) / 1e3)
 
     # prefill throughput (prompt ids uploaded from the host, frame 0 returned)
     pre_ms = []
@@ -302,10 +310,10 @@ def main():
         p1.synchronize()
         pre_ms.append(p0.elapsed_time(p1))
     pre = float(np.median(pre_ms))
-    pre_tflops = prefill_flops(d, wl.prefill) / (pre / 1e3) / 1e12
+    pre_tflops = B * prefill_flops(d, wl.prefill) / (pre / 1e3) / 1e12
 
-    bytes_avg = float(np.mean([frame_bytes(d, wl.weight_dtype, p)["total"] for p in positions]))
-    frame_gbs = bytes_avg * value / world / 1e9
+    bytes_avg = float(np.mean([frame_bytes(d, wl.weight_dtype, p, B)["total"] for p in positions]))
+    frame_gbs = bytes_avg * (value / B) / world / 1e9
     page_gib = PAGE_LOAD_ELEMENTS * (1 if wl.weight_dtype == "fp8" else 2) / 2 ** 30
     cpu = oracle_sample(wl, bits, prompt) if want_cpu else None
     dec.close()
@@ -325,8 +333,9 @@ def main():
                        "l2": f"inputs larger than L2: {bytes_avg / 1e9:.2f} GB streamed per frame",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "tok_s": round(value, 3), "codebook_tok_s": round(10 * value, 3),
-            "prefill": {"tokens": wl.prefill, "ms": round(pre, 3),
-                        "tok_s": round(wl.prefill / (pre / 1e3), 1),
+            "steps_per_s": round(value / B / world, 3),
+            "prefill": {"tokens": wl.prefill * B, "ms": round(pre, 3),
+                        "tok_s": round(B * wl.prefill / (pre / 1e3), 1),
                         "tflops": round(pre_tflops, 2), "bf16_peak_tflops": peaks["bf16_tflops"],
                         "frac": round(pre_tflops / peaks["bf16_tflops"], 4),
                         "note": "tcgen05 GEMMs (activations as bf16 hi+lo: tensor work is 2x the "
@@ -335,18 +344,19 @@ def main():
                           "peak_gbs": peaks["hbm_gbs"], "frac": round(frame_gbs / peaks["hbm_gbs"], 4),
                           "peak_source": peaks["source"],
                           "page_convention_gib_s": round(value / world * page_gib, 1)},
-            "roofline": {"kernel": "k_gemv (slow gate/up, RMSNorm prologue, SwiGLU epilogue)",
+            "roofline": {"kernel": "k_gemv (slow gate/up, RMSNorm prologue, SwiGLU epilogue)" if B == 1
+                         else f"k_umma_skinny (slow gate/up, {B} rows, split-K tcgen05, SwiGLU epilogue)",
                          "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "peak_source": peaks["source"], "bytes_per_launch": prof_bytes,
                          "ms_per_launch": round(prof_ms, 5),
                          # dram__bytes_read.sum + dram__bytes_write.sum of k_gemv<bf16,1,1> on the
                          # 19456x2560 case (profiles/gemv_gate_up_19456x2560_bf16.md)
-                         "traffic": GATE_UP_TRAFFIC if wl.weight_dtype == "bf16" else None},
+                         "traffic": GATE_UP_TRAFFIC if wl.weight_dtype == "bf16" and B == 1 else None},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "frames/s",
-                    "h2d_bytes_per_step": round((wl.prefill * 4 + 4 * (e2e_frames + 1)) / e2e_frames, 2),
-                    "d2h_bytes_per_step": 44,
+                    "h2d_bytes_per_step": round((B * wl.prefill * 4 + 4 * (e2e_frames + 1)) / e2e_frames, 2),
+                    "d2h_bytes_per_step": 4 + 40 * B,
                     "note": "tf_prefill (host prompt) + one tf_decode_frame per frame (host frame out)"},
             "gpu_launches": info["graph_nodes"] * args.steps,
             "clocks": clk,
@@ -430,7 +440,7 @@ def run_reference(args, wl, world, rank):
     from synth import make_prompt, make_weights
     d = wl.dims
     w = make_weights(d, args.seed)
-    prompt = make_prompt(d, wl.prefill, seed=args.seed)
+    prompt = make_prompt(d, wl.prefill, seed=args.seed, batch=wl.batch)
     per_step = []
     for _ in range(args.warmup + args.steps if d.slow_layers <= 2 else 1):
         s = oracle_sample(wl, w, prompt, budget_s=10.0)

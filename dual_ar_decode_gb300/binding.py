@@ -77,6 +77,9 @@ EXPORTS = {
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+    "tf_op_gemm_skinny": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                         ctypes.c_void_p]),
     "tf_op_gemv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]),
@@ -145,9 +148,10 @@ def _ptr(a):
 class Decoder:
     """One decode context (tf_create ... tf_destroy)."""
 
-    def __init__(self, dims, weight_dtype: str = "bf16", device: int = 0):
+    def __init__(self, dims, weight_dtype: str = "bf16", device: int = 0, max_batch: int = 1):
         self.dims = dims
-        self.cfg = config_from_dims(dims, weight_dtype)
+        self.cfg = config_from_dims(dims, weight_dtype, max_batch)
+        self.batch = 1  # sequences of the last prefill
         h = ctypes.c_void_p()
         _check(lib().tf_create(ctypes.byref(self.cfg), device, ctypes.byref(h)), None)
         self.h = h
@@ -196,11 +200,13 @@ class Decoder:
         s = _sampling(sampling)
         _check(lib().tf_prefill(self.h, _ptr(tok), tok.shape[0], tok.shape[1], ctypes.byref(s),
                                 _ptr(fo), _ptr(frame), _ptr(lg)), self.h)
+        self.batch = tok.shape[0]
         return frame, lg
 
     def decode_frame(self, sampling=None, forced=None, logits=False):
-        frame = np.zeros((1, self.ncb), np.int32)
-        lg = np.zeros((1, self.ncb, self.vmax), np.float32) if logits else None
+        B = self.batch
+        frame = np.zeros((B, self.ncb), np.int32)
+        lg = np.zeros((B, self.ncb, self.vmax), np.float32) if logits else None
         fo = None if forced is None else np.ascontiguousarray(forced, dtype=np.int32)
         s = _sampling(sampling)
         _check(lib().tf_decode_frame(self.h, ctypes.byref(s), _ptr(fo), _ptr(frame), _ptr(lg)),
@@ -208,7 +214,7 @@ class Decoder:
         return frame, lg
 
     def decode_frames(self, n: int, sampling=None, out=None):
-        frames = out if out is not None else np.zeros((n, 1, self.ncb), np.int32)
+        frames = out if out is not None else np.zeros((n, self.batch, self.ncb), np.int32)
         s = _sampling(sampling)
         _check(lib().tf_decode_frames(self.h, ctypes.byref(s), n, _ptr(frames)), self.h)
         return frames
@@ -262,6 +268,10 @@ def op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev
 
 def op_gemm(A_dev, W_dev, M, N, K, C_dev, stream=0):
     _check(lib().tf_op_gemm(A_dev, W_dev, M, N, K, C_dev, stream))
+
+
+def op_gemm_skinny(A_dev, W_dev, M, N, K, C_dev, stream=0):
+    _check(lib().tf_op_gemm_skinny(A_dev, W_dev, M, N, K, C_dev, stream))
 
 
 def op_gemv(W_dev, dtype, scale_dev, rows, cols, x_dev, y_dev, repeat=1, stream=0):

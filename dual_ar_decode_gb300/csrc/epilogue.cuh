@@ -6,8 +6,15 @@
 
 namespace tf {
 
+// Position of activation row m: rows are grouped by sequence (p.rps rows
+// each, consecutive positions from the shared base) or all belong to one.
 __device__ __forceinline__ int row_pos(const GemvParams& p, int m) {
-  return (p.pos_ptr ? __ldg(p.pos_ptr) : p.pos_fixed) + m;
+  return (p.pos_ptr ? __ldg(p.pos_ptr) : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
+}
+
+// Offset of row m's sequence in the KV caches.
+__device__ __forceinline__ size_t row_kv_offset(const GemvParams& p, int m) {
+  return p.rps > 0 ? static_cast<size_t>(m / p.rps) * static_cast<size_t>(p.kv_seq) : 0;
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -75,16 +82,30 @@ __device__ __forceinline__ void epi_qkv_pair(const GemvParams& p, int m, int pai
       q[i] = r0;
       q[i + half] = r1;
     } else {
-      uint16_t* k = p.Kc + ((size_t)h * p.T + pos) * p.head_dim;
+      uint16_t* k = p.Kc + row_kv_offset(p, m) + ((size_t)h * p.T + pos) * p.head_dim;
       k[i] = f32_to_bf16(r0);
       k[i + half] = f32_to_bf16(r1);
     }
   } else {
     const int d0 = 2 * (pair - qp - kp);
     const int g = d0 / p.head_dim, d = d0 - g * p.head_dim;
-    uint16_t* v = p.Vc + ((size_t)g * p.T + pos) * p.head_dim + d;
+    uint16_t* v = p.Vc + row_kv_offset(p, m) + ((size_t)g * p.T + pos) * p.head_dim + d;
     v[0] = f32_to_bf16(v0);
     v[1] = f32_to_bf16(v1);
+  }
+}
+
+// SwiGLU output u = silu(gate) * up of row m, column i: fp32, or bf16 hi / lo
+// parts when the next GEMM reads it from the tensor cores.
+__device__ __forceinline__ void epi_swiglu(const GemvParams& p, int m, int i, float g, float u) {
+  const float v = silu(g) * u;
+  const size_t o = (size_t)m * p.ldo + i;
+  if (p.out_hi) {
+    const uint16_t h = f32_to_bf16(v);
+    p.out_hi[o] = h;
+    p.out_lo[o] = f32_to_bf16(v - bf16_to_f32(h));
+  } else {
+    p.out[o] = v;
   }
 }
 

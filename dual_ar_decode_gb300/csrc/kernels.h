@@ -50,6 +50,8 @@ struct GemvParams {
   int32_t epi;
   float* out;            // [M][ldo]
   int32_t ldo;
+  uint16_t* out_hi;      // EPI_SWIGLU: if set, the result goes out as bf16
+  uint16_t* out_lo;      // hi / lo parts [M][ldo] instead of fp32 to out
   // EPI_QKV
   int32_t q_dim, kv_dim, head_dim;
   float* qout;           // [M][q_dim]
@@ -58,6 +60,10 @@ struct GemvParams {
   int32_t T;
   const int32_t* pos_ptr;  // row m sits at position pos_ptr[0] + m, or
   int32_t pos_fixed;       // pos_fixed + m when pos_ptr is null
+  int32_t rps;           // rows per sequence: > 0 -> row m is row m % rps of
+                         // sequence m / rps (position base + m % rps, KV cache
+                         // Kc/Vc + (m / rps) * kv_seq); 0 -> one sequence
+  int64_t kv_seq;        // elements between two sequences' caches
   const float2* rope;    // [T][head_dim/2] (cos, sin)
   // EPI_LOGITS
   int32_t select;        // 1: argmax -> sel[cb], fb[cb]
@@ -91,20 +97,25 @@ struct AttnParams {
   int32_t T, Hq, Hkv, D;
   const int32_t* pos_ptr;
   int32_t pos_fixed;
+  int32_t rps;           // rows per sequence (as GemvParams::rps)
+  int64_t kv_seq;        // elements between two sequences' caches
   int32_t S;             // splits over the key range (grid.x)
   float* part;           // [M][Hq][S][D + 2] partial (m, l, acc)
   uint32_t* counters;    // [M][Hkv], zero between launches
   float* out;            // [M][Hq*D]
+  uint16_t* out_hi;      // if set: the output as bf16 hi / lo parts [M][Hq*D]
+  uint16_t* out_lo;      // instead of fp32 to out
   uint32_t* err;
 };
 cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t s);
 
 // ----------------------------------------------------------------- misc
-// Builds the input rows of a decoder pass.
+// Builds the input rows of a decoder pass.  Sequence b's ids sit at
+// ids[b * id_stride] (the slot of the codebook the pass feeds from).
 enum BuildMode : int32_t {
-  BUILD_SLOW = 0,    // x[0] = text_embed[sem_base + fb[0]]
-  BUILD_FAST1 = 1,   // x[0] = RMSNorm(xs) * w_final; x[1] = cb_embed[0][fb[0]]
-  BUILD_FASTJ = 2,   // x[0] = cb_embed[j-1][fb[j-1]]
+  BUILD_SLOW = 0,    // x[b] = text_embed[sem_base + fb_b[0]]
+  BUILD_FAST1 = 1,   // x[2b] = RMSNorm(xs[b]) * w_final; x[2b+1] = cb_embed[0][fb_b[0]]
+  BUILD_FASTJ = 2,   // x[b] = cb_embed[j-1][fb_b[j-1]]
   BUILD_TOKENS = 3,  // x[m] = text_embed[tokens[m]]  (prefill)
 };
 struct BuildParams {
@@ -113,7 +124,8 @@ struct BuildParams {
   int32_t table_rows;      // rows the id may address
   int32_t row_base;        // added to the id (sem_base for BUILD_SLOW)
   const int32_t* ids;      // id source (fb slot, or tokens for BUILD_TOKENS)
-  const float* xs;         // slow residual (BUILD_FAST1)
+  int32_t id_stride;       // ids between two sequences' slots
+  const float* xs;         // slow residuals [B][H] (BUILD_FAST1)
   const uint16_t* nw;      // final slow norm (BUILD_FAST1)
   float eps;
   float* x;                // output rows [M][H]
@@ -122,12 +134,14 @@ struct BuildParams {
 cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s);
 
 // Per-frame bookkeeping after the last codebook: pos += advance,
-// frame_index += 1, history[hist_idx++] = sel.
+// frame_index += 1, history[hist_idx++] = sel of every sequence.
 struct FrameEndParams {
   int32_t* pos;
   int32_t advance;
   int32_t* frame_index;
-  const int32_t* sel;
+  const int32_t* sel;    // sequence b's ids at sel[b * sel_stride]
+  int32_t sel_stride;
+  int32_t nseq;          // history row = [nseq][ncb]
   int32_t ncb;
   int32_t* hist;         // [hist_cap][ncb]
   int32_t* hist_idx;
@@ -144,8 +158,11 @@ struct SelectParams {
   uint32_t key0, key1;   // Philox key (seed low / high)
   const int32_t* frame_ptr;  // frame index from device (or null -> frame)
   int32_t frame;
-  int32_t codebook0;     // row i uses codebook0 + i
+  int32_t codebook0;     // row i uses codebook0 + i (seq_rows = 0)
   int32_t sequence;
+  int32_t seq_rows;      // 1: row i is sequence `sequence + i` at codebook0,
+                         // its slots sel/fb/forced[i * id_stride]
+  int32_t id_stride;
   int32_t* sel;          // [n]
   int32_t* fb;           // [n] fed-back ids or null
   const int32_t* forced;
@@ -183,6 +200,21 @@ bool gemm_tc_supported(int N, int K);
 size_t gemm_tc_smem_bytes();
 cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
                            cudaStream_t s);
+// Skinny tensor-core GEMM for batched decode (M <= 64 activation rows):
+// out = epi(A[M][K] * W[N][K]^T), the weight rows on the MMA's 128-row side,
+// the activation rows (bf16 hi / lo parts, [M][K]) on its N side, split over K
+// so that the grid covers the GPU; the last CTA of a weight tile sums the
+// splits' partials in split order (part: skinny_part_floats(), tickets: one
+// per weight tile, zero between launches).
+int skinny_splits(int N, int K, int num_sms);
+size_t skinny_part_floats(int N, int K, int M, int num_sms);
+cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo,
+                               int M, float* part, uint32_t* tickets, int num_sms, bool pdl,
+                               cudaStream_t s);
+// a = RMSNorm(x[m]) * w (w null: a = x[m]) for M rows x[m * ldx], written as
+// bf16 hi / lo parts [M][K].
+cudaError_t launch_rows_split(const float* x, int ldx, int M, int K, const uint16_t* w, float eps,
+                              uint16_t* hi, uint16_t* lo, bool pdl, cudaStream_t s);
 // e4m3 codes -> bf16 bits of the same values (n even).
 cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaStream_t s);
 // hi = bf16(a), lo = bf16(a - hi) elementwise.

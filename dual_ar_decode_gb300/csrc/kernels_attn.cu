@@ -28,6 +28,18 @@ constexpr int kWarps = 8;
 constexpr int kUnroll = 4;
 constexpr int kMinKeys = 32;
 
+// Output element i of row data: fp32, or bf16 hi / lo parts for a GEMM that
+// reads its activations from the tensor cores.
+__device__ __forceinline__ void store_out(const AttnParams& p, size_t i, float v) {
+  if (p.out_hi) {
+    const uint16_t h = f32_to_bf16(v);
+    p.out_hi[i] = h;
+    p.out_lo[i] = f32_to_bf16(v - bf16_to_f32(h));
+  } else {
+    p.out[i] = v;
+  }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
   constexpr int DL = D / 32;  // dims per lane
@@ -40,7 +52,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
 
   pdl_launch_dependents();
   pdl_wait();
-  const int pos = (p.pos_ptr ? p.pos_ptr[0] : p.pos_fixed) + m;
+  // Row m is row m % rps of sequence m / rps (rps = 0: one sequence).
+  const int pos = (p.pos_ptr ? p.pos_ptr[0] : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
+  const size_t kvo = p.rps > 0 ? static_cast<size_t>(m / p.rps) * static_cast<size_t>(p.kv_seq) : 0;
   if (pos < 0 || pos >= p.T) {
     if (tid == 0 && s == 0) atomicOr(p.err, ERR_BAD_POS);
     return;
@@ -71,8 +85,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
     for (int d = 0; d < DL; ++d) acc[h][d] = 0.f;
   }
 
-  const uint16_t* Kg = p.Kc + (size_t)g * p.T * D + lane * DL;
-  const uint16_t* Vg = p.Vc + (size_t)g * p.T * D + lane * DL;
+  const uint16_t* Kg = p.Kc + kvo + (size_t)g * p.T * D + lane * DL;
+  const uint16_t* Vg = p.Vc + kvo + (size_t)g * p.T * D + lane * DL;
   for (int t0 = k0 + warp * kUnroll; t0 < k1; t0 += kWarps * kUnroll) {
     // Load up to kUnroll rows of K and V (DL bf16 per lane).
     uint32_t kr[kUnroll][DL / 2], vr[kUnroll][DL / 2];
@@ -154,7 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
   if (sact == 1) {
     for (int e = tid; e < G * D; e += kWarps * 32) {
       const int h = e / D, d = e - h * D;
-      p.out[(size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d] = sm_f[h][d] / sm_f[h][D + 1];
+      store_out(p, (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d, sm_f[h][d] / sm_f[h][D + 1]);
     }
     return;
   }
@@ -184,7 +198,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
       Ls += __ldcg(ph + (size_t)j * (D + 2) + D + 1) * f;
       A += __ldcg(ph + (size_t)j * (D + 2) + d) * f;
     }
-    p.out[(size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d] = A / Ls;
+    store_out(p, (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d, A / Ls);
   }
   if (tid == 0) p.counters[m * p.Hkv + g] = 0u;
 }

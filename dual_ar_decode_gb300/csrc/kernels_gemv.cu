@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
             v1 *= __ldg(&p.scale[rg + 1]);
           }
           if (p.epi == EPI_SWIGLU) {
-            p.out[(size_t)m * p.ldo + (rg >> 1)] = silu(v0) * v1;
+            epi_swiglu(p, m, rg >> 1, v0, v1);
           } else {  // EPI_QKV
             epi_qkv_pair(p, m, rg >> 1, v0, v1);
           }

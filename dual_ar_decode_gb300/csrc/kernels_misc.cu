@@ -39,7 +39,8 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 }
 
 // ------------------------------------------------------------------ build
-// Rows that start a decoder pass (see BuildMode).  fp32 residual rows.
+// Rows that start a decoder pass (see BuildMode).  fp32 residual rows; one
+// CTA per row.
 __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
   __shared__ float red[32];
   pdl_launch_dependents();
@@ -47,18 +48,25 @@ __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
   const int tid = threadIdx.x;
   const int m = blockIdx.x;
   float* xo = p.x + (size_t)m * p.H;
-  if (p.mode == BUILD_FAST1 && m == 0) {
-    // h = RMSNorm(slow residual) * w_final: the vector the semantic head reads.
-    float ss = 0.f;
-    for (int k = tid; k < p.H; k += blockDim.x) ss = fmaf(p.xs[k], p.xs[k], ss);
-    ss = block_sum_256(ss, red);
-    const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
-    for (int k = tid; k < p.H; k += blockDim.x) xo[k] = p.xs[k] * rstd * bf16_to_f32(p.nw[k]);
-    return;
-  }
   int id;
-  if (p.mode == BUILD_TOKENS) id = p.ids[m];
-  else id = p.ids[0];
+  if (p.mode == BUILD_FAST1) {
+    const int b = m >> 1;
+    if ((m & 1) == 0) {
+      // h = RMSNorm(slow residual) * w_final: the vector the semantic head reads.
+      const float* xs = p.xs + (size_t)b * p.H;
+      float ss = 0.f;
+      for (int k = tid; k < p.H; k += blockDim.x) ss = fmaf(xs[k], xs[k], ss);
+      ss = block_sum_256(ss, red);
+      const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
+      for (int k = tid; k < p.H; k += blockDim.x) xo[k] = xs[k] * rstd * bf16_to_f32(p.nw[k]);
+      return;
+    }
+    id = p.ids[(size_t)b * p.id_stride];
+  } else if (p.mode == BUILD_TOKENS) {
+    id = p.ids[m];
+  } else {
+    id = p.ids[(size_t)m * p.id_stride];
+  }
   if (id < 0 || id >= p.table_rows) {
     if (tid == 0) atomicOr(p.err, ERR_BAD_ID);
     id = 0;
@@ -77,7 +85,9 @@ __global__ void k_frame_end(const FrameEndParams p) {
     if (p.hist) {
       const int i = *p.hist_idx;
       if (i < p.hist_cap) {
-        for (int c = 0; c < p.ncb; ++c) p.hist[(size_t)i * p.ncb + c] = p.sel[c];
+        for (int b = 0; b < p.nseq; ++b)
+          for (int c = 0; c < p.ncb; ++c)
+            p.hist[((size_t)i * p.nseq + b) * p.ncb + c] = p.sel[(size_t)b * p.sel_stride + c];
         *p.hist_idx = i + 1;
       }
     }
@@ -257,9 +267,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
       float S = 0.f;
       for (int j = 0; j < k; ++j) S = __fadd_rn(S, wts[j]);
       const int frame = p.frame_ptr ? *p.frame_ptr : p.frame;
-      const uint32_t w0 = philox_w0(static_cast<uint32_t>(frame),
-                                    static_cast<uint32_t>(p.codebook0 + row),
-                                    static_cast<uint32_t>(p.sequence), 0u, p.key0, p.key1);
+      const uint32_t cb = static_cast<uint32_t>(p.seq_rows ? p.codebook0 : p.codebook0 + row);
+      const uint32_t sq = static_cast<uint32_t>(p.seq_rows ? p.sequence + row : p.sequence);
+      const uint32_t w0 = philox_w0(static_cast<uint32_t>(frame), cb, sq, 0u, p.key0, p.key1);
       const float u = __fmul_rn(static_cast<float>(w0 >> 8), 5.9604644775390625e-8f);  // 2^-24
       const float t = __fmul_rn(u, S);
       int pk = k - 1;
@@ -277,8 +287,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
     pick = static_cast<int>(s_prefix);
   }
   if (tid == 0) {
-    p.sel[row] = pick;
-    if (p.fb) p.fb[row] = (p.forced_on && *p.forced_on) ? p.forced[row] : pick;
+    const size_t slot = p.seq_rows ? (size_t)row * p.id_stride : (size_t)row;
+    p.sel[slot] = pick;
+    if (p.fb) p.fb[slot] = (p.forced_on && *p.forced_on) ? p.forced[slot] : pick;
   }
 }
 
@@ -355,6 +366,31 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* x, const uint
   const float rstd = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
   for (int k = threadIdx.x; k < H; k += blockDim.x)
     a[(size_t)m * H + k] = xm[k] * rstd * bf16_to_f32(w[k]);
+}
+
+// Activation rows for the skinny tensor-core GEMM: a = RMSNorm(x[m]) * w (or
+// x[m] when w is null) as bf16 hi / lo parts; one CTA per row.
+__global__ void __launch_bounds__(256) k_rows_split(const float* x, int ldx, int K,
+                                                    const uint16_t* w, float eps, uint16_t* hi,
+                                                    uint16_t* lo) {
+  __shared__ float red[32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int m = blockIdx.x;
+  const float* xm = x + (size_t)m * ldx;
+  float rstd = 1.0f;
+  if (w) {
+    float ss = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
+    ss = block_sum_256(ss, red);
+    rstd = 1.0f / sqrtf(ss / static_cast<float>(K) + eps);
+  }
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const float a = w ? xm[k] * rstd * bf16_to_f32(w[k]) : xm[k];
+    const uint16_t h = f32_to_bf16(a);
+    hi[(size_t)m * K + k] = h;
+    lo[(size_t)m * K + k] = f32_to_bf16(a - bf16_to_f32(h));
+  }
 }
 
 // C[m][n] = sum_k A[m][k] W[n][k], 64x64 tile per CTA, 4x4 per thread,
@@ -437,7 +473,7 @@ __global__ void __launch_bounds__(256) k_gemm_rows(const GemvParams p, int M) {
       if (p.epi == EPI_QKV) {
         epi_qkv_pair(p, m, n >> 1, v0, v1);
       } else if (p.epi == EPI_SWIGLU) {
-        p.out[(size_t)m * p.ldo + (n >> 1)] = silu(v0) * v1;
+        epi_swiglu(p, m, n >> 1, v0, v1);
       } else if (p.epi == EPI_RESID) {
         p.out[(size_t)m * p.ldo + n] += v0;
         p.out[(size_t)m * p.ldo + n + 1] += v1;
@@ -495,6 +531,15 @@ cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int
                                 float eps, cudaStream_t s) {
   k_rmsnorm_rows<<<M, 256, 0, s>>>(x, w, a, H, eps);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rows_split(const float* x, int ldx, int M, int K, const uint16_t* w, float eps,
+                              uint16_t* hi, uint16_t* lo, bool pdl, cudaStream_t s) {
+  if (M < 1) return cudaSuccess;
+  if (cudaError_t e = carveout(k_rows_split)) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), 0, pdl, s, attr);
+  return cudaLaunchKernelEx(&cfg, k_rows_split, x, ldx, K, w, eps, hi, lo);
 }
 
 cudaError_t launch_gemm_rows(const GemvParams& p, int wt, int M, cudaStream_t s) {

@@ -19,9 +19,15 @@
 //     the decode path's fused epilogues (RoPE + KV append, residual add,
 //     SwiGLU, store).
 // Every wait is bounded; the TMEM columns are always released.
+//
+// Batched decode (several sequences in lockstep, one row each per step) turns
+// every decode GEMV into a skinny GEMM with M = 16..64 rows: k_umma_skinny
+// swaps the operands (weight rows on the MMA's 128-row side, activation rows
+// on its N side) and splits K so that the grid covers the GPU; see there.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -110,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* consumed = tmem_slot + 2;  // K slices the MMA warp took
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
+    *consumed = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -139,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      int issued = 0;
       for (int k = 0; k < nk; ++k) {
         const int s = k % kStages;
         if (k >= kStages && !mbar_wait(&empty[s], ((k / kStages) & 1) ^ 1, p.err)) {
@@ -150,7 +159,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(st, &map_ahi, k * BK, m0, &full[s]);
         tma_load_2d(st + kTileA, &map_alo, k * BK, m0, &full[s]);
         tma_load_2d(st + 2 * kTileA, &map_w, k * BK, n0, &full[s]);
+        issued = k + 1;
       }
+      // After an abort, let the copies still in flight land before the CTA
+      // leaves (bounded).
+      if (*abort_flag)
+        for (int k = static_cast<int>(*consumed); k < issued; ++k)
+          if (!mbar_wait(&full[k % kStages], (k / kStages) & 1, p.err)) break;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -161,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           break;
         }
+        *consumed = static_cast<uint32_t>(k + 1);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t st = smem_u32(smem + s * kStageBytes);
 #pragma unroll
@@ -182,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int m = m0 + row;
-    const bool ok = mbar_wait(done, 0, p.err);
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok && !*abort_flag) {
+    if (ok) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
         float v[16];
@@ -201,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.epi == EPI_QKV) {
             epi_qkv_pair(p, m, n >> 1, v0, v1);
           } else if (p.epi == EPI_SWIGLU) {
-            p.out[(size_t)m * p.ldo + (n >> 1)] = silu(v0) * v1;
+            epi_swiglu(p, m, n >> 1, v0, v1);
           } else if (p.epi == EPI_RESID) {
             p.out[(size_t)m * p.ldo + n] += v0;
             p.out[(size_t)m * p.ldo + n + 1] += v1;
@@ -219,6 +235,258 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+}
+
+// ---------------------------------------------------------------- skinny GEMM
+// D[n][m] = sum_k W[n][k] a[m][k] for one 128-row weight tile and one slice of
+// K per CTA (grid: weight tiles x K splits).  Warp 0 streams 64-wide K slices
+// of the weight tile and of the activation rows (hi and lo parts) into a
+// 4-stage ring; warp 1 issues tcgen05.mma with the weight slice as the
+// 128-row A operand and the NB activation rows as the N = NB operand, so one
+// accumulator column per activation row; warps 2-5 read their TMEM lane
+// quarter (one weight row per thread, NB values).  With more than one split
+// each CTA stores its partial [128][NB] and takes a ticket; the last CTA of
+// the tile adds the partials in split order (deterministic) and runs the
+// epilogue.  Rows n >= N and k >= K come in as zeros (TMA out-of-bounds fill).
+constexpr int kSkStages = 4;
+constexpr int kSkThreads = 6 * 32;
+
+template <int NB>
+struct Skinny {
+  static constexpr int kW = 128 * BK * 2;            // weight slice, 16 KB
+  static constexpr int kA = NB * BK * 2;             // one activation part
+  static constexpr int kStage = kW + 2 * kA;
+  static constexpr uint32_t kCols = NB < 32 ? 32u : static_cast<uint32_t>(NB);
+  // kind::f16, fp32 accumulate, bf16 A and B, both K-major, M = 128, N = NB.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  static constexpr size_t kSmem = 1024 + (size_t)kSkStages * kStage + (2 * kSkStages + 1) * 8 + 32;
+};
+
+template <int NB>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    k_umma_skinny(const __grid_constant__ CUtensorMap map_w,
+                  const __grid_constant__ CUtensorMap map_ahi,
+                  const __grid_constant__ CUtensorMap map_alo, const GemvParams p, int M, int S,
+                  float* part, uint32_t* tickets) {
+  using C = Skinny<NB>;
+  static_assert(C::kStage % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSkStages * C::kStage);
+  uint64_t* empty = full + kSkStages;
+  uint64_t* done = empty + kSkStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* last_flag = tmem_slot + 2;
+  volatile uint32_t* consumed = tmem_slot + 3;   // k slices the MMA warp took
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int n0 = tile * 128;
+  const int nk = (p.K + BK - 1) / BK;
+  const int kb0 = static_cast<int>((int64_t)split * nk / S);
+  const int kb1 = static_cast<int>((int64_t)(split + 1) * nk / S);
+  const int nkb = kb1 - kb0;
+  const size_t Np = (size_t)gridDim.x * 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSkStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      // The weights do not depend on the previous kernel: fill the ring with
+      // weight slices first, then wait for the activations' producer.
+      const int pre = nkb < kSkStages ? nkb : kSkStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], C::kStage);
+        tma_load_2d_hint(smem + i * C::kStage, &map_w, (kb0 + i) * BK, n0, &full[i], pol);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* st = smem + i * C::kStage;
+        tma_load_2d(st + C::kW, &map_ahi, (kb0 + i) * BK, 0, &full[i]);
+        tma_load_2d(st + C::kW + C::kA, &map_alo, (kb0 + i) * BK, 0, &full[i]);
+      }
+      int issued = pre;
+      for (int i = pre; i < nkb; ++i) {
+        const int s = i % kSkStages;
+        if (!mbar_wait(&empty[s], ((i / kSkStages) & 1) ^ 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* st = smem + s * C::kStage;
+        mbar_arrive_expect_tx(&full[s], C::kStage);
+        tma_load_2d_hint(st, &map_w, (kb0 + i) * BK, n0, &full[s], pol);
+        tma_load_2d(st + C::kW, &map_ahi, (kb0 + i) * BK, 0, &full[s]);
+        tma_load_2d(st + C::kW + C::kA, &map_alo, (kb0 + i) * BK, 0, &full[s]);
+        issued = i + 1;
+      }
+      // After an abort, let the copies still in flight land before the CTA
+      // leaves (bounded).
+      const int from = static_cast<int>(*consumed);
+      if (*abort_flag)
+        for (int i = from; i < issued; ++i)
+          if (!mbar_wait(&full[i % kSkStages], (i / kSkStages) & 1, p.err)) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kSkStages;
+        if (*abort_flag || !mbar_wait(&full[s], (i / kSkStages) & 1, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        *consumed = static_cast<uint32_t>(i + 1);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t st = smem_u32(smem + s * C::kStage);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+#pragma unroll
+          for (int prt = 0; prt < 2; ++prt) {
+            const uint64_t wd = smem_desc_sw128(st + kk * 32);
+            const uint64_t ad = smem_desc_sw128(st + C::kW + prt * C::kA + kk * 32);
+            const uint32_t acc = (i > 0 || kk > 0 || prt > 0) ? 1u : 0u;
+            asm volatile(
+                "{\n\t.reg .pred q;\n\t"
+                "setp.ne.b32 q, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t}" ::"r"(tmem),
+                "l"(wd), "l"(ad), "r"(C::kIdesc), "r"(acc)
+                : "memory");
+          }
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(done);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();
+    const int q = warp & 3;
+    const int nl = q * 32 + lane;  // weight row within the tile
+    const int n = n0 + nl;
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    float v[NB];
+#pragma unroll
+    for (int c = 0; c < NB; ++c) v[c] = 0.f;
+    if (ok) {
+#pragma unroll
+      for (int c = 0; c < NB; c += 16) {
+        float t[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[c + i] = t[i];
+      }
+    }
+    bool run = ok;
+    if (S > 1) {
+      float* mine = part + ((size_t)split * Np + n) * NB;
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < NB; c += 4)
+          __stcg(reinterpret_cast<float4*>(mine + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+      }
+      __threadfence();
+      epi_bar_sync();
+      if (warp == 2 && lane == 0) {
+        const uint32_t t = atomicAdd(&tickets[tile], 1u);
+        *last_flag = (t == static_cast<uint32_t>(S) - 1u) ? 1u : 0u;
+      }
+      epi_bar_sync();
+      run = *last_flag != 0;
+      if (run) {
+        __threadfence();
+#pragma unroll
+        for (int c = 0; c < NB; ++c) v[c] = 0.f;
+        for (int j = 0; j < S; ++j) {
+          const float* pj = part + ((size_t)j * Np + n) * NB;
+#pragma unroll
+          for (int c = 0; c < NB; c += 4) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(pj + c));
+            v[c] += f.x;
+            v[c + 1] += f.y;
+            v[c + 2] += f.z;
+            v[c + 3] += f.w;
+          }
+        }
+        if (warp == 2 && lane == 0) tickets[tile] = 0u;
+      }
+    }
+    if (run) {
+      const float sc = (p.scale && n < p.N) ? __ldg(&p.scale[n]) : 1.0f;
+#pragma unroll
+      for (int c = 0; c < NB; ++c) v[c] *= sc;
+      if (p.epi == EPI_QKV || p.epi == EPI_SWIGLU) {
+        // rows (n, n + 1) pair up across neighbouring lanes; the even lane
+        // takes the even activation rows, the odd lane the odd ones.
+        const int pr = (n0 + (nl & ~1)) >> 1;
+        const bool odd = lane & 1;
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          const float o = __shfl_xor_sync(0xFFFFFFFFu, v[c], 1);
+          if (c < M && (c & 1) == (odd ? 1 : 0) && 2 * pr < p.N) {
+            const float v0 = odd ? o : v[c], v1 = odd ? v[c] : o;
+            if (p.epi == EPI_QKV) epi_qkv_pair(p, c, pr, v0, v1);
+            else epi_swiglu(p, c, pr, v0, v1);
+          }
+        }
+      } else if (n < p.N) {
+#pragma unroll
+        for (int c = 0; c < NB; ++c) {
+          if (c >= M) break;
+          float* o = p.out + (size_t)c * p.ldo + n;
+          if (p.epi == EPI_RESID) *o += v[c];
+          else *o = v[c];
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kCols)
                  : "memory");
   }
 }
@@ -280,7 +548,63 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int NB>
+cudaError_t launch_skinny_nb(const GemvParams& p, const CUtensorMap& mw, const CUtensorMap& mhi,
+                             const CUtensorMap& mlo, int M, int S, float* part, uint32_t* tickets,
+                             bool pdl, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_umma_skinny<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Skinny<NB>::kSmem);
+    if (e) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.N + 127) / 128, S);
+  cfg.blockDim = dim3(kSkThreads);
+  cfg.dynamicSmemBytes = Skinny<NB>::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_umma_skinny<NB>, mw, mhi, mlo, p, M, S, part, tickets);
+}
+
+int skinny_nb(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
 }  // namespace
+
+int skinny_splits(int N, int K, int num_sms) {
+  const int tiles = (N + 127) / 128, nk = (K + BK - 1) / BK;
+  const int target = 2 * num_sms;  // two CTAs per SM
+  int S = (target + tiles / 2) / tiles;
+  return std::max(1, std::min(S, nk));
+}
+
+size_t skinny_part_floats(int N, int K, int M, int num_sms) {
+  const int S = skinny_splits(N, K, num_sms);
+  return S > 1 ? (size_t)S * ((N + 127) / 128) * 128 * skinny_nb(M) : 0;
+}
+
+cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo,
+                               int M, float* part, uint32_t* tickets, int num_sms, bool pdl,
+                               cudaStream_t s) {
+  if (M < 1 || M > 64 || p.N < 2 || (p.N & 1) || p.K < 8 || (p.K % 8)) return cudaErrorInvalidValue;
+  const int NB = skinny_nb(M);
+  CUtensorMap mw, mhi, mlo;
+  if (!make_map(&mw, p.W, p.N, p.K, 128) || !make_map(&mhi, a_hi, M, p.K, NB) ||
+      !make_map(&mlo, a_lo, M, p.K, NB))
+    return cudaErrorInvalidValue;
+  const int S = skinny_splits(p.N, p.K, num_sms);
+  if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
+  switch (NB) {
+    case 16: return launch_skinny_nb<16>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+    case 32: return launch_skinny_nb<32>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+    default: return launch_skinny_nb<64>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+  }
+}
 
 bool gemm_tc_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && encode_fn() != nullptr; }
 

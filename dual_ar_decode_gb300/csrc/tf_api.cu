@@ -34,6 +34,8 @@ using namespace tf;
 namespace {
 
 constexpr int kAlign = 256;
+constexpr int kMaxBatch = 32;  // sequences per context (fast step 1: 2 rows each <= 64)
+constexpr int kIdStride = 16;  // id slots per sequence in the device state
 thread_local std::string g_create_error;
 
 struct Lin {
@@ -50,7 +52,8 @@ struct Layer {
   uint16_t* V = nullptr;
 };
 
-// Device-resident frame state (one sequence).
+// Device-resident frame state.  Sequences advance in lockstep (one shared
+// position); sequence b's ids sit at [b * kIdStride + codebook].
 struct DevState {
   int32_t pos;
   int32_t frame_index;
@@ -58,10 +61,10 @@ struct DevState {
   int32_t hist_idx;
   uint32_t err;
   uint32_t samp[3];       // Philox key low, high; temperature bits
-  int32_t forced[16];
-  int32_t sel[16];
-  int32_t fb[16];
-  unsigned long long best[16];
+  int32_t forced[kMaxBatch * kIdStride];
+  int32_t sel[kMaxBatch * kIdStride];
+  int32_t fb[kMaxBatch * kIdStride];
+  unsigned long long best[16];   // fused argmax of the batch-1 heads
   uint32_t ticket[16];
 };
 
@@ -106,8 +109,17 @@ struct tf_ctx {
   float *px = nullptr, *pa = nullptr, *pq = nullptr, *po = nullptr, *pu = nullptr;
   int32_t* tokens = nullptr;
   uint16_t *a_hi = nullptr, *a_lo = nullptr;  // prompt GEMM inputs as bf16 hi / lo parts
-  uint16_t* wconv = nullptr;  // fp8 weight converted to bf16 for one prompt GEMM
+  uint16_t* wconv = nullptr;  // fp8 weight converted to bf16 for one tensor-core GEMM
   bool prefill_tc = false;
+  // batched decode
+  int Bmax = 1;               // sequences the context holds
+  int Bc = 1;                 // sequences of the current prefill
+  int64_t kv_seq = 0;         // elements between two sequences' KV caches
+  uint16_t* bh[2] = {nullptr, nullptr};  // skinny-GEMM activations, bf16 hi parts [64][Kmax]
+  uint16_t* bl[2] = {nullptr, nullptr};  // and lo parts (two sets, alternating)
+  float* sk_part = nullptr;   // split-K partials
+  uint32_t* sk_tickets = nullptr;
+  int graph_B = 1;            // batch the captured graphs were built for
   int32_t* hist = nullptr;
   DevState* st = nullptr;
   int S_slow = 1;
@@ -196,7 +208,7 @@ bool valid_config(const tf_config* cfg, std::string* why) {
   if (cfg->semantic_vocab > 8192 || cfg->codebook_size > 8192 || cfg->codebook_size < 1)
     return bad("semantic_vocab and codebook_size must be in [1, 8192]");
   if (cfg->max_seq_len < 10 || cfg->max_seq_len > 65536) return bad("max_seq_len must be in [10, 65536]");
-  if (cfg->max_batch != 1) return bad("max_batch must be 1 (batched decode is not built)");
+  if (cfg->max_batch < 1 || cfg->max_batch > kMaxBatch) return bad("max_batch must be in [1, 32]");
   if (!(cfg->rms_eps > 0.f) || !(cfg->rope_theta > 1.f)) return bad("rms_eps > 0 and rope_theta > 1 required");
   if (cfg->weight_dtype != TF_WEIGHT_BF16 && cfg->weight_dtype != TF_WEIGHT_FP8)
     return bad("weight_dtype must be TF_WEIGHT_BF16 or TF_WEIGHT_FP8");
@@ -355,6 +367,8 @@ cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_
   f.advance = advance;
   f.frame_index = &c->st->frame_index;
   f.sel = c->st->sel;
+  f.sel_stride = kIdStride;
+  f.nseq = 1;
   f.ncb = c->NCB;
   f.hist = c->hist;
   f.hist_idx = &c->st->hist_idx;
@@ -362,7 +376,189 @@ cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_
   return launch_frame_end(f, true, c->stream);
 }
 
+// ------------------------------------------------------------ batched decode
+// B > 1 sequences in lockstep: every linear layer is one skinny tensor-core
+// GEMM over the B (fast step 1: 2B) activation rows, which enter as bf16
+// hi / lo parts; attention, selection and the input rows work per sequence.
+
+// Activation rows -> bf16 parts in set `set` (RMSNorm first when nw is set).
+cudaError_t split_rows(tf_ctx* c, const float* x, int ldx, int M, int K, const uint16_t* nw, int set) {
+  return launch_rows_split(x, ldx, M, K, nw, c->cfg.rms_eps, c->bh[set], c->bl[set], true, c->stream);
+}
+
+// out = epi(W * a) for the M activation rows held in part set `set`.
+cudaError_t skinny(tf_ctx* c, const Lin& L, int set, int M, int epi, float* out, int ldo,
+                   const Layer* layer = nullptr, int rps = 0, const int32_t* pos_ptr = nullptr,
+                   int pos_fixed = 0, int out_set = -1) {
+  GemvParams p = {};
+  p.W = L.w;
+  p.scale = L.s;
+  p.N = L.N;
+  p.K = L.K;
+  p.epi = epi;
+  p.out = out;
+  p.ldo = ldo;
+  if (out_set >= 0) {
+    p.out_hi = c->bh[out_set];
+    p.out_lo = c->bl[out_set];
+  }
+  p.q_dim = c->Q;
+  p.kv_dim = c->KV;
+  p.head_dim = c->D;
+  p.qout = c->qbuf;
+  if (layer) {
+    p.Kc = layer->K;
+    p.Vc = layer->V;
+  }
+  p.T = c->T;
+  p.pos_ptr = pos_ptr;
+  p.pos_fixed = pos_fixed;
+  p.rps = rps;
+  p.kv_seq = c->kv_seq;
+  p.rope = c->rope;
+  p.err = &c->st->err;
+  // The GEMM streams its weight slices before it waits for the previous
+  // kernel (programmatic dependent launch), which is only right for weights
+  // no kernel writes: a converted fp8 weight is launched without the overlap.
+  bool pdl = true;
+  if (L.s) {  // fp8: bf16 copy of the e4m3 values; the row scale stays in p.scale
+    if (cudaError_t e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream)) return e;
+    p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+    pdl = false;
+  }
+  return launch_gemm_skinny(p, c->bh[set], c->bl[set], M, c->sk_part, c->sk_tickets, c->num_sms,
+                            pdl, c->stream);
+}
+
+// One decoder layer over M rows (rps rows per sequence) of the residual x.
+cudaError_t layer_batched(tf_ctx* c, const Layer& L, float* x, int M, int rps,
+                          const int32_t* pos_ptr, int pos_fixed, int S) {
+  cudaError_t e;
+  if ((e = split_rows(c, x, c->H, M, c->H, L.attn_norm, 0))) return e;
+  if ((e = skinny(c, L.qkv, 0, M, EPI_QKV, nullptr, 0, &L, rps, pos_ptr, pos_fixed))) return e;
+  AttnParams a = {};
+  a.q = c->qbuf;
+  a.Kc = L.K;
+  a.Vc = L.V;
+  a.T = c->T;
+  a.Hq = c->Hq;
+  a.Hkv = c->Hkv;
+  a.D = c->D;
+  a.pos_ptr = pos_ptr;
+  a.pos_fixed = pos_fixed;
+  a.rps = rps;
+  a.kv_seq = c->kv_seq;
+  a.S = S;
+  a.part = c->part;
+  a.counters = c->counters;
+  a.out = c->obuf;
+  a.out_hi = c->bh[1];
+  a.out_lo = c->bl[1];
+  a.err = &c->st->err;
+  if ((e = launch_attention(a, M, true, c->stream))) return e;
+  if ((e = skinny(c, L.o, 1, M, EPI_RESID, x, c->H))) return e;
+  if ((e = split_rows(c, x, c->H, M, c->H, L.ffn_norm, 0))) return e;
+  if ((e = skinny(c, L.w13, 0, M, EPI_SWIGLU, nullptr, c->F, nullptr, 0, nullptr, 0, 1))) return e;
+  return skinny(c, L.w2, 1, M, EPI_RESID, x, c->H);
+}
+
+cudaError_t select_batched(tf_ctx* c, int cb, int B, const tf_sampling* s) {
+  SelectParams q = {};
+  q.logits = c->logits + (size_t)cb * c->Vmax;
+  q.ld = c->NCB * c->Vmax;
+  q.vocab = cb == 0 ? c->Vs : c->Vc;
+  q.n = B;
+  q.top_k = s->top_k;
+  q.temperature = s->temperature;
+  q.key0 = static_cast<uint32_t>(s->seed & 0xFFFFFFFFull);
+  q.key1 = static_cast<uint32_t>(s->seed >> 32);
+  q.frame_ptr = &c->st->frame_index;
+  q.codebook0 = cb;
+  q.sequence = 0;
+  q.seq_rows = 1;
+  q.id_stride = kIdStride;
+  q.sel = c->st->sel + cb;
+  q.fb = c->st->fb + cb;
+  q.forced = c->st->forced + cb;
+  q.forced_on = &c->st->forced_on;
+  q.err = &c->st->err;
+  return launch_select(q, true, c->stream);
+}
+
+// Semantic heads, fast loop and bookkeeping for B sequences whose final slow
+// residuals are xs[0..B).
+cudaError_t enqueue_tail_batched(tf_ctx* c, const tf_sampling* s, int B, int advance) {
+  cudaError_t e;
+  const int ldl = c->NCB * c->Vmax;
+  Lin sem;
+  sem.w = reinterpret_cast<uint8_t*>(c->text_embed + (size_t)c->sem_base * c->H);
+  sem.N = c->Vs;
+  sem.K = c->H;
+  if ((e = split_rows(c, c->xs, c->H, B, c->H, c->slow_norm, 0))) return e;
+  if ((e = skinny(c, sem, 0, B, EPI_STORE, c->logits, ldl))) return e;
+  if ((e = select_batched(c, 0, B, s))) return e;
+  for (int j = 1; j < c->NCB; ++j) {
+    const int rps = j == 1 ? 2 : 1;
+    const int M = rps * B;
+    BuildParams b = {};
+    b.mode = j == 1 ? BUILD_FAST1 : BUILD_FASTJ;
+    b.j = j;
+    b.H = c->H;
+    b.M = M;
+    b.table = c->cb_embed + (size_t)(j - 1) * c->Vc * c->H;
+    b.table_rows = c->Vc;
+    b.row_base = 0;
+    b.ids = c->st->fb + (j - 1);
+    b.id_stride = kIdStride;
+    b.xs = c->xs;
+    b.nw = c->slow_norm;
+    b.eps = c->cfg.rms_eps;
+    b.x = c->xf;
+    b.err = &c->st->err;
+    if ((e = launch_build(b, true, c->stream))) return e;
+    for (const Layer& L : c->fast)
+      if ((e = layer_batched(c, L, c->xf, M, rps, nullptr, j == 1 ? 0 : j, 1))) return e;
+    // the head reads each sequence's last row
+    if ((e = split_rows(c, c->xf + (size_t)(rps - 1) * c->H, rps * c->H, B, c->H, c->fast_norm, 0)))
+      return e;
+    if ((e = skinny(c, c->fast_head, 0, B, EPI_STORE, c->logits + (size_t)j * c->Vmax, ldl))) return e;
+    if ((e = select_batched(c, j, B, s))) return e;
+  }
+  FrameEndParams f = {};
+  f.pos = &c->st->pos;
+  f.advance = advance;
+  f.frame_index = &c->st->frame_index;
+  f.sel = c->st->sel;
+  f.sel_stride = kIdStride;
+  f.nseq = B;
+  f.ncb = c->NCB;
+  f.hist = c->hist;
+  f.hist_idx = &c->st->hist_idx;
+  f.hist_cap = c->T;
+  return launch_frame_end(f, true, c->stream);
+}
+
+cudaError_t enqueue_decode_batched(tf_ctx* c, const tf_sampling* s, int B) {
+  cudaError_t e;
+  BuildParams b = {};
+  b.mode = BUILD_SLOW;
+  b.H = c->H;
+  b.M = B;
+  b.table = c->text_embed;
+  b.table_rows = c->Vs;
+  b.row_base = c->sem_base;
+  b.ids = c->st->fb;
+  b.id_stride = kIdStride;
+  b.x = c->xs;
+  b.err = &c->st->err;
+  if ((e = launch_build(b, false, c->stream))) return e;
+  for (const Layer& L : c->slow)
+    if ((e = layer_batched(c, L, c->xs, B, 1, &c->st->pos, 0, c->S_slow))) return e;
+  return enqueue_tail_batched(c, s, B, 1);
+}
+
 cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
+  if (c->Bc > 1) return enqueue_decode_batched(c, s, c->Bc);
   cudaError_t e;
   BuildParams b = {};
   b.mode = BUILD_SLOW;
@@ -563,6 +759,14 @@ bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
 }
 
 tf_status get_graph(tf_ctx* c, const tf_sampling* s, cudaGraphExec_t* out) {
+  if (c->graph_B != c->Bc) {  // graphs are per batch size
+    for (auto& g : c->graph)
+      if (g) {
+        cudaGraphExecDestroy(g);
+        g = nullptr;
+      }
+    c->graph_B = c->Bc;
+  }
   const int gi = s->top_k > 0 ? 1 : 0;
   if (c->graph[gi] && (gi == 0 || same_sampling(c->graph_samp, *s))) {
     *out = c->graph[gi];
@@ -607,29 +811,42 @@ tf_status check_sampling(tf_ctx* c, const tf_sampling* s, tf_sampling* out) {
   return TF_OK;
 }
 
-tf_status set_forced(tf_ctx* c, const int32_t* forced) {
+// forced: NULL or host [B][NCB]; checked before anything is copied.
+tf_status set_forced(tf_ctx* c, const int32_t* forced, int B) {
   int32_t on = forced ? 1 : 0;
   if (forced) {
-    for (int j = 0; j < c->NCB; ++j) {
-      const int lim = j == 0 ? c->Vs : c->Vc;
-      if (forced[j] < 0 || forced[j] >= lim)
-        return fail(c, TF_E_INVAL, "forced id out of range at codebook " + std::to_string(j));
-    }
-    CK(cudaMemcpyAsync(c->st->forced, forced, sizeof(int32_t) * c->NCB, cudaMemcpyHostToDevice,
-                       c->stream));
+    std::vector<int32_t> slots((size_t)B * kIdStride, 0);
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < c->NCB; ++j) {
+        const int lim = j == 0 ? c->Vs : c->Vc;
+        const int32_t v = forced[(size_t)b * c->NCB + j];
+        if (v < 0 || v >= lim)
+          return fail(c, TF_E_INVAL, "forced id out of range at sequence " + std::to_string(b) +
+                                         ", codebook " + std::to_string(j));
+        slots[(size_t)b * kIdStride + j] = v;
+      }
+    CK(cudaMemcpyAsync(c->st->forced, slots.data(), sizeof(int32_t) * slots.size(),
+                       cudaMemcpyHostToDevice, c->stream));
+    CK(cudaStreamSynchronize(c->stream));  // `slots` is a host temporary
   }
   CK(cudaMemcpyAsync(&c->st->forced_on, &on, sizeof(on), cudaMemcpyHostToDevice, c->stream));
   return TF_OK;
 }
 
-tf_status read_frame(tf_ctx* c, int32_t* frame, float* logits) {
-  if (frame)
-    CK(cudaMemcpyAsync(frame, c->st->sel, sizeof(int32_t) * c->NCB, cudaMemcpyDeviceToHost,
-                       c->stream));
+// frame: host [B][NCB]; logits: NULL or host [B][NCB][Vmax].
+tf_status read_frame(tf_ctx* c, int32_t* frame, float* logits, int B) {
+  std::vector<int32_t> slots((size_t)B * kIdStride);
+  CK(cudaMemcpyAsync(slots.data(), c->st->sel, sizeof(int32_t) * slots.size(),
+                     cudaMemcpyDeviceToHost, c->stream));
   if (logits)
-    CK(cudaMemcpyAsync(logits, c->logits, sizeof(float) * c->NCB * c->Vmax, cudaMemcpyDeviceToHost,
-                       c->stream));
-  return check_kernel_errors(c);
+    CK(cudaMemcpyAsync(logits, c->logits, sizeof(float) * B * c->NCB * c->Vmax,
+                       cudaMemcpyDeviceToHost, c->stream));
+  tf_status r = check_kernel_errors(c);  // synchronises the stream
+  if (frame)
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < c->NCB; ++j)
+        frame[(size_t)b * c->NCB + j] = slots[(size_t)b * kIdStride + j];
+  return r;
 }
 
 bool all_loaded(tf_ctx* c, std::string* missing);
@@ -698,6 +915,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
 
   c->fp8 = cfg->weight_dtype == TF_WEIGHT_FP8;
   c->eb = c->fp8 ? 1 : 2;
+  c->Bmax = cfg->max_batch;
   c->H = cfg->hidden;
   c->D = cfg->head_dim;
   c->Hq = cfg->n_heads;
@@ -770,12 +988,15 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   c->fast_head = make_lin(c->Vc, c->H);
   c->cb_embed = reinterpret_cast<uint16_t*>(take((size_t)(c->NCB - 1) * c->Vc * H * 2));
 
-  // ---- KV caches
+  // ---- KV caches: [sequence][Hkv][T][D] per layer
   const size_t kv_elems = (size_t)c->Hkv * c->T * c->D;
+  c->kv_seq = static_cast<int64_t>(kv_elems);
+  const size_t B = c->Bmax;
   for (Layer& L : c->slow) {
-    if (dev_alloc_t(c, &L.K, kv_elems) || dev_alloc_t(c, &L.V, kv_elems)) return bail(TF_E_NOMEM);
+    if (dev_alloc_t(c, &L.K, B * kv_elems) || dev_alloc_t(c, &L.V, B * kv_elems))
+      return bail(TF_E_NOMEM);
   }
-  const size_t fkv = (size_t)c->Hkv * c->T * c->D;  // fast uses positions 0..9 of a T-slot cache
+  const size_t fkv = B * kv_elems;  // fast uses positions 0..9 of a T-slot cache
   for (Layer& L : c->fast) {
     if (dev_alloc_t(c, &L.K, fkv) || dev_alloc_t(c, &L.V, fkv)) return bail(TF_E_NOMEM);
   }
@@ -788,15 +1009,16 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
 
   // ---- activations and state
   const int T = c->T;
-  if (dev_alloc_t(c, &c->xs, H) || dev_alloc_t(c, &c->xf, 2 * H) || dev_alloc_t(c, &c->qbuf, 2 * c->Q) ||
-      dev_alloc_t(c, &c->obuf, 2 * c->Q) || dev_alloc_t(c, &c->ubuf, 2 * c->F) ||
-      dev_alloc_t(c, &c->logits, (size_t)c->NCB * c->Vmax) ||
-      dev_alloc_t(c, &c->part, (size_t)2 * c->Hq * c->S_slow * (c->D + 2)) ||
-      dev_alloc_t(c, &c->counters, (size_t)2 * c->Hkv) ||
+  if (dev_alloc_t(c, &c->xs, B * H) || dev_alloc_t(c, &c->xf, 2 * B * H) ||
+      dev_alloc_t(c, &c->qbuf, 2 * B * c->Q) || dev_alloc_t(c, &c->obuf, 2 * B * c->Q) ||
+      dev_alloc_t(c, &c->ubuf, 2 * B * c->F) ||
+      dev_alloc_t(c, &c->logits, B * c->NCB * c->Vmax) ||
+      dev_alloc_t(c, &c->part, std::max<size_t>(2, B) * c->Hq * c->S_slow * (c->D + 2)) ||
+      dev_alloc_t(c, &c->counters, 2 * B * c->Hkv) ||
       dev_alloc_t(c, &c->px, (size_t)T * H) || dev_alloc_t(c, &c->pa, (size_t)T * H) ||
       dev_alloc_t(c, &c->pq, (size_t)T * c->Q) || dev_alloc_t(c, &c->po, (size_t)T * c->Q) ||
-      dev_alloc_t(c, &c->pu, (size_t)T * c->F) || dev_alloc_t(c, &c->tokens, (size_t)T) ||
-      dev_alloc_t(c, &c->hist, (size_t)T * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
+      dev_alloc_t(c, &c->pu, (size_t)T * c->F) || dev_alloc_t(c, &c->tokens, (size_t)T * B) ||
+      dev_alloc_t(c, &c->hist, (size_t)T * B * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
       dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)) ||
       dev_alloc_t(c, &c->d_ops, (size_t)4 * kMaxOps) || dev_alloc_t(c, &c->gbar, 1) ||
       dev_alloc_t(c, &c->trace, (size_t)kMaxOps * 6))
@@ -806,11 +1028,30 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
                   gemm_tc_supported(2 * c->F, c->H) && gemm_tc_supported(c->H, c->F);
   if (c->prefill_tc &&
       (dev_alloc_t(c, &c->a_hi, (size_t)T * std::max({c->H, c->Q, c->F})) ||
-       dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F})) ||
-       (c->fp8 && dev_alloc_t(c, &c->wconv,
-                              std::max({(size_t)c->QKV * H, (size_t)H * c->Q, (size_t)2 * c->F * H,
-                                        (size_t)H * c->F})))))
+       dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F}))))
     return bail(TF_E_NOMEM);
+  if (c->fp8 && (c->prefill_tc || B > 1) &&
+      dev_alloc_t(c, &c->wconv,
+                  std::max({(size_t)c->QKV * H, (size_t)H * c->Q, (size_t)2 * c->F * H,
+                            (size_t)H * c->F, (size_t)c->Vc * H})))
+    return bail(TF_E_NOMEM);
+  // Batched decode: skinny-GEMM activation parts and split-K scratch.
+  if (B > 1) {
+    const size_t kmax = std::max({c->H, c->Q, c->F});
+    size_t part = 0;
+    const int shapes[6][2] = {{c->QKV, c->H}, {c->H, c->Q}, {2 * c->F, c->H},
+                              {c->H, c->F}, {c->Vs, c->H}, {c->Vc, c->H}};
+    for (auto& sh : shapes)
+      part = std::max(part, skinny_part_floats(sh[0], sh[1], 2 * c->Bmax, c->num_sms));
+    for (int i = 0; i < 2; ++i)
+      if (dev_alloc_t(c, &c->bh[i], 2 * B * kmax) || dev_alloc_t(c, &c->bl[i], 2 * B * kmax))
+        return bail(TF_E_NOMEM);
+    if (dev_alloc_t(c, &c->sk_part, std::max<size_t>(part, 64)) ||
+        dev_alloc_t(c, &c->sk_tickets, 1024) || cudaMemset(c->sk_tickets, 0, 1024 * 4)) {
+      if (c->err.empty()) c->err = "batched decode buffers";
+      return bail(TF_E_NOMEM);
+    }
+  }
 
   // RoPE table: angle pos * theta^(-2i/D) evaluated in double, stored as float.
   {
@@ -826,7 +1067,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       return bail(TF_E_CUDA);
     }
   }
-  if (cudaMemset(c->st, 0, sizeof(DevState)) || cudaMemset(c->counters, 0, 2 * c->Hkv * 4)) {
+  if (cudaMemset(c->st, 0, sizeof(DevState)) || cudaMemset(c->counters, 0, 2 * B * c->Hkv * 4)) {
     c->err = "state init failed";
     return bail(TF_E_CUDA);
   }
@@ -1003,18 +1244,18 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
   if (!c) return TF_E_INVAL;
   if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
   if (!tokens || !frame0) return fail(c, TF_E_INVAL, "tokens and frame0 are required");
-  if (B != 1) return fail(c, TF_E_INVAL, "B must be 1");
+  if (B < 1 || B > c->Bmax) return fail(c, TF_E_INVAL, "B must be in [1, max_batch]");
   if (P < 1 || P > c->T) return fail(c, TF_E_INVAL, "P must be in [1, max_seq_len]");
   std::string missing;
   if (!all_loaded(c, &missing)) return fail(c, TF_E_STATE, missing);
-  for (int i = 0; i < P; ++i)
+  for (int64_t i = 0; i < (int64_t)B * P; ++i)
     if (tokens[i] < 0 || tokens[i] >= c->Vt) return fail(c, TF_E_INVAL, "prompt id out of range");
   tf_sampling s;
   tf_status r = check_sampling(c, sampling, &s);
   if (r) return r;
   CK(cudaSetDevice(c->device));
-  if ((r = set_forced(c, forced))) return r;
-  CK(cudaMemcpyAsync(c->tokens, tokens, sizeof(int32_t) * P, cudaMemcpyHostToDevice, c->stream));
+  if ((r = set_forced(c, forced, B))) return r;
+  CK(cudaMemcpyAsync(c->tokens, tokens, sizeof(int32_t) * B * P, cudaMemcpyHostToDevice, c->stream));
   const int32_t zero4[4] = {0, 0, 0, 0};  // pos, frame_index, forced_on kept, hist_idx
   CK(cudaMemcpyAsync(&c->st->pos, &zero4[0], 4, cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(&c->st->frame_index, &zero4[1], 4, cudaMemcpyHostToDevice, c->stream));
@@ -1023,81 +1264,90 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
     const uint32_t samp[3] = {(uint32_t)(s.seed & 0xFFFFFFFFu), (uint32_t)(s.seed >> 32), 0};
     CK(cudaMemcpyAsync(c->st->samp, samp, sizeof(samp), cudaMemcpyHostToDevice, c->stream));
   }
+  CK(cudaStreamSynchronize(c->stream));  // the host copies above read stack memory
+  c->Bc = B;
+  c->prefilled = false;
 
-  // Slow decoder over the prompt: row m at position m.
-  BuildParams b = {};
-  b.mode = BUILD_TOKENS;
-  b.H = c->H;
-  b.M = P;
-  b.table = c->text_embed;
-  b.table_rows = c->Vt;
-  b.ids = c->tokens;
-  b.x = c->px;
-  b.err = &c->st->err;
-  CK(launch_build(b, false, c->stream));
   const int wt = c->fp8 ? 1 : 0;
-  auto gemm = [&](const Lin& L, const float* A, int epi, float* out, int ldo, const Layer* layer) {
-    GemvParams p = {};
-    p.W = L.w;
-    p.scale = L.s;
-    p.N = L.N;
-    p.K = L.K;
-    p.x = A;
-    p.ldx = L.K;
-    p.epi = epi;
-    p.out = out;
-    p.ldo = ldo;
-    p.q_dim = c->Q;
-    p.kv_dim = c->KV;
-    p.head_dim = c->D;
-    p.qout = c->pq;
-    if (layer) {
-      p.Kc = layer->K;
-      p.Vc = layer->V;
-    }
-    p.T = c->T;
-    p.pos_fixed = 0;
-    p.rope = c->rope;
-    p.err = &c->st->err;
-    if (c->prefill_tc) {
-      cudaError_t e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream);
-      if (e) return e;
-      if (c->fp8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
-        if ((e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e;
-        p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+  // Slow decoder over sequence b's prompt: row m at position m, KV caches of
+  // sequence b; its last residual row goes to xs[b].
+  for (int sb = 0; sb < B; ++sb) {
+    BuildParams b = {};
+    b.mode = BUILD_TOKENS;
+    b.H = c->H;
+    b.M = P;
+    b.table = c->text_embed;
+    b.table_rows = c->Vt;
+    b.ids = c->tokens + (size_t)sb * P;
+    b.x = c->px;
+    b.err = &c->st->err;
+    CK(launch_build(b, false, c->stream));
+    const size_t kvo = (size_t)sb * c->kv_seq;
+    auto gemm = [&](const Lin& L, const float* A, int epi, float* out, int ldo, const Layer* layer) {
+      GemvParams p = {};
+      p.W = L.w;
+      p.scale = L.s;
+      p.N = L.N;
+      p.K = L.K;
+      p.x = A;
+      p.ldx = L.K;
+      p.epi = epi;
+      p.out = out;
+      p.ldo = ldo;
+      p.q_dim = c->Q;
+      p.kv_dim = c->KV;
+      p.head_dim = c->D;
+      p.qout = c->pq;
+      if (layer) {
+        p.Kc = layer->K + kvo;
+        p.Vc = layer->V + kvo;
       }
-      return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
+      p.T = c->T;
+      p.pos_fixed = 0;
+      p.rope = c->rope;
+      p.err = &c->st->err;
+      if (c->prefill_tc) {
+        cudaError_t e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream);
+        if (e) return e;
+        if (c->fp8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
+          if ((e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e;
+          p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+        }
+        return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
+      }
+      return launch_gemm_rows(p, wt, P, c->stream);
+    };
+    for (const Layer& L : c->slow) {
+      CK(launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
+      CK(gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L));
+      AttnParams a = {};
+      a.q = c->pq;
+      a.Kc = L.K + kvo;
+      a.Vc = L.V + kvo;
+      a.T = c->T;
+      a.Hq = c->Hq;
+      a.Hkv = c->Hkv;
+      a.D = c->D;
+      a.pos_fixed = 0;
+      a.S = 1;
+      a.part = c->part;
+      a.counters = c->counters;
+      a.out = c->po;
+      a.err = &c->st->err;
+      CK(launch_attention(a, P, false, c->stream));
+      CK(gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr));
+      CK(launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
+      CK(gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr));
+      CK(gemm(L.w2, c->pu, EPI_RESID, c->px, c->H, nullptr));
     }
-    return launch_gemm_rows(p, wt, P, c->stream);
-  };
-  for (const Layer& L : c->slow) {
-    CK(launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
-    CK(gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L));
-    AttnParams a = {};
-    a.q = c->pq;
-    a.Kc = L.K;
-    a.Vc = L.V;
-    a.T = c->T;
-    a.Hq = c->Hq;
-    a.Hkv = c->Hkv;
-    a.D = c->D;
-    a.pos_fixed = 0;
-    a.S = 1;
-    a.part = c->part;
-    a.counters = c->counters;
-    a.out = c->po;
-    a.err = &c->st->err;
-    CK(launch_attention(a, P, false, c->stream));
-    CK(gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr));
-    CK(launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
-    CK(gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr));
-    CK(gemm(L.w2, c->pu, EPI_RESID, c->px, c->H, nullptr));
+    CK(cudaMemcpyAsync(c->xs + (size_t)sb * c->H, c->px + (size_t)(P - 1) * c->H,
+                       sizeof(float) * c->H, cudaMemcpyDeviceToDevice, c->stream));
   }
-  CK(cudaMemcpyAsync(c->xs, c->px + (size_t)(P - 1) * c->H, sizeof(float) * c->H,
-                     cudaMemcpyDeviceToDevice, c->stream));
   const int32_t posP = P;
   CK(cudaMemcpyAsync(&c->st->pos, &posP, 4, cudaMemcpyHostToDevice, c->stream));
-  if (c->use_graph) {
+  if (B > 1) {
+    CK(enqueue_tail_batched(c, &s, B, 0));
+  } else if (c->use_graph) {
     CK(enqueue_tail(c, &s, 0, false));
   } else if ((r = run_frames(c, false, &s, 1))) {
     return r;
@@ -1105,7 +1355,7 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
   c->pos_host = P;
   c->frame_host = 1;
   c->prefilled = true;
-  return read_frame(c, frame0, logits);
+  return read_frame(c, frame0, logits, B);
 }
 
 tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t* forced,
@@ -1119,8 +1369,8 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
   tf_status r = check_sampling(c, sampling, &s);
   if (r) return r;
   CK(cudaSetDevice(c->device));
-  if ((r = set_forced(c, forced))) return r;
-  if (c->use_graph) {
+  if ((r = set_forced(c, forced, c->Bc))) return r;
+  if (c->use_graph || c->Bc > 1) {
     cudaGraphExec_t g;
     if ((r = get_graph(c, &s, &g))) return r;
     CK(cudaGraphLaunch(g, c->stream));
@@ -1129,13 +1379,14 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
   }
   c->pos_host += 1;
   c->frame_host += 1;
-  return read_frame(c, frame, logits);
+  return read_frame(c, frame, logits, c->Bc);
 }
 
 tf_status tf_decode_trace(tf_ctx* c, const tf_sampling* sampling, int64_t* stamps, int32_t* kinds,
                           int32_t cap, int32_t* n_ops) {
   if (!c || !stamps || !kinds || !n_ops || cap < 1) return TF_E_INVAL;
-  if (c->use_graph) return fail(c, TF_E_STATE, "tracing needs the persistent frame kernel");
+  if (c->use_graph || c->Bc > 1)
+    return fail(c, TF_E_STATE, "tracing needs the persistent frame kernel and one sequence");
   int32_t frame[16];
   c->tracing = true;
   tf_status r = tf_decode_frame(c, sampling, nullptr, frame, nullptr);
@@ -1168,10 +1419,10 @@ tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, in
   tf_status r = check_sampling(c, sampling, &s);
   if (r) return r;
   CK(cudaSetDevice(c->device));
-  if ((r = set_forced(c, nullptr))) return r;
+  if ((r = set_forced(c, nullptr, c->Bc))) return r;
   const int32_t zero = 0;
   CK(cudaMemcpyAsync(&c->st->hist_idx, &zero, 4, cudaMemcpyHostToDevice, c->stream));
-  if (c->use_graph) {
+  if (c->use_graph || c->Bc > 1) {
     cudaGraphExec_t g;
     if ((r = get_graph(c, &s, &g))) return r;
     for (int i = 0; i < n; ++i) CK(cudaGraphLaunch(g, c->stream));
@@ -1180,32 +1431,54 @@ tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, in
   }
   c->pos_host += n;
   c->frame_host += n;
-  CK(cudaMemcpyAsync(frames, c->hist, sizeof(int32_t) * c->NCB * n, cudaMemcpyDeviceToHost, c->stream));
+  CK(cudaMemcpyAsync(frames, c->hist, sizeof(int32_t) * c->NCB * c->Bc * n, cudaMemcpyDeviceToHost,
+                     c->stream));
   return check_kernel_errors(c);
 }
 
 tf_status tf_profile_kernel(tf_ctx* c, int32_t which, int32_t iters, float* ms_per_launch,
                             int64_t* bytes_per_launch) {
-  if (!c || iters < 1 || which < 0 || which > 3) return TF_E_INVAL;
+  if (!c || iters < 1 || which < 0 || which > 7) return TF_E_INVAL;
   if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  const bool batched = which >= 4;
+  if (batched && c->Bmax < 2) return fail(c, TF_E_INVAL, "skinny-GEMM kernels need max_batch > 1");
   std::string missing;
   if (!all_loaded(c, &missing)) return fail(c, TF_E_STATE, missing);
   CK(cudaSetDevice(c->device));
   const int Ls = static_cast<int>(c->slow.size());
+  const int Lf = static_cast<int>(c->fast.size());
+  const int M = batched ? c->Bmax : 1;
+  const int kind = which & 3;
   // Scratch input rows: finite values in every activation buffer the kernel reads.
-  CK(cudaMemsetAsync(c->pa, 0, sizeof(float) * c->H, c->stream));
   std::vector<float> ones(std::max({c->H, c->Q, c->F}), 0.01f);
   CK(cudaMemcpyAsync(c->pa, ones.data(), sizeof(float) * c->H, cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->po, ones.data(), sizeof(float) * c->Q, cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->pu, ones.data(), sizeof(float) * c->F, cudaMemcpyHostToDevice, c->stream));
+  if (batched) {
+    const size_t n = (size_t)2 * c->Bmax * std::max({c->H, c->Q, c->F});
+    std::vector<uint16_t> hi(n, 0x3c24), lo(n, 0);  // bf16(0.01) and 0
+    CK(cudaMemcpyAsync(c->bh[0], hi.data(), n * 2, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaMemcpyAsync(c->bl[0], lo.data(), n * 2, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+  }
   CK(cudaStreamSynchronize(c->stream));
-  const int32_t pos0 = 0;
+  // The QKV epilogue appends K/V rows: it writes position 0 of the fast
+  // decoder's caches, which every frame rewrites before it reads them.
   auto launch = [&](int i, bool pdl) -> cudaError_t {
     const Layer& L = c->slow[i % Ls];
-    switch (which) {
+    const Layer& F = c->fast[i % Lf];
+    if (batched) {
+      switch (kind) {
+        case 0: return skinny(c, L.w13, 0, M, EPI_SWIGLU, nullptr, c->F, nullptr, 0, nullptr, 0, 1);
+        case 1: return skinny(c, L.qkv, 0, M, EPI_QKV, nullptr, 0, &F, 1, nullptr, 0);
+        case 2: return skinny(c, L.o, 0, M, EPI_RESID, c->xf, c->H);
+        default: return skinny(c, L.w2, 0, M, EPI_RESID, c->xf, c->H);
+      }
+    }
+    switch (kind) {
       case 0: return gemv(c, L.w13, PRO_NORM, c->pa, L.ffn_norm, EPI_SWIGLU, c->pq, c->F, 1, pdl);
-      case 1: return gemv(c, L.qkv, PRO_NORM, c->pa, L.attn_norm, EPI_QKV, nullptr, 0, 1, pdl,
-                          &c->slow[(i + 1) % Ls], nullptr, pos0);
+      case 1: return gemv(c, L.qkv, PRO_NORM, c->pa, L.attn_norm, EPI_QKV, nullptr, 0, 1, pdl, &F,
+                          nullptr, 0);
       case 2: return gemv(c, L.o, PRO_PLAIN, c->po, nullptr, EPI_RESID, c->px, c->H, 1, pdl);
       default: return gemv(c, L.w2, PRO_PLAIN, c->pu, nullptr, EPI_RESID, c->px, c->H, 1, pdl);
     }
@@ -1225,12 +1498,18 @@ tf_status tf_profile_kernel(tf_ctx* c, int32_t which, int32_t iters, float* ms_p
   cudaEventDestroy(e1);
   if (ms_per_launch) *ms_per_launch = ms / iters;
   const Layer& L0 = c->slow[0];
-  const Lin& lin = which == 0 ? L0.w13 : which == 1 ? L0.qkv : which == 2 ? L0.o : L0.w2;
+  const Lin& lin = kind == 0 ? L0.w13 : kind == 1 ? L0.qkv : kind == 2 ? L0.o : L0.w2;
   int64_t bytes = (int64_t)lin.N * lin.K * c->eb + (c->fp8 ? (int64_t)lin.N * 4 : 0);
-  bytes += (int64_t)lin.K * 4;                        // activation row in
-  if (which == 0 || which == 1) bytes += (int64_t)lin.K * 2;  // RMSNorm weight
-  bytes += which == 0 ? (int64_t)c->F * 4 : which == 1 ? (int64_t)(c->Q * 4 + 2 * c->KV * 2)
+  if (batched) {
+    bytes += (int64_t)M * lin.K * 4;                   // activation rows in (bf16 hi + lo)
+    bytes += (int64_t)M * (kind == 0 ? (int64_t)c->F * 4 : kind == 1 ? (int64_t)(c->Q * 4 + 2 * c->KV * 2)
+                                                             : (int64_t)c->H * 8);
+  } else {
+    bytes += (int64_t)lin.K * 4;                        // activation row in
+    if (kind == 0 || kind == 1) bytes += (int64_t)lin.K * 2;  // RMSNorm weight
+    bytes += kind == 0 ? (int64_t)c->F * 4 : kind == 1 ? (int64_t)(c->Q * 4 + 2 * c->KV * 2)
                                                        : (int64_t)c->H * 8;  // out (+ residual read)
+  }
   if (bytes_per_launch) *bytes_per_launch = bytes;
   return check_kernel_errors(c);
 }
@@ -1373,6 +1652,57 @@ tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, in
   cudaFree(hi);
   cudaFree(lo);
   cudaFree(err);
+  if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
+  return r;
+}
+
+tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K,
+                            float* C, void* stream) {
+  if (!A || !W || !C || M < 1 || M > 64 || N < 2 || (N & 1) || K < 8 || (K % 8)) return TF_E_INVAL;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return TF_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t *hi = nullptr, *lo = nullptr;
+  uint32_t *err = nullptr, *tickets = nullptr;
+  float* part = nullptr;
+  const size_t n = (size_t)M * K;
+  const size_t pf = std::max<size_t>(skinny_part_floats(N, K, M, sms), 4);
+  const size_t nt = (size_t)(N + 127) / 128;
+  if (cudaMalloc(&hi, n * 2) != cudaSuccess || cudaMalloc(&lo, n * 2) != cudaSuccess ||
+      cudaMalloc(&err, 4) != cudaSuccess || cudaMalloc(&tickets, nt * 4) != cudaSuccess ||
+      cudaMalloc(&part, pf * 4) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFree(hi);
+    cudaFree(lo);
+    cudaFree(err);
+    cudaFree(tickets);
+    cudaFree(part);
+    return TF_E_NOMEM;
+  }
+  tf_status r = TF_OK;
+  GemvParams p = {};
+  p.W = reinterpret_cast<const uint8_t*>(W);
+  p.N = N;
+  p.K = K;
+  p.epi = EPI_STORE;
+  p.out = C;
+  p.ldo = N;
+  p.err = err;
+  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || cudaMemsetAsync(tickets, 0, nt * 4, s) != cudaSuccess ||
+      launch_split_bf16(A, hi, lo, n, s) != cudaSuccess ||
+      launch_gemm_skinny(p, hi, lo, M, part, tickets, sms, false, s) != cudaSuccess)
+    r = TF_E_CUDA;
+  uint32_t e = 0;
+  if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                     cudaStreamSynchronize(s) != cudaSuccess))
+    r = TF_E_CUDA;
+  cudaFree(hi);
+  cudaFree(lo);
+  cudaFree(err);
+  cudaFree(tickets);
+  cudaFree(part);
   if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
   return r;
 }

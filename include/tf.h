@@ -68,7 +68,7 @@ typedef struct {
   int32_t n_codebooks;      /* ids per frame (10)                               */
   int32_t codebook_size;    /* rows of the fast head and of each codebook table */
   int32_t max_seq_len;      /* static slow KV length T                          */
-  int32_t max_batch;        /* sequences per context (this build: 1)            */
+  int32_t max_batch;        /* sequences per context, 1..32 (lockstep batch)    */
   float rms_eps, rope_theta;
   int32_t weight_dtype;     /* TF_WEIGHT_BF16 or TF_WEIGHT_FP8                  */
 } tf_config;
@@ -132,9 +132,15 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out);
  * Errors: TF_E_INVAL (unknown name, wrong shape or dtype), TF_E_CUDA. */
 tf_status tf_load_weights(tf_ctx* ctx, const tf_tensor* t, int32_t n);
 
-/* Prompt in, frame 0 out.  tokens: host int32 [B][P], ids in [0, text_vocab).
- * Resets every sequence to position 0, runs the slow decoder over the prompt
- * (positions 0..P-1), then selects frame 0 from the last row.
+/* Prompt in, frame 0 out.  tokens: host int32 [B][P], ids in [0, text_vocab),
+ * 1 <= B <= max_batch: B independent sequences with prompts of one length P.
+ * Resets every sequence to position 0, runs the slow decoder over each
+ * prompt (positions 0..P-1, the sequence's own KV cache), then selects frame
+ * 0 of every sequence from its last row.  The B sequences then decode in
+ * lockstep: each later decode call advances all B by one frame (B > 1 runs
+ * every linear layer as one skinny tensor-core GEMM over the B rows, see
+ * tf_op_gemm_skinny).  Sampling draws use the sequence index b as the
+ * Philox counter's third word.
  * forced: NULL, or host int32 [B][n_codebooks] ids that replace the selected
  *   ids wherever they are fed back (teacher forcing); frame0 still reports the
  *   library's own selections.
@@ -147,7 +153,8 @@ tf_status tf_prefill(tf_ctx* ctx, const int32_t* tokens, int32_t B, int32_t P,
                      int32_t* frame0, float* logits);
 
 /* One decode frame: feeds each sequence's last codebook-0 id at its next
- * position, emits the next frame.  Arguments as tf_prefill.  At position ==
+ * position, emits the next frame of every sequence of the last prefill.
+ * Arguments as tf_prefill (B = that prefill's B).  At position ==
  * max_seq_len returns TF_E_CAPACITY and changes nothing. */
 tf_status tf_decode_frame(tf_ctx* ctx, const tf_sampling* sampling,
                           const int32_t* forced, int32_t* frame, float* logits);
@@ -178,11 +185,15 @@ void tf_destroy(tf_ctx* ctx);
  * stream with CUDA events: `iters` back-to-back launches cycling through the
  * slow decoder's layers, so every launch streams a distinct weight from HBM.
  * which: 0 = gate/up GEMV (RMSNorm prologue, SwiGLU epilogue),
- *        1 = QKV GEMV, 2 = O GEMV, 3 = down GEMV.
+ *        1 = QKV GEMV, 2 = O GEMV, 3 = down GEMV;
+ *        4..7 = the same four layers as the batched step's skinny
+ *        tensor-core GEMMs over max_batch activation rows (needs
+ *        max_batch > 1; the RMSNorm runs in a separate row kernel there).
  * Outputs the mean device time per launch and the algorithmic bytes one
  * launch moves (weights + scales + activations in and out).  Touches only
- * scratch activations; the decode state is unchanged.  Needs loaded weights.
- * Errors: TF_E_INVAL, TF_E_STATE, TF_E_CUDA. */
+ * scratch activations and position 0 of the fast decoder's KV caches (which
+ * every frame rewrites before reading); the decode state is unchanged.
+ * Needs loaded weights.  Errors: TF_E_INVAL, TF_E_STATE, TF_E_CUDA. */
 tf_status tf_profile_kernel(tf_ctx* ctx, int32_t which, int32_t iters,
                             float* ms_per_launch, int64_t* bytes_per_launch);
 
@@ -263,6 +274,21 @@ tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, const uint1
  * Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA. */
 tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
                      void* stream);
+
+/* Skinny GEMM on the tensor cores, the batched decode step's matrix kernel
+ * (each linear layer of B lockstep sequences is a GEMM with B activation
+ * rows; tuna-fish README, "Inference estimation": decode streams every
+ * weight once per step, so one weight pass serves all B rows):
+ * C[m][n] = sum_k A[m][k] W[n][k] for M <= 64 rows.  Weight rows sit on the
+ * 128-row side of tcgen05.mma and the activation rows on its N side; K is
+ * split so that the grid covers the GPU and the splits are added in a fixed
+ * order (deterministic).  A: float32 [M][K] device, split into bf16 hi and lo
+ * parts as in tf_op_gemm; W: bf16 bits [N][K] device; C: float32 [M][N]
+ * device.  N even, K a multiple of 8 (ragged tiles are zero-filled).
+ * Allocates and frees its scratch.  Errors: TF_E_INVAL, TF_E_NOMEM,
+ * TF_E_CUDA, TF_E_TIMEOUT. */
+tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K,
+                            float* C, void* stream);
 
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype

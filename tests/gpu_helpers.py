@@ -40,41 +40,50 @@ def topk_robust(z, k, tol_abs, seed, frame, codebook, sequence=0, temperature=1.
 
 class TeacherForced:
     """Runs the oracle free (greedy or sampled) and the GPU with the
-    oracle's ids forced, frame by frame, keeping both sides' logits."""
+    oracle's ids forced, frame by frame, keeping both sides' logits; with
+    batch > 1, B independent sequences decode in lockstep on both sides."""
 
-    def __init__(self, dims, fmt="bf16", seed=0, weights=None, dec=None):
+    def __init__(self, dims, fmt="bf16", seed=0, weights=None, dec=None, batch=1):
         self.d = dims
+        self.batch = batch
         self.w = weights if weights is not None else make_weights(dims, seed)
-        self.ref = oracle.DualAROracle(dims, self.w, fmt)
-        self.dec = dec if dec is not None else Decoder(dims, fmt)
+        self.ref = oracle.DualAROracle(dims, self.w, fmt, batch=batch)
+        self.dec = dec if dec is not None else Decoder(dims, fmt, max_batch=batch)
         if dec is None:
             self.dec.load_weights(self.w)
-        self.frames = []
+        self.frames = []   # (frame t, sequence b, oracle ids, oracle logits, gpu ids, gpu logits)
+        self.t = 0
+
+    def _keep(self, rf, rz, gf, gz):
+        for b in range(self.batch):
+            self.frames.append((self.t, b, rf[b], rz[b], gf[b], gz[b]))
+        self.t += 1
 
     def prefill(self, prompt, sampling=None):
         rf, rz = self.ref.prefill(prompt, sampling)
         gf, gz = self.dec.prefill(prompt, sampling, forced=rf, logits=True)
-        self.frames.append((rf[0], rz[0], gf[0], gz[0]))
-        return self.frames[-1]
+        self.t = 0
+        self._keep(rf, rz, gf, gz)
+        return rf, rz, gf, gz
 
     def decode(self, sampling=None):
         rf, rz = self.ref.decode_frame(sampling)
         gf, gz = self.dec.decode_frame(sampling, forced=rf, logits=True)
-        self.frames.append((rf[0], rz[0], gf[0], gz[0]))
-        return self.frames[-1]
+        self._keep(rf, rz, gf, gz)
+        return rf, rz, gf, gz
 
     def check(self, tol, sampling=None):
-        """Asserts the parity gates on every frame; returns (worst rel-L2,
-        ids compared, ids skipped)."""
+        """Asserts the parity gates on every frame of every sequence; returns
+        (worst rel-L2, ids compared, ids skipped)."""
         worst, compared, skipped = 0.0, 0, 0
         k = int(sampling.get("top_k", 0)) if sampling else 0
-        for t, (rf, rz, gf, gz) in enumerate(self.frames):
+        for t, b, rf, rz, gf, gz in self.frames:
             for j in range(self.d.n_codebooks):
                 V = vocab_of(self.d, j)
                 o, g = rz[j, :V], gz[j, :V]
                 e = rel_l2(g, o)
                 worst = max(worst, e)
-                assert e <= tol, f"frame {t} codebook {j}: rel-L2 {e:.3e} > {tol}"
+                assert e <= tol, f"frame {t} sequence {b} codebook {j}: rel-L2 {e:.3e} > {tol}"
                 # size of the perturbation actually present in this vector
                 # (itself bounded by the rel-L2 gate above)
                 pert = 2.0 * float(np.max(np.abs(g.astype(np.float64) - o))) + 1e-6
@@ -82,17 +91,17 @@ class TeacherForced:
                     robust = margin(o) > MARGIN
                 else:
                     robust = topk_robust(o, k, pert, int(sampling.get("seed", 0)), t, j,
-                                         0, float(sampling.get("temperature", 1.0)))
+                                         b, float(sampling.get("temperature", 1.0)))
                 if robust:
                     compared += 1
-                    assert gf[j] == rf[j], f"frame {t} codebook {j}: id {gf[j]} != {rf[j]}"
+                    assert gf[j] == rf[j], f"frame {t} sequence {b} codebook {j}: id {gf[j]} != {rf[j]}"
                 else:
                     skipped += 1
                     # the rest must still be valid: a near-tied argmax, or a
                     # member of the oracle's candidate set
                     if k <= 1:
-                        assert o[gf[j]] >= np.max(o) - MARGIN, (t, j, gf[j])
+                        assert o[gf[j]] >= np.max(o) - MARGIN, (t, b, j, gf[j])
                     else:
                         cand = oracle.topk_candidates(o.astype(np.float32), k + 2)
-                        assert gf[j] in set(int(c) for c in cand), (t, j, gf[j])
+                        assert gf[j] in set(int(c) for c in cand), (t, b, j, gf[j])
         return worst, compared, skipped

@@ -1,0 +1,204 @@
+"""GPU parity of batched decode: B independent sequences in lockstep, every
+linear layer one skinny tensor-core GEMM over the B activation rows.
+
+The oracle runs each sequence on its own (no batching in its arithmetic);
+the gates are those of single-sequence decode: logits relative L2 <= 1e-2
+(bf16) / 2e-2 (fp8) for every sequence, codebook and frame under teacher
+forcing, ids equal wherever the oracle's margin allows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dual_ar_decode_gb300 import Decoder, TfError, op_gemm_skinny
+from synth import FULL, TINY, make_prompt, make_weights, f32_to_bf16_bits
+
+from gpu_helpers import BF16_TOL, FP8_TOL, TeacherForced, rel_l2, vocab_of
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV)
+
+
+# ------------------------------------------------------------------ op
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (3, 200, 200), (16, 6144, 2560),
+                                   (32, 19456, 2560), (17, 2560, 9728), (64, 4096, 2560),
+                                   (2, 64, 256), (33, 2560, 4096), (16, 130, 72)])
+def test_skinny_gemm_matches_oracle(M, N, K):
+    """Split-K swap-AB tcgen05 GEMM against A @ W^T in float64, including
+    ragged weight tiles (N % 128) and ragged K slices (K % 64)."""
+    rng = np.random.default_rng(M * 13 + N + K)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    Wb = f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32) * 0.02)
+    Ad = torch.from_numpy(A).to(DEV)
+    Wd = dev_u16(Wb)
+    C = torch.full((M, N), np.nan, dtype=torch.float32, device=DEV)
+    op_gemm_skinny(Ad.data_ptr(), Wd.data_ptr(), M, N, K, C.data_ptr())
+    ref = oracle.linear(oracle.bf16_bits_to_f64(Wb), A.astype(np.float64))
+    got = C.cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.isfinite(got).all()
+    # as the prompt GEMM: bf16 hi + lo parts carry A to ~2^-17 relative, fp32
+    # accumulation in TMEM and over the K splits adds about as much again
+    assert np.max(np.abs(got - ref)) <= 2e-4 * rms
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-5
+
+
+def test_skinny_gemm_is_deterministic_and_rejects_bad_shapes():
+    rng = np.random.default_rng(3)
+    M, N, K = 16, 2560, 9728
+    Ad = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(DEV)
+    Wd = dev_u16(f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32) * 0.02))
+    outs = []
+    for _ in range(3):
+        C = torch.empty((M, N), dtype=torch.float32, device=DEV)
+        op_gemm_skinny(Ad.data_ptr(), Wd.data_ptr(), M, N, K, C.data_ptr())
+        outs.append(C.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    C = torch.empty((65, N), dtype=torch.float32, device=DEV)
+    with pytest.raises(TfError, match="INVAL"):      # more than 64 rows
+        op_gemm_skinny(Ad.data_ptr(), Wd.data_ptr(), 65, N, K, C.data_ptr())
+    with pytest.raises(TfError, match="INVAL"):      # odd N
+        op_gemm_skinny(Ad.data_ptr(), Wd.data_ptr(), M, N - 1, K, C.data_ptr())
+
+
+# ------------------------------------------------------------------ model
+
+TINY_ODD = TINY.replace(hidden=192, ffn=320, n_heads=4, n_kv_heads=4, head_dim=64,
+                        text_vocab=300, semantic_vocab=40, codebook_size=48, max_seq_len=40)
+TINY_G8 = TINY.replace(hidden=256, ffn=512, n_heads=8, n_kv_heads=1, head_dim=128,
+                       max_seq_len=64)
+
+
+@pytest.mark.parametrize("dims,fmt,tol,B,P", [(TINY, "bf16", BF16_TOL, 3, 16),
+                                              (TINY, "fp8", FP8_TOL, 2, 16),
+                                              (TINY_ODD, "bf16", BF16_TOL, 5, 12),
+                                              (TINY_G8, "bf16", BF16_TOL, 4, 40),
+                                              (TINY, "bf16", BF16_TOL, 32, 8)])
+def test_tiny_batched_teacher_forced(dims, fmt, tol, B, P):
+    """B sequences with their own prompts; P = 40 reaches the split
+    attention path (more than 32 keys) with one ticket per row."""
+    tf = TeacherForced(dims, fmt, seed=0, batch=B)
+    tf.prefill(make_prompt(dims, P, seed=10, batch=B))
+    for _ in range(5):
+        tf.decode()
+    worst, compared, skipped = tf.check(tol)
+    assert compared > 0.5 * (compared + skipped)
+    tf.dec.close()
+
+
+@pytest.mark.parametrize("k", [30, 4])
+def test_tiny_batched_topk_teacher_forced(k):
+    """Sampling draws per sequence: Philox counter (frame, codebook, sequence)."""
+    s = {"top_k": k, "seed": 99}
+    tf = TeacherForced(TINY, "bf16", seed=0, batch=4)
+    tf.prefill(make_prompt(TINY, 16, seed=3, batch=4), s)
+    for _ in range(4):
+        tf.decode(s)
+    worst, compared, skipped = tf.check(BF16_TOL, s)
+    assert compared >= 20
+    tf.dec.close()
+
+
+def test_batched_decode_frames_equal_single_calls_and_deterministic():
+    w = make_weights(TINY, seed=5)
+    prompt = make_prompt(TINY, 12, seed=5, batch=5)
+    runs = []
+    for mode in ("single", "batched", "batched"):
+        dec = Decoder(TINY, "bf16", max_batch=8)
+        dec.load_weights(w)
+        f0, _ = dec.prefill(prompt)
+        if mode == "single":
+            fr = np.stack([dec.decode_frame()[0] for _ in range(6)])
+        else:
+            fr = dec.decode_frames(6)
+        assert fr.shape == (6, 5, 10)
+        runs.append(np.concatenate([f0[None], fr]))
+        dec.close()
+    assert np.array_equal(runs[0], runs[1]) and np.array_equal(runs[1], runs[2])
+
+
+def test_batch_size_changes_and_errors():
+    """Prefills of different B on one context; B beyond max_batch and a bad
+    forced row are refused without changing the state."""
+    d = TINY
+    w = make_weights(d, seed=6)
+    dec = Decoder(d, "bf16", max_batch=4)
+    dec.load_weights(w)
+    with pytest.raises(TfError, match="INVAL"):
+        dec.prefill(make_prompt(d, 4, batch=5))
+    f3, _ = dec.prefill(make_prompt(d, 6, seed=1, batch=3))
+    assert f3.shape == (3, 10)
+    bad = np.zeros((3, 10), np.int32)
+    bad[2, 4] = d.codebook_size
+    with pytest.raises(TfError, match="INVAL"):
+        dec.decode_frame(forced=bad)
+    g3, _ = dec.decode_frame()
+    assert g3.shape == (3, 10)
+    # back to one sequence (the batch-1 kernels) and again to four
+    ref1 = oracle.DualAROracle(d, w)
+    rf, rz = ref1.prefill(make_prompt(d, 6, seed=2))
+    gf, gz = dec.prefill(make_prompt(d, 6, seed=2), forced=rf, logits=True)
+    for j in range(10):
+        V = vocab_of(d, j)
+        assert rel_l2(gz[0, j, :V], rz[0, j, :V]) <= BF16_TOL
+    f4, _ = dec.prefill(make_prompt(d, 6, seed=3, batch=4))
+    assert dec.decode_frames(3).shape == (3, 4, 10)
+    dec.close()
+
+
+# ------------------------------------------------------------------ full size
+
+def test_full_size_batched16_sampled_sequences():
+    """Full-size model, 16 sequences, KV length 4096 (the batched benchmark's
+    context), prompts of 64 tokens (more than 32 keys: split attention),
+    2 decode frames.  The oracle runs sequences 0 and 15 on their own; the
+    other sequences are teacher-forced with fixed ids."""
+    d = FULL.replace(max_seq_len=4096)
+    B, P = 16, 64
+    w = make_weights(d, seed=0)
+    prompts = make_prompt(d, P, seed=20, batch=B)
+    checked = (0, 15)
+    refs = {b: oracle.DualAROracle(d, w) for b in checked}
+    dec = Decoder(d, "bf16", max_batch=B)
+    dec.load_weights(w)
+    forced = np.zeros((B, 10), np.int32)
+    ref_out = {}
+    for b in checked:
+        ref_out[b] = refs[b].prefill(prompts[b:b + 1])
+        forced[b] = ref_out[b][0][0]
+    gf, gz = dec.prefill(prompts, forced=forced, logits=True)
+    results = [(ref_out, gf, gz)]
+    for _ in range(2):
+        ref_out = {b: refs[b].decode_frame() for b in checked}
+        for b in checked:
+            forced[b] = ref_out[b][0][0]
+        gf, gz = dec.decode_frame(forced=forced, logits=True)
+        results.append((ref_out, gf, gz))
+    compared = 0
+    for t, (ro, gf, gz) in enumerate(results):
+        for b in checked:
+            rf, rz = ro[b][0][0], ro[b][1][0]
+            for j in range(10):
+                V = vocab_of(d, j)
+                e = rel_l2(gz[b, j, :V], rz[j, :V])
+                assert e <= BF16_TOL, (t, b, j, e)
+                s = np.sort(rz[j, :V])
+                if s[-1] - s[-2] > 5e-2:
+                    compared += 1
+                    assert gf[b, j] == rf[j], (t, b, j)
+    assert compared >= 30
+    dec.close()

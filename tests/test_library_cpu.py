@@ -52,7 +52,8 @@ def test_destroy_null_and_last_error(L):
     (dict(n_codebooks=8), b"n_codebooks"),
     (dict(semantic_vocab=10_000), b"semantic_vocab"),
     (dict(max_seq_len=5), b"max_seq_len"),
-    (dict(max_batch=2), b"max_batch"),
+    (dict(max_batch=0), b"max_batch"),
+    (dict(max_batch=33), b"max_batch"),
     (dict(hidden=250), b"hidden"),
 ])
 def test_create_rejects_bad_config_before_touching_a_device(L, change, needle):
@@ -80,3 +81,7 @@ def test_op_argument_validation_is_host_side(L):
     assert L.tf_op_select(None, 1, 64, ctypes.byref(s), 0, 0, 0, None, None) == 1
     assert L.tf_op_quantize_fp8(None, 1, 16, None, None, None) == 1
     assert L.tf_op_gemv(None, 0, None, 1, 16, None, None, 1, None, None) == 1
+    assert L.tf_op_gemm_skinny(None, None, 16, 256, 256, None, None) == 1
+    assert L.tf_op_gemm_skinny(1, 1, 65, 256, 256, 1, None) == 1   # more than 64 rows
+    assert L.tf_op_gemm_skinny(1, 1, 16, 255, 256, 1, None) == 1   # odd N
+    assert L.tf_op_gemm_skinny(1, 1, 16, 256, 100, 1, None) == 1   # K not a multiple of 8

@@ -60,11 +60,11 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   return v;
 }
 
-// Pair epilogue for RoPE-ordered q/k rows and plain v rows.
-__device__ __forceinline__ void epi_qkv_pair(const GemvParams& p, int m, int pair, float v0,
-                                             float v1) {
+// Pair epilogue for RoPE-ordered q/k rows and plain v rows, given row m's
+// position and the (cos, sin) of this pair at that position (unused for v).
+__device__ __forceinline__ void epi_qkv_pair_at(const GemvParams& p, int m, int pair, float v0,
+                                                float v1, int pos, float2 cs) {
   const int half = p.head_dim >> 1;
-  const int pos = row_pos(p, m);
   if (pos < 0 || pos >= p.T) {
     atomicOr(p.err, ERR_BAD_POS);
     return;
@@ -74,7 +74,6 @@ __device__ __forceinline__ void epi_qkv_pair(const GemvParams& p, int m, int pai
     const bool isq = pair < qp;
     const int pr = isq ? pair : pair - qp;
     const int h = pr / half, i = pr - h * half;
-    const float2 cs = __ldg(&p.rope[(size_t)pos * half + i]);
     const float r0 = v0 * cs.x - v1 * cs.y;
     const float r1 = v1 * cs.x + v0 * cs.y;
     if (isq) {
@@ -93,6 +92,23 @@ __device__ __forceinline__ void epi_qkv_pair(const GemvParams& p, int m, int pai
     v[0] = f32_to_bf16(v0);
     v[1] = f32_to_bf16(v1);
   }
+}
+
+// (cos, sin) of a q/k pair at a position; (1, 0) for v pairs and positions
+// outside the table (the caller reports those).
+__device__ __forceinline__ float2 qkv_pair_rope(const GemvParams& p, int pair, int pos) {
+  const int half = p.head_dim >> 1;
+  const int qp = p.q_dim >> 1, kp = p.kv_dim >> 1;
+  if (pair >= qp + kp || pos < 0 || pos >= p.T) return make_float2(1.f, 0.f);
+  const int pr = pair < qp ? pair : pair - qp;
+  return __ldg(&p.rope[(size_t)pos * half + (pr % half)]);
+}
+
+// Pair epilogue for RoPE-ordered q/k rows and plain v rows.
+__device__ __forceinline__ void epi_qkv_pair(const GemvParams& p, int m, int pair, float v0,
+                                             float v1) {
+  const int pos = row_pos(p, m);
+  epi_qkv_pair_at(p, m, pair, v0, v1, pos, qkv_pair_rope(p, pair, pos));
 }
 
 // SwiGLU output u = silu(gate) * up of row m, column i: fp32, or bf16 hi / lo

@@ -74,7 +74,21 @@ struct GemvParams {
   const int32_t* forced;     // forced id slot (if *forced_on)
   const int32_t* forced_on;
   uint32_t* err;
+  // Deferred RMSNorm of the skinny tensor-core GEMM (batched decode).
+  // RMSNorm(x) * w = rstd * (x * w) with rstd = 1 / sqrt(mean(x^2) + eps), a
+  // per-row scalar, so W (RMSNorm(x) * w) = rstd * W (x * w): the GEMM that
+  // produces x emits x * w as bf16 parts plus partial sums of x^2, and the
+  // GEMM that consumes it scales its rows by rstd in the epilogue.
+  const uint16_t* nw_next;   // producer (EPI_RESID): norm weight of the consumer
+  uint16_t* nx_hi;           //   x * nw_next as bf16 hi / lo parts [M][ldo]
+  uint16_t* nx_lo;
+  float* ssq_out;            //   sum of x^2 over this tile's columns: [tile][kSsqRows]
+  const float* ssq_in;       // consumer: partial sums [ssq_n][kSsqRows] of its rows
+  int32_t ssq_n;
+  int32_t in_rps;            // consumer row m is producer row m * in_rps + in_rps - 1
+                             // (activation parts and sums); 0 or 1: the same row
 };
+constexpr int kSsqRows = 64;   // row stride of the partial sums of squares
 
 // Shared memory bytes a launch with these params needs.
 size_t gemv_smem_bytes(const GemvParams& p, int M);
@@ -130,6 +144,11 @@ struct BuildParams {
   float eps;
   float* x;                // output rows [M][H]
   uint32_t* err;
+  // optional, for the skinny GEMM that reads the rows next (see GemvParams):
+  const uint16_t* nw_next; // x * nw_next as bf16 parts [M][H], sum of x^2 per row
+  uint16_t* nx_hi;
+  uint16_t* nx_lo;
+  float* ssq_out;          // [kSsqRows]
 };
 cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s);
 
@@ -211,10 +230,10 @@ size_t skinny_part_floats(int N, int K, int M, int num_sms);
 cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo,
                                int M, float* part, uint32_t* tickets, int num_sms, bool pdl,
                                cudaStream_t s);
-// a = RMSNorm(x[m]) * w (w null: a = x[m]) for M rows x[m * ldx], written as
-// bf16 hi / lo parts [M][K].
-cudaError_t launch_rows_split(const float* x, int ldx, int M, int K, const uint16_t* w, float eps,
-                              uint16_t* hi, uint16_t* lo, bool pdl, cudaStream_t s);
+// Rows for a skinny GEMM with a deferred RMSNorm: a = x[m] * w as bf16 hi / lo
+// parts [M][K] and ssq[m] = sum_k x[m][k]^2, for M rows x[m * ldx].
+cudaError_t launch_rows_prep(const float* x, int ldx, int M, int K, const uint16_t* w,
+                             uint16_t* hi, uint16_t* lo, float* ssq, bool pdl, cudaStream_t s);
 // e4m3 codes -> bf16 bits of the same values (n even).
 cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaStream_t s);
 // hi = bf16(a), lo = bf16(a - hi) elementwise.

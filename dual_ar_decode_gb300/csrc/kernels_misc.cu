@@ -39,6 +39,22 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 }
 
 // ------------------------------------------------------------------ build
+// Row m of a decoder pass's input as the skinny GEMM reads it: x * nw_next
+// as bf16 parts and the row's sum of squares (deferred RMSNorm).
+__device__ void build_norm_out(const BuildParams& p, int m, const float* xo, float* red) {
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < p.H; k += blockDim.x) {
+    const float v = xo[k];
+    ss = fmaf(v, v, ss);
+    const float a = v * bf16_to_f32(p.nw_next[k]);
+    const uint16_t h = f32_to_bf16(a);
+    p.nx_hi[(size_t)m * p.H + k] = h;
+    p.nx_lo[(size_t)m * p.H + k] = f32_to_bf16(a - bf16_to_f32(h));
+  }
+  ss = block_sum_256(ss, red);
+  if (threadIdx.x == 0) p.ssq_out[m] = ss;
+}
+
 // Rows that start a decoder pass (see BuildMode).  fp32 residual rows; one
 // CTA per row.
 __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
@@ -59,6 +75,10 @@ __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
       ss = block_sum_256(ss, red);
       const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.H) + p.eps);
       for (int k = tid; k < p.H; k += blockDim.x) xo[k] = xs[k] * rstd * bf16_to_f32(p.nw[k]);
+      if (p.nx_hi) {
+        __syncthreads();
+        build_norm_out(p, m, xo, red);
+      }
       return;
     }
     id = p.ids[(size_t)b * p.id_stride];
@@ -73,6 +93,7 @@ __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
   }
   const uint16_t* row = p.table + (size_t)(p.row_base + id) * p.H;
   for (int k = tid; k < p.H; k += blockDim.x) xo[k] = bf16_to_f32(row[k]);
+  if (p.nx_hi) build_norm_out(p, m, xo, red);
 }
 
 // ------------------------------------------------------------------ frame end
@@ -368,29 +389,27 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* x, const uint
     a[(size_t)m * H + k] = xm[k] * rstd * bf16_to_f32(w[k]);
 }
 
-// Activation rows for the skinny tensor-core GEMM: a = RMSNorm(x[m]) * w (or
-// x[m] when w is null) as bf16 hi / lo parts; one CTA per row.
-__global__ void __launch_bounds__(256) k_rows_split(const float* x, int ldx, int K,
-                                                    const uint16_t* w, float eps, uint16_t* hi,
-                                                    uint16_t* lo) {
+// Rows for a skinny GEMM with a deferred RMSNorm: x[m] * w as bf16 hi / lo
+// parts and the row's sum of squares; one CTA per row.
+__global__ void __launch_bounds__(256) k_rows_prep(const float* x, int ldx, int K,
+                                                   const uint16_t* w, uint16_t* hi, uint16_t* lo,
+                                                   float* ssq) {
   __shared__ float red[32];
   pdl_launch_dependents();
   pdl_wait();
   const int m = blockIdx.x;
   const float* xm = x + (size_t)m * ldx;
-  float rstd = 1.0f;
-  if (w) {
-    float ss = 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
-    ss = block_sum_256(ss, red);
-    rstd = 1.0f / sqrtf(ss / static_cast<float>(K) + eps);
-  }
+  float ss = 0.f;
   for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    const float a = w ? xm[k] * rstd * bf16_to_f32(w[k]) : xm[k];
+    const float v = xm[k];
+    ss = fmaf(v, v, ss);
+    const float a = w ? v * bf16_to_f32(w[k]) : v;
     const uint16_t h = f32_to_bf16(a);
     hi[(size_t)m * K + k] = h;
     lo[(size_t)m * K + k] = f32_to_bf16(a - bf16_to_f32(h));
   }
+  ss = block_sum_256(ss, red);
+  if (ssq && threadIdx.x == 0) ssq[m] = ss;
 }
 
 // C[m][n] = sum_k A[m][k] W[n][k], 64x64 tile per CTA, 4x4 per thread,
@@ -533,13 +552,13 @@ cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_rows_split(const float* x, int ldx, int M, int K, const uint16_t* w, float eps,
-                              uint16_t* hi, uint16_t* lo, bool pdl, cudaStream_t s) {
+cudaError_t launch_rows_prep(const float* x, int ldx, int M, int K, const uint16_t* w,
+                             uint16_t* hi, uint16_t* lo, float* ssq, bool pdl, cudaStream_t s) {
   if (M < 1) return cudaSuccess;
-  if (cudaError_t e = carveout(k_rows_split)) return e;
+  if (cudaError_t e = carveout(k_rows_prep)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), 0, pdl, s, attr);
-  return cudaLaunchKernelEx(&cfg, k_rows_split, x, ldx, K, w, eps, hi, lo);
+  return cudaLaunchKernelEx(&cfg, k_rows_prep, x, ldx, K, w, hi, lo, ssq);
 }
 
 cudaError_t launch_gemm_rows(const GemvParams& p, int wt, int M, cudaStream_t s) {

@@ -248,6 +248,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
 }
@@ -263,8 +272,39 @@ __device__ __forceinline__ void epi_bar_sync() {
 // each CTA stores its partial [128][NB] and takes a ticket; the last CTA of
 // the tile adds the partials in split order (deterministic) and runs the
 // epilogue.  Rows n >= N and k >= K come in as zeros (TMA out-of-bounds fill).
-constexpr int kSkStages = 4;
+#ifndef TF_SKINNY_STAGES
+#define TF_SKINNY_STAGES 4
+#endif
+#ifndef TF_SKINNY_CTAS_PER_SM
+#define TF_SKINNY_CTAS_PER_SM 2
+#endif
+#ifndef TF_SKINNY_PREFETCH
+#define TF_SKINNY_PREFETCH 8   // weight slices requested into L2 ahead of the ring
+#endif
+constexpr int kSkPrefetch = TF_SKINNY_PREFETCH;
+
+// Fire-and-forget request of one weight box into L2.
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+constexpr int kSkStages = TF_SKINNY_STAGES;
 constexpr int kSkThreads = 6 * 32;
+
+// Ticket of a split-K tile: the add releases this CTA's partial (stored by
+// the four epilogue warps before the barrier that precedes it) and acquires
+// the partials of the CTAs that came earlier.
+__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* t) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
 
 template <int NB>
 struct Skinny {
@@ -275,11 +315,15 @@ struct Skinny {
   // kind::f16, fp32 accumulate, bf16 A and B, both K-major, M = 128, N = NB.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                      ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-  static constexpr size_t kSmem = 1024 + (size_t)kSkStages * kStage + (2 * kSkStages + 1) * 8 + 32;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kSkStages * kStage + (2 * kSkStages + 2) * 8 + 64 + (64 + 4 * NB) * 4;
+  // one split's partial of a tile: [NB][128] fp32
+  static constexpr uint32_t kChunk = NB * 128 * 4;
+  static constexpr int kChunksPerRound = (kSkStages * kStage) / kChunk;
 };
 
 template <int NB>
-__global__ void __launch_bounds__(kSkThreads, 1)
+__global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM : 1)
     k_umma_skinny(const __grid_constant__ CUtensorMap map_w,
                   const __grid_constant__ CUtensorMap map_ahi,
                   const __grid_constant__ CUtensorMap map_alo, const GemvParams p, int M, int S,
@@ -292,10 +336,15 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSkStages * C::kStage);
   uint64_t* empty = full + kSkStages;
   uint64_t* done = empty + kSkStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* red = done + 1;   // split partials staged into the (idle) ring
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* last_flag = tmem_slot + 2;
   volatile uint32_t* consumed = tmem_slot + 3;   // k slices the MMA warp took
+  volatile uint32_t* okv = tmem_slot + 4;        // [4] epilogue warps' verdicts
+  volatile uint32_t* red_fail = tmem_slot + 8;   // a staging wait expired
+  float* rstd_s = reinterpret_cast<float*>(tmem_slot + 16);  // [64] row rstd
+  float* red_s = rstd_s + 64;                               // [4][NB] sums of squares
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
@@ -312,8 +361,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
+    mbar_init(red, 1);
     *abort_flag = 0;
     *consumed = 0;
+    *red_fail = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -333,13 +384,21 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
+      prefetch_tensormap(&map_w);
+      prefetch_tensormap(&map_ahi);
+      prefetch_tensormap(&map_alo);
       // The weights do not depend on the previous kernel: fill the ring with
-      // weight slices first, then wait for the activations' producer.
+      // weight slices and ask L2 for the next kSkPrefetch slices, then wait
+      // for the activations' producer.  The L2 requests keep HBM busy while
+      // this kernel waits and while the ring drains; the ring's loads then
+      // mostly hit L2.
       const int pre = nkb < kSkStages ? nkb : kSkStages;
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], C::kStage);
         tma_load_2d_hint(smem + i * C::kStage, &map_w, (kb0 + i) * BK, n0, &full[i], pol);
       }
+      for (int i = pre; i < nkb && i < pre + kSkPrefetch; ++i)
+        tma_prefetch_l2(&map_w, (kb0 + i) * BK, n0);
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
         uint8_t* st = smem + i * C::kStage;
@@ -359,6 +418,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         tma_load_2d(st + C::kW, &map_ahi, (kb0 + i) * BK, 0, &full[s]);
         tma_load_2d(st + C::kW + C::kA, &map_alo, (kb0 + i) * BK, 0, &full[s]);
         issued = i + 1;
+        if (i + kSkPrefetch < nkb) tma_prefetch_l2(&map_w, (kb0 + i + kSkPrefetch) * BK, n0);
       }
       // After an abort, let the copies still in flight land before the CTA
       // leaves (bounded).
@@ -402,9 +462,36 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // ------------------------------------------------------------ epilogue
     pdl_wait();
     const int q = warp & 3;
-    const int nl = q * 32 + lane;  // weight row within the tile
+    const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    const int nl = q * 32 + lane;     // weight row within the tile (TMEM lane)
     const int n = n0 + nl;
-    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
+    // Everything the epilogue reads from global memory is loaded while the
+    // weights stream (the loads would otherwise queue behind its stores):
+    // the row rstd of a deferred RMSNorm, the residual, the RoPE factors.
+    if (p.ssq_in && et < M) {
+      const int r = p.in_rps > 1 ? et * p.in_rps + p.in_rps - 1 : et;
+      float ss = 0.f;
+      for (int t = 0; t < p.ssq_n; ++t) ss += p.ssq_in[t * kSsqRows + r];
+      rstd_s[et] = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
+    }
+    float xr[NB];                          // residual rows (EPI_RESID)
+    float2 cs_t = make_float2(1.f, 0.f);   // RoPE (cos, sin) of this thread's pair (EPI_QKV)
+    int pos0 = 0;
+    if (p.epi == EPI_RESID) {
+#pragma unroll
+      for (int c = 0; c < NB; ++c)
+        xr[c] = (c < M && n < p.N) ? p.out[(size_t)c * p.ldo + n] : 0.f;
+    } else if (p.epi == EPI_QKV) {
+      // pair (et & 63) of the tile, rows of parity et >> 6: with one or two
+      // rows per sequence they all sit at one position
+      pos0 = p.pos_ptr ? *p.pos_ptr : p.pos_fixed;
+      if (p.rps == 1 || p.rps == 2)
+        cs_t = qkv_pair_rope(p, (n0 >> 1) + (et & 63), pos0 + (p.rps == 2 ? (et >> 6) : 0));
+    }
+    const bool wok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
+    if (lane == 0) okv[q] = wok ? 1u : 0u;
+    epi_bar_sync();  // publishes rstd_s and every warp's verdict
+    const bool ok = okv[0] && okv[1] && okv[2] && okv[3];
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     float v[NB];
 #pragma unroll
@@ -418,65 +505,116 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         for (int i = 0; i < 16; ++i) v[c + i] = t[i];
       }
     }
-    bool run = ok;
+    bool run = ok;  // CTA-uniform from here on
     if (S > 1) {
-      float* mine = part + ((size_t)split * Np + n) * NB;
+      // this split's partial of the tile, [NB][128] (coalesced per row c)
+      float* mine = part + ((size_t)split * gridDim.x + tile) * (NB * 128);
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < NB; c += 4)
-          __stcg(reinterpret_cast<float4*>(mine + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+        for (int c = 0; c < NB; ++c) __stcg(mine + c * 128 + nl, v[c]);
       }
-      __threadfence();
       epi_bar_sync();
-      if (warp == 2 && lane == 0) {
-        const uint32_t t = atomicAdd(&tickets[tile], 1u);
+      if (et == 0) {
+        const uint32_t t = ticket_acq_rel(&tickets[tile]);
         *last_flag = (t == static_cast<uint32_t>(S) - 1u) ? 1u : 0u;
       }
       epi_bar_sync();
-      run = *last_flag != 0;
+      run = ok && *last_flag != 0;
       if (run) {
-        __threadfence();
+        // The last CTA of the tile stages all splits' partials into its ring
+        // (idle now: every MMA has completed) with bulk copies, one round
+        // trip per kChunksPerRound splits, and adds them in split order.
+        const float* st = reinterpret_cast<const float*>(smem);
 #pragma unroll
         for (int c = 0; c < NB; ++c) v[c] = 0.f;
-        for (int j = 0; j < S; ++j) {
-          const float* pj = part + ((size_t)j * Np + n) * NB;
-#pragma unroll
-          for (int c = 0; c < NB; c += 4) {
-            const float4 f = __ldcg(reinterpret_cast<const float4*>(pj + c));
-            v[c] += f.x;
-            v[c + 1] += f.y;
-            v[c + 2] += f.z;
-            v[c + 3] += f.w;
+        int round = 0;
+        for (int j0 = 0; j0 < S; j0 += C::kChunksPerRound, ++round) {
+          const int nr = (S - j0) < C::kChunksPerRound ? (S - j0) : C::kChunksPerRound;
+          if (*red_fail) break;  // CTA-uniform (read after a barrier)
+          if (et == 0) {
+            // the partials were written through the generic proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_arrive_expect_tx(red, nr * C::kChunk);
+            for (int r = 0; r < nr; ++r)
+              bulk_g2s_plain(smem + r * C::kChunk,
+                             part + ((size_t)(j0 + r) * gridDim.x + tile) * (NB * 128), C::kChunk, red);
           }
+          if (mbar_wait(red, round & 1, p.err)) {
+            for (int r = 0; r < nr; ++r) {
+#pragma unroll
+              for (int c = 0; c < NB; ++c) v[c] += st[(r * NB + c) * 128 + nl];
+            }
+          } else {
+            *red_fail = 1;
+          }
+          epi_bar_sync();  // the ring is refilled by the next round
         }
-        if (warp == 2 && lane == 0) tickets[tile] = 0u;
+        if (et == 0) tickets[tile] = 0u;
       }
     }
     if (run) {
       const float sc = (p.scale && n < p.N) ? __ldg(&p.scale[n]) : 1.0f;
 #pragma unroll
-      for (int c = 0; c < NB; ++c) v[c] *= sc;
+      for (int c = 0; c < NB; ++c)
+        v[c] *= p.ssq_in ? (c < M ? sc * rstd_s[c] : 0.f) : sc;
       if (p.epi == EPI_QKV || p.epi == EPI_SWIGLU) {
-        // rows (n, n + 1) pair up across neighbouring lanes; the even lane
-        // takes the even activation rows, the odd lane the odd ones.
-        const int pr = (n0 + (nl & ~1)) >> 1;
-        const bool odd = lane & 1;
+        // The tile's results go through shared memory (the ring is idle) so
+        // that the pair epilogue runs as one short loop: its code stays in
+        // the instruction cache instead of being fetched once per row.
+        // Thread et takes pair pl of the tile for the rows of parity par.
+        float* vs = reinterpret_cast<float*>(smem);
 #pragma unroll
-        for (int c = 0; c < NB; ++c) {
-          const float o = __shfl_xor_sync(0xFFFFFFFFu, v[c], 1);
-          if (c < M && (c & 1) == (odd ? 1 : 0) && 2 * pr < p.N) {
-            const float v0 = odd ? o : v[c], v1 = odd ? v[c] : o;
-            if (p.epi == EPI_QKV) epi_qkv_pair(p, c, pr, v0, v1);
-            else epi_swiglu(p, c, pr, v0, v1);
+        for (int c = 0; c < NB; ++c) vs[c * 128 + nl] = v[c];
+        epi_bar_sync();
+        const int pl = et & 63, par = et >> 6;
+        const int pair = (n0 >> 1) + pl;
+        if (2 * pair < p.N) {
+#pragma unroll 1
+          for (int c = par; c < M; c += 2) {
+            const float v0 = vs[c * 128 + 2 * pl], v1 = vs[c * 128 + 2 * pl + 1];
+            if (p.epi == EPI_QKV) {
+              const int pos = pos0 + (p.rps > 0 ? c % p.rps : c);
+              const bool pre = p.rps == 1 || p.rps == 2;  // position fixed by parity
+              epi_qkv_pair_at(p, c, pair, v0, v1, pos, pre ? cs_t : qkv_pair_rope(p, pair, pos));
+            } else {
+              epi_swiglu(p, c, pair, v0, v1);
+            }
           }
         }
-      } else if (n < p.N) {
+      } else {
+        // store / residual add; with nw_next also the consumer's input
+        // (x * nw_next as bf16 parts) and this tile's sums of x^2 per row
+        const bool nx = p.nx_hi != nullptr;
+        const float wn = (nx && n < p.N) ? bf16_to_f32(p.nw_next[n]) : 0.f;
 #pragma unroll
         for (int c = 0; c < NB; ++c) {
-          if (c >= M) break;
-          float* o = p.out + (size_t)c * p.ldo + n;
-          if (p.epi == EPI_RESID) *o += v[c];
-          else *o = v[c];
+          float xn = 0.f;
+          if (c < M && n < p.N) {
+            xn = p.epi == EPI_RESID ? xr[c] + v[c] : v[c];
+            p.out[(size_t)c * p.ldo + n] = xn;
+            if (nx) {
+              const float a = xn * wn;
+              const uint16_t h = f32_to_bf16(a);
+              p.nx_hi[(size_t)c * p.ldo + n] = h;
+              p.nx_lo[(size_t)c * p.ldo + n] = f32_to_bf16(a - bf16_to_f32(h));
+            }
+          }
+          v[c] = xn * xn;
+        }
+        if (nx) {
+#pragma unroll
+          for (int c = 0; c < NB; ++c) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v[c] += __shfl_xor_sync(0xFFFFFFFFu, v[c], o);
+          }
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < NB; ++c) red_s[q * NB + c] = v[c];
+          }
+          epi_bar_sync();
+          if (et < M)
+            p.ssq_out[tile * kSsqRows + et] =
+                ((red_s[et] + red_s[NB + et]) + red_s[2 * NB + et]) + red_s[3 * NB + et];
         }
       }
     }
@@ -535,12 +673,14 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// bf16 [rows][cols] row-major, box of 64 columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// bf16 [rows][cols] with rows `ld` elements apart (0: cols), box of 64
+// columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint64_t ld = 0) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {(ld ? ld : cols) * 2};
   const cuuint32_t box[2] = {BK, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -578,7 +718,7 @@ int skinny_nb(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
 int skinny_splits(int N, int K, int num_sms) {
   const int tiles = (N + 127) / 128, nk = (K + BK - 1) / BK;
-  const int target = 2 * num_sms;  // two CTAs per SM
+  const int target = TF_SKINNY_CTAS_PER_SM * num_sms;
   int S = (target + tiles / 2) / tiles;
   return std::max(1, std::min(S, nk));
 }
@@ -593,9 +733,12 @@ cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const 
                                cudaStream_t s) {
   if (M < 1 || M > 64 || p.N < 2 || (p.N & 1) || p.K < 8 || (p.K % 8)) return cudaErrorInvalidValue;
   const int NB = skinny_nb(M);
+  // activation row m is row m * in_rps + in_rps - 1 of the parts
+  const int rs = p.in_rps > 1 ? p.in_rps : 1;
+  const size_t a0 = (size_t)(rs - 1) * p.K;
   CUtensorMap mw, mhi, mlo;
-  if (!make_map(&mw, p.W, p.N, p.K, 128) || !make_map(&mhi, a_hi, M, p.K, NB) ||
-      !make_map(&mlo, a_lo, M, p.K, NB))
+  if (!make_map(&mw, p.W, p.N, p.K, 128) || !make_map(&mhi, a_hi + a0, M, p.K, NB, (size_t)rs * p.K) ||
+      !make_map(&mlo, a_lo + a0, M, p.K, NB, (size_t)rs * p.K))
     return cudaErrorInvalidValue;
   const int S = skinny_splits(p.N, p.K, num_sms);
   if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;

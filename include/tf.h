@@ -183,7 +183,9 @@ void tf_destroy(tf_ctx* ctx);
 /* Times one kernel of the decode frame in its in-frame configuration
  * (same parameters, prologue, epilogue and launch chaining) on the context's
  * stream with CUDA events: `iters` back-to-back launches cycling through the
- * slow decoder's layers, so every launch streams a distinct weight from HBM.
+ * slow decoder's layers (so every launch streams a distinct weight from HBM),
+ * captured as one CUDA graph like the decode frame and replayed once to
+ * warm up, then once timed.
  * which: 0 = gate/up GEMV (RMSNorm prologue, SwiGLU epilogue),
  *        1 = QKV GEMV, 2 = O GEMV, 3 = down GEMV;
  *        4..7 = the same four layers as the batched step's skinny

@@ -25,14 +25,21 @@ def margin(z):
 
 def topk_robust(z, k, tol_abs, seed, frame, codebook, sequence=0, temperature=1.0):
     """True when the top-k draw from logits z cannot change under logit
-    perturbations of size tol_abs: the k-th / (k+1)-th gap is wide, and the
-    draw u*S sits away from every running-sum boundary by more than the
-    relative change such a perturbation can make to the weights."""
+    perturbations of size tol_abs: the k-th / (k+1)-th gap is wide, the
+    picked candidate cannot trade places with a neighbour in the (logit
+    desc, index asc) order, and the draw u*S sits away from every running-sum
+    boundary by more than the relative change such a perturbation can make
+    to the weights."""
     z32 = np.asarray(z, np.float32)
     s = np.sort(z32.astype(np.float64))[::-1]
     if len(s) > k and (s[k - 1] - s[k]) <= 4 * tol_abs:
         return False
     _, det = oracle.topk_sample(z32, k, seed, frame, codebook, sequence, temperature)
+    zc = z32[det["cand"]].astype(np.float64)
+    i = det["pick"]
+    for nb in (i - 1, i + 1):
+        if 0 <= nb < len(zc) and abs(zc[i] - zc[nb]) <= 4 * tol_abs:
+            return False
     rel = 4 * tol_abs / temperature
     gaps = np.abs(det["c"].astype(np.float64) - float(det["t"]))
     return bool(np.min(gaps) > rel * float(det["S"]))

@@ -7,13 +7,17 @@
 // head h / (Hq/Hkv)), scaled by 1/sqrt(D), softmax over the keys.
 //
 // Flash-decode split: grid (S, Hkv, M).  CTA (s, g, m) takes a contiguous
-// slice of the key range and all Hq/Hkv query heads that share KV head g, so
-// every K/V row is read from HBM once per layer.  Each warp walks keys with
-// lanes across the head dimension (one coalesced 8-byte load per lane per
-// row, four rows in flight), keeps an online softmax per head, and the warps
-// merge in shared memory.  The last CTA of each (g, m) to finish (ticket on
-// a global counter) merges the S partials in split order, so the result is
-// deterministic, and re-arms the counter.
+// slice of row m's key range and all Hq/Hkv query heads that share KV head g,
+// so every K/V row is read from HBM once per layer.  The slice's K and V rows
+// are contiguous in the cache ([Hkv][T][D] per sequence), so the CTA stages
+// them into shared memory with bulk copies, 64 keys at a time, two chunks in
+// flight; scores, an online softmax per head and the weighted sum of V run
+// out of shared memory.  With more than one slice, each CTA publishes its
+// (max, sum, weighted V) and takes a ticket; the last CTA of each (g, m)
+// merges the slices in slice order (deterministic) and re-arms the counter.
+// Every dependent global round trip costs on this two-die part, so the kernel
+// issues each group of loads at once: the K/V chunks, then all slices'
+// (max, sum) pairs, then their weighted V in batches.
 #include <mutex>
 
 #include "../../include/tf.h"
@@ -24,9 +28,10 @@ namespace tf {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kUnroll = 4;
-constexpr int kMinKeys = 32;
+constexpr int kThreads = 256;
+constexpr int kChunk = 64;      // keys per staged chunk
+constexpr int kMinKeys = 32;    // keys per slice at least
+constexpr int kMaxSlices = 64;  // slices a combine can hold
 
 // Output element i of row data: fp32, or bf16 hi / lo parts for a GEMM that
 // reads its activations from the tensor cores.
@@ -40,15 +45,51 @@ __device__ __forceinline__ void store_out(const AttnParams& p, size_t i, float v
   }
 }
 
+__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* t) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
-  constexpr int DL = D / 32;  // dims per lane
+struct AttnSmem {
+  static constexpr int kRow = D * 2;                          // bytes of one K or V row
+  static constexpr int kBuf = kChunk * kRow;                  // one K (or V) chunk
+  static constexpr size_t kOffQ = 4 * (size_t)kBuf;           // K0 V0 K1 V1, then q
+  static constexpr size_t kOffSc = kOffQ + (size_t)G * D * 4;  // scores [G][kChunk]
+  static constexpr size_t kOffStat = kOffSc + (size_t)G * kChunk * 4;  // max, sum, rescale [G]
+  static constexpr size_t kOffBar = (kOffStat + 3 * G * 4 + 15) / 16 * 16;
+  static constexpr size_t kBytes = kOffBar + 2 * 8 + 16;
+  static_assert(4 * (size_t)kBuf >= 2 * (size_t)G * kMaxSlices * 4 + G * 4,
+                "the combine's statistics reuse the K/V buffers");
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads) k_attn(const AttnParams p) {
+  using SL = AttnSmem<D, G>;
+  constexpr int DL = D / 32;                                 // dims per lane (score step)
+  constexpr int NP = (G * D + kThreads - 1) / kThreads;      // (head, dim) outputs per thread
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint16_t* kv = reinterpret_cast<uint16_t*>(sm);
+  float* q_s = reinterpret_cast<float*>(sm + SL::kOffQ);
+  float* sc = reinterpret_cast<float*>(sm + SL::kOffSc);
+  float* m_run = reinterpret_cast<float*>(sm + SL::kOffStat);
+  float* l_run = m_run + G;
+  float* corr = l_run + G;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SL::kOffBar);
+  volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(bar + 2);
+
   const int s = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  __shared__ float sm_m[kWarps][G], sm_l[kWarps][G];
-  __shared__ float sm_acc[kWarps][G][D];
-  __shared__ float sm_f[G][D + 2];
-  __shared__ uint32_t sm_last;
 
   pdl_launch_dependents();
   pdl_wait();
@@ -60,161 +101,215 @@ __global__ void __launch_bounds__(kWarps * 32) k_attn(const AttnParams p) {
     return;
   }
   const int n = pos + 1;
-  // At least kMinKeys keys per split: short contexts use fewer CTAs.
+  // At least kMinKeys keys per slice: short contexts use fewer CTAs.
   const int L = max((n + p.S - 1) / p.S, kMinKeys);
   const int sact = (n + L - 1) / L;
   if (s >= sact) return;
-  const int k0 = s * L, k1 = min(n, k0 + L);
+  const int k0 = s * L, nk = min(n, k0 + L) - k0;
+  const int nch = (nk + kChunk - 1) / kChunk;
+  const uint16_t* Kg = p.Kc + kvo + ((size_t)g * p.T + k0) * D;
+  const uint16_t* Vg = p.Vc + kvo + ((size_t)g * p.T + k0) * D;
 
+  auto issue = [&](int ch) {  // one thread: chunk ch of K and V into buffer ch & 1
+    const int b = ch & 1;
+    const int rows = min(kChunk, nk - ch * kChunk);
+    const uint32_t bytes = static_cast<uint32_t>(rows * SL::kRow);
+    mbar_arrive_expect_tx(&bar[b], 2 * bytes);
+    bulk_g2s_plain(kv + (size_t)(2 * b) * kChunk * D, Kg + (size_t)ch * kChunk * D, bytes, &bar[b]);
+    bulk_g2s_plain(kv + (size_t)(2 * b + 1) * kChunk * D, Vg + (size_t)ch * kChunk * D, bytes,
+                   &bar[b]);
+  };
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    *flag = 0u;
+    issue(0);
+    if (nch > 1) issue(1);
+  }
   // Queries of the G heads of this group, pre-scaled by 1/sqrt(D).
   const float scale = rsqrtf(static_cast<float>(D));
-  float q[G][DL];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const float* qh = p.q + (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + lane * DL;
-#pragma unroll
-    for (int d = 0; d < DL; ++d) q[h][d] = qh[d] * scale;
+  for (int e = tid; e < G * D; e += kThreads) {
+    const int h = e / D, d = e - h * D;
+    q_s[e] = p.q[(size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d] * scale;
   }
-
-  float mx[G], l[G], acc[G][DL];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mx[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int d = 0; d < DL; ++d) acc[h][d] = 0.f;
+  if (tid < G) {
+    m_run[tid] = -INFINITY;
+    l_run[tid] = 0.f;
   }
+  __syncthreads();
 
-  const uint16_t* Kg = p.Kc + kvo + (size_t)g * p.T * D + lane * DL;
-  const uint16_t* Vg = p.Vc + kvo + (size_t)g * p.T * D + lane * DL;
-  for (int t0 = k0 + warp * kUnroll; t0 < k1; t0 += kWarps * kUnroll) {
-    // Load up to kUnroll rows of K and V (DL bf16 per lane).
-    uint32_t kr[kUnroll][DL / 2], vr[kUnroll][DL / 2];
+  float acc[NP];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = t0 + u;
-      if (t < k1) {
-        if constexpr (DL == 4) {
-          const uint2 kk = *reinterpret_cast<const uint2*>(Kg + (size_t)t * D);
-          const uint2 vv = *reinterpret_cast<const uint2*>(Vg + (size_t)t * D);
-          kr[u][0] = kk.x; kr[u][1] = kk.y;
-          vr[u][0] = vv.x; vr[u][1] = vv.y;
-        } else {
-          kr[u][0] = *reinterpret_cast<const uint32_t*>(Kg + (size_t)t * D);
-          vr[u][0] = *reinterpret_cast<const uint32_t*>(Vg + (size_t)t * D);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (t0 + u >= k1) break;
-      float kf[DL], vf[DL];
-#pragma unroll
-      for (int i = 0; i < DL / 2; ++i) {
-        kf[2 * i] = bf16_lo(kr[u][i]);
-        kf[2 * i + 1] = bf16_hi(kr[u][i]);
-        vf[2 * i] = bf16_lo(vr[u][i]);
-        vf[2 * i + 1] = bf16_hi(vr[u][i]);
+  for (int i = 0; i < NP; ++i) acc[i] = 0.f;
+  for (int ch = 0; ch < nch; ++ch) {
+    const int b = ch & 1;
+    const int rows = min(kChunk, nk - ch * kChunk);
+    const bool got = mbar_wait(&bar[b], (ch >> 1) & 1, p.err);
+    if (__syncthreads_or(got ? 0 : 1)) return;  // expired (reported): give up together
+    const uint16_t* Ks = kv + (size_t)(2 * b) * kChunk * D;
+    const uint16_t* Vs = Ks + (size_t)kChunk * D;
+    // scores: warp w takes keys w, w + 8, ...; lanes across the head dimension
+    for (int t = warp; t < rows; t += kThreads / 32) {
+      float kf[DL];
+      if constexpr (DL == 4) {
+        const uint2 kk = *reinterpret_cast<const uint2*>(Ks + (size_t)t * D + lane * DL);
+        kf[0] = bf16_lo(kk.x);
+        kf[1] = bf16_hi(kk.x);
+        kf[2] = bf16_lo(kk.y);
+        kf[3] = bf16_hi(kk.y);
+      } else {
+        const uint32_t kk = *reinterpret_cast<const uint32_t*>(Ks + (size_t)t * D + lane * DL);
+        kf[0] = bf16_lo(kk);
+        kf[1] = bf16_hi(kk);
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float sc = 0.f;
+        float d = 0.f;
 #pragma unroll
-        for (int d = 0; d < DL; ++d) sc = fmaf(q[h][d], kf[d], sc);
-        sc = warp_sum(sc);
-        const float mn = fmaxf(mx[h], sc);
-        const float corr = expf(mx[h] - mn);
-        const float pr = expf(sc - mn);
-        l[h] = l[h] * corr + pr;
-#pragma unroll
-        for (int d = 0; d < DL; ++d) acc[h][d] = fmaf(acc[h][d], corr, pr * vf[d]);
-        mx[h] = mn;
+        for (int i = 0; i < DL; ++i) d = fmaf(q_s[h * D + lane * DL + i], kf[i], d);
+        d = warp_sum(d);
+        if (lane == 0) sc[h * kChunk + t] = d;
       }
     }
-  }
-
-  // Merge the warps of this CTA.
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    if (lane == 0) {
-      sm_m[warp][h] = mx[h];
-      sm_l[warp][h] = l[h];
+    __syncthreads();
+    // online softmax: warp h updates head h's running max and sum
+    if (warp < G) {
+      const int h = warp;
+      float mx = -INFINITY;
+      for (int t = lane; t < rows; t += 32) mx = fmaxf(mx, sc[h * kChunk + t]);
+      mx = warp_max(mx);
+      const float mo = m_run[h];
+      const float mn = fmaxf(mo, mx);
+      float sum = 0.f;
+      for (int t = lane; t < rows; t += 32) {
+        const float e = expf(sc[h * kChunk + t] - mn);
+        sc[h * kChunk + t] = e;
+        sum += e;
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) {
+        const float cr = expf(mo - mn);
+        corr[h] = cr;
+        l_run[h] = l_run[h] * cr + sum;
+        m_run[h] = mn;
+      }
     }
+    __syncthreads();
+    // weighted V: thread owns (head, dim) outputs
 #pragma unroll
-    for (int d = 0; d < DL; ++d) sm_acc[warp][h][lane * DL + d] = acc[h][d];
-  }
-  __syncthreads();
-  for (int e = tid; e < G * D; e += kWarps * 32) {
-    const int h = e / D, d = e - h * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
-    float Ls = 0.f, A = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      if (sm_m[w][h] == -INFINITY) continue;  // warp saw no keys
-      const float f = expf(sm_m[w][h] - M);
-      Ls += sm_l[w][h] * f;
-      A += sm_acc[w][h][d] * f;
+    for (int i = 0; i < NP; ++i) {
+      const int e = tid + i * kThreads;
+      if (e < G * D) {
+        const int h = e / D, d = e - h * D;
+        const float* ph = sc + h * kChunk;
+        float a = acc[i] * corr[h];
+        for (int t = 0; t < rows; ++t) a = fmaf(ph[t], bf16_to_f32(Vs[(size_t)t * D + d]), a);
+        acc[i] = a;
+      }
     }
-    sm_f[h][d] = A;
-    if (d == 0) {
-      sm_f[h][D] = M;
-      sm_f[h][D + 1] = Ls;
-    }
+    __syncthreads();  // buffer b is free again
+    if (tid == 0 && ch + 2 < nch) issue(ch + 2);
   }
-  __syncthreads();
 
   if (sact == 1) {
-    for (int e = tid; e < G * D; e += kWarps * 32) {
-      const int h = e / D, d = e - h * D;
-      store_out(p, (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d, sm_f[h][d] / sm_f[h][D + 1]);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const int e = tid + i * kThreads;
+      if (e < G * D) {
+        const int h = e / D, d = e - h * D;
+        store_out(p, (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d, acc[i] / l_run[h]);
+      }
     }
     return;
   }
 
-  // Publish this split's partial and take a ticket.
-  for (int e = tid; e < G * (D + 2); e += kWarps * 32) {
-    const int h = e / (D + 2), d = e - h * (D + 2);
-    p.part[(((size_t)m * p.Hq + g * G + h) * p.S + s) * (D + 2) + d] = sm_f[h][d];
+  // Publish this slice: part[m][head][slice][D + 2] = (weighted V, max, sum).
+  float* pb = p.part + ((size_t)m * p.Hq + (size_t)g * G) * p.S * (D + 2);
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int e = tid + i * kThreads;
+    if (e < G * D) {
+      const int h = e / D, d = e - h * D;
+      __stcg(pb + ((size_t)h * p.S + s) * (D + 2) + d, acc[i]);
+    }
   }
-  __threadfence();
+  if (tid < G) {
+    __stcg(pb + ((size_t)tid * p.S + s) * (D + 2) + D, m_run[tid]);
+    __stcg(pb + ((size_t)tid * p.S + s) * (D + 2) + D + 1, l_run[tid]);
+  }
   __syncthreads();
   if (tid == 0) {
-    const uint32_t t = atomicAdd(&p.counters[m * p.Hkv + g], 1u);
-    sm_last = (t == static_cast<uint32_t>(sact) - 1u);
+    const uint32_t t = ticket_acq_rel(&p.counters[m * p.Hkv + g]);
+    *flag = (t == static_cast<uint32_t>(sact) - 1u) ? 1u : 0u;
   }
   __syncthreads();
-  if (!sm_last) return;
-  __threadfence();
-  for (int e = tid; e < G * D; e += kWarps * 32) {
-    const int h = e / D, d = e - h * D;
-    const float* ph = p.part + (((size_t)m * p.Hq + g * G + h) * p.S) * (D + 2);
+  if (!*flag) return;
+
+  // Merge (last CTA): every slice's (max, sum) at once, then the slices'
+  // weights exp(max_j - max) and the total sum per head, then the weighted
+  // V of all slices in batches of independent loads.
+  float* wj = reinterpret_cast<float*>(kv);  // [G][sact]: max, then weight
+  float* lj = wj + G * kMaxSlices;           // [G][sact]: sums
+  float* lt = lj + G * kMaxSlices;           // [G]: total
+  for (int e = tid; e < G * sact; e += kThreads) {
+    const int h = e / sact, j = e - h * sact;
+    wj[h * kMaxSlices + j] = __ldcg(pb + ((size_t)h * p.S + j) * (D + 2) + D);
+    lj[h * kMaxSlices + j] = __ldcg(pb + ((size_t)h * p.S + j) * (D + 2) + D + 1);
+  }
+  __syncthreads();
+  if (warp < G) {
+    const int h = warp;
     float M = -INFINITY;
-    for (int j = 0; j < sact; ++j) M = fmaxf(M, __ldcg(ph + (size_t)j * (D + 2) + D));
-    float Ls = 0.f, A = 0.f;
-    for (int j = 0; j < sact; ++j) {
-      const float f = expf(__ldcg(ph + (size_t)j * (D + 2) + D) - M);
-      Ls += __ldcg(ph + (size_t)j * (D + 2) + D + 1) * f;
-      A += __ldcg(ph + (size_t)j * (D + 2) + d) * f;
+    for (int j = lane; j < sact; j += 32) M = fmaxf(M, wj[h * kMaxSlices + j]);
+    M = warp_max(M);
+    __syncwarp();
+    for (int j = lane; j < sact; j += 32) wj[h * kMaxSlices + j] = expf(wj[h * kMaxSlices + j] - M);
+    __syncwarp();
+    if (lane == 0) {  // total in slice order
+      float Ls = 0.f;
+      for (int j = 0; j < sact; ++j) Ls += lj[h * kMaxSlices + j] * wj[h * kMaxSlices + j];
+      lt[h] = Ls;
     }
-    store_out(p, (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d, A / Ls);
+  }
+  __syncthreads();
+  constexpr int kB = 16;  // independent loads in flight per thread
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int e = tid + i * kThreads;
+    if (e < G * D) {
+      const int h = e / D, d = e - h * D;
+      const float* ph = pb + (size_t)h * p.S * (D + 2) + d;
+      float A = 0.f;
+      for (int j0 = 0; j0 < sact; j0 += kB) {
+        float v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) v[u] = (j0 + u < sact) ? __ldcg(ph + (size_t)(j0 + u) * (D + 2)) : 0.f;
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+          if (j0 + u < sact) A = fmaf(v[u], wj[h * kMaxSlices + j0 + u], A);
+      }
+      store_out(p, (size_t)m * p.Hq * D + (size_t)(g * G + h) * D + d, A / lt[h]);
+    }
   }
   if (tid == 0) p.counters[m * p.Hkv + g] = 0u;
 }
 
 template <int D, int G>
 cudaError_t launch_dg(const AttnParams& p, int M, bool pdl, cudaStream_t s) {
+  using SL = AttnSmem<D, G>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = cudaFuncSetAttribute(k_attn<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SL::kBytes));
     if (e) return e;
     attr_set = true;
   }
+  if (p.S < 1 || p.S > kMaxSlices || M < 1) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, p.Hkv, M);
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SL::kBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -195,6 +195,46 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
       }
     }
   }
+  // Everything else the consumers will read from global memory is loaded
+  // now, in one round trip with the activations: the RMSNorm weight of their
+  // chunks, and the epilogue inputs of their first row (residual, or the
+  // position and RoPE factors of a q/k pair).
+  // (The RMSNorm inputs are hidden-size rows, J <= 2; wider variants keep
+  // their registers for the activations.)
+  constexpr int NWU = WT ? 2 : 1;  // 16-byte norm-weight pieces per chunk
+  constexpr bool kNwRegs = J <= 2;
+  uint4 nwc[kNwRegs ? J : 1][NWU];
+  if (kNwRegs && p.pro == PRO_NORM) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int ch = tid + j * NT;
+#pragma unroll
+      for (int u = 0; u < NWU; ++u)
+        nwc[j][u] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(p.nw + ch * EPC) + u)
+                             : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  const int nb0 = min(kRowBatch, nrows);
+  float xr0[M];
+  float2 cs0[M];
+  int pos0[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    xr0[m] = 0.f;
+    cs0[m] = make_float2(1.f, 0.f);
+    pos0[m] = 0;
+  }
+  if (p.epi == EPI_QKV && tid < (nb0 >> 1)) {
+    const int pair = (r0 >> 1) + tid;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      pos0[m] = row_pos(p, m);
+      cs0[m] = qkv_pair_rope(p, pair, pos0[m]);
+    }
+  } else if (p.epi == EPI_RESID && tid < nb0) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) xr0[m] = p.out[(size_t)m * p.ldo + r0 + tid];
+  }
   if (p.pro == PRO_NORM) {
 #pragma unroll
     for (int m = 0; m < M; ++m) {
@@ -214,11 +254,20 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
       const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        const int ch = tid + j * NT;
-        if (ch < nch) {
+        if constexpr (kNwRegs) {
+          const uint32_t* wv = reinterpret_cast<const uint32_t*>(&nwc[j][0]);
 #pragma unroll
-          for (int e = 0; e < EPC; ++e)
-            a[m][j][e] = a[m][j][e] * rstd * bf16_to_f32(__ldg(&p.nw[ch * EPC + e]));
+          for (int e = 0; e < EPC; e += 2) {
+            a[m][j][e] = a[m][j][e] * rstd * bf16_lo(wv[e >> 1]);
+            a[m][j][e + 1] = a[m][j][e + 1] * rstd * bf16_hi(wv[e >> 1]);
+          }
+        } else {
+          const int ch = tid + j * NT;
+          if (ch < nch) {
+#pragma unroll
+            for (int e = 0; e < EPC; ++e)
+              a[m][j][e] = a[m][j][e] * rstd * bf16_to_f32(__ldg(&p.nw[ch * EPC + e]));
+          }
         }
       }
     }
@@ -285,7 +334,9 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
           }
           if (p.epi == EPI_SWIGLU) {
             epi_swiglu(p, m, rg >> 1, v0, v1);
-          } else {  // EPI_QKV
+          } else if (b0 == 0 && pi == tid) {  // EPI_QKV, inputs loaded up front
+            epi_qkv_pair_at(p, m, rg >> 1, v0, v1, pos0[m], cs0[m]);
+          } else {
             epi_qkv_pair(p, m, rg >> 1, v0, v1);
           }
         }
@@ -300,7 +351,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
           if (p.scale) v *= __ldg(&p.scale[rg]);
           float* o = p.out + (size_t)m * p.ldo + rg;
           if (p.epi == EPI_RESID) {
-            *o += v;
+            *o = ((b0 == 0 && ri == tid) ? xr0[m] : *o) + v;
           } else {
             *o = v;
             if (p.epi == EPI_LOGITS) {

@@ -36,6 +36,10 @@ namespace {
 constexpr int kAlign = 256;
 constexpr int kMaxBatch = 32;  // sequences per context (fast step 1: 2 rows each <= 64)
 constexpr int kIdStride = 16;  // id slots per sequence in the device state
+#ifndef TF_BATCH_ATTN_CTAS
+#define TF_BATCH_ATTN_CTAS 8
+#endif
+constexpr int kBatchAttnCtasPerSm = TF_BATCH_ATTN_CTAS;  // batched attention grid density
 thread_local std::string g_create_error;
 
 struct Lin {
@@ -611,8 +615,8 @@ cudaError_t enqueue_decode_batched(tf_ctx* c, const tf_sampling* s, int B) {
   b.ssq_out = c->ssq;
   if ((e = launch_build(b, false, c->stream))) return e;
   // Key-range splits: B * Hkv (row, KV head) pairs already spread the work,
-  // so split each range only as far as about four CTAs per SM.
-  const int S = std::max(1, std::min(c->S_slow, 4 * c->num_sms / (B * c->Hkv)));
+  // so split each range only as far as a few CTAs per SM.
+  const int S = std::max(1, std::min(c->S_slow, kBatchAttnCtasPerSm * c->num_sms / (B * c->Hkv)));
   const int Ls = static_cast<int>(c->slow.size());
   for (int i = 0; i < Ls; ++i)
     if ((e = layer_batched(c, c->slow[i], c->xs, B, 1, &c->st->pos, 0, S,

@@ -40,7 +40,7 @@ from synth import WORKLOADS, tensor_specs  # noqa: E402
 METRIC = "Dual-AR decode frames/s at batch 1; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 PAGE_LOAD_ELEMENTS = 7_377_351_168   # tuna-fish README, "Inference estimation"
-GATE_UP_TRAFFIC = 99_663_872 + 2_707_712  # ncu DRAM bytes per launch, gate/up-shaped k_gemv
+GATE_UP_TRAFFIC = 99_670_272 + 3_020_800  # ncu DRAM bytes per launch, gate/up-shaped k_gemv
 
 
 # ---------------------------------------------------------------- accounting
@@ -196,17 +196,24 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--op", default=None, choices=["gemv", "gemm"],
+    ap.add_argument("--profile-range", action="store_true",
+                    help="mark the timed decode frames as the profiler range (ncu --profile-from-start off)")
+    ap.add_argument("--op", default=None, choices=["gemv", "gemm", "skinny"],
                     help="time one kernel on its own instead of the decode step")
     ap.add_argument("--rows", type=int, default=19456)
     ap.add_argument("--cols", type=int, default=2560)
     ap.add_argument("--fp8", action="store_true")
-    ap.add_argument("--m", type=int, default=1024, help="--op gemm: prompt rows")
+    ap.add_argument("--m", type=int, default=None,
+                    help="--op gemm: prompt rows (1024); --op skinny: activation rows (16)")
     args = ap.parse_args()
     if args.op == "gemv":
         return run_gemv_case(args)
     if args.op == "gemm":
+        args.m = args.m or 1024
         return run_gemm_case(args)
+    if args.op == "skinny":
+        args.m = args.m or 16
+        return run_skinny_case(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -258,7 +265,12 @@ def main():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        if args.profile_range:
+            torch.cuda.profiler.start()
         dec.decode_frames(k, sampling)
+        if args.profile_range:
+            torch.cuda.synchronize(device)
+            torch.cuda.profiler.stop()
         e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize(device)
@@ -432,6 +444,36 @@ def run_gemm_case(args):
                       "frac": round(tflops / peaks["bf16_tflops"], 4),
                       "note": "per call: hi/lo split + GEMM; tensor work is 2x the algorithmic flops"}),
           flush=True)
+
+
+def run_skinny_case(args):
+    """The batched step's skinny tensor-core GEMMs in their in-frame
+    configuration (tf_profile_kernel 4..7: deferred-RMSNorm input, fused
+    epilogue, launches chained with PDL and replayed as a graph) over --m
+    activation rows, on a full-width model cut to 8 slow layers (1.6 GB of
+    distinct weights per pass, far above L2).  Prints one JSON line."""
+    import torch
+    from dual_ar_decode_gb300 import Decoder
+    from synth import FULL
+    d = FULL.replace(slow_layers=8, fast_layers=1, max_seq_len=64)
+    dev = torch.device("cuda", 0)
+    w = device_weights(d, args.seed, dev)
+    dec = Decoder(d, "bf16", max_batch=args.m)
+    dec.load_weights(w)
+    del w
+    peaks = measured_peaks()
+    out = {}
+    for which, name in ((4, "gate_up_19456x2560"), (5, "qkv_6144x2560"), (6, "o_2560x4096"),
+                        (7, "down_2560x9728")):
+        for _ in range(args.warmup):
+            dec.profile_kernel(which, 16)
+        ms, nbytes = dec.profile_kernel(which, 64)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"us_per_launch": round(ms * 1e3, 3), "bytes_per_launch": nbytes,
+                     "achieved_gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    dec.close()
+    print(json.dumps({"op": "skinny", "rows_m": args.m, "shapes": out, "peak_gbs": peaks["hbm_gbs"],
+                      "peak_source": peaks["source"]}), flush=True)
 
 
 def run_reference(args, wl, world, rank):

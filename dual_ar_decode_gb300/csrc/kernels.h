@@ -87,6 +87,13 @@ struct GemvParams {
   int32_t ssq_n;
   int32_t in_rps;            // consumer row m is producer row m * in_rps + in_rps - 1
                              // (activation parts and sums); 0 or 1: the same row
+  // Cross-kernel L2 prefetch (batch-1 GEMV): once CTA c has issued its last
+  // weight copy, it asks L2 for the first pf_bytes of the row block that CTA
+  // c of the next GEMV in the stream will stream (that GEMV's partition:
+  // pf_units units of pf_unit rows of pf_rowbytes, over pf_grid CTAs), so
+  // HBM keeps streaming across the kernel boundary.
+  const uint8_t* pf_w;
+  int32_t pf_units, pf_unit, pf_rowbytes, pf_grid, pf_bytes;
 };
 constexpr int kSsqRows = 64;   // row stride of the partial sums of squares
 

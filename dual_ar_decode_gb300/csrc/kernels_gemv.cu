@@ -162,6 +162,21 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
           ++s;
         }
       }
+      // Hint L2 with the start of the next GEMV's matching row block.
+      if (p.pf_w && !*abort_flag) {
+        for (int cn = c; cn < p.pf_grid; cn += G) {
+          const int v0 = (int)((long long)p.pf_units * cn / p.pf_grid);
+          const int v1 = (int)((long long)p.pf_units * (cn + 1) / p.pf_grid);
+          const size_t start = (size_t)v0 * p.pf_unit * p.pf_rowbytes;
+          size_t len = (size_t)(v1 - v0) * p.pf_unit * p.pf_rowbytes;
+          if (len > (size_t)p.pf_bytes) len = (size_t)p.pf_bytes;
+          for (size_t o = 0; o + 16 <= len; o += 32768) {
+            const uint32_t n = static_cast<uint32_t>(std::min<size_t>(32768, len - o) & ~size_t(15));
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.pf_w + start + o), "r"(n)
+                         : "memory");
+          }
+        }
+      }
       // Drain: the last (up to nst) issued copies may still be in flight.
       for (int t = max(0, s - p.nst); t < s; ++t)
         mbar_wait(&full[t % p.nst], (t / p.nst) & 1, p.err);

@@ -99,6 +99,7 @@ struct tf_ctx {
   uint16_t* slow_norm = nullptr;
   uint16_t* fast_norm = nullptr;
   Lin fast_head;
+  Lin sem;                    // semantic head: the tied text-embedding slice (bf16)
   uint16_t* cb_embed = nullptr;
   std::vector<std::string> loaded;
   float2* rope = nullptr;
@@ -237,10 +238,22 @@ tf_status check_kernel_errors(tf_ctx* c) {
 }
 
 // ------------------------------------------------------------------ launches
+#ifndef TF_GEMV_PREFETCH_BYTES
+#define TF_GEMV_PREFETCH_BYTES (32 * 1024)
+#endif
+constexpr int kGemvPrefetch = TF_GEMV_PREFETCH_BYTES;  // per CTA, into L2, across a boundary
+
+// The GEMV that follows in the stream (its weight is prefetched into L2).
+struct NextGemv {
+  const Lin* L = nullptr;
+  int epi = EPI_STORE;
+  int M = 1;
+};
+
 cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_t* nw, int epi,
                  float* out, int ldo, int M, bool pdl, const Layer* layer = nullptr,
                  const int32_t* pos_ptr = nullptr, int pos_fixed = 0, int cb = -1,
-                 bool select = false) {
+                 bool select = false, const NextGemv& next = NextGemv()) {
   GemvParams p = {};
   p.W = L.w;
   p.scale = L.s;
@@ -279,14 +292,28 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
   const int eb = (L.s != nullptr) ? 1 : 2;
   gemv_plan(p, eb, c->num_sms, M);
   const int grid = gemv_grid(p, c->num_sms);
+  if (next.L && kGemvPrefetch > 0) {
+    GemvParams q = {};
+    q.N = next.L->N;
+    q.K = next.L->K;
+    q.epi = next.epi;
+    const int neb = (next.L->s != nullptr) ? 1 : 2;
+    gemv_plan(q, neb, c->num_sms, next.M);
+    p.pf_w = next.L->w;
+    p.pf_units = q.units;
+    p.pf_unit = q.unit;
+    p.pf_rowbytes = q.K * neb;
+    p.pf_grid = gemv_grid(q, c->num_sms);
+    p.pf_bytes = kGemvPrefetch;
+  }
   return launch_gemv(p, eb == 1 ? 1 : 0, M, grid, pdl, c->stream);
 }
 
 cudaError_t layer_decode(tf_ctx* c, const Layer& L, float* x, int M, const int32_t* pos_ptr,
-                         int pos_fixed, int S, bool pdl_first) {
+                         int pos_fixed, int S, bool pdl_first, const NextGemv& after) {
   cudaError_t e;
   if ((e = gemv(c, L.qkv, PRO_NORM, x, L.attn_norm, EPI_QKV, nullptr, 0, M, pdl_first, &L, pos_ptr,
-                pos_fixed)))
+                pos_fixed, -1, false, NextGemv{&L.o, EPI_RESID, M})))
     return e;
   AttnParams a = {};
   a.q = c->qbuf;
@@ -304,9 +331,14 @@ cudaError_t layer_decode(tf_ctx* c, const Layer& L, float* x, int M, const int32
   a.out = c->obuf;
   a.err = &c->st->err;
   if ((e = launch_attention(a, M, true, c->stream))) return e;
-  if ((e = gemv(c, L.o, PRO_PLAIN, c->obuf, nullptr, EPI_RESID, x, c->H, M, true))) return e;
-  if ((e = gemv(c, L.w13, PRO_NORM, x, L.ffn_norm, EPI_SWIGLU, c->ubuf, c->F, M, true))) return e;
-  return gemv(c, L.w2, PRO_PLAIN, c->ubuf, nullptr, EPI_RESID, x, c->H, M, true);
+  if ((e = gemv(c, L.o, PRO_PLAIN, c->obuf, nullptr, EPI_RESID, x, c->H, M, true, nullptr, nullptr,
+                0, -1, false, NextGemv{&L.w13, EPI_SWIGLU, M})))
+    return e;
+  if ((e = gemv(c, L.w13, PRO_NORM, x, L.ffn_norm, EPI_SWIGLU, c->ubuf, c->F, M, true, nullptr,
+                nullptr, 0, -1, false, NextGemv{&L.w2, EPI_RESID, M})))
+    return e;
+  return gemv(c, L.w2, PRO_PLAIN, c->ubuf, nullptr, EPI_RESID, x, c->H, M, true, nullptr, nullptr, 0,
+              -1, false, after);
 }
 
 cudaError_t enqueue_select(tf_ctx* c, int cb, const tf_sampling* s) {
@@ -334,12 +366,9 @@ cudaError_t enqueue_select(tf_ctx* c, int cb, const tf_sampling* s) {
 cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_first) {
   cudaError_t e;
   const bool topk = s->top_k > 0;
-  Lin sem;
-  sem.w = reinterpret_cast<uint8_t*>(c->text_embed + (size_t)c->sem_base * c->H);
-  sem.N = c->Vs;
-  sem.K = c->H;
-  if ((e = gemv(c, sem, PRO_NORM, c->xs, c->slow_norm, EPI_LOGITS, c->logits, 0, 1, pdl_first,
-                nullptr, nullptr, 0, 0, !topk)))
+  const int Lf = static_cast<int>(c->fast.size());
+  if ((e = gemv(c, c->sem, PRO_NORM, c->xs, c->slow_norm, EPI_LOGITS, c->logits, 0, 1, pdl_first,
+                nullptr, nullptr, 0, 0, !topk, NextGemv{&c->fast[0].qkv, EPI_QKV, 2})))
     return e;
   if (topk && (e = enqueue_select(c, 0, s))) return e;
   for (int j = 1; j < c->NCB; ++j) {
@@ -359,11 +388,18 @@ cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_
     b.err = &c->st->err;
     if ((e = launch_build(b, true, c->stream))) return e;
     const int M = b.M;
-    for (const Layer& L : c->fast)
-      if ((e = layer_decode(c, L, c->xf, M, nullptr, j == 1 ? 0 : j, 1, true))) return e;
+    for (int i = 0; i < Lf; ++i) {
+      const NextGemv after = i + 1 < Lf ? NextGemv{&c->fast[i + 1].qkv, EPI_QKV, M}
+                                        : NextGemv{&c->fast_head, EPI_LOGITS, 1};
+      if ((e = layer_decode(c, c->fast[i], c->xf, M, nullptr, j == 1 ? 0 : j, 1, true, after)))
+        return e;
+    }
+    // after the last head: the next frame's first slow GEMV
+    const NextGemv after_head = j + 1 < c->NCB ? NextGemv{&c->fast[0].qkv, EPI_QKV, 1}
+                                               : NextGemv{&c->slow[0].qkv, EPI_QKV, 1};
     if ((e = gemv(c, c->fast_head, PRO_NORM, c->xf + (size_t)(M - 1) * c->H, c->fast_norm,
                   EPI_LOGITS, c->logits + (size_t)j * c->Vmax, 0, 1, true, nullptr, nullptr, 0, j,
-                  !topk)))
+                  !topk, after_head)))
       return e;
     if (topk && (e = enqueue_select(c, j, s))) return e;
   }
@@ -640,8 +676,13 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
   b.x = c->xs;
   b.err = &c->st->err;
   if ((e = launch_build(b, false, c->stream))) return e;
-  for (const Layer& L : c->slow)
-    if ((e = layer_decode(c, L, c->xs, 1, &c->st->pos, 0, c->S_slow, true))) return e;
+  const int Ls = static_cast<int>(c->slow.size());
+  for (int i = 0; i < Ls; ++i) {
+    const NextGemv after = i + 1 < Ls ? NextGemv{&c->slow[i + 1].qkv, EPI_QKV, 1}
+                                      : NextGemv{&c->sem, EPI_LOGITS, 1};
+    if ((e = layer_decode(c, c->slow[i], c->xs, 1, &c->st->pos, 0, c->S_slow, true, after)))
+      return e;
+  }
   return enqueue_tail(c, s, 1, true);
 }
 
@@ -1056,6 +1097,9 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   c->fast_norm = reinterpret_cast<uint16_t*>(take(H * 2));
   c->fast_head = make_lin(c->Vc, c->H);
   c->cb_embed = reinterpret_cast<uint16_t*>(take((size_t)(c->NCB - 1) * c->Vc * H * 2));
+  c->sem.w = reinterpret_cast<uint8_t*>(c->text_embed + (size_t)c->sem_base * H);
+  c->sem.N = c->Vs;
+  c->sem.K = c->H;
 
   // ---- KV caches: [sequence][Hkv][T][D] per layer
   const size_t kv_elems = (size_t)c->Hkv * c->T * c->D;

@@ -73,6 +73,23 @@ def schedule_bytes(d, weight_dtype, prefill, frames) -> float:
                           for p in range(prefill, prefill + frames)]))
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    when there is one rank): a timed region lasts as long as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the
+    max-over-ranks time in milliseconds (replicas do equal work)."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -279,12 +296,8 @@ def main():
         remaining -= k
         segs += 1
     clk = clocks.stop()
-    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    frames_all = args.steps * world * B          # sequence-frames
-    value = frames_all / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, device)
+    value = job_rate(args.steps * B, world, total_ms)   # sequence-frames/s
     info = dec.info()
 
     # dominant kernel, live: the slow gate/up GEMV (batch 1) or skinny
@@ -304,11 +317,7 @@ def main():
         dec.decode_frame(sampling)
     h1.record(stream)
     h1.synchronize()
-    e2e_ms = h0.elapsed_time(h1)
-    e2e_t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e_value = e2e_frames * world * B / (float(e2e_t.item()) / 1e3)
+    e2e_value = job_rate(e2e_frames * B, world, max_over_ranks(h0.elapsed_time(h1), device))
 
     # prefill throughput (prompt ids uploaded from the host, frame 0 returned)
     pre_ms = []

@@ -129,6 +129,8 @@ struct AttnParams {
   uint32_t* err;
 };
 cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t s);
+// The same attention for prompt rows (many rows, one long key slice each).
+cudaError_t launch_attention_rows(const AttnParams& p, int M, bool pdl, cudaStream_t s);
 
 // ----------------------------------------------------------------- misc
 // Builds the input rows of a decoder pass.  Sequence b's ids sit at

@@ -1448,7 +1448,7 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
       a.counters = c->counters;
       a.out = c->po;
       a.err = &c->st->err;
-      CK(launch_attention(a, P, false, c->stream));
+      CK(launch_attention_rows(a, P, false, c->stream));
       CK(gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr));
       CK(launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
       CK(gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr));

@@ -37,9 +37,15 @@ constexpr int kAlign = 256;
 constexpr int kMaxBatch = 32;  // sequences per context (fast step 1: 2 rows each <= 64)
 constexpr int kIdStride = 16;  // id slots per sequence in the device state
 #ifndef TF_BATCH_ATTN_CTAS
-#define TF_BATCH_ATTN_CTAS 8
+#define TF_BATCH_ATTN_CTAS 4
 #endif
 constexpr int kBatchAttnCtasPerSm = TF_BATCH_ATTN_CTAS;  // batched attention grid density
+#ifndef TF_BATCH_ATTN_STREAM
+#define TF_BATCH_ATTN_STREAM 1
+#endif
+// Batched attention kernel: 1 = streaming (keys straight from the cache, small
+// shared-memory footprint), 0 = staged (key chunks bulk-copied to shared memory).
+constexpr bool kBatchAttnStream = TF_BATCH_ATTN_STREAM != 0;
 thread_local std::string g_create_error;
 
 struct Lin {
@@ -526,7 +532,8 @@ cudaError_t layer_batched(tf_ctx* c, const Layer& L, float* x, int M, int rps,
   a.out_hi = c->bh[1];
   a.out_lo = c->bl[1];
   a.err = &c->st->err;
-  if ((e = launch_attention(a, M, true, c->stream))) return e;
+  if ((e = (kBatchAttnStream ? launch_attention_rows : launch_attention)(a, M, true, c->stream)))
+    return e;
   SkOpt oo;
   oo.nw_next = L.ffn_norm;
   if ((e = skinny(c, L.o, 1, M, EPI_RESID, x, c->H, oo))) return e;

@@ -215,7 +215,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--profile-range", action="store_true",
                     help="mark the timed decode frames as the profiler range (ncu --profile-from-start off)")
-    ap.add_argument("--op", default=None, choices=["gemv", "gemm", "skinny"],
+    ap.add_argument("--op", default=None, choices=["gemv", "gemm", "skinny", "attn"],
                     help="time one kernel on its own instead of the decode step")
     ap.add_argument("--rows", type=int, default=19456)
     ap.add_argument("--cols", type=int, default=2560)
@@ -231,6 +231,8 @@ def main():
     if args.op == "skinny":
         args.m = args.m or 16
         return run_skinny_case(args)
+    if args.op == "attn":
+        return run_attn_case(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -483,6 +485,50 @@ def run_skinny_case(args):
     dec.close()
     print(json.dumps({"op": "skinny", "rows_m": args.m, "shapes": out, "peak_gbs": peaks["hbm_gbs"],
                       "peak_source": peaks["source"]}), flush=True)
+
+
+def run_attn_case(args):
+    """Decode attention alone (tf_op_attention_noalloc: the staged split-key
+    kernel, no device allocation per call) for one query row at position
+    T - 1 of a full-size KV head layout (32 q / 8 kv heads of 128, T = 1024,
+    38 key slices as in the batch-1 frame), cycling over 64 distinct caches
+    (268 MB, above L2).  Each call waits for its error word, so the time per
+    call includes one host round trip.  Prints one JSON line."""
+    import ctypes
+    import torch
+    from dual_ar_decode_gb300 import binding
+    dev = torch.device("cuda", 0)
+    T, Hq, Hkv, D, S, ncache = 1024, 32, 8, 128, 38, 64
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    K = (torch.randn(ncache, Hkv, T, D, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+    V = (torch.randn(ncache, Hkv, T, D, device=dev, generator=g) * 0.5).to(torch.bfloat16)
+    q = torch.randn(Hq * D, device=dev, generator=g)
+    out = torch.empty(Hq * D, device=dev)
+    L = binding.lib()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def call(i):
+        st = L.tf_op_attention_noalloc(q.data_ptr(), K[i % ncache].data_ptr(), V[i % ncache].data_ptr(),
+                                       T, Hq, Hkv, D, 1, T - 1, S, out.data_ptr(), ctypes.c_void_p(stream))
+        if st:
+            raise RuntimeError(f"tf_op_attention_noalloc returned {st}")
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        call(i)
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    nbytes = 2 * Hkv * T * D * 2 + 2 * Hq * D * 4
+    print(json.dumps({"op": "attn", "T": T, "Hq": Hq, "Hkv": Hkv, "D": D, "slices": S,
+                      "us_per_call_incl_host_sync": round(us, 3), "kv_bytes": nbytes,
+                      "note": "one query row at position T-1; each call syncs for its error word"}),
+          flush=True)
 
 
 def run_reference(args, wl, world, rank):

@@ -442,3 +442,41 @@ def test_tiny_golden_frames_reproduce():
         sums.append(float(np.sum(z)))
     assert frames == g["greedy_frames"]
     assert np.allclose(sums, g["greedy_logit_sums"], rtol=1e-9)
+
+
+def test_batched_oracle_is_independent_sequences():
+    """R17: a batch of B sequences computes what B single-sequence runs
+    compute; under top-k sampling, sequence b draws with Philox counter word
+    3 = b (so the draws differ between otherwise equal sequences)."""
+    d = TINY
+    w = make_weights(d, seed=12)
+    prompts = make_prompt(d, 7, seed=30, batch=3)
+    ob = oracle.DualAROracle(d, w, batch=3)
+    fb, zb = ob.prefill(prompts)
+    frames_b, logits_b = [fb], [zb]
+    for _ in range(3):
+        f, z = ob.decode_frame()
+        frames_b.append(f)
+        logits_b.append(z)
+    for b in range(3):
+        o1 = oracle.DualAROracle(d, w)
+        f, z = o1.prefill(prompts[b:b + 1])
+        assert np.array_equal(f[0], frames_b[0][b]) and np.array_equal(z[0], logits_b[0][b])
+        for t in range(1, 4):
+            f, z = o1.decode_frame()
+            assert np.array_equal(f[0], frames_b[t][b]) and np.array_equal(z[0], logits_b[t][b])
+
+    # top-k: two copies of one prompt have identical logits, and each draw is
+    # the sampler's pick for its own sequence index
+    s = {"top_k": 8, "seed": 77}
+    same = np.repeat(prompts[:1], 2, axis=0)
+    ot = oracle.DualAROracle(d, w, batch=2)
+    ft, zt = ot.prefill(same, s)
+    assert np.array_equal(zt[0][0], zt[1][0])            # codebook-0 logits: same prompt
+    for b in range(2):
+        z32 = zt[b][0, : d.semantic_vocab].astype(np.float32)
+        pick, _ = oracle.topk_sample(z32, 8, 77, 0, 0, b)
+        assert ft[b][0] == pick
+    draws = [oracle.topk_sample(zt[0][0, : d.semantic_vocab].astype(np.float32), 8, 77, 0, 0, b)[0]
+             for b in range(16)]
+    assert len(set(draws)) > 1                            # the sequence index reaches the draw

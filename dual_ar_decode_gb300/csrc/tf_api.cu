@@ -15,6 +15,12 @@
 // with programmatic dependent launch, and replayed per decode call; all
 // frame-varying state (position, fed-back ids, forced ids, frame index)
 // lives in device memory.
+//
+// A batch of B sequences (lockstep, prompts of one length) runs the same
+// frame with each linear layer as one skinny tensor-core GEMM over the B rows
+// (the weights stream once per step for all sequences), per-sequence KV
+// caches, attention and selection; the RMSNorm in front of a GEMM is deferred
+// into it (RMSNorm(x) * w = rstd * (x * w), rstd applied in the epilogue).
 #include <cuda_runtime.h>
 
 #include <algorithm>

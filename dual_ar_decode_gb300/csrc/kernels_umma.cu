@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* last_flag = tmem_slot + 2;
   volatile uint32_t* consumed = tmem_slot + 3;   // k slices the MMA warp took
-  volatile uint32_t* okv = tmem_slot + 4;        // [4] epilogue warps' verdicts
+  volatile uint32_t* okv = tmem_slot + 4;        // [4] epilogue warps' wait outcomes
   volatile uint32_t* red_fail = tmem_slot + 8;   // a staging wait expired
   float* rstd_s = reinterpret_cast<float*>(tmem_slot + 16);  // [64] row rstd
   float* red_s = rstd_s + 64;                               // [4][NB] sums of squares
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
     }
     const bool wok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
     if (lane == 0) okv[q] = wok ? 1u : 0u;
-    epi_bar_sync();  // publishes rstd_s and every warp's verdict
+    epi_bar_sync();  // publishes rstd_s and every warp's wait outcome
     const bool ok = okv[0] && okv[1] && okv[2] && okv[3];
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     float v[NB];

@@ -64,6 +64,20 @@ def test_e4m3_all_codes_match_torch():
     assert ours[0x08] == 2.0 ** -6          # smallest normal
 
 
+def test_e4m3_bit_placement_identity():
+    """An e4m3 code s.eeee.mmm placed as float32 bits (s << 31) | (eeeemmm << 20)
+    is the code's value times 2^-120 exactly, subnormal codes included (both
+    formats put the hidden bit in the same place once the exponent bias
+    difference, 127 - 7 = 120, is taken out)."""
+    codes = np.arange(256, dtype=np.uint32)
+    bits = ((codes & 0x80) << 24) | ((codes & 0x7F) << 20)
+    placed = bits.astype(np.uint32).view(np.float32).astype(np.float64) * 2.0 ** 120
+    ref = oracle.e4m3_decode(codes.astype(np.uint8))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(placed[ok], ref[ok])
+    assert np.all(np.isfinite(placed))       # the NaN codes become finite: decode must mask them
+
+
 def test_e4m3_encode_matches_torch_cast_including_ties():
     vals = oracle.e4m3_decode(np.arange(127, dtype=np.uint8))
     mids = (vals[1:] + vals[:-1]) / 2                     # exact ties

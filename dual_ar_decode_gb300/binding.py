@@ -61,8 +61,6 @@ EXPORTS = {
     "tf_profile_kernel": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_int64)]),
-    "tf_decode_trace": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(TfSampling), ctypes.c_void_p,
-                                       ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "tf_op_quantize_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_select": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -232,18 +230,6 @@ class Decoder:
         _check(lib().tf_profile_kernel(self.h, which, iters, ctypes.byref(ms), ctypes.byref(b)),
                self.h)
         return ms.value, b.value
-
-    def decode_trace(self, sampling=None, cap: int = 1024):
-        """One decode frame with per-op %globaltimer stamps: returns
-        (stamps int64 [n][2][3], kinds int32 [n])."""
-        st = np.zeros((cap, 2, 3), np.int64)
-        kinds = np.zeros(cap, np.int32)
-        n = ctypes.c_int32(0)
-        s = _sampling(sampling)
-        _check(lib().tf_decode_trace(self.h, ctypes.byref(s), _ptr(st), _ptr(kinds), cap,
-                                     ctypes.byref(n)), self.h)
-        k = min(n.value, cap)
-        return st[:k], kinds[:k]
 
     def info(self) -> dict:
         i = TfInfo()

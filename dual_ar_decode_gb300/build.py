@@ -16,8 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libtf_dualar.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["tf_api.cu", "kernels_gemv.cu", "kernels_attn.cu", "kernels_misc.cu", "kernels_frame.cu",
-           "kernels_umma.cu"]
+SOURCES = ["tf_api.cu", "kernels_gemv.cu", "kernels_attn.cu", "kernels_misc.cu", "kernels_umma.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "--expt-relaxed-constexpr",

@@ -252,105 +252,3 @@ cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int
                                 float eps, cudaStream_t s);
 
 }  // namespace tf
-
-namespace tf {
-
-// ----------------------------------------------------------------- frame
-// Persistent decode-frame kernel: one cooperative launch runs a program of
-// ops with grid barriers between them, while a producer warp per CTA streams
-// the CTA's slice of every GEMV weight through a shared-memory ring.
-enum OpKind : int32_t { OPK_GEMV = 0, OPK_ATTN = 1, OPK_SELECT = 2, OPK_END = 3 };
-// How a GEMV op obtains its input rows before the optional RMSNorm.
-enum SrcMode : int32_t {
-  SRC_X = 0,      // rows of x (fp32, ld = ldx)
-  SRC_EMBED = 1,  // row 0 = table[row_base + *id_ptr] (bf16), stored to xres by CTA 0
-  SRC_FAST1 = 2,  // row 0 = RMSNorm(xs) * nw_src, row 1 = table[*id_ptr]; stored to xres
-};
-
-struct FrameOp {
-  int32_t kind;
-  // GEMV ---------------------------------------------------------------
-  const uint8_t* W;       // [N][K] bf16 or e4m3
-  const float* scale;     // per-row scale (fp8) or null
-  int32_t N, K, wt;       // wt: 0 bf16, 1 fp8
-  int32_t unit;           // rows per partition unit
-  int32_t rs;             // rows per stage
-  int32_t nt, J;          // active consumer threads, chunks per thread
-  int32_t M;              // rows of activations (1 or 2)
-  int32_t src;            // SrcMode
-  const float* x;
-  int32_t ldx;
-  const uint16_t* table;
-  int32_t table_rows, row_base;
-  const int32_t* id_ptr;
-  const float* xs;
-  const uint16_t* nw_src;
-  float* xres;            // built residual rows [M][K]
-  int32_t pro;            // PRO_PLAIN / PRO_NORM
-  const uint16_t* nw;
-  int32_t epi;
-  float* out;
-  int32_t ldo;
-  uint16_t* Kc;           // KV cache of the layer [Hkv][T][D]
-  uint16_t* Vc;
-  int32_t use_pos;        // rows sit at (*pos + m) if set, else pos_fixed + m
-  int32_t pos_fixed;
-  int32_t cb;             // codebook slot (EPI_LOGITS / SELECT)
-  int32_t select;         // EPI_LOGITS: grid argmax into sel/fb
-  // ATTN ---------------------------------------------------------------
-  const float* q;         // [M][Hq*D]
-  float* o;               // [M][Hq*D]
-  int32_t S;              // key splits
-  // SELECT -------------------------------------------------------------
-  const float* logits;
-  int32_t vocab;
-  // END ----------------------------------------------------------------
-  int32_t advance;
-};
-
-struct FrameParams {
-  const FrameOp* ops;
-  int32_t n_ops, n_frames;
-  int32_t T, Hq, Hkv, D, q_dim, kv_dim;
-  const float2* rope;
-  float eps;
-  int32_t slots;          // ring slots
-  int32_t stage;          // bytes per ring slot (multiple of 128)
-  int32_t un_bytes;       // union scratch bytes
-  int32_t* pos;
-  int32_t* frame_index;
-  int32_t* sel;
-  int32_t* fb;
-  const int32_t* forced;
-  const int32_t* forced_on;
-  unsigned long long* best;
-  uint32_t* ticket;
-  int32_t* hist;
-  int32_t* hist_idx;
-  int32_t hist_cap, ncb;
-  int32_t top_k;
-  float temperature;
-  uint32_t key0, key1;
-  float* part;            // attention partials [M][Hq][S][D+2]
-  uint32_t* counters;     // attention tickets [M][Hkv]
-  uint32_t* gbar;         // grid barrier counter, zero at launch
-  uint32_t* err;
-  // optional trace: per op, for CTA 0 and the last CTA, %globaltimer at
-  // barrier-wait start, barrier-wait end and op end: [n_ops][2][3]
-  unsigned long long* trace;
-};
-
-constexpr int kFrameStage = 40 * 1024;     // largest ring slot
-constexpr int kFrameConsumerWarps = 10;
-constexpr int kFrameCtasPerSm = 2;         // two CTAs per SM: 20 consumer warps
-constexpr int kFrameSmemPerCta = 112 * 1024;
-// Plans a GEMV op's staging and thread split; returns false if it does not fit.
-bool frame_plan_gemv(FrameOp& op, int stage);
-// Shared memory the frame kernel needs for these params.
-size_t frame_smem_bytes(int slots, int stage, int un_bytes);
-// Union-scratch bytes for the given shapes.
-int frame_union_bytes(int G, int D, int max_vocab);
-cudaError_t frame_set_attributes();
-cudaError_t launch_frame(const FrameParams& p, int grid, cudaStream_t s);
-
-}  // namespace tf

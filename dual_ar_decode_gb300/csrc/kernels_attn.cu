@@ -22,6 +22,7 @@
 
 #include "../../include/tf.h"
 #include "common.cuh"
+#include "device_once.h"
 #include "kernels.h"
 
 namespace tf {
@@ -146,7 +147,15 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnParams p) {
     const int b = ch & 1;
     const int rows = min(kChunk, nk - ch * kChunk);
     const bool got = mbar_wait(&bar[b], (ch >> 1) & 1, p.err);
-    if (__syncthreads_or(got ? 0 : 1)) return;  // expired (reported): give up together
+    if (__syncthreads_or(got ? 0 : 1)) {
+      // Expired (reported): before the CTA gives up, let the copies still in
+      // flight into its shared memory land (chunks ch .. ch + 1), each wait
+      // bounded again, so none of them writes into a later CTA's memory.
+      if (tid == 0)
+        for (int c2 = ch; c2 < min(nch, ch + 2); ++c2)
+          if (!mbar_wait(&bar[c2 & 1], (c2 >> 1) & 1, p.err)) break;
+      return;
+    }
     const uint16_t* Ks = kv + (size_t)(2 * b) * kChunk * D;
     const uint16_t* Vs = Ks + (size_t)kChunk * D;
     // scores: warp w takes keys w, w + 8, ...; lanes across the head dimension
@@ -298,13 +307,12 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnParams p) {
 template <int D, int G>
 cudaError_t launch_dg(const AttnParams& p, int M, bool pdl, cudaStream_t s) {
   using SL = AttnSmem<D, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SL::kBytes));
-    if (e) return e;
-    attr_set = true;
-  }
+  static DeviceOnce once;
+  cudaError_t ea = device_once(once, [] {
+    return cudaFuncSetAttribute(k_attn<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SL::kBytes));
+  });
+  if (ea) return ea;
   if (p.S < 1 || p.S > kMaxSlices || M < 1) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, p.Hkv, M);
@@ -492,13 +500,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p
 
 template <int D, int G>
 cudaError_t launch_rows_dg(const AttnParams& p, int M, bool pdl, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_rows<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
-    if (e) return e;
-    attr_set = true;
-  }
+  static DeviceOnce once;
+  cudaError_t ea = device_once(once, [] {
+    return cudaFuncSetAttribute(k_attn_rows<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+  });
+  if (ea) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, p.Hkv, M);
   cfg.blockDim = dim3(kRowWarps * 32);
@@ -562,33 +569,38 @@ cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t 
 // The array lives in device memory on every GPU that loads the library,
 // until the process exits.  Host code cannot use the array's name as a
 // device address (on the host it only stands for the symbol), so the device
-// address is looked up once per device with cudaGetSymbolAddress, with that
-// device current, on the first call on it; that first call should happen
-// before any stream capture.  All calls share the one array and it keeps
-// what the last call left: tickets and the error word are cleared on every
-// call, and calls that overlap on the GPU (different streams, or different
-// host threads) race on it.
+// address is looked up once per device (and again in a new context on it)
+// with cudaGetSymbolAddress, with that device current, on the first call
+// there; that first call should happen before any stream capture.  All calls
+// share the one array and it keeps what the last call left: tickets and the
+// error word are cleared on every call, and calls that overlap on the GPU
+// (different streams, or different host threads) race on it.
 constexpr size_t kNoAllocPartFloats = 512 * 1024;  // 2 MiB of split partials
 constexpr size_t kNoAllocTickets = 1024;
 constexpr size_t kNoAllocBytes = kNoAllocPartFloats * 4 + kNoAllocTickets * 4 + 256;
 static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kNoAllocBytes];
 
 namespace {
-constexpr int kNoAllocMaxDevices = 64;
+// Device address of the scratch array on the current device, looked up with
+// that device current and kept per device together with the id of the
+// context it belongs to: a new context on the device (after cudaDeviceReset)
+// looks it up again.
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+void* g_noalloc_ptr[kMaxDevices] = {};
+uint64_t g_noalloc_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once).
 void* noalloc_scratch(int dev) {
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  const uint64_t ctx = current_context_id();
+  if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_attn_noalloc_scratch) != cudaSuccess) {
       (void)cudaGetLastError();
       return nullptr;
     }
     g_noalloc_ptr[dev] = ptr;
+    g_noalloc_ctx[dev] = current_context_id();
   }
   return g_noalloc_ptr[dev];
 }
@@ -641,5 +653,6 @@ extern "C" tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, 
   if (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return TF_E_CUDA;
+  if (e & ERR_TIMEOUT) return TF_E_TIMEOUT;
   return e ? TF_E_INVAL : TF_OK;
 }

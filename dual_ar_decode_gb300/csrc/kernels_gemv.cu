@@ -26,6 +26,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "device_once.h"
 #include "epilogue.cuh"
 #include "kernels.h"
 
@@ -543,11 +544,14 @@ cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, 
 }
 
 cudaError_t gemv_set_attributes() {
-  cudaError_t e;
-  if ((e = set_attr_m<0, 1>())) return e;
-  if ((e = set_attr_m<0, 2>())) return e;
-  if ((e = set_attr_m<1, 1>())) return e;
-  return set_attr_m<1, 2>();
+  static DeviceOnce once;
+  return device_once(once, [] {
+    cudaError_t e;
+    if ((e = set_attr_m<0, 1>())) return e;
+    if ((e = set_attr_m<0, 2>())) return e;
+    if ((e = set_attr_m<1, 1>())) return e;
+    return set_attr_m<1, 2>();
+  });
 }
 
 }  // namespace tf

@@ -6,6 +6,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "device_once.h"
 #include "epilogue.cuh"
 #include "kernels.h"
 
@@ -509,23 +510,24 @@ __global__ void __launch_bounds__(256) k_gemm_rows(const GemvParams p, int M) {
 // Full shared-memory carveout for the small decode kernels too (see the
 // GEMV): kernels with equal carveouts can share an SM under PDL.
 template <typename K>
-cudaError_t carveout(K kernel) {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  done = true;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+cudaError_t carveout(DeviceOnce& once, K kernel) {
+  return device_once(once, [kernel] {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+  });
 }
 
 cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s) {
-  if (cudaError_t e = carveout(k_build)) return e;
+  static DeviceOnce once;
+  if (cudaError_t e = carveout(once, k_build)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(p.M), dim3(256), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_build, p);
 }
 
 cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s) {
-  if (cudaError_t e = carveout(k_frame_end)) return e;
+  static DeviceOnce once;
+  if (cudaError_t e = carveout(once, k_frame_end)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(1), dim3(32), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_frame_end, p);
@@ -534,7 +536,8 @@ cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s) 
 cudaError_t launch_select(const SelectParams& p, bool pdl, cudaStream_t s) {
   if (p.vocab < 1 || p.vocab > kSelMaxVocab || p.top_k > kSelMaxK || p.n < 1)
     return cudaErrorInvalidValue;
-  if (cudaError_t e = carveout(k_select)) return e;
+  static DeviceOnce once;
+  if (cudaError_t e = carveout(once, k_select)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(p.n), dim3(kSelThreads), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_select, p);
@@ -555,7 +558,8 @@ cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int
 cudaError_t launch_rows_prep(const float* x, int ldx, int M, int K, const uint16_t* w,
                              uint16_t* hi, uint16_t* lo, float* ssq, bool pdl, cudaStream_t s) {
   if (M < 1) return cudaSuccess;
-  if (cudaError_t e = carveout(k_rows_prep)) return e;
+  static DeviceOnce once;
+  if (cudaError_t e = carveout(once, k_rows_prep)) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_rows_prep, x, ldx, K, w, hi, lo, ssq);

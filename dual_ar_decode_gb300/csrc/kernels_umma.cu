@@ -31,6 +31,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "device_once.h"
 #include "epilogue.cuh"
 #include "kernels.h"
 
@@ -692,13 +693,12 @@ template <int NB>
 cudaError_t launch_skinny_nb(const GemvParams& p, const CUtensorMap& mw, const CUtensorMap& mhi,
                              const CUtensorMap& mlo, int M, int S, float* part, uint32_t* tickets,
                              bool pdl, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_umma_skinny<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Skinny<NB>::kSmem);
-    if (e) return e;
-    attr = true;
-  }
+  static DeviceOnce once;
+  cudaError_t ea = device_once(once, [] {
+    return cudaFuncSetAttribute(k_umma_skinny<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Skinny<NB>::kSmem);
+  });
+  if (ea) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.N + 127) / 128, S);
   cfg.blockDim = dim3(kSkThreads);
@@ -767,13 +767,12 @@ cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaS
 
 cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
                            cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_umma_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemm_tc_smem_bytes());
-    if (e) return e;
-    attr = true;
-  }
+  static DeviceOnce once;
+  cudaError_t ea = device_once(once, [] {
+    return cudaFuncSetAttribute(k_umma_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)gemm_tc_smem_bytes());
+  });
+  if (ea) return ea;
   if (!gemm_tc_supported(p.N, p.K) || M < 1) return cudaErrorInvalidValue;
   CUtensorMap ma_hi, ma_lo, mw;
   if (!make_map(&ma_hi, a_hi, M, p.K, BM) || !make_map(&ma_lo, a_lo, M, p.K, BM) ||

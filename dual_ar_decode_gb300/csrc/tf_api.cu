@@ -151,15 +151,6 @@ struct tf_ctx {
   int graph_nodes = 0;
   tf_sampling graph_samp{};
 
-  // persistent frame kernel
-  bool use_graph = true;          // false: persistent frame kernel (TF_DECODE_DRIVER=persistent)
-  FrameOp* d_ops = nullptr;       // [4][kMaxOps]: decode/tail x greedy/top-k
-  int n_ops[4] = {0, 0, 0, 0};
-  int frame_slots = 0, frame_union = 0, frame_stage = 0;
-  int S_frame = 1;
-  uint32_t* gbar = nullptr;
-  unsigned long long* trace = nullptr;  // [kMaxOps][2][3]
-  bool tracing = false;
 };
 
 namespace {
@@ -699,184 +690,6 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
   return enqueue_tail(c, s, 1, true);
 }
 
-// ------------------------------------------------------------------ programs
-constexpr int kMaxOps = 1024;
-
-// Op program of one decode frame (decode = true) or of the frame tail after a
-// prefill (semantic head + fast loop + bookkeeping).
-tf_status build_program(tf_ctx* c, bool decode, bool topk, std::vector<FrameOp>* out) {
-  std::vector<FrameOp>& ops = *out;
-  ops.clear();
-  auto gemv = [&](const Lin& L, int wt, int M, int src, const float* x, int pro, const uint16_t* nw,
-                  int epi, float* o, int ldo) -> FrameOp& {
-    FrameOp op = {};
-    op.kind = OPK_GEMV;
-    op.W = L.w;
-    op.scale = L.s;
-    op.N = L.N;
-    op.K = L.K;
-    op.wt = wt;
-    op.M = M;
-    op.src = src;
-    op.x = x;
-    op.ldx = L.K;
-    op.pro = pro;
-    op.nw = nw;
-    op.epi = epi;
-    op.out = o;
-    op.ldo = ldo;
-    ops.push_back(op);
-    return ops.back();
-  };
-  const int wt = c->fp8 ? 1 : 0;
-  auto layer = [&](const Layer& L, float* x, int M, bool use_pos, int pos_fixed, int S,
-                   const FrameOp* first_src) {
-    FrameOp& q = gemv(L.qkv, wt, M, SRC_X, x, PRO_NORM, L.attn_norm, EPI_QKV, c->qbuf, 0);
-    if (first_src) {
-      q.src = first_src->src;
-      q.table = first_src->table;
-      q.table_rows = first_src->table_rows;
-      q.row_base = first_src->row_base;
-      q.id_ptr = first_src->id_ptr;
-      q.xs = first_src->xs;
-      q.nw_src = first_src->nw_src;
-      q.xres = x;
-    }
-    q.Kc = L.K;
-    q.Vc = L.V;
-    q.use_pos = use_pos;
-    q.pos_fixed = pos_fixed;
-    FrameOp a = {};
-    a.kind = OPK_ATTN;
-    a.M = M;
-    a.q = c->qbuf;
-    a.o = c->obuf;
-    a.Kc = L.K;
-    a.Vc = L.V;
-    a.use_pos = use_pos;
-    a.pos_fixed = pos_fixed;
-    a.S = S;
-    ops.push_back(a);
-    gemv(L.o, wt, M, SRC_X, c->obuf, PRO_PLAIN, nullptr, EPI_RESID, x, c->H);
-    gemv(L.w13, wt, M, SRC_X, x, PRO_NORM, L.ffn_norm, EPI_SWIGLU, c->ubuf, c->F);
-    gemv(L.w2, wt, M, SRC_X, c->ubuf, PRO_PLAIN, nullptr, EPI_RESID, x, c->H);
-  };
-  auto select = [&](int cb, const float* logits, int vocab) {
-    FrameOp op = {};
-    op.kind = OPK_SELECT;
-    op.cb = cb;
-    op.logits = logits;
-    op.vocab = vocab;
-    ops.push_back(op);
-  };
-  if (decode) {
-    FrameOp src = {};
-    src.src = SRC_EMBED;
-    src.table = c->text_embed;
-    src.table_rows = c->Vs;
-    src.row_base = c->sem_base;
-    src.id_ptr = &c->st->fb[0];
-    for (size_t l = 0; l < c->slow.size(); ++l)
-      layer(c->slow[l], c->xs, 1, true, 0, c->S_frame, l == 0 ? &src : nullptr);
-  }
-  Lin sem;
-  sem.w = reinterpret_cast<uint8_t*>(c->text_embed + (size_t)c->sem_base * c->H);
-  sem.N = c->Vs;
-  sem.K = c->H;
-  FrameOp& h0 = gemv(sem, 0, 1, SRC_X, c->xs, PRO_NORM, c->slow_norm, EPI_LOGITS, c->logits, 0);
-  h0.cb = 0;
-  h0.select = topk ? 0 : 1;
-  if (topk) select(0, c->logits, c->Vs);
-  for (int j = 1; j < c->NCB; ++j) {
-    const int M = j == 1 ? 2 : 1;
-    FrameOp src = {};
-    src.src = j == 1 ? SRC_FAST1 : SRC_EMBED;
-    src.table = c->cb_embed + (size_t)(j - 1) * c->Vc * c->H;
-    src.table_rows = c->Vc;
-    src.row_base = 0;
-    src.id_ptr = &c->st->fb[j - 1];
-    src.xs = c->xs;
-    src.nw_src = c->slow_norm;
-    for (size_t l = 0; l < c->fast.size(); ++l)
-      layer(c->fast[l], c->xf, M, false, j == 1 ? 0 : j, 1, l == 0 ? &src : nullptr);
-    FrameOp& h = gemv(c->fast_head, wt, 1, SRC_X, c->xf + (size_t)(M - 1) * c->H, PRO_NORM,
-                      c->fast_norm, EPI_LOGITS, c->logits + (size_t)j * c->Vmax, 0);
-    h.cb = j;
-    h.select = topk ? 0 : 1;
-    if (topk) select(j, c->logits + (size_t)j * c->Vmax, c->Vc);
-  }
-  FrameOp end = {};
-  end.kind = OPK_END;
-  end.advance = decode ? 1 : 0;
-  ops.push_back(end);
-  for (FrameOp& op : ops)
-    if (op.kind == OPK_GEMV && !frame_plan_gemv(op, c->frame_stage))
-      return fail(c, TF_E_INVAL, "a GEMV shape does not fit the frame kernel");
-  if ((int)ops.size() > kMaxOps) return fail(c, TF_E_INVAL, "op program too long");
-  return TF_OK;
-}
-
-tf_status get_program(tf_ctx* c, bool decode, bool topk, const FrameOp** ops, int* n) {
-  const int idx = (decode ? 0 : 2) + (topk ? 1 : 0);
-  if (!c->n_ops[idx]) {
-    std::vector<FrameOp> v;
-    tf_status r = build_program(c, decode, topk, &v);
-    if (r) return r;
-    CK(cudaMemcpy(c->d_ops + (size_t)idx * kMaxOps, v.data(), v.size() * sizeof(FrameOp),
-                  cudaMemcpyHostToDevice));
-    c->n_ops[idx] = static_cast<int>(v.size());
-  }
-  *ops = c->d_ops + (size_t)idx * kMaxOps;
-  *n = c->n_ops[idx];
-  return TF_OK;
-}
-
-tf_status run_frames(tf_ctx* c, bool decode, const tf_sampling* s, int n_frames) {
-  const FrameOp* ops;
-  int n;
-  tf_status r = get_program(c, decode, s->top_k > 0, &ops, &n);
-  if (r) return r;
-  FrameParams P = {};
-  P.ops = ops;
-  P.n_ops = n;
-  P.n_frames = n_frames;
-  P.T = c->T;
-  P.Hq = c->Hq;
-  P.Hkv = c->Hkv;
-  P.D = c->D;
-  P.q_dim = c->Q;
-  P.kv_dim = c->KV;
-  P.rope = c->rope;
-  P.eps = c->cfg.rms_eps;
-  P.slots = c->frame_slots;
-  P.stage = c->frame_stage;
-  P.un_bytes = c->frame_union;
-  P.pos = &c->st->pos;
-  P.frame_index = &c->st->frame_index;
-  P.sel = c->st->sel;
-  P.fb = c->st->fb;
-  P.forced = c->st->forced;
-  P.forced_on = &c->st->forced_on;
-  P.best = c->st->best;
-  P.ticket = c->st->ticket;
-  P.hist = c->hist;
-  P.hist_idx = &c->st->hist_idx;
-  P.hist_cap = c->T;
-  P.ncb = c->NCB;
-  P.top_k = s->top_k;
-  P.temperature = s->temperature;
-  P.key0 = static_cast<uint32_t>(s->seed & 0xFFFFFFFFull);
-  P.key1 = static_cast<uint32_t>(s->seed >> 32);
-  P.part = c->part;
-  P.counters = c->counters;
-  P.gbar = c->gbar;
-  P.err = &c->st->err;
-  P.trace = c->tracing ? c->trace : nullptr;
-  CK(cudaMemsetAsync(c->gbar, 0, sizeof(uint32_t), c->stream));
-  CK(launch_frame(P, kFrameCtasPerSm * c->num_sms, c->stream));
-  return TF_OK;
-}
-
 bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
   return a.top_k == b.top_k && a.temperature == b.temperature && a.seed == b.seed;
 }
@@ -1025,15 +838,9 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
     return bail(TF_E_CUDA);
   }
   c->stream = c->own_stream;
-  if (gemv_set_attributes() != cudaSuccess || frame_set_attributes() != cudaSuccess) {
+  if (gemv_set_attributes() != cudaSuccess) {
     c->err = "cudaFuncSetAttribute failed";
     return bail(TF_E_CUDA);
-  }
-  {
-    // Default: one kernel per op replayed as a CUDA graph with PDL chaining;
-    // TF_DECODE_DRIVER=persistent selects the persistent frame kernel.
-    const char* drv = std::getenv("TF_DECODE_DRIVER");
-    c->use_graph = !(drv && std::string(drv) == "persistent");
   }
 
   c->fp8 = cfg->weight_dtype == TF_WEIGHT_FP8;
@@ -1055,16 +862,6 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   c->Vmax = std::max(c->Vs, c->Vc);
   c->sem_base = c->Vt - c->Vs;
   c->S_slow = std::max(1, std::min(64, 2 * c->num_sms / c->Hkv));
-  c->S_frame = std::max(1, std::min(c->S_slow, kFrameCtasPerSm * c->num_sms / c->Hkv));
-  c->frame_union = frame_union_bytes(c->Hq / c->Hkv, c->D, c->Vmax);
-  // Two ring slots of up to 40 KB in what the union scratch leaves of a
-  // CTA's share; a slot must hold one whole weight row.
-  c->frame_slots = 2;
-  c->frame_stage = std::min(kFrameStage, ((kFrameSmemPerCta - c->frame_union - 1024) / 2) / 128 * 128);
-  if (c->frame_stage < std::max(c->H, std::max(c->Q, c->F)) * c->eb) {
-    c->err = "frame kernel shared memory does not fit";
-    return bail(TF_E_INVAL);
-  }
 
   // ---- weights: one allocation
   const size_t eb = c->eb, H = c->H;
@@ -1145,9 +942,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       dev_alloc_t(c, &c->pq, (size_t)T * c->Q) || dev_alloc_t(c, &c->po, (size_t)T * c->Q) ||
       dev_alloc_t(c, &c->pu, (size_t)T * c->F) || dev_alloc_t(c, &c->tokens, (size_t)T * B) ||
       dev_alloc_t(c, &c->hist, (size_t)T * B * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
-      dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)) ||
-      dev_alloc_t(c, &c->d_ops, (size_t)4 * kMaxOps) || dev_alloc_t(c, &c->gbar, 1) ||
-      dev_alloc_t(c, &c->trace, (size_t)kMaxOps * 6))
+      dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)))
     return bail(TF_E_NOMEM);
   // Tensor-core prompt GEMMs for bf16 weights whenever every shape tiles.
   c->prefill_tc = gemm_tc_supported(c->QKV, c->H) && gemm_tc_supported(c->H, c->Q) &&
@@ -1474,10 +1269,8 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
   CK(cudaMemcpyAsync(&c->st->pos, &posP, 4, cudaMemcpyHostToDevice, c->stream));
   if (B > 1) {
     CK(enqueue_tail_batched(c, &s, B, 0, true));
-  } else if (c->use_graph) {
+  } else {
     CK(enqueue_tail(c, &s, 0, false));
-  } else if ((r = run_frames(c, false, &s, 1))) {
-    return r;
   }
   c->pos_host = P;
   c->frame_host = 1;
@@ -1497,42 +1290,12 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
   if (r) return r;
   CK(cudaSetDevice(c->device));
   if ((r = set_forced(c, forced, c->Bc))) return r;
-  if (c->use_graph || c->Bc > 1) {
-    cudaGraphExec_t g;
-    if ((r = get_graph(c, &s, &g))) return r;
-    CK(cudaGraphLaunch(g, c->stream));
-  } else if ((r = run_frames(c, true, &s, 1))) {
-    return r;
-  }
+  cudaGraphExec_t g;
+  if ((r = get_graph(c, &s, &g))) return r;
+  CK(cudaGraphLaunch(g, c->stream));
   c->pos_host += 1;
   c->frame_host += 1;
   return read_frame(c, frame, logits, c->Bc);
-}
-
-tf_status tf_decode_trace(tf_ctx* c, const tf_sampling* sampling, int64_t* stamps, int32_t* kinds,
-                          int32_t cap, int32_t* n_ops) {
-  if (!c || !stamps || !kinds || !n_ops || cap < 1) return TF_E_INVAL;
-  if (c->use_graph || c->Bc > 1)
-    return fail(c, TF_E_STATE, "tracing needs the persistent frame kernel and one sequence");
-  int32_t frame[16];
-  c->tracing = true;
-  tf_status r = tf_decode_frame(c, sampling, nullptr, frame, nullptr);
-  c->tracing = false;
-  if (r) return r;
-  tf_sampling s;
-  check_sampling(c, sampling, &s);
-  const FrameOp* ops;
-  int n;
-  if ((r = get_program(c, true, s.top_k > 0, &ops, &n))) return r;
-  *n_ops = n;
-  const int k = std::min(n, cap);
-  std::vector<unsigned long long> buf((size_t)k * 6);
-  CK(cudaMemcpy(buf.data(), c->trace, buf.size() * 8, cudaMemcpyDeviceToHost));
-  for (size_t i = 0; i < buf.size(); ++i) stamps[i] = static_cast<int64_t>(buf[i]);
-  std::vector<FrameOp> host(k);
-  CK(cudaMemcpy(host.data(), ops, (size_t)k * sizeof(FrameOp), cudaMemcpyDeviceToHost));
-  for (int i = 0; i < k; ++i) kinds[i] = host[i].kind;
-  return TF_OK;
 }
 
 tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, int32_t* frames) {
@@ -1549,13 +1312,9 @@ tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, in
   if ((r = set_forced(c, nullptr, c->Bc))) return r;
   const int32_t zero = 0;
   CK(cudaMemcpyAsync(&c->st->hist_idx, &zero, 4, cudaMemcpyHostToDevice, c->stream));
-  if (c->use_graph || c->Bc > 1) {
-    cudaGraphExec_t g;
-    if ((r = get_graph(c, &s, &g))) return r;
-    for (int i = 0; i < n; ++i) CK(cudaGraphLaunch(g, c->stream));
-  } else if ((r = run_frames(c, true, &s, n))) {
-    return r;
-  }
+  cudaGraphExec_t g;
+  if ((r = get_graph(c, &s, &g))) return r;
+  for (int i = 0; i < n; ++i) CK(cudaGraphLaunch(g, c->stream));
   c->pos_host += n;
   c->frame_host += n;
   CK(cudaMemcpyAsync(frames, c->hist, sizeof(int32_t) * c->NCB * c->Bc * n, cudaMemcpyDeviceToHost,
@@ -1775,7 +1534,8 @@ tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, 
   cudaFree(part);
   cudaFree(cnt);
   cudaFree(err);
-  if (r == TF_OK && e) r = TF_E_INVAL;
+  if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
+  else if (r == TF_OK && e) r = TF_E_INVAL;
   return r;
 }
 

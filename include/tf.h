@@ -199,18 +199,6 @@ void tf_destroy(tf_ctx* ctx);
 tf_status tf_profile_kernel(tf_ctx* ctx, int32_t which, int32_t iters,
                             float* ms_per_launch, int64_t* bytes_per_launch);
 
-/* One decode frame, like tf_decode_frame, with per-op timing: the persistent
- * frame kernel stamps %globaltimer (ns) for each op of its program, on CTA 0
- * and on the last CTA: barrier-wait start, barrier-wait end, op end.
- * stamps: host int64 [cap][2][3]; kinds: host int32 [cap] (0 GEMV,
- * 1 attention, 2 selection, 3 bookkeeping); *n_ops receives the program
- * length (stamps beyond cap are dropped).  Errors as tf_decode_frame;
- * TF_E_STATE when the context uses the kernel-per-op driver (the default;
- * the persistent frame kernel is selected by TF_DECODE_DRIVER=persistent in
- * the environment of tf_create). */
-tf_status tf_decode_trace(tf_ctx* ctx, const tf_sampling* sampling, int64_t* stamps,
-                          int32_t* kinds, int32_t cap, int32_t* n_ops);
-
 /* ---------------------------------------------------------------------------
  * Single-operation entry points, for parity tests and profiling.  Each runs
  * one kernel of the decode path on caller-provided DEVICE buffers on `stream`
@@ -247,7 +235,8 @@ tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab,
  * softmax results are merged afterwards.  Allocates its scratch (partials,
  * tickets, error word) with cudaMalloc and frees it before returning.
  * D must be 64 or 128, Hq / Hkv one of 1, 2, 4, 8, pos0 + rows <= T.
- * Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA. */
+ * Errors: TF_E_INVAL (bad argument or position), TF_E_NOMEM, TF_E_CUDA,
+ * TF_E_TIMEOUT (a bounded wait for a key/value copy expired). */
 tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
                           int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
                           int32_t splits, float* out, void* stream);
@@ -260,8 +249,9 @@ tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, 
  * tf_op_attention, but the scratch comes from one fixed array built into the
  * library (present on every GPU that loads it, until the process exits):
  * calls need rows*Hq*splits*(D+2) <= 524288 and rows*Hkv <= 1024, else
- * TF_E_INVAL.  The first call on a device looks up the array's device
- * address (make it before any stream capture).  All calls share the array:
+ * TF_E_INVAL.  The first call on a device (and the first after its context
+ * was reset) looks up the array's device address: make it before any stream
+ * capture.  All calls share the array:
  * calls that overlap on the GPU race on it. */
 tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
                                   int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,

@@ -35,7 +35,7 @@ from __future__ import annotations
 import numpy as np
 
 from .numerics import (bf16_bits_to_f64, round_to_bf16, fp8_quantize_rows, fp8_dequant_rows,
-                       rmsnorm, apply_rope, attention_row, silu, linear)
+                       rmsnorm, apply_rope, attention_row, causal_attention, silu, linear)
 from .sampler import argmax_lowest, topk_sample
 
 LINEAR_SUFFIXES = ("wqkv", "wo", "w1", "w3", "w2")
@@ -149,13 +149,14 @@ class DualAROracle:
         q = qkv[:, : d.q_dim].reshape(-1, d.n_heads, d.head_dim)
         k = qkv[:, d.q_dim: d.q_dim + d.kv_dim].reshape(-1, d.n_kv_heads, d.head_dim)
         v = qkv[:, d.q_dim + d.kv_dim:].reshape(-1, d.n_kv_heads, d.head_dim)
-        o = np.empty((x.shape[0], d.q_dim))
         for r, p in enumerate(positions):
             K[:, p] = round_to_bf16(apply_rope(k[r], p, d.rope_theta))
             V[:, p] = round_to_bf16(v[r])
-        for r, p in enumerate(positions):
-            qr = apply_rope(q[r], p, d.rope_theta)
-            o[r] = attention_row(qr, K, V, p + 1).reshape(-1)
+        qr = np.stack([apply_rope(q[r], p, d.rope_theta) for r, p in enumerate(positions)])
+        if len(positions) == 1:
+            o = attention_row(qr[0], K, V, positions[0] + 1).reshape(1, -1)
+        else:
+            o = causal_attention(qr, K, V, positions).reshape(len(positions), -1)
         x = x + linear(self.W(f"{prefix}.wo"), o)
         m = rmsnorm(x, bf16_bits_to_f64(self.raw[f"{prefix}.ffn_norm"]), d.rms_eps)
         g = linear(self.W(f"{prefix}.w1"), m)

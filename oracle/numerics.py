@@ -181,6 +181,31 @@ def attention_row(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_valid: int) -> 
     return out
 
 
+def causal_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, positions) -> np.ndarray:
+    """attention_row for a block of query rows at once (the prompt pass).
+
+    q [R][Hq][D], row r at position positions[r]; K, V [Hkv][T][D].  Row r
+    attends to keys 0..positions[r], exactly as attention_row(q[r], K, V,
+    positions[r] + 1): the same scores, scale, max subtraction and grouping,
+    with the keys a row may not see masked out of its softmax.  Returns
+    o [R][Hq][D].
+    """
+    R, Hq, D = q.shape
+    Hkv = K.shape[0]
+    group = Hq // Hkv
+    pos = np.asarray(positions, dtype=np.int64)
+    n = int(pos.max()) + 1
+    visible = np.arange(n)[None, :] <= pos[:, None]          # [R][n]
+    out = np.empty((R, Hq, D), dtype=np.float64)
+    for h in range(Hq):
+        g = h // group
+        s = q[:, h, :] @ K[g, :n].T / np.sqrt(D)             # [R][n]
+        s = np.where(visible, s, -np.inf)
+        p = np.exp(s - np.max(s, axis=1, keepdims=True))
+        out[:, h, :] = (p / np.sum(p, axis=1, keepdims=True)) @ V[g, :n]
+    return out
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     """SiLU: z / (1 + exp(-z)) (the gate of the SwiGLU MLP)."""
     return z / (1.0 + np.exp(-z))

@@ -22,17 +22,6 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-@pytest.fixture(params=["persistent", "graph"])
-def driver(request, monkeypatch):
-    """Decode driver: one kernel per op replayed as a CUDA graph (default) or
-    the persistent frame kernel."""
-    if request.param == "persistent":
-        monkeypatch.setenv("TF_DECODE_DRIVER", "persistent")
-    else:
-        monkeypatch.delenv("TF_DECODE_DRIVER", raising=False)
-    return request.param
-
-
 @pytest.fixture(scope="module", autouse=True)
 def built():
     import __graft_entry__
@@ -176,7 +165,7 @@ TINY_G8 = TINY.replace(hidden=256, ffn=512, n_heads=8, n_kv_heads=1, head_dim=12
 
 @pytest.mark.parametrize("dims,fmt,tol", [(TINY, "bf16", BF16_TOL), (TINY, "fp8", FP8_TOL),
                                           (TINY_ODD, "bf16", BF16_TOL), (TINY_G8, "bf16", BF16_TOL)])
-def test_tiny_teacher_forced(dims, fmt, tol, driver):
+def test_tiny_teacher_forced(dims, fmt, tol):
     tf = TeacherForced(dims, fmt, seed=0)
     tf.prefill(make_prompt(dims, 16, seed=0))
     for _ in range(8):
@@ -189,7 +178,7 @@ def test_tiny_teacher_forced(dims, fmt, tol, driver):
 
 
 @pytest.mark.parametrize("k", [30, 4])
-def test_tiny_topk_teacher_forced(k, driver):
+def test_tiny_topk_teacher_forced(k):
     # With 64 codes and k = 30 most candidate boundaries sit within the
     # measured logit perturbation; those draws are only checked for validity.
     s = {"top_k": k, "seed": 1234}
@@ -221,7 +210,7 @@ def test_prompt_edges_and_capacity():
     tf.dec.close()
 
 
-def test_decode_frames_equals_single_calls_and_is_deterministic(driver):
+def test_decode_frames_equals_single_calls_and_is_deterministic():
     w = make_weights(TINY, seed=5)
     prompt = make_prompt(TINY, 12, seed=5)
     runs = []
@@ -266,7 +255,7 @@ def full_weights():
 
 
 @pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL)])
-def test_full_size_teacher_forced_sampled_frames(full_weights, fmt, tol, driver):
+def test_full_size_teacher_forced_sampled_frames(full_weights, fmt, tol):
     """Full-size model (36+4 layers, hidden 2560), prefill 128 then 2 decode
     frames, in the launch configuration the benchmark times."""
     tf = TeacherForced(FULL, fmt, weights=full_weights)

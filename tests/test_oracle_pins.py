@@ -207,6 +207,31 @@ def test_attention_brute_force_and_sdpa():
     assert np.allclose(oracle.attention_row(q, Kf, Vf, n), out, rtol=1e-14, atol=1e-14)
 
 
+def test_causal_attention_block_matches_sdpa_and_rows():
+    """The prompt pass's block attention: torch SDPA with an explicit causal
+    mask over grouped-query heads, and row by row the single-row routine."""
+    rng = np.random.default_rng(21)
+    Hq, Hkv, T, D = 8, 2, 12, 16
+    pos = [2, 3, 4, 5, 6, 7, 8]
+    q = rng.standard_normal((len(pos), Hq, D))
+    K = rng.standard_normal((Hkv, T, D))
+    V = rng.standard_normal((Hkv, T, D))
+    out = oracle.causal_attention(q, K, V, pos)
+    n = max(pos) + 1
+    mask = torch.from_numpy(np.arange(n)[None, :] <= np.array(pos)[:, None])
+    sd = F.scaled_dot_product_attention(
+        torch.from_numpy(q).transpose(0, 1)[None], torch.from_numpy(K[:, :n])[None],
+        torch.from_numpy(V[:, :n])[None], attn_mask=mask, enable_gqa=True).numpy()[0]
+    assert np.allclose(out, sd.transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
+    for r, p in enumerate(pos):
+        assert np.allclose(out[r], oracle.attention_row(q[r], K, V, p + 1), rtol=1e-13, atol=1e-13)
+    # keys past a row's position never matter
+    K2, V2 = K.copy(), V.copy()
+    K2[:, n:] = 1e3
+    V2[:, n:] = -1e3
+    assert np.array_equal(oracle.causal_attention(q, K2, V2, pos), out)
+
+
 def test_silu_matches_torch():
     z = np.linspace(-30, 30, 1001)
     assert np.allclose(oracle.silu(z), F.silu(torch.from_numpy(z)).numpy(), rtol=1e-14, atol=1e-14)
@@ -270,6 +295,34 @@ def test_topk_frequencies_follow_truncated_softmax():
         counts[pos[idx]] += 1
     chi2 = np.sum((counts - n * p) ** 2 / (n * p))
     assert chi2 < 30.0          # 7 degrees of freedom: p-value ~ 1e-4
+
+
+def test_topk_temperature_frequencies_follow_tempered_softmax():
+    """At temperature T the draw frequencies over the top-k candidates follow
+    softmax(z / T): a slip such as multiplying by T, or dividing before the
+    max subtraction in a way that changes the weights, moves them off it."""
+    z = make_logits(1, 64, seed=6, scale=1.0)[0]
+    k, temp = 6, 0.7
+    cand = oracle.topk_candidates(z, k)
+    zc = z[cand].astype(np.float64)
+    p = np.exp((zc - zc[0]) / temp)
+    p /= p.sum()
+    # the untempered weights differ enough for the test to tell them apart
+    p1 = np.exp(zc - zc[0])
+    p1 /= p1.sum()
+    n = 6000
+    assert np.sum((n * p1 - n * p) ** 2 / (n * p)) > 60.0
+    counts = np.zeros(k)
+    pos = {int(c): i for i, c in enumerate(cand)}
+    for t in range(n):
+        idx, det = oracle.topk_sample(z, k, seed=99, frame=t, codebook=5, temperature=temp)
+        counts[pos[idx]] += 1
+    chi2 = np.sum((counts - n * p) ** 2 / (n * p))
+    assert chi2 < 26.0          # 5 degrees of freedom: p-value ~ 1e-4
+    # the weights themselves: exp32 of the tempered differences, largest first
+    _, det = oracle.topk_sample(z, k, seed=99, frame=0, codebook=5, temperature=temp)
+    assert det["p"][0] == 1.0
+    assert np.allclose(det["p"], np.exp((zc - zc[0]) / temp), rtol=1e-6)
 
 
 # ----------------------------------------------------------------- load formula

@@ -86,10 +86,12 @@ class DualAROracle:
     (fp8_quantize_rows) and use the dequantised values; embeddings and norms
     stay bf16 (drbaph s2-pro-fp8 model card, "Quantization Details").
     batch: number of independent sequences.
+    fp8_codes: optional name -> (codes, scale) of fp8_quantize_rows already
+    computed for these weights (the quantisation is then not repeated).
     """
 
     def __init__(self, dims, weights: dict, weight_format: str = "bf16",
-                 batch: int = 1, cache_f64: bool | None = None):
+                 batch: int = 1, cache_f64: bool | None = None, fp8_codes: dict | None = None):
         self.d = dims
         self.raw = weights
         self.fmt = weight_format
@@ -104,7 +106,8 @@ class DualAROracle:
         self.fp8 = {}
         if weight_format == "fp8":
             for name in linear_names(dims):
-                self.fp8[name] = fp8_quantize_rows(weights[name])
+                self.fp8[name] = (fp8_codes[name] if fp8_codes is not None
+                                  else fp8_quantize_rows(weights[name]))
         elif weight_format != "bf16":
             raise ValueError(weight_format)
         self.reset()

@@ -72,11 +72,11 @@ class TeacherForced:
     oracle's ids forced, frame by frame, keeping both sides' logits; with
     batch > 1, B independent sequences decode in lockstep on both sides."""
 
-    def __init__(self, dims, fmt="bf16", seed=0, weights=None, dec=None, batch=1):
+    def __init__(self, dims, fmt="bf16", seed=0, weights=None, dec=None, batch=1, fp8_codes=None):
         self.d = dims
         self.batch = batch
         self.w = weights if weights is not None else make_weights(dims, seed)
-        self.ref = oracle.DualAROracle(dims, self.w, fmt, batch=batch)
+        self.ref = oracle.DualAROracle(dims, self.w, fmt, batch=batch, fp8_codes=fp8_codes)
         self.dec = dec if dec is not None else Decoder(dims, fmt, max_batch=batch)
         if dec is None:
             self.dec.load_weights(self.w)

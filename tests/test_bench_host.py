@@ -107,3 +107,38 @@ def test_reference_arm_is_rank0_only():
         warmup = 3
     # rank 1 of a torchrun job returns at once without running the oracle
     assert bench.run_reference(A(), bench.WORKLOADS["tiny"], 2, 1) is None
+
+
+@pytest.mark.parametrize("steps", [1, 5, 20, 64, 895, 896, 897, 2000])
+def test_schedule_plan_spreads_timed_frames_over_the_schedule(steps):
+    prefill, cap = 128, 896
+    plan = bench.schedule_plan(prefill, cap, steps)
+    assert sum(k for _, k in plan) == steps
+    for start, k in plan:
+        assert k >= 1 and prefill <= start and start + k <= prefill + cap
+    partial = plan[steps // cap:]
+    if len(partial) > 1:
+        # the first segment starts the schedule, the last one ends it
+        assert partial[0][0] == prefill
+        assert partial[-1][0] + partial[-1][1] == prefill + cap
+        starts = [s for s, _ in partial]
+        assert starts == sorted(starts)
+
+
+def test_reference_arm_times_what_it_prints(capsys):
+    """The oracle arm prints the workload config the GPU arm prints and, as
+    `steps`, the number of frames it actually timed."""
+    import json
+
+    class A:
+        seed = 0
+        steps = 3
+        warmup = 3
+    wl = bench.WORKLOADS["tiny"]
+    bench.run_reference(A(), wl, 1, 0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.workload_config(wl, 1)
+    assert line["steps"] == 3 and line["warmup"] == 3
+    assert line["ms_per_step"] == pytest.approx(1e3 / line["value"], rel=1e-3)
+    assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]

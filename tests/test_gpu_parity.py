@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import model as om
 from dual_ar_decode_gb300 import (Decoder, TfError, op_attention, op_gemm, op_gemv,
                                   op_quantize_fp8, op_select)
 from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
@@ -114,6 +115,8 @@ def test_gemv_matches_oracle_linear(rows, cols, fp8):
     (32, 8, 128, 1, 77, 38),     # short context: fewer splits than asked
     (4, 2, 64, 3, 200, 7),       # tiny heads, ragged split sizes
     (8, 1, 128, 1, 333, 5),      # 8 query heads per KV head
+    (32, 8, 128, 1, 4095, 38),   # long context: the last slot of a 4096 cache, batch-1 splits
+    (32, 8, 128, 2, 3070, 38),   # two rows deep in a long cache
 ])
 def test_attention_matches_oracle(Hq, Hkv, D, rows, pos0, splits):
     T = pos0 + rows + 5
@@ -254,14 +257,52 @@ def full_weights():
     return make_weights(FULL, seed=0)
 
 
+@pytest.fixture(scope="module")
+def full_fp8_codes(full_weights):
+    """Per-row fp8 codes of every linear weight, computed once by the oracle."""
+    return {n: oracle.fp8_quantize_rows(full_weights[n]) for n in om.linear_names(FULL)}
+
+
 @pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL)])
-def test_full_size_teacher_forced_sampled_frames(full_weights, fmt, tol):
+def test_full_size_teacher_forced_sampled_frames(full_weights, full_fp8_codes, fmt, tol):
     """Full-size model (36+4 layers, hidden 2560), prefill 128 then 2 decode
     frames, in the launch configuration the benchmark times."""
-    tf = TeacherForced(FULL, fmt, weights=full_weights)
+    tf = TeacherForced(FULL, fmt, weights=full_weights,
+                       fp8_codes=full_fp8_codes if fmt == "fp8" else None)
     tf.prefill(make_prompt(FULL, 128, seed=0))
     tf.decode()
     tf.decode()
     worst, compared, skipped = tf.check(tol)
     assert compared >= 15
+    tf.dec.close()
+
+
+def test_full_size_prefill_heavy_1024(full_weights):
+    """Prefill-heavy workload at batch 1 (full-size bf16, T = 2048): a
+    1024-id prompt through the tensor-core prompt path and the prompt
+    attention, then 2 decode frames at positions 1024 and 1025."""
+    d = FULL.replace(max_seq_len=2048)
+    tf = TeacherForced(d, "bf16", weights=full_weights)
+    tf.prefill(make_prompt(d, 1024, seed=0))
+    tf.decode()
+    tf.decode()
+    worst, compared, skipped = tf.check(BF16_TOL)
+    assert compared >= 15
+    tf.dec.close()
+
+
+def test_full_size_fp8_long_context_topk30(full_weights, full_fp8_codes):
+    """Long-context workload (full-size fp8 per-row weights, T = 4096): a
+    3072-id prompt, then 2 decode frames at positions 3072 and 3073, every
+    codebook drawn by top-k 30 from the seeded Philox stream (seed 1234)."""
+    d = FULL.replace(max_seq_len=4096)
+    s = {"top_k": 30, "seed": 1234}
+    tf = TeacherForced(d, "fp8", weights=full_weights, fp8_codes=full_fp8_codes)
+    tf.prefill(make_prompt(d, 3072, seed=0), s)
+    tf.decode(s)
+    tf.decode(s)
+    worst, compared, skipped = tf.check(FP8_TOL, s)
+    # draws the a-priori perturbation cannot move must agree exactly; the
+    # rest must be members of the oracle's candidate set (checked in check)
+    assert compared + skipped == 30
     tf.dec.close()

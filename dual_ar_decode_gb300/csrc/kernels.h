@@ -12,6 +12,7 @@ enum : uint32_t {
   ERR_NAN = 1u << 1,       // NaN logit met by a selection
   ERR_BAD_ID = 1u << 2,    // an id fed back was outside its table
   ERR_BAD_POS = 1u << 3,   // a position outside the KV cache
+  ERR_BAD_CODE = 1u << 4,  // an e4m3 NaN code in a weight handed over as codes
 };
 
 // ----------------------------------------------------------------- GEMV
@@ -215,6 +216,7 @@ struct PackParams {
   int32_t map;
   int32_t q_dim, kv_dim, head_dim;
   int32_t mode;          // 0 copy bf16, 1 quantise bf16 -> fp8, 2 copy fp8 + scale
+  uint32_t* err;         // mode 2: ERR_BAD_CODE if a code is NaN (0x7F / 0xFF)
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
 

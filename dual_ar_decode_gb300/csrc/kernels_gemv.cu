@@ -57,8 +57,44 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return *reinterpret_cast<float2*>(&D);
 }
 
+// How e4m3 weight codes become numbers in the fp8 GEMV (compile-time):
+//   0  cvt.rn.f16x2.e4m3x2, then f16 -> f32, packed f32 FMA (fp32 activations);
+//   1  bit placement into f32: code s.eeee.mmm placed as float32 bits
+//      s << 31 | eeeemmm << 20 is the code's value times 2^-120 exactly
+//      (subnormal codes included); activations carry 2^60 and the row scale
+//      the other 2^60, so products stay in float32's normal range;
+//   2  bit placement into f16: the same code placed as f16 bits
+//      s << 15 | eeeemmm << 7 is its value times 2^-8 exactly (f16 has 5
+//      exponent bits, bias 15); f16 activations (more precise than the bf16
+//      activations of the fp8 model card), mixed f16 x f16 + f32 FMA;
+//   3  cvt.rn.f16x2.e4m3x2 (exact), f16 activations, mixed FMA.
+#ifndef TF_FP8_PATH
+#define TF_FP8_PATH 0
+#endif
+constexpr int kFp8Path = TF_FP8_PATH;
+// Power of two the finished fp8 dot product is multiplied by, besides the row scale.
+constexpr float kFp8Rescale = kFp8Path == 1 ? 1.152921504606846976e18f   // 2^60
+                            : kFp8Path == 2 ? 256.0f : 1.0f;
+// Power of two the fp8 activations are multiplied by before the dot product.
+constexpr float kFp8ActScale = kFp8Path == 1 ? 1.152921504606846976e18f : 1.0f;
+constexpr bool kFp8HalfAct = kFp8Path == 2 || kFp8Path == 3;   // activations as packed f16 pairs
+
+// d = a * b + c with a, b the two f16 halves selected by the template and c float.
+__device__ __forceinline__ float fma_h(uint32_t w2, uint32_t a2, float c, int half) {
+  float d;
+  if (half == 0)
+    asm("{.reg .b16 wl, wh, al, ah; mov.b32 {wl, wh}, %1; mov.b32 {al, ah}, %2;"
+        " fma.rn.f32.f16 %0, wl, al, %3;}" : "=f"(d) : "r"(w2), "r"(a2), "f"(c));
+  else
+    asm("{.reg .b16 wl, wh, al, ah; mov.b32 {wl, wh}, %1; mov.b32 {al, ah}, %2;"
+        " fma.rn.f32.f16 %0, wh, ah, %3;}" : "=f"(d) : "r"(w2), "r"(a2), "f"(c));
+  return d;
+}
+
 // Accumulates one 16-byte weight chunk times its activations into acc
-// (two interleaved partial sums).
+// (two interleaved partial sums).  For fp8 with half activations, a[] holds
+// the packed f16 pairs (as float bit patterns) in the order the decode below
+// pairs the codes.
 template <int WT, int EPC>
 __device__ __forceinline__ float2 chunk_fma(const uint4 w, const float* a, float2 acc) {
   const uint32_t v[4] = {w.x, w.y, w.z, w.w};
@@ -66,7 +102,7 @@ __device__ __forceinline__ float2 chunk_fma(const uint4 w, const float* a, float
 #pragma unroll
     for (int i = 0; i < 4; ++i)
       acc = fma2(make_float2(bf16_lo(v[i]), bf16_hi(v[i])), make_float2(a[2 * i], a[2 * i + 1]), acc);
-  } else {
+  } else if constexpr (kFp8Path == 0) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(v[i] & 0xFFFFu));
@@ -74,8 +110,77 @@ __device__ __forceinline__ float2 chunk_fma(const uint4 w, const float* a, float
       acc = fma2(lo, make_float2(a[4 * i], a[4 * i + 1]), acc);
       acc = fma2(hi, make_float2(a[4 * i + 2], a[4 * i + 3]), acc);
     }
+  } else if constexpr (kFp8Path == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // byte b of v at bits 31..24 (zeros below), then (x >>arith 4) & 0x87F00000
+      float f[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint32_t x;
+        asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(v[i]), "r"(0x0444u | (static_cast<uint32_t>(b) << 12)));
+        f[b] = __uint_as_float(static_cast<uint32_t>(static_cast<int32_t>(x) >> 4) & 0x87F00000u);
+      }
+      acc = fma2(make_float2(f[0], f[1]), make_float2(a[4 * i], a[4 * i + 1]), acc);
+      acc = fma2(make_float2(f[2], f[3]), make_float2(a[4 * i + 2], a[4 * i + 3]), acc);
+    }
+  } else if constexpr (kFp8Path == 2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // lanes (b0, b2) and (b1, b3) of v as f16 bit patterns
+      const uint32_t t = v[i] << 8;
+      const uint32_t p02 = (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
+      const uint32_t p13 = (v[i] & 0x80008000u) | ((v[i] >> 1) & 0x3F803F80u);
+      const uint32_t a02 = __float_as_uint(a[2 * i]), a13 = __float_as_uint(a[2 * i + 1]);
+      acc.x = fma_h(p02, a02, acc.x, 0);
+      acc.y = fma_h(p13, a13, acc.y, 0);
+      acc.x = fma_h(p02, a02, acc.x, 1);
+      acc.y = fma_h(p13, a13, acc.y, 1);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t h01, h23;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(v[i] & 0xFFFFu)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(v[i] >> 16)));
+      const uint32_t a01 = __float_as_uint(a[2 * i]), a23 = __float_as_uint(a[2 * i + 1]);
+      acc.x = fma_h(h01, a01, acc.x, 0);
+      acc.y = fma_h(h01, a01, acc.y, 1);
+      acc.x = fma_h(h23, a23, acc.x, 0);
+      acc.y = fma_h(h23, a23, acc.y, 1);
+    }
   }
   return acc;
+}
+
+// f16 bits of x, round to nearest even (finite activations).
+__device__ __forceinline__ uint32_t f16_bits(float x) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
+}
+
+// Rewrites one chunk's EPC fp32 activations for the fp8 decode in use: the
+// 2^60 pre-scale (bit placement into f32), or packed f16 pairs in a[0..7] in
+// the pairing chunk_fma expects (f16 paths).
+template <int WT, int EPC>
+__device__ __forceinline__ void fp8_prepare(float* a) {
+  if constexpr (WT == 1 && kFp8Path == 1) {
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) a[e] *= kFp8ActScale;
+  } else if constexpr (WT == 1 && kFp8HalfAct) {
+    float pk[EPC / 2];
+#pragma unroll
+    for (int i = 0; i < EPC / 4; ++i) {
+      if constexpr (kFp8Path == 2) {   // (a0, a2), (a1, a3) of each 4 codes
+        pk[2 * i] = __uint_as_float(f16_bits(a[4 * i]) | (f16_bits(a[4 * i + 2]) << 16));
+        pk[2 * i + 1] = __uint_as_float(f16_bits(a[4 * i + 1]) | (f16_bits(a[4 * i + 3]) << 16));
+      } else {                         // (a0, a1), (a2, a3)
+        pk[2 * i] = __uint_as_float(f16_bits(a[4 * i]) | (f16_bits(a[4 * i + 1]) << 16));
+        pk[2 * i + 1] = __uint_as_float(f16_bits(a[4 * i + 2]) | (f16_bits(a[4 * i + 3]) << 16));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < EPC / 2; ++i) a[i] = pk[i];
+  }
 }
 
 // Sums V values over the 32 lanes of a warp with a transposing butterfly:
@@ -289,6 +394,13 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
     }
   }
 
+  if constexpr (WT == 1) {
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+      for (int j = 0; j < J; ++j) fp8_prepare<WT, EPC>(a[m][j]);
+  }
+
   unsigned long long best = 0ull;  // EPI_LOGITS: best (value, lowest index) key seen
   int s = 0;
   for (int b0 = 0; b0 < nrows; b0 += kRowBatch) {
@@ -345,8 +457,8 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
             v1 += red[((2 * pi + 1) * NW + w) * M + m];
           }
           if (p.scale) {
-            v0 *= __ldg(&p.scale[rg]);
-            v1 *= __ldg(&p.scale[rg + 1]);
+            v0 *= __ldg(&p.scale[rg]) * kFp8Rescale;
+            v1 *= __ldg(&p.scale[rg + 1]) * kFp8Rescale;
           }
           if (p.epi == EPI_SWIGLU) {
             epi_swiglu(p, m, rg >> 1, v0, v1);
@@ -364,7 +476,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
         for (int m = 0; m < M; ++m) {
           float v = 0.f;
           for (int w = 0; w < NW; ++w) v += red[(ri * NW + w) * M + m];
-          if (p.scale) v *= __ldg(&p.scale[rg]);
+          if (p.scale) v *= __ldg(&p.scale[rg]) * kFp8Rescale;
           float* o = p.out + (size_t)m * p.ldo + rg;
           if (p.epi == EPI_RESID) {
             *o = ((b0 == 0 && ri == tid) ? xr0[m] : *o) + v;

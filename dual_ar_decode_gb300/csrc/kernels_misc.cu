@@ -344,9 +344,19 @@ __global__ void __launch_bounds__(256) k_pack(const PackParams p) {
     return;
   }
   if (p.mode == 2) {
+    // Codes handed over as they are: NaN codes (S.1111.111) are refused, since
+    // the GEMV's decode reads every code as a finite number.
     const uint4* src = reinterpret_cast<const uint4*>(p.src + s * p.cols);
     uint4* dst = reinterpret_cast<uint4*>(p.dst + d * p.cols);
-    for (int64_t i = tid; i < p.cols / 16; i += blockDim.x) dst[i] = src[i];
+    uint32_t nan = 0;
+    for (int64_t i = tid; i < p.cols / 16; i += blockDim.x) {
+      const uint4 v = src[i];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) nan |= ((w[k] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+      dst[i] = v;
+    }
+    if (nan && p.err) atomicOr(p.err, ERR_BAD_CODE);
     if (tid == 0) p.dst_scale[d] = p.src_scale[s];
     return;
   }

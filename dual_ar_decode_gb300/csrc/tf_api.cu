@@ -1093,10 +1093,21 @@ tf_status tf_load_weights(tf_ctx* c, const tf_tensor* t, int32_t n) {
         CK(cudaMemcpyAsync(c->staging_scale, x.row_scale, (size_t)rows * 4, cudaMemcpyDefault, c->stream));
         p.src_scale = c->staging_scale;
         p.mode = 2;
+        p.err = &c->st->err;
       } else {
         return fail(c, TF_E_INVAL, name + ": unknown dtype");
       }
       CK(launch_pack(p, c->stream));
+      if (p.mode == 2) {
+        uint32_t e = 0;
+        CK(cudaMemcpyAsync(&e, &c->st->err, sizeof(e), cudaMemcpyDeviceToHost, c->stream));
+        CK(cudaStreamSynchronize(c->stream));
+        if (e & ERR_BAD_CODE) {
+          CK(cudaMemsetAsync(&c->st->err, 0, sizeof(uint32_t), c->stream));
+          CK(cudaStreamSynchronize(c->stream));
+          return fail(c, TF_E_INVAL, name + ": e4m3 NaN code (0x7F or 0xFF) in the weight");
+        }
+      }
       return TF_OK;
     };
     tf_status s = TF_OK;

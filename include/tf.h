@@ -87,7 +87,8 @@ typedef struct {
  * Linear weights are [out][in] row-major.  Embeddings and norms are bf16.
  * In an FP8 context a linear weight is given either as bf16 (the library
  * quantises it per row, exactly as tf_op_quantize_fp8) or as
- * TF_DTYPE_FP8_E4M3 codes with row_scale[out] (float32). */
+ * TF_DTYPE_FP8_E4M3 codes with row_scale[out] (float32); codes must be
+ * finite (NaN codes 0x7F / 0xFF are refused with TF_E_INVAL). */
 typedef struct {
   const char* name;
   int32_t dtype;
@@ -289,6 +290,8 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
  * back to back (each launch with weights W + i * rows * cols elements, so the
  * caller can rotate through distinct matrices) and returns the mean device
  * time per launch in *ms (CUDA events on `stream`), if ms is not NULL.
+ * e4m3 codes must be finite: a NaN code (0x7F, 0xFF) gives an undefined
+ * result here (tf_load_weights refuses them).
  * Errors: TF_E_INVAL, TF_E_CUDA. */
 tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale,
                      int64_t rows, int64_t cols, const float* x, float* y,

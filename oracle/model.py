@@ -32,6 +32,9 @@ Readings taken where the pages are open (each is tested):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 from .numerics import (bf16_bits_to_f64, round_to_bf16, fp8_quantize_rows, fp8_dequant_rows,
@@ -105,9 +108,12 @@ class DualAROracle:
         self._cache = {}
         self.fp8 = {}
         if weight_format == "fp8":
-            for name in linear_names(dims):
-                self.fp8[name] = (fp8_codes[name] if fp8_codes is not None
-                                  else fp8_quantize_rows(weights[name]))
+            names = linear_names(dims)
+            if fp8_codes is not None:
+                self.fp8 = {n: fp8_codes[n] for n in names}
+            else:   # one tensor per task; NumPy releases the GIL in its loops
+                with ThreadPoolExecutor(min(32, os.cpu_count() or 1)) as ex:
+                    self.fp8 = dict(zip(names, ex.map(lambda n: fp8_quantize_rows(weights[n]), names)))
         elif weight_format != "bf16":
             raise ValueError(weight_format)
         self.reset()

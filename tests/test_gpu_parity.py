@@ -10,7 +10,6 @@ import pytest
 import torch
 
 import oracle
-from oracle import model as om
 from dual_ar_decode_gb300 import (Decoder, TfError, op_attention, op_gemm, op_gemv,
                                   op_quantize_fp8, op_select)
 from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
@@ -260,7 +259,7 @@ def full_weights():
 @pytest.fixture(scope="module")
 def full_fp8_codes(full_weights):
     """Per-row fp8 codes of every linear weight, computed once by the oracle."""
-    return {n: oracle.fp8_quantize_rows(full_weights[n]) for n in om.linear_names(FULL)}
+    return oracle.DualAROracle(FULL, full_weights, "fp8").fp8
 
 
 @pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL)])

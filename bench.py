@@ -42,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 PAGE_LOAD_ELEMENTS = 7_377_351_168   # tuna-fish README, "Inference estimation"
 # ncu DRAM bytes (read + write) of one 19456 x 2560 gate/up-shaped k_gemv
 # launch, per weight format, from the capture of the kernel as it stands.
-GATE_UP_TRAFFIC = {"bf16": 99_670_272 + 3_020_800}
+GATE_UP_TRAFFIC = {"bf16": 99_670_272 + 3_020_800, "fp8": 49_942_272 + 0}
 
 
 # ---------------------------------------------------------------- accounting

@@ -40,8 +40,13 @@ constexpr int kRowBatch = 128;  // rows reduced per epilogue round
 #define TF_GEMV_STAGE_BYTES (40 * 1024)
 #endif
 constexpr int kStageTarget = TF_GEMV_STAGE_BYTES;  // bytes of whole rows per stage
-constexpr int kRingTwo = 80 * 1024;   // ring per CTA when two CTAs share an SM
-constexpr int kRingOne = 160 * 1024;  // ring of a lone CTA
+constexpr int kRingPerSm = 160 * 1024;  // ring bytes per SM, split over its CTAs
+#ifndef TF_GEMV_QUAD
+#define TF_GEMV_QUAD 1
+#endif
+// Narrow rows (few consumer warps per CTA) run four CTAs per SM, so that an
+// SM still has about 20 consumer warps to hide the reduction latencies.
+constexpr int kQuadMaxThreads = TF_GEMV_QUAD ? 192 : 0;
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
@@ -69,7 +74,7 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 //      activations of the fp8 model card), mixed f16 x f16 + f32 FMA;
 //   3  cvt.rn.f16x2.e4m3x2 (exact), f16 activations, mixed FMA.
 #ifndef TF_FP8_PATH
-#define TF_FP8_PATH 0
+#define TF_FP8_PATH 3
 #endif
 constexpr int kFp8Path = TF_FP8_PATH;
 // Power of two the finished fp8 dot product is multiplied by, besides the row scale.
@@ -588,8 +593,11 @@ const void* kernel_for(int wt, int M, int J) {
   return t[wt][M - 1][J - 1];
 }
 
+// Ring of `ring` bytes in stages of about min(kStageTarget, ring / 2) bytes
+// of whole rows (at least one row and two stages).
 void set_ring(GemvParams& p, int rowbytes, int ring) {
-  p.rs = rowbytes >= kStageTarget ? 1 : kStageTarget / rowbytes;
+  const int target = std::min(kStageTarget, ring / 2);
+  p.rs = rowbytes >= target ? 1 : target / rowbytes;
   p.stb = ((p.rs * rowbytes + 127) / 128) * 128;
   p.nst = std::max(2, std::min(16, ring / p.stb));
 }
@@ -627,25 +635,28 @@ void gemv_plan(GemvParams& p, int eb, int num_sms, int M) {
     if (b.eff > a.eff + 1e-9) return false;
     return std::abs(a.nt - 320) < std::abs(b.nt - 320);
   });
-  set_ring(p, rowbytes, kRingTwo);
   for (int i = 0; i < nc; ++i) {
     if (cand[i].eff < 0.9) break;  // not worth a second CTA
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, kernel_for(eb == 1 ? 1 : 0, M, cand[i].J), cand[i].nt + 32, gemv_smem_bytes(p, M)) ==
-            cudaSuccess &&
-        n >= 2) {
-      p.ctas_per_sm = 2;
-      p.nt = cand[i].nt;
-      p.J = cand[i].J;
-      return;
+    for (int ctas = 4; ctas >= 2; ctas -= 2) {
+      if (ctas == 4 && cand[i].nt + 32 > kQuadMaxThreads) continue;
+      set_ring(p, rowbytes, kRingPerSm / ctas);
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+              &n, kernel_for(eb == 1 ? 1 : 0, M, cand[i].J), cand[i].nt + 32, gemv_smem_bytes(p, M)) ==
+              cudaSuccess &&
+          n >= ctas) {
+        p.ctas_per_sm = ctas;
+        p.nt = cand[i].nt;
+        p.J = cand[i].J;
+        return;
+      }
+      (void)cudaGetLastError();
     }
-    (void)cudaGetLastError();
   }
   p.ctas_per_sm = 1;
   p.nt = nc ? cand[0].nt : 32;
   p.J = nc ? cand[0].J : 5;
-  set_ring(p, rowbytes, kRingOne);
+  set_ring(p, rowbytes, kRingPerSm);
 }
 
 cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, cudaStream_t s) {

@@ -101,11 +101,58 @@ def test_gemv_matches_oracle_linear(rows, cols, fp8):
         op_gemv(Wd.data_ptr(), TF_DTYPE_BF16, None, rows, cols, xd.data_ptr(), y.data_ptr())
         ref = oracle.linear(oracle.bf16_bits_to_f64(w), x.astype(np.float64))
     got = y.cpu().numpy().astype(np.float64)
-    # float32 accumulation of K products: errors ~ sqrt(K) * 2^-24 * |w||x|,
-    # far below 1e-4 of the output's RMS
     rms = np.sqrt(np.mean(ref ** 2))
-    assert np.max(np.abs(got - ref)) <= 1e-4 * rms
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-5
+    if fp8:
+        # The fp8 GEMV multiplies the exact e4m3 values by activations rounded
+        # to f16 (relative error <= 2^-11 each; the model card keeps bf16
+        # activations, coarser still) and accumulates in float32 (<= K * 2^-24
+        # relative to the sum of |products|): a bound per output row.
+        Wf = oracle.fp8_dequant_rows(codes, scale)
+        absdot = np.abs(Wf) @ np.abs(x.astype(np.float64))
+        assert np.all(np.abs(got - ref) <= (2.0 ** -11 + cols * 2.0 ** -24) * absdot)
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-3
+    else:
+        # float32 accumulation of K products: errors ~ sqrt(K) * 2^-24 * |w||x|,
+        # far below 1e-4 of the output's RMS
+        assert np.max(np.abs(got - ref)) <= 1e-4 * rms
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-5
+
+
+def test_fp8_gemv_decodes_every_code():
+    """Every finite e4m3 code (subnormals, +-448, both zeros) through the
+    fp8 GEMV: row r holds code r in column 0 and zeros elsewhere, x[0] = 1,
+    so row r's result is exactly scale * value(code r) (products with 1 and
+    0 and the power-of-two row scale are exact)."""
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)  # 254 codes
+    rows, cols = codes.size, 256
+    W = np.zeros((rows, cols), np.uint8)
+    W[:, 0] = codes
+    scale = np.full(rows, 0.5, np.float32)
+    x = np.random.default_rng(11).standard_normal(cols).astype(np.float32)
+    x[0] = 1.0
+    Wd = torch.from_numpy(W).to(DEV)
+    sd = torch.from_numpy(scale).to(DEV)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.full((rows,), np.nan, dtype=torch.float32, device=DEV)
+    op_gemv(Wd.data_ptr(), TF_DTYPE_FP8_E4M3, sd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr())
+    want = 0.5 * oracle.e4m3_decode(codes)
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), want)
+
+
+def test_fp8_nan_codes_refused_at_load():
+    d = TINY
+    w = make_weights(d, seed=1)
+    codes, scale = oracle.fp8_quantize_rows(w["slow.0.wo"])
+    codes[3, 5] = 0xFF
+    dec = Decoder(d, "fp8")
+    with pytest.raises(TfError, match="INVAL"):
+        dec.load_weights({"slow.0.wo": w["slow.0.wo"]}, fp8={"slow.0.wo": (codes, scale)})
+    codes[3, 5] = 0x7F
+    with pytest.raises(TfError, match="INVAL"):
+        dec.load_weights({"slow.0.wo": w["slow.0.wo"]}, fp8={"slow.0.wo": (codes, scale)})
+    codes[3, 5] = 0x7E        # 448 is a code like any other
+    dec.load_weights({"slow.0.wo": w["slow.0.wo"]}, fp8={"slow.0.wo": (codes, scale)})
+    dec.close()
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,rows,pos0,splits", [

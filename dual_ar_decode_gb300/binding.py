@@ -32,7 +32,8 @@ class TfTensor(ctypes.Structure):
 
 class TfSampling(ctypes.Structure):
     _fields_ = [("top_k", ctypes.c_int32), ("temperature", ctypes.c_float),
-                ("seed", ctypes.c_uint64)]
+                ("seed", ctypes.c_uint64), ("top_p", ctypes.c_float),
+                ("rep_penalty", ctypes.c_float), ("rep_window", ctypes.c_int32)]
 
 
 class TfInfo(ctypes.Structure):
@@ -65,7 +66,8 @@ EXPORTS = {
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_select": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(TfSampling), ctypes.c_int32, ctypes.c_int32,
-                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+                                    ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                    ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_attention": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
@@ -127,9 +129,10 @@ def config_from_dims(d, weight_dtype: str = "bf16", max_batch: int = 1) -> TfCon
 
 def _sampling(s) -> TfSampling:
     if s is None:
-        return TfSampling(0, 1.0, 0)
+        return TfSampling(0, 1.0, 0, 1.0, 1.0, 0)
     return TfSampling(int(s.get("top_k", 0)), float(s.get("temperature", 1.0)),
-                      int(s.get("seed", 0)) & 0xFFFFFFFFFFFFFFFF)
+                      int(s.get("seed", 0)) & 0xFFFFFFFFFFFFFFFF, float(s.get("top_p", 1.0)),
+                      float(s.get("rep_penalty", 1.0)), int(s.get("rep_window", 0)))
 
 
 def _ptr(a):
@@ -241,10 +244,11 @@ def op_quantize_fp8(w_dev, rows, cols, codes_dev, scale_dev, stream=0):
     _check(lib().tf_op_quantize_fp8(w_dev, rows, cols, codes_dev, scale_dev, stream))
 
 
-def op_select(logits_dev, n, vocab, sampling, frame, codebook0, sequence, ids_dev, stream=0):
+def op_select(logits_dev, n, vocab, sampling, frame, codebook0, sequence, ids_dev, stream=0,
+              recent_dev=None, n_recent=0):
     s = _sampling(sampling)
     _check(lib().tf_op_select(logits_dev, n, vocab, ctypes.byref(s), frame, codebook0, sequence,
-                              ids_dev, stream))
+                              recent_dev, n_recent, ids_dev, stream))
 
 
 def op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev, stream=0):

@@ -175,7 +175,13 @@ struct FrameEndParams {
   int32_t* hist;         // [hist_cap][ncb]
   int32_t* hist_idx;
   int32_t hist_cap;
+  const int32_t* fb;     // ids fed back this frame, sequence b's at fb[b * sel_stride]
+  int32_t* fb_ring;      // [nseq][kRepRing][kRepIds]: slot frame_index % kRepRing
 };
+// Frames of fed-back ids kept per sequence for the repetition window, and
+// id slots per frame in that ring.
+constexpr int kRepRing = 64;
+constexpr int kRepIds = 16;
 cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s);
 
 // Top-k / argmax selection of one row of logits per CTA.
@@ -197,6 +203,13 @@ struct SelectParams {
   const int32_t* forced;
   const int32_t* forced_on;
   uint32_t* err;
+  // nucleus and repetition window (see tf_sampling)
+  float top_p;             // >= 1: no nucleus cut
+  float rep_penalty;
+  int32_t rep_window;      // frames of the ring the window covers (0: off)
+  const int32_t* fb_ring;  // [sequences][kRepRing][kRepIds] fed-back ids
+  const int32_t* recent;   // or explicit window ids [n][n_recent] (< 0: empty)
+  int32_t n_recent;
 };
 cudaError_t launch_select(const SelectParams& p, bool pdl, cudaStream_t s);
 

@@ -102,6 +102,12 @@ __global__ void k_frame_end(const FrameEndParams p) {
   pdl_launch_dependents();
   pdl_wait();
   if (threadIdx.x == 0) {
+    if (p.fb_ring) {  // the ids fed back this frame, for later repetition windows
+      const int slot = *p.frame_index % kRepRing;
+      for (int b = 0; b < p.nseq; ++b)
+        for (int c = 0; c < p.ncb; ++c)
+          p.fb_ring[((size_t)b * kRepRing + slot) * kRepIds + c] = p.fb[(size_t)b * p.sel_stride + c];
+    }
     *p.pos += p.advance;
     *p.frame_index += 1;
     if (p.hist) {
@@ -181,6 +187,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
   __shared__ int sort_idx[kSelMaxK];
   __shared__ float sort_z[kSelMaxK];
   __shared__ float wts[kSelMaxK];
+  __shared__ uint32_t rep_bits[kSelMaxVocab / 32];   // ids of the repetition window
 
   pdl_launch_dependents();
   pdl_wait();
@@ -188,11 +195,38 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
   const int row = blockIdx.x;
   const float* z = p.logits + (size_t)row * p.ld;
   const int V = p.vocab;
+  const int frame = p.frame_ptr ? *p.frame_ptr : p.frame;
+  const uint32_t cb = static_cast<uint32_t>(p.seq_rows ? p.codebook0 : p.codebook0 + row);
+  const uint32_t sq = static_cast<uint32_t>(p.seq_rows ? p.sequence + row : p.sequence);
+
+  // Repetition window: the ids this codebook fed back in the previous
+  // rep_window frames of the sequence (or the explicit list), as a bitmap.
+  const bool rep = (p.recent && p.n_recent > 0) || (p.fb_ring && p.rep_window > 0);
+  if (rep) {
+    for (int w = tid; w < kSelMaxVocab / 32; w += kSelThreads) rep_bits[w] = 0u;
+    __syncthreads();
+    int id = -1;
+    if (p.recent) {
+      if (tid < p.n_recent) id = p.recent[(size_t)row * p.n_recent + tid];
+    } else if (tid < p.rep_window && frame - 1 - tid >= 0) {
+      const int t = frame - 1 - tid;  // one of the previous rep_window frames
+      id = p.fb_ring[((size_t)sq * kRepRing + t % kRepRing) * kRepIds + cb];
+    }
+    if (id >= 0 && id < V) atomicOr(&rep_bits[id >> 5], 1u << (id & 31));
+    __syncthreads();
+  }
+  // logit i as the selection sees it (repetition penalty applied)
+  auto zsel = [&](int i) {
+    float v = z[i];
+    if (rep && ((rep_bits[i >> 5] >> (i & 31)) & 1u))
+      v = v > 0.f ? __fdiv_rn(v, p.rep_penalty) : __fmul_rn(v, p.rep_penalty);
+    return v;
+  };
 
   bool nan = false;
   unsigned long long best = 0ull;
   for (int i = tid; i < V; i += kSelThreads) {
-    const float v = z[i];
+    const float v = zsel(i);
     nan |= (v != v);
     keys[i] = sel_key(v);
     const unsigned long long k = pack_key(v, i);
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
         r += (kj > ki) || (kj == ki && cand_idx[j] < ii);
       }
       sort_idx[r] = ii;
-      sort_z[r] = z[ii];
+      sort_z[r] = zsel(ii);
     }
     __syncthreads();
     if (tid < k) {
@@ -285,20 +319,31 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
     }
     __syncthreads();
     if (tid == 0) {
-      float cum[1];
       float S = 0.f;
       for (int j = 0; j < k; ++j) S = __fadd_rn(S, wts[j]);
-      const int frame = p.frame_ptr ? *p.frame_ptr : p.frame;
-      const uint32_t cb = static_cast<uint32_t>(p.seq_rows ? p.codebook0 : p.codebook0 + row);
-      const uint32_t sq = static_cast<uint32_t>(p.seq_rows ? p.sequence + row : p.sequence);
+      // nucleus: the shortest prefix whose running sum reaches top_p * S
+      int nk = k;
+      float Sk = S;
+      if (p.top_p < 1.0f) {
+        const float tp = __fmul_rn(p.top_p, S);
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+          acc = __fadd_rn(acc, wts[j]);
+          if (acc >= tp) {
+            nk = j + 1;
+            Sk = acc;
+            break;
+          }
+        }
+      }
       const uint32_t w0 = philox_w0(static_cast<uint32_t>(frame), cb, sq, 0u, p.key0, p.key1);
       const float u = __fmul_rn(static_cast<float>(w0 >> 8), 5.9604644775390625e-8f);  // 2^-24
-      const float t = __fmul_rn(u, S);
-      int pk = k - 1;
-      cum[0] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        cum[0] = __fadd_rn(cum[0], wts[j]);
-        if (t < cum[0]) {
+      const float t = __fmul_rn(u, Sk);
+      int pk = nk - 1;
+      float cum = 0.f;
+      for (int j = 0; j < nk; ++j) {
+        cum = __fadd_rn(cum, wts[j]);
+        if (t < cum) {
           pk = j;
           break;
         }
@@ -544,7 +589,8 @@ cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s) 
 }
 
 cudaError_t launch_select(const SelectParams& p, bool pdl, cudaStream_t s) {
-  if (p.vocab < 1 || p.vocab > kSelMaxVocab || p.top_k > kSelMaxK || p.n < 1)
+  if (p.vocab < 1 || p.vocab > kSelMaxVocab || p.top_k > kSelMaxK || p.n < 1 ||
+      p.rep_window > kRepRing || p.n_recent > kSelThreads)
     return cudaErrorInvalidValue;
   static DeviceOnce once;
   if (cudaError_t e = carveout(once, k_select)) return e;

@@ -42,6 +42,7 @@ namespace {
 constexpr int kAlign = 256;
 constexpr int kMaxBatch = 32;  // sequences per context (fast step 1: 2 rows each <= 64)
 constexpr int kIdStride = 16;  // id slots per sequence in the device state
+static_assert(kIdStride == kRepIds, "the repetition ring keeps one frame's id slots");
 #ifndef TF_BATCH_ATTN_CTAS
 #define TF_BATCH_ATTN_CTAS 4
 #endif
@@ -139,6 +140,7 @@ struct tf_ctx {
   uint32_t* sk_tickets = nullptr;
   int graph_B = 1;            // batch the captured graphs were built for
   int32_t* hist = nullptr;
+  int32_t* fb_ring = nullptr;  // [Bmax][kRepRing][kRepIds] fed-back ids (repetition window)
   DevState* st = nullptr;
   int S_slow = 1;
 
@@ -239,6 +241,10 @@ tf_status check_kernel_errors(tf_ctx* c) {
   c->poisoned = true;
   return fail(c, TF_E_STATE, "device reported an id or position out of range");
 }
+
+// Sampling that needs the selection kernel (a draw or a repetition window);
+// plain greedy decoding takes the argmax inside the head GEMVs.
+bool uses_select(const tf_sampling* s) { return s->top_k > 0 || s->rep_window > 0; }
 
 // ------------------------------------------------------------------ launches
 #ifndef TF_GEMV_PREFETCH_BYTES
@@ -354,6 +360,10 @@ cudaError_t enqueue_select(tf_ctx* c, int cb, const tf_sampling* s) {
   q.temperature = s->temperature;
   q.key0 = static_cast<uint32_t>(s->seed & 0xFFFFFFFFull);
   q.key1 = static_cast<uint32_t>(s->seed >> 32);
+  q.top_p = s->top_p;
+  q.rep_penalty = s->rep_penalty;
+  q.rep_window = s->rep_window;
+  q.fb_ring = c->fb_ring;
   q.frame_ptr = &c->st->frame_index;
   q.codebook0 = cb;
   q.sequence = 0;
@@ -368,7 +378,7 @@ cudaError_t enqueue_select(tf_ctx* c, int cb, const tf_sampling* s) {
 // Semantic head + fast loop + bookkeeping, from the slow residual xs.
 cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_first) {
   cudaError_t e;
-  const bool topk = s->top_k > 0;
+  const bool topk = uses_select(s);  // otherwise the head GEMVs take the argmax themselves
   const int Lf = static_cast<int>(c->fast.size());
   if ((e = gemv(c, c->sem, PRO_NORM, c->xs, c->slow_norm, EPI_LOGITS, c->logits, 0, 1, pdl_first,
                 nullptr, nullptr, 0, 0, !topk, NextGemv{&c->fast[0].qkv, EPI_QKV, 2})))
@@ -417,6 +427,8 @@ cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_
   f.hist = c->hist;
   f.hist_idx = &c->st->hist_idx;
   f.hist_cap = c->T;
+  f.fb = c->st->fb;
+  f.fb_ring = c->fb_ring;
   return launch_frame_end(f, true, c->stream);
 }
 
@@ -553,6 +565,10 @@ cudaError_t select_batched(tf_ctx* c, int cb, int B, const tf_sampling* s) {
   q.temperature = s->temperature;
   q.key0 = static_cast<uint32_t>(s->seed & 0xFFFFFFFFull);
   q.key1 = static_cast<uint32_t>(s->seed >> 32);
+  q.top_p = s->top_p;
+  q.rep_penalty = s->rep_penalty;
+  q.rep_window = s->rep_window;
+  q.fb_ring = c->fb_ring;
   q.frame_ptr = &c->st->frame_index;
   q.codebook0 = cb;
   q.sequence = 0;
@@ -633,6 +649,8 @@ cudaError_t enqueue_tail_batched(tf_ctx* c, const tf_sampling* s, int B, int adv
   f.hist = c->hist;
   f.hist_idx = &c->st->hist_idx;
   f.hist_cap = c->T;
+  f.fb = c->st->fb;
+  f.fb_ring = c->fb_ring;
   return launch_frame_end(f, true, c->stream);
 }
 
@@ -691,7 +709,8 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
 }
 
 bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
-  return a.top_k == b.top_k && a.temperature == b.temperature && a.seed == b.seed;
+  return a.top_k == b.top_k && a.temperature == b.temperature && a.seed == b.seed &&
+         a.top_p == b.top_p && a.rep_penalty == b.rep_penalty && a.rep_window == b.rep_window;
 }
 
 tf_status get_graph(tf_ctx* c, const tf_sampling* s, cudaGraphExec_t* out) {
@@ -703,7 +722,7 @@ tf_status get_graph(tf_ctx* c, const tf_sampling* s, cudaGraphExec_t* out) {
       }
     c->graph_B = c->Bc;
   }
-  const int gi = s->top_k > 0 ? 1 : 0;
+  const int gi = uses_select(s) ? 1 : 0;
   if (c->graph[gi] && (gi == 0 || same_sampling(c->graph_samp, *s))) {
     *out = c->graph[gi];
     return TF_OK;
@@ -733,15 +752,27 @@ tf_status get_graph(tf_ctx* c, const tf_sampling* s, cudaGraphExec_t* out) {
 }
 
 tf_status check_sampling(tf_ctx* c, const tf_sampling* s, tf_sampling* out) {
-  tf_sampling d = {0, 1.0f, 0};
+  tf_sampling d = {0, 1.0f, 0, 1.0f, 1.0f, 0};
   if (s) d = *s;
   if (d.top_k < 0 || d.top_k > 256) return fail(c, TF_E_INVAL, "top_k must be in [0, 256]");
   if (!(d.temperature > 0.f) || !std::isfinite(d.temperature))
     return fail(c, TF_E_INVAL, "temperature must be finite and > 0");
+  if (d.top_p == 0.f) d.top_p = 1.0f;  // unset
+  if (!(d.top_p > 0.f && d.top_p <= 1.0f)) return fail(c, TF_E_INVAL, "top_p must be in (0, 1]");
+  if (d.rep_penalty == 0.f) d.rep_penalty = 1.0f;  // unset
+  if (!(d.rep_penalty > 0.f) || !std::isfinite(d.rep_penalty))
+    return fail(c, TF_E_INVAL, "rep_penalty must be finite and > 0");
+  if (d.rep_window < 0 || d.rep_window > kRepRing)
+    return fail(c, TF_E_INVAL, "rep_window must be in [0, 64]");
+  if (d.rep_window == 0 || d.rep_penalty == 1.0f) {  // no window
+    d.rep_window = 0;
+    d.rep_penalty = 1.0f;
+  }
   if (d.top_k == 1) d.top_k = 0;  // one candidate: the argmax
   if (d.top_k == 0) {
     d.temperature = 1.0f;
     d.seed = 0;
+    d.top_p = 1.0f;
   }
   *out = d;
   return TF_OK;
@@ -942,6 +973,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       dev_alloc_t(c, &c->pq, (size_t)T * c->Q) || dev_alloc_t(c, &c->po, (size_t)T * c->Q) ||
       dev_alloc_t(c, &c->pu, (size_t)T * c->F) || dev_alloc_t(c, &c->tokens, (size_t)T * B) ||
       dev_alloc_t(c, &c->hist, (size_t)T * B * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
+      dev_alloc_t(c, &c->fb_ring, B * kRepRing * kRepIds) ||
       dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)))
     return bail(TF_E_NOMEM);
   // Tensor-core prompt GEMMs for bf16 weights whenever every shape tiles.
@@ -1464,10 +1496,13 @@ tf_status tf_op_quantize_fp8(const uint16_t* w, int64_t rows, int64_t cols, uint
 }
 
 tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab, const tf_sampling* sampling,
-                       int32_t frame, int32_t codebook0, int32_t sequence, int32_t* ids,
-                       void* stream) {
+                       int32_t frame, int32_t codebook0, int32_t sequence, const int32_t* recent,
+                       int32_t n_recent, int32_t* ids, void* stream) {
   if (!logits || !ids || !sampling || n < 1 || vocab < 1 || vocab > 8192) return TF_E_INVAL;
   if (sampling->top_k < 0 || sampling->top_k > 256 || !(sampling->temperature > 0.f)) return TF_E_INVAL;
+  if (!(sampling->top_p >= 0.f && sampling->top_p <= 1.0f) || !(sampling->rep_penalty >= 0.f) ||
+      n_recent < 0 || n_recent > kRepRing || (n_recent > 0 && !recent))
+    return TF_E_INVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* err = nullptr;
   if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return TF_E_NOMEM;
@@ -1479,6 +1514,10 @@ tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab, const tf_s
   q.n = n;
   q.top_k = sampling->top_k;
   q.temperature = sampling->temperature;
+  q.top_p = sampling->top_p == 0.f ? 1.0f : sampling->top_p;
+  q.rep_penalty = sampling->rep_penalty == 0.f ? 1.0f : sampling->rep_penalty;
+  q.recent = n_recent > 0 ? recent : nullptr;
+  q.n_recent = n_recent;
   q.key0 = static_cast<uint32_t>(sampling->seed & 0xFFFFFFFFull);
   q.key1 = static_cast<uint32_t>(sampling->seed >> 32);
   q.frame = frame;

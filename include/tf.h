@@ -98,16 +98,30 @@ typedef struct {
   const float* row_scale;   /* FP8 codes only: [shape[0]] float32, else NULL   */
 } tf_tensor;
 
-/* Codebook-id selection.  top_k = 0: greedy argmax (lowest index on ties).
- * top_k > 0: keep the top_k logits ordered by (logit desc, index asc),
+/* Codebook-id selection ("Fish Speech" tour, "Why You Need This": the
+ * generation loop samples with top-k and top-p and keeps repetition
+ * windows).  top_k = 0 (or 1): greedy argmax (lowest index on ties).
+ * top_k > 1: keep the top_k logits ordered by (logit desc, index asc),
  * weights exp((z - z_max) / temperature) summed in that order in float32,
  * u = (w0 >> 8) * 2^-24 from Philox4x32-10 with counter
  * (frame index, codebook, sequence, 0) and key (seed low, seed high 32 bits);
- * the pick is the first candidate whose running sum exceeds u * sum. */
+ * the pick is the first candidate whose running sum exceeds u * sum.
+ * top_p in (0, 1) (top_k > 1 only): the draw is restricted to the shortest
+ *   prefix of the ordered candidates whose running sum reaches
+ *   top_p * sum (float32), with that prefix's sum in place of sum;
+ *   top_p = 1 keeps every candidate.
+ * rep_window W in [0, 64], rep_penalty r > 0: before selection, the logit of
+ *   every id that codebook fed back in the previous W frames of the same
+ *   sequence (each id once) becomes z / r if z > 0, else z * r (float32);
+ *   W = 0 or r = 1 turns it off.  Returned logits are the model's, before
+ *   the penalty. */
 typedef struct {
   int32_t top_k;
   float temperature;
   uint64_t seed;
+  float top_p;
+  float rep_penalty;
+  int32_t rep_window;
 } tf_sampling;
 
 /* Read-only facts about a context. */
@@ -218,11 +232,14 @@ tf_status tf_op_quantize_fp8(const uint16_t* w_bf16, int64_t rows, int64_t cols,
 /* Codebook-id selection over float32 logits [n][vocab] (device); row i uses
  * Philox counter (frame, codebook0 + i, sequence, 0).  Writes ids [n] (device,
  * int32).  sampling as tf_sampling (top_k 0 = argmax).  vocab <= 8192.
+ * recent: NULL, or device int32 [n][n_recent] ids that row i's repetition
+ * window holds (entries < 0 are empty; sampling->rep_window is ignored here,
+ * rep_penalty applies to these ids).  n_recent <= 64.
  * Errors: TF_E_INVAL, TF_E_NUMERIC (NaN logit), TF_E_CUDA. */
 tf_status tf_op_select(const float* logits, int32_t n, int32_t vocab,
                        const tf_sampling* sampling, int32_t frame,
-                       int32_t codebook0, int32_t sequence, int32_t* ids,
-                       void* stream);
+                       int32_t codebook0, int32_t sequence, const int32_t* recent,
+                       int32_t n_recent, int32_t* ids, void* stream);
 
 /* Grouped-query decode attention ("Fish Speech" tour, "Why You Need This":
  * rotary embeddings and grouped-query attention; tuna-fish README,

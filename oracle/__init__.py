@@ -27,7 +27,7 @@ from .numerics import (bf16_bits_to_f64, bf16_bits_to_f32, round_to_bf16, e4m3_d
                        rmsnorm, rope_angles, apply_rope, attention_row,
                        causal_attention, silu, linear)
 from .sampler import (philox4x32_10, exp_f32, argmax_lowest, topk_candidates,
-                      topk_sample, uniform24)
+                      topk_sample, uniform24, apply_repetition_penalty)
 from .model import DualAROracle, load_formula
 
 __all__ = [
@@ -35,5 +35,6 @@ __all__ = [
     "fp8_quantize_rows", "fp8_dequant_rows", "rmsnorm", "rope_angles",
     "apply_rope", "attention_row", "causal_attention", "silu", "linear", "philox4x32_10", "exp_f32",
     "argmax_lowest", "topk_candidates", "topk_sample", "uniform24",
+    "apply_repetition_penalty",
     "DualAROracle", "load_formula",
 ]

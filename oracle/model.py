@@ -39,7 +39,7 @@ import numpy as np
 
 from .numerics import (bf16_bits_to_f64, round_to_bf16, fp8_quantize_rows, fp8_dequant_rows,
                        rmsnorm, apply_rope, attention_row, causal_attention, silu, linear)
-from .sampler import argmax_lowest, topk_sample
+from .sampler import argmax_lowest, apply_repetition_penalty, topk_sample
 
 LINEAR_SUFFIXES = ("wqkv", "wo", "w1", "w3", "w2")
 
@@ -141,6 +141,7 @@ class DualAROracle:
         self.Vs = [np.zeros(shape) for _ in range(self.batch)]
         self.pos = [0] * self.batch
         self.feedback_c0 = [None] * self.batch
+        self.fed_hist = [[] for _ in range(self.batch)]   # ids fed back, per frame
         self.frame_index = 0
 
     # ---- one decoder layer over a block of rows -------------------------
@@ -217,19 +218,29 @@ class DualAROracle:
 
     # ---- selection --------------------------------------------------------
     def _selector(self, b, sampling, forced_row):
-        top_k = int(sampling.get("top_k", 0)) if sampling else 0
-        seed = int(sampling.get("seed", 0)) if sampling else 0
-        temp = float(sampling.get("temperature", 1.0)) if sampling else 1.0
+        s = sampling or {}
+        top_k = int(s.get("top_k", 0))
+        seed = int(s.get("seed", 0))
+        temp = float(s.get("temperature", 1.0))
+        top_p = float(s.get("top_p", 1.0))
+        window = int(s.get("rep_window", 0))
+        penalty = float(s.get("rep_penalty", 1.0))
         frame = self.frame_index
+        past = self.fed_hist[b][max(0, len(self.fed_hist[b]) - window):] if window > 0 else []
+        fed_now = {}
 
         def select(j, z):
             z32 = z.astype(np.float32)
-            if top_k > 0:
-                chosen, _ = topk_sample(z32, top_k, seed, frame, j, b, temp)
+            if window > 0:
+                z32 = apply_repetition_penalty(z32, [f[j] for f in past], penalty)
+            if top_k > 1:
+                chosen, _ = topk_sample(z32, top_k, seed, frame, j, b, temp, top_p)
             else:
                 chosen = argmax_lowest(z32)
             fed = chosen if forced_row is None else int(forced_row[j])
+            fed_now[j] = fed
             return chosen, fed
+        select.fed = fed_now
         return select
 
     def _frame_tail(self, b, x_last, sampling, forced_row):
@@ -241,6 +252,7 @@ class DualAROracle:
         c0, c0_fed = select(0, z0)
         ids, zf = self._fast_frame(h, c0_fed, select)
         self.feedback_c0[b] = c0_fed
+        self.fed_hist[b].append([select.fed[j] for j in range(d.n_codebooks)])
         logits = np.zeros((d.n_codebooks, max(d.semantic_vocab, d.codebook_size)))
         logits[0, : d.semantic_vocab] = z0
         logits[1:, : d.codebook_size] = zf

@@ -16,7 +16,9 @@ index bit for bit:
   * S = sum of p_i in candidate order, c_i the running sums, all float32;
   * u = (w0 >> 8) * 2^-24 with w0 the first word of
     Philox4x32-10(counter = (frame, codebook, sequence, 0), key = seed);
-  * the pick is the first candidate with u * S < c_i, else the last one.
+  * the pick is the first candidate with u * S < c_i, else the last one;
+  * optional nucleus (top_p) and repetition window: see topk_sample and
+    apply_repetition_penalty.
 """
 from __future__ import annotations
 
@@ -111,12 +113,36 @@ def topk_candidates(z32: np.ndarray, k: int) -> np.ndarray:
     return order[: min(k, z32.size)]
 
 
+def apply_repetition_penalty(z32: np.ndarray, recent, penalty: float) -> np.ndarray:
+    """Repetition window ("Fish Speech" tour, "Why You Need This": the
+    generation loop has repetition windows; the pages give no formula).
+
+    Reading: every id in `recent` (the ids this codebook fed back in the
+    previous W frames of the sequence; each id counts once) has its float32
+    logit divided by `penalty` when it is positive and multiplied by it
+    otherwise (the CTRL-style penalty), one IEEE float32 operation each.
+    penalty 1 leaves the logits unchanged.  Returns a new float32 array.
+    """
+    z = np.array(z32, dtype=np.float32, copy=True)
+    r = F32(penalty)
+    for i in sorted(set(int(v) for v in recent if 0 <= int(v) < z.size)):
+        z[i] = F32(z[i] / r) if z[i] > F32(0.0) else F32(z[i] * r)
+    return z
+
+
 def topk_sample(z32: np.ndarray, k: int, seed: int, frame: int, codebook: int,
-                sequence: int = 0, temperature: float = 1.0):
-    """Seeded top-k draw from float32 logits (rule in the module docstring).
+                sequence: int = 0, temperature: float = 1.0, top_p: float = 1.0):
+    """Seeded top-k draw from float32 logits (rule in the module docstring),
+    optionally restricted to a nucleus ("Fish Speech" tour: top-p sampling).
+
+    Nucleus reading: with top_p < 1, keep the shortest prefix of the ordered
+    candidates whose running weight sum c_i reaches top_p * S (float32
+    product), i.e. up to the first i with c_i >= top_p * S, and draw within it
+    with S' = c_i in place of S.  top_p >= 1 keeps every candidate.
 
     Returns (index, details) where details holds the candidate list, the
-    float32 weights, cumulative sums, S and u, for robustness checks.
+    float32 weights, cumulative sums, S, the kept count n and its sum S', u
+    and t, for robustness checks.
     """
     z32 = np.asarray(z32, dtype=np.float32)
     if np.any(np.isnan(z32)):
@@ -136,15 +162,23 @@ def topk_sample(z32: np.ndarray, k: int, seed: int, frame: int, codebook: int,
         acc = F32(acc + v)
         c.append(acc)
     S = acc
+    n = len(cand)
+    if F32(top_p) < F32(1.0):
+        tp = F32(F32(top_p) * S)
+        for i, ci in enumerate(c):
+            if ci >= tp:
+                n = i + 1
+                break
+    Sk = c[n - 1]
     key = (seed & _MASK32, (seed >> 32) & _MASK32)
     w0 = philox4x32_10((frame, codebook, sequence, 0), key)[0]
     u = uniform24(w0)
-    t = F32(u * S)
-    pick = len(cand) - 1
-    for j, cj in enumerate(c):
-        if t < cj:
+    t = F32(u * Sk)
+    pick = n - 1
+    for j in range(n):
+        if t < c[j]:
             pick = j
             break
     return int(cand[pick]), dict(cand=cand, p=np.array(p, np.float32),
-                                 c=np.array(c, np.float32), S=S, u=u, t=t,
+                                 c=np.array(c, np.float32), S=S, n=n, Sk=Sk, u=u, t=t,
                                  pick=pick)

@@ -31,7 +31,7 @@ def margin(z):
     return s[-1] - s[-2]
 
 
-def topk_robust(z, k, delta, seed, frame, codebook, sequence=0, temperature=1.0):
+def topk_robust(z, k, delta, seed, frame, codebook, sequence=0, temperature=1.0, top_p=1.0):
     """True when the oracle's top-k draw from logits z stays the same under
     any change of every logit by at most delta (an a-priori bound taken from
     the oracle's logits and the parity tolerance, never from the GPU's).
@@ -43,9 +43,12 @@ def topk_robust(z, k, delta, seed, frame, codebook, sequence=0, temperature=1.0)
     r e^-a / (r e^-a + (1 - r) e^a), a = 2*delta/T.  The pick i (the first
     candidate with u < r_i) is stable when the picked candidate cannot trade
     places with a neighbour, cannot be displaced from the set when it is the
-    last candidate, and u keeps clear of the moved r_{i-1} and r_i."""
+    last candidate, and u keeps clear of the moved r_{i-1} and r_i.  With a
+    nucleus (top_p < 1) the cut must also stay where it is (the moved
+    r_{n-1} stays >= top_p and r_{n-2} below it), and the draw is judged on
+    the sums normalised by the nucleus' own sum."""
     z32 = np.asarray(z, np.float32)
-    _, det = oracle.topk_sample(z32, k, seed, frame, codebook, sequence, temperature)
+    _, det = oracle.topk_sample(z32, k, seed, frame, codebook, sequence, temperature, top_p)
     zc = z32[det["cand"]].astype(np.float64)
     i = det["pick"]
     for nb in (i - 1, i + 1):
@@ -56,14 +59,18 @@ def topk_robust(z, k, delta, seed, frame, codebook, sequence=0, temperature=1.0)
         if zc[i] - nxt <= 2 * delta:
             return False
     a = 2 * delta / temperature
-    S = float(det["S"])
-    r = det["c"].astype(np.float64) / S
     up = lambda x: x * np.exp(a) / (x * np.exp(a) + (1 - x) * np.exp(-a))
     dn = lambda x: x * np.exp(-a) / (x * np.exp(-a) + (1 - x) * np.exp(a))
-    u = float(det["u"])
     eps = 1e-6   # float32 rounding of the running sums and of u * S
+    n = int(det["n"])
+    if n < len(zc):   # a nucleus cut: it must not move
+        rS = det["c"].astype(np.float64) / float(det["S"])
+        if dn(rS[n - 1]) < top_p + eps or (n >= 2 and up(rS[n - 2]) > top_p - eps):
+            return False
+    r = det["c"][:n].astype(np.float64) / float(det["Sk"])
+    u = float(det["u"])
     lo_ok = i == 0 or u > up(r[i - 1]) + eps
-    hi_ok = i == len(zc) - 1 or u < dn(r[i]) - eps
+    hi_ok = i == n - 1 or u < dn(r[i]) - eps
     return bool(lo_ok and hi_ok)
 
 
@@ -103,9 +110,20 @@ class TeacherForced:
 
     def check(self, tol, sampling=None):
         """Asserts the parity gates on every frame of every sequence; returns
-        (worst rel-L2, ids compared, ids skipped)."""
+        (worst rel-L2, ids compared, ids skipped).  With a repetition window
+        the selection input is the oracle's logits after the penalty over the
+        ids fed back (under teacher forcing, the oracle's own picks) in the
+        previous rep_window frames; a penalty r scales a logit's change by at
+        most max(1, r), so the bounds scale with it."""
         worst, compared, skipped = 0.0, 0, 0
-        k = int(sampling.get("top_k", 0)) if sampling else 0
+        s = sampling or {}
+        k = int(s.get("top_k", 0))
+        W = int(s.get("rep_window", 0))
+        r = float(s.get("rep_penalty", 1.0))
+        amp = max(1.0, r) if W else 1.0
+        fed = {}    # (sequence, frame) -> oracle ids fed back
+        for t, b, rf, rz, gf, gz in self.frames:
+            fed[(b, t)] = rf
         for t, b, rf, rz, gf, gz in self.frames:
             for j in range(self.d.n_codebooks):
                 V = vocab_of(self.d, j)
@@ -113,14 +131,18 @@ class TeacherForced:
                 e = rel_l2(g, o)
                 worst = max(worst, e)
                 assert e <= tol, f"frame {t} sequence {b} codebook {j}: rel-L2 {e:.3e} > {tol}"
+                if W:
+                    recent = [fed[(b, u)][j] for u in range(max(0, t - W), t)]
+                    o = oracle.apply_repetition_penalty(o.astype(np.float32), recent, r)
                 if k <= 1:
-                    robust = margin(o) > MARGIN
+                    robust = margin(o) > MARGIN * amp
                 else:
                     # per-logit change the gate allows if the error were
-                    # spread like noise at the tolerance: 3 * tol * rms(o)
-                    delta = topk_delta(o, tol)
-                    robust = topk_robust(o, k, delta, int(sampling.get("seed", 0)), t, j,
-                                         b, float(sampling.get("temperature", 1.0)))
+                    # spread like noise at the tolerance: 3 * tol * rms
+                    delta = topk_delta(rz[j, :V], tol) * amp
+                    robust = topk_robust(o, k, delta, int(s.get("seed", 0)), t, j,
+                                         b, float(s.get("temperature", 1.0)),
+                                         float(s.get("top_p", 1.0)))
                 if robust:
                     compared += 1
                     assert gf[j] == rf[j], f"frame {t} sequence {b} codebook {j}: id {gf[j]} != {rf[j]}"
@@ -129,7 +151,7 @@ class TeacherForced:
                     # the rest must still be valid: a near-tied argmax, or a
                     # member of the oracle's candidate set
                     if k <= 1:
-                        assert o[gf[j]] >= np.max(o) - MARGIN, (t, b, j, gf[j])
+                        assert o[gf[j]] >= np.max(o) - MARGIN * amp, (t, b, j, gf[j])
                     else:
                         cand = oracle.topk_candidates(o.astype(np.float32), k + 2)
                         assert gf[j] in set(int(c) for c in cand), (t, b, j, gf[j])

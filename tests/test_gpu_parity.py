@@ -51,23 +51,39 @@ def test_quantize_fp8_bit_exact(rows, cols):
 
 
 @pytest.mark.parametrize("vocab", [64, 4096, 1000])
-@pytest.mark.parametrize("top_k,temp", [(0, 1.0), (1, 1.0), (2, 1.0), (30, 1.0), (30, 0.7), (256, 1.0)])
+@pytest.mark.parametrize("top_k,temp,top_p", [(0, 1.0, 1.0), (1, 1.0, 1.0), (2, 1.0, 1.0),
+                                              (30, 1.0, 1.0), (30, 0.7, 1.0), (256, 1.0, 1.0),
+                                              (30, 1.0, 0.8), (256, 0.9, 0.5), (30, 1.0, 1e-7)])
 @pytest.mark.parametrize("ties", [False, True])
-def test_select_bit_exact(vocab, top_k, temp, ties):
+@pytest.mark.parametrize("window", [0, 12])
+def test_select_bit_exact(vocab, top_k, temp, top_p, ties, window):
+    """The selection kernel against the oracle's rule on the same float32
+    logits: argmax, top-k draw, nucleus, temperature, and the repetition
+    penalty on an explicit window of recent ids (with repeats, misses and
+    empty slots)."""
     n = 48
     z = make_logits(n, vocab, seed=vocab + top_k, scale=2.0, ties=ties)
     zd = torch.from_numpy(z).to(DEV)
     ids = torch.full((n,), -1, dtype=torch.int32, device=DEV)
     seed = 0x1234_5678_9ABC
     frame, cb0, seq = 17, 3, 0
-    op_select(zd.data_ptr(), n, vocab, {"top_k": top_k, "temperature": temp, "seed": seed},
-              frame, cb0, seq, ids.data_ptr())
+    penalty = 1.7 if window else 1.0
+    rng = np.random.default_rng(vocab * 3 + top_k)
+    recent = rng.integers(-2, vocab, size=(n, max(window, 1))).astype(np.int32)
+    for i in range(n):                      # put each row's top ids in its window
+        recent[i, :2] = np.argsort(-z[i])[:2]
+    rd = torch.from_numpy(recent).to(DEV)
+    op_select(zd.data_ptr(), n, vocab, {"top_k": top_k, "temperature": temp, "seed": seed,
+                                        "top_p": top_p, "rep_penalty": penalty},
+              frame, cb0, seq, ids.data_ptr(), recent_dev=rd.data_ptr() if window else None,
+              n_recent=window)
     got = ids.cpu().numpy()
     for i in range(n):
+        zi = oracle.apply_repetition_penalty(z[i], recent[i], penalty) if window else z[i]
         if top_k <= 1:
-            want = oracle.argmax_lowest(z[i])
+            want = oracle.argmax_lowest(zi)
         else:
-            want, _ = oracle.topk_sample(z[i], top_k, seed, frame, cb0 + i, seq, temp)
+            want, _ = oracle.topk_sample(zi, top_k, seed, frame, cb0 + i, seq, temp, top_p)
         assert got[i] == want, (i, got[i], want)
 
 
@@ -236,6 +252,24 @@ def test_tiny_topk_teacher_forced(k):
     for _ in range(8):
         tf.decode(s)
     worst, compared, skipped = tf.check(BF16_TOL, s)
+    assert compared >= 10
+    tf.dec.close()
+
+
+@pytest.mark.parametrize("sampling", [
+    # the nucleus cuts every draw here (the tiny model's top-8 are near-flat)
+    {"top_k": 8, "seed": 77, "temperature": 1.0, "top_p": 0.8, "rep_window": 8, "rep_penalty": 1.3},
+    {"top_k": 8, "seed": 77, "temperature": 0.5, "top_p": 0.9, "rep_window": 8, "rep_penalty": 1.3},
+    {"top_k": 0, "rep_window": 4, "rep_penalty": 2.0},
+])
+def test_tiny_topp_and_repetition_window_teacher_forced(sampling):
+    """Nucleus sampling and the repetition window through the whole decode
+    path (the window comes from the device's ring of fed-back ids)."""
+    tf = TeacherForced(TINY, "bf16", seed=0)
+    tf.prefill(make_prompt(TINY, 16, seed=0), sampling)
+    for _ in range(12):
+        tf.decode(sampling)
+    worst, compared, skipped = tf.check(BF16_TOL, sampling)
     assert compared >= 10
     tf.dec.close()
 

@@ -77,8 +77,13 @@ def test_create_without_device_fails_cleanly(L):
 
 
 def test_op_argument_validation_is_host_side(L):
-    s = binding.TfSampling(0, 1.0, 0)
-    assert L.tf_op_select(None, 1, 64, ctypes.byref(s), 0, 0, 0, None, None) == 1
+    s = binding.TfSampling(0, 1.0, 0, 1.0, 1.0, 0)
+    assert L.tf_op_select(None, 1, 64, ctypes.byref(s), 0, 0, 0, None, 0, None, None) == 1
+    ok = ctypes.c_void_p(16)   # never dereferenced: the arguments are refused first
+    bad_p = binding.TfSampling(30, 1.0, 0, 1.5, 1.0, 0)
+    assert L.tf_op_select(ok, 1, 64, ctypes.byref(bad_p), 0, 0, 0, None, 0, ok, None) == 1
+    assert L.tf_op_select(ok, 1, 64, ctypes.byref(s), 0, 0, 0, None, 3, ok, None) == 1   # window, no ids
+    assert L.tf_op_select(ok, 1, 64, ctypes.byref(s), 0, 0, 0, ok, 65, ok, None) == 1    # window > 64
     assert L.tf_op_quantize_fp8(None, 1, 16, None, None, None) == 1
     assert L.tf_op_gemv(None, 0, None, 1, 16, None, None, 1, None, None) == 1
     assert L.tf_op_gemm_skinny(None, None, 16, 256, 256, None, None) == 1

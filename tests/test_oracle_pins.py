@@ -325,6 +325,81 @@ def test_topk_temperature_frequencies_follow_tempered_softmax():
     assert np.allclose(det["p"], np.exp((zc - zc[0]) / temp), rtol=1e-6)
 
 
+def test_topp_frequencies_follow_the_renormalised_nucleus():
+    """top-p: draws follow softmax over the shortest ordered prefix of the
+    top-k candidates whose probability reaches top_p, renormalised."""
+    z = make_logits(1, 64, seed=8, scale=1.2)[0]
+    k, top_p = 12, 0.6
+    cand = oracle.topk_candidates(z, k)
+    w = np.exp(z[cand].astype(np.float64) - z[cand[0]])
+    cum = np.cumsum(w) / w.sum()
+    n = int(np.argmax(cum >= top_p)) + 1          # shortest prefix reaching top_p
+    assert 1 < n < k
+    p = w[:n] / w[:n].sum()
+    N = 6000
+    counts = np.zeros(n)
+    pos = {int(c): i for i, c in enumerate(cand)}
+    for t in range(N):
+        idx, det = oracle.topk_sample(z, k, seed=7, frame=t, codebook=2, top_p=top_p)
+        assert det["n"] == n
+        counts[pos[idx]] += 1                     # never outside the nucleus
+    chi2 = np.sum((counts - N * p) ** 2 / (N * p))
+    assert chi2 < 10.0 + 3.0 * n                  # ~p = 1e-4 for n - 1 degrees of freedom
+
+
+def test_topp_limits():
+    Z = make_logits(40, 128, seed=9, scale=1.0)
+    for t, z in enumerate(Z):
+        # a tiny nucleus is the first candidate: the argmax
+        idx, _ = oracle.topk_sample(z, 30, seed=3, frame=t, codebook=1, top_p=1e-6)
+        assert idx == oracle.argmax_lowest(z)
+        # top_p = 1 keeps every candidate: the plain top-k draw
+        a, _ = oracle.topk_sample(z, 30, seed=3, frame=t, codebook=1, top_p=1.0)
+        b, _ = oracle.topk_sample(z, 30, seed=3, frame=t, codebook=1)
+        assert a == b
+
+
+def test_repetition_penalty_closed_form():
+    z = np.array([2.0, -1.5, 0.0, 3.0, -0.25, 1.0], np.float32)
+    out = oracle.apply_repetition_penalty(z, [0, 1, 1, 2, 4, 99, -3], 2.0)
+    # positive logits divided, the rest multiplied; each id once; others untouched
+    assert out.tolist() == [1.0, -3.0, 0.0, 3.0, -0.5, 1.0]
+    assert np.array_equal(oracle.apply_repetition_penalty(z, [0, 3, 5], 1.0), z)
+    assert np.array_equal(oracle.apply_repetition_penalty(z, [], 5.0), z)
+    assert z.tolist() == [2.0, -1.5, 0.0, 3.0, -0.25, 1.0]   # input untouched
+
+
+def test_repetition_window_blocks_recent_ids_in_the_model():
+    """With a huge penalty and greedy selection, no codebook repeats an id it
+    fed back within the last W frames (every codebook has a positive logit
+    outside the window); without the window the same run does repeat."""
+    d = TINY
+    w = make_weights(d, seed=12)
+    prompt = make_prompt(d, 8, seed=13)
+    W = 3
+
+    def run(sampling):
+        o = oracle.DualAROracle(d, w)
+        fr = [o.prefill(prompt, sampling)[0][0]]
+        for _ in range(9):
+            fr.append(o.decode_frame(sampling)[0][0])
+        return np.array(fr)
+
+    plain = run(None)
+    pen = run({"top_k": 0, "rep_window": W, "rep_penalty": 1e6})
+    assert any(plain[t, j] in plain[max(0, t - W):t, j] for t in range(1, 10) for j in range(10))
+    for t in range(1, 10):
+        for j in range(10):
+            assert pen[t, j] not in pen[max(0, t - W):t, j], (t, j)
+    # the window holds the ids fed back: under teacher forcing, the forced ones
+    forced = np.array([[[5] * 10]] * 10, np.int32)            # always feed id 5
+    o = oracle.DualAROracle(d, w)
+    f0, _ = o.prefill(prompt, {"rep_window": W, "rep_penalty": 1e6}, forced=forced[0])
+    for t in range(1, 10):
+        f, _ = o.decode_frame({"rep_window": W, "rep_penalty": 1e6}, forced=forced[t])
+        assert (f[0] != 5).all()                                # 5 sits in every window
+
+
 # ----------------------------------------------------------------- load formula
 
 def test_load_formula_page_numbers():

@@ -14,6 +14,7 @@ STATUS = {0: "TF_OK", 1: "TF_E_INVAL", 2: "TF_E_NOMEM", 3: "TF_E_CUDA", 4: "TF_E
           5: "TF_E_CAPACITY", 6: "TF_E_TIMEOUT", 7: "TF_E_NUMERIC"}
 TF_WEIGHT_BF16, TF_WEIGHT_FP8 = 0, 1
 TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3 = 0, 1
+TF_FLAG_QK_NORM, TF_FLAG_QK_NORM_FAST, TF_FLAG_SLOW_CB_SUM = 1, 2, 4
 
 
 class TfConfig(ctypes.Structure):
@@ -21,7 +22,7 @@ class TfConfig(ctypes.Structure):
         "slow_layers", "fast_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn",
         "text_vocab", "semantic_vocab", "n_codebooks", "codebook_size", "max_seq_len",
         "max_batch")] + [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
-                         ("weight_dtype", ctypes.c_int32)]
+                         ("weight_dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class TfTensor(ctypes.Structure):
@@ -124,7 +125,10 @@ def config_from_dims(d, weight_dtype: str = "bf16", max_batch: int = 1) -> TfCon
     return TfConfig(d.slow_layers, d.fast_layers, d.hidden, d.n_heads, d.n_kv_heads, d.head_dim,
                     d.ffn, d.text_vocab, d.semantic_vocab, d.n_codebooks, d.codebook_size,
                     d.max_seq_len, max_batch, d.rms_eps, d.rope_theta,
-                    TF_WEIGHT_FP8 if weight_dtype == "fp8" else TF_WEIGHT_BF16)
+                    TF_WEIGHT_FP8 if weight_dtype == "fp8" else TF_WEIGHT_BF16,
+                    (TF_FLAG_QK_NORM if getattr(d, "qk_norm", False) else 0)
+                    | (TF_FLAG_QK_NORM_FAST if getattr(d, "qk_norm_fast", False) else 0)
+                    | (TF_FLAG_SLOW_CB_SUM if getattr(d, "slow_cb_sum", False) else 0))
 
 
 def _sampling(s) -> TfSampling:

@@ -70,6 +70,12 @@ __device__ __forceinline__ void epi_qkv_pair_at(const GemvParams& p, int m, int 
     return;
   }
   const int qp = p.q_dim >> 1, kp = p.kv_dim >> 1;
+  if (pair < qp + kp && p.qk_raw) {  // q/k norm follows in k_qknorm
+    float* r = p.qk_raw + (size_t)m * (p.q_dim + p.kv_dim) + 2 * (size_t)pair;
+    r[0] = v0;
+    r[1] = v1;
+    return;
+  }
   if (pair < qp + kp) {
     const bool isq = pair < qp;
     const int pr = isq ? pair : pair - qp;

@@ -95,7 +95,16 @@ struct GemvParams {
   // HBM keeps streaming across the kernel boundary.
   const uint8_t* pf_w;
   int32_t pf_units, pf_unit, pf_rowbytes, pf_grid, pf_bytes;
+  // q/k RMSNorm option: the QKV epilogue stores the q and k pairs as they
+  // are (RoPE-pair order, [M][q_dim + kv_dim]) for k_qknorm to finish
+  float* qk_raw;
+  const uint16_t* q_norm;  // k_qknorm: per-head RMSNorm weights [head_dim]
+  const uint16_t* k_norm;
 };
+// Finishes q and k after a QKV GEMM that left them raw (GemvParams::qk_raw):
+// each head of each row is RMSNorm-ed with q_norm / k_norm, rotated by RoPE
+// at the row's position, q stored to qout and k appended to the KV cache.
+cudaError_t launch_qknorm(const GemvParams& p, int M, bool pdl, cudaStream_t s);
 constexpr int kSsqRows = 64;   // row stride of the partial sums of squares
 
 // Shared memory bytes a launch with these params needs.
@@ -154,6 +163,11 @@ struct BuildParams {
   float eps;
   float* x;                // output rows [M][H]
   uint32_t* err;
+  // BUILD_SLOW option: add the previous frame's codes 1..9 (id slots
+  // ids[b * id_stride + j]) as rows of cb_sum [ncb - 1][cb_rows][H]
+  const uint16_t* cb_sum;
+  int32_t cb_rows;
+  int32_t ncb;
   // optional, for the skinny GEMM that reads the rows next (see GemvParams):
   const uint16_t* nw_next; // x * nw_next as bf16 parts [M][H], sum of x^2 per row
   uint16_t* nx_hi;

@@ -93,8 +93,70 @@ __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
     id = 0;
   }
   const uint16_t* row = p.table + (size_t)(p.row_base + id) * p.H;
-  for (int k = tid; k < p.H; k += blockDim.x) xo[k] = bf16_to_f32(row[k]);
+  if (p.mode == BUILD_SLOW && p.cb_sum) {
+    // the previous frame's codes 1..ncb-1 add their rows, in codebook order
+    int cid[16];
+    for (int j = 1; j < p.ncb; ++j) {
+      int v = p.ids[(size_t)m * p.id_stride + j];
+      if (v < 0 || v >= p.cb_rows) {
+        if (tid == 0) atomicOr(p.err, ERR_BAD_ID);
+        v = 0;
+      }
+      cid[j] = v;
+    }
+    for (int k = tid; k < p.H; k += blockDim.x) {
+      float acc = bf16_to_f32(row[k]);
+      for (int j = 1; j < p.ncb; ++j)
+        acc += bf16_to_f32(p.cb_sum[((size_t)(j - 1) * p.cb_rows + cid[j]) * p.H + k]);
+      xo[k] = acc;
+    }
+  } else {
+    for (int k = tid; k < p.H; k += blockDim.x) xo[k] = bf16_to_f32(row[k]);
+  }
   if (p.nx_hi) build_norm_out(p, m, xo, red);
+}
+
+// ------------------------------------------------------------------ q/k norm
+// One CTA per (head of q or k, row), one thread per RoPE pair (i, i + D/2):
+// RMSNorm over the head's D raw values with the head-dim weight, then the
+// rotation at the row's position; q to qout, k (bf16) to the row's KV cache.
+__global__ void __launch_bounds__(64) k_qknorm(const GemvParams p) {
+  __shared__ float red[2];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int half = p.head_dim >> 1, i = threadIdx.x;
+  const int hq = p.q_dim / p.head_dim;
+  const int h = blockIdx.x, m = blockIdx.y;
+  const bool isq = h < hq;
+  const int hh = isq ? h : h - hq;
+  const size_t pair = (size_t)(isq ? 0 : p.q_dim >> 1) + (size_t)hh * half + i;
+  const float* r = p.qk_raw + (size_t)m * (p.q_dim + p.kv_dim) + 2 * pair;
+  const float v0 = r[0], v1 = r[1];
+  float ss = warp_sum(fmaf(v0, v0, v1 * v1));
+  if ((i & 31) == 0) red[i >> 5] = ss;
+  __syncthreads();
+  ss = half > 32 ? red[0] + red[1] : red[0];
+  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(p.head_dim) + p.eps);
+  const uint16_t* w = isq ? p.q_norm : p.k_norm;
+  const float a = v0 * rstd * bf16_to_f32(w[i]);
+  const float b = v1 * rstd * bf16_to_f32(w[i + half]);
+  const int pos = row_pos(p, m);
+  if (pos < 0 || pos >= p.T) {
+    if (i == 0) atomicOr(p.err, ERR_BAD_POS);
+    return;
+  }
+  const float2 cs = __ldg(&p.rope[(size_t)pos * half + i]);
+  const float r0 = a * cs.x - b * cs.y;
+  const float r1 = b * cs.x + a * cs.y;
+  if (isq) {
+    float* q = p.qout + (size_t)m * p.q_dim + (size_t)hh * p.head_dim;
+    q[i] = r0;
+    q[i + half] = r1;
+  } else {
+    uint16_t* k = p.Kc + row_kv_offset(p, m) + ((size_t)hh * p.T + pos) * p.head_dim;
+    k[i] = f32_to_bf16(r0);
+    k[i + half] = f32_to_bf16(r1);
+  }
 }
 
 // ------------------------------------------------------------------ frame end
@@ -578,6 +640,16 @@ cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(p.M), dim3(256), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_build, p);
+}
+
+cudaError_t launch_qknorm(const GemvParams& p, int M, bool pdl, cudaStream_t s) {
+  if (p.head_dim != 64 && p.head_dim != 128) return cudaErrorInvalidValue;
+  static DeviceOnce once;
+  if (cudaError_t e = carveout(once, k_qknorm)) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((p.q_dim + p.kv_dim) / p.head_dim, M), dim3(p.head_dim / 2),
+                                    0, pdl, s, attr);
+  return cudaLaunchKernelEx(&cfg, k_qknorm, p);
 }
 
 cudaError_t launch_frame_end(const FrameEndParams& p, bool pdl, cudaStream_t s) {

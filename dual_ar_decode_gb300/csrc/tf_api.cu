@@ -65,6 +65,8 @@ struct Layer {
   Lin qkv, o, w13, w2;
   uint16_t* attn_norm = nullptr;
   uint16_t* ffn_norm = nullptr;
+  uint16_t* q_norm = nullptr;  // per-head q/k RMSNorm weights [D] (TF_FLAG_QK_NORM*)
+  uint16_t* k_norm = nullptr;
   uint16_t* K = nullptr;  // [Hkv][T][D]
   uint16_t* V = nullptr;
 };
@@ -113,7 +115,9 @@ struct tf_ctx {
   uint16_t* fast_norm = nullptr;
   Lin fast_head;
   Lin sem;                    // semantic head: the tied text-embedding slice (bf16)
-  uint16_t* cb_embed = nullptr;
+  uint16_t* cb_embed = nullptr;  // [NCB-1][Vmax][H]
+  uint16_t* slow_cb = nullptr;   // [NCB-1][Vc][H] (TF_FLAG_SLOW_CB_SUM)
+  float* qk_raw = nullptr;       // raw q/k pairs of a QKV GEMM (q/k norm options)
   std::vector<std::string> loaded;
   float2* rope = nullptr;
   uint8_t* staging = nullptr;
@@ -223,6 +227,8 @@ bool valid_config(const tf_config* cfg, std::string* why) {
   if (!(cfg->rms_eps > 0.f) || !(cfg->rope_theta > 1.f)) return bad("rms_eps > 0 and rope_theta > 1 required");
   if (cfg->weight_dtype != TF_WEIGHT_BF16 && cfg->weight_dtype != TF_WEIGHT_FP8)
     return bad("weight_dtype must be TF_WEIGHT_BF16 or TF_WEIGHT_FP8");
+  if (cfg->flags & ~(TF_FLAG_QK_NORM | TF_FLAG_QK_NORM_FAST | TF_FLAG_SLOW_CB_SUM))
+    return bad("unknown flags");
   return true;
 }
 
@@ -283,6 +289,7 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
   if (layer) {
     p.Kc = layer->K;
     p.Vc = layer->V;
+    if (layer->q_norm && epi == EPI_QKV) p.qk_raw = c->qk_raw;
   }
   p.T = c->T;
   p.pos_ptr = pos_ptr;
@@ -318,12 +325,38 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
   return launch_gemv(p, eb == 1 ? 1 : 0, M, grid, pdl, c->stream);
 }
 
+// The q/k norm option: finish the q and k a QKV GEMM left raw (rows at
+// pos_ptr / pos_fixed, rps rows per sequence, caches of `L` + kv_off).
+cudaError_t qknorm(tf_ctx* c, const Layer& L, int M, const int32_t* pos_ptr, int pos_fixed, int rps,
+                   size_t kv_off, float* qout, bool pdl) {
+  GemvParams p = {};
+  p.q_dim = c->Q;
+  p.kv_dim = c->KV;
+  p.head_dim = c->D;
+  p.qk_raw = c->qk_raw;
+  p.q_norm = L.q_norm;
+  p.k_norm = L.k_norm;
+  p.eps = c->cfg.rms_eps;
+  p.qout = qout;
+  p.Kc = L.K + kv_off;
+  p.Vc = L.V + kv_off;
+  p.T = c->T;
+  p.pos_ptr = pos_ptr;
+  p.pos_fixed = pos_fixed;
+  p.rps = rps;
+  p.kv_seq = c->kv_seq;
+  p.rope = c->rope;
+  p.err = &c->st->err;
+  return launch_qknorm(p, M, pdl, c->stream);
+}
+
 cudaError_t layer_decode(tf_ctx* c, const Layer& L, float* x, int M, const int32_t* pos_ptr,
                          int pos_fixed, int S, bool pdl_first, const NextGemv& after) {
   cudaError_t e;
   if ((e = gemv(c, L.qkv, PRO_NORM, x, L.attn_norm, EPI_QKV, nullptr, 0, M, pdl_first, &L, pos_ptr,
                 pos_fixed, -1, false, NextGemv{&L.o, EPI_RESID, M})))
     return e;
+  if (L.q_norm && (e = qknorm(c, L, M, pos_ptr, pos_fixed, 0, 0, c->qbuf, true))) return e;
   AttnParams a = {};
   a.q = c->qbuf;
   a.Kc = L.K;
@@ -390,8 +423,8 @@ cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_
     b.j = j;
     b.H = c->H;
     b.M = j == 1 ? 2 : 1;
-    b.table = c->cb_embed + (size_t)(j - 1) * c->Vc * c->H;
-    b.table_rows = c->Vc;
+    b.table = c->cb_embed + (size_t)(j - 1) * c->Vmax * c->H;
+    b.table_rows = j == 1 ? c->Vs : c->Vc;  // step 1 feeds code 0
     b.row_base = 0;
     b.ids = &c->st->fb[j - 1];
     b.xs = c->xs;
@@ -475,6 +508,7 @@ cudaError_t skinny(tf_ctx* c, const Lin& L, int set, int M, int epi, float* out,
   if (o.layer) {
     p.Kc = o.layer->K;
     p.Vc = o.layer->V;
+    if (o.layer->q_norm && epi == EPI_QKV) p.qk_raw = c->qk_raw;
   }
   p.T = c->T;
   p.pos_ptr = o.pos_ptr;
@@ -522,6 +556,7 @@ cudaError_t layer_batched(tf_ctx* c, const Layer& L, float* x, int M, int rps,
   q.pos_fixed = pos_fixed;
   q.ssq_n = ssq_in;
   if ((e = skinny(c, L.qkv, 0, M, EPI_QKV, nullptr, 0, q))) return e;
+  if (L.q_norm && (e = qknorm(c, L, M, pos_ptr, pos_fixed, rps, 0, c->qbuf, true))) return e;
   AttnParams a = {};
   a.q = c->qbuf;
   a.Kc = L.K;
@@ -610,8 +645,8 @@ cudaError_t enqueue_tail_batched(tf_ctx* c, const tf_sampling* s, int B, int adv
     b.j = j;
     b.H = c->H;
     b.M = M;
-    b.table = c->cb_embed + (size_t)(j - 1) * c->Vc * c->H;
-    b.table_rows = c->Vc;
+    b.table = c->cb_embed + (size_t)(j - 1) * c->Vmax * c->H;
+    b.table_rows = j == 1 ? c->Vs : c->Vc;  // step 1 feeds code 0
     b.row_base = 0;
     b.ids = c->st->fb + (j - 1);
     b.id_stride = kIdStride;
@@ -665,6 +700,9 @@ cudaError_t enqueue_decode_batched(tf_ctx* c, const tf_sampling* s, int B) {
   b.row_base = c->sem_base;
   b.ids = c->st->fb;
   b.id_stride = kIdStride;
+  b.cb_sum = c->slow_cb;
+  b.cb_rows = c->Vc;
+  b.ncb = c->NCB;
   b.x = c->xs;
   b.err = &c->st->err;
   b.nw_next = c->slow[0].attn_norm;
@@ -695,6 +733,9 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
   b.table_rows = c->Vs;
   b.row_base = c->sem_base;
   b.ids = &c->st->fb[0];
+  b.cb_sum = c->slow_cb;
+  b.cb_rows = c->Vc;
+  b.ncb = c->NCB;
   b.x = c->xs;
   b.err = &c->st->err;
   if ((e = launch_build(b, false, c->stream))) return e;
@@ -901,9 +942,14 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   };
   const size_t layer_bytes = lin_bytes(c->QKV, H) + lin_bytes(H, c->Q) + lin_bytes(2 * c->F, H) +
                              lin_bytes(H, c->F) + 2 * align_up(H * 2);
+  const bool qk_slow = cfg->flags & TF_FLAG_QK_NORM, qk_fast = cfg->flags & TF_FLAG_QK_NORM_FAST;
+  const bool cb_sum = cfg->flags & TF_FLAG_SLOW_CB_SUM;
+  const size_t qk_bytes = 2 * align_up((size_t)c->D * 2);
   size_t wtotal = align_up((size_t)c->Vt * H * 2) + (cfg->slow_layers + cfg->fast_layers) * layer_bytes +
                   2 * align_up(H * 2) + lin_bytes(c->Vc, H) +
-                  align_up((size_t)(c->NCB - 1) * c->Vc * H * 2);
+                  align_up((size_t)(c->NCB - 1) * c->Vmax * H * 2) +
+                  (qk_slow ? cfg->slow_layers * qk_bytes : 0) + (qk_fast ? cfg->fast_layers * qk_bytes : 0) +
+                  (cb_sum ? align_up((size_t)(c->NCB - 1) * c->Vc * H * 2) : 0);
   if (dev_alloc(c, reinterpret_cast<void**>(&c->wbuf), wtotal) != TF_OK) return bail(TF_E_NOMEM);
   c->weight_bytes = wtotal;
   uint8_t* cur = c->wbuf;
@@ -921,7 +967,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
     return L;
   };
   c->text_embed = reinterpret_cast<uint16_t*>(take((size_t)c->Vt * H * 2));
-  auto make_layers = [&](std::vector<Layer>& v, int n) {
+  auto make_layers = [&](std::vector<Layer>& v, int n, bool qk) {
     v.resize(n);
     for (Layer& L : v) {
       L.qkv = make_lin(c->QKV, c->H);
@@ -930,14 +976,19 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       L.w2 = make_lin(c->H, c->F);
       L.attn_norm = reinterpret_cast<uint16_t*>(take(H * 2));
       L.ffn_norm = reinterpret_cast<uint16_t*>(take(H * 2));
+      if (qk) {
+        L.q_norm = reinterpret_cast<uint16_t*>(take((size_t)c->D * 2));
+        L.k_norm = reinterpret_cast<uint16_t*>(take((size_t)c->D * 2));
+      }
     }
   };
-  make_layers(c->slow, cfg->slow_layers);
-  make_layers(c->fast, cfg->fast_layers);
+  make_layers(c->slow, cfg->slow_layers, qk_slow);
+  make_layers(c->fast, cfg->fast_layers, qk_fast);
   c->slow_norm = reinterpret_cast<uint16_t*>(take(H * 2));
   c->fast_norm = reinterpret_cast<uint16_t*>(take(H * 2));
   c->fast_head = make_lin(c->Vc, c->H);
-  c->cb_embed = reinterpret_cast<uint16_t*>(take((size_t)(c->NCB - 1) * c->Vc * H * 2));
+  c->cb_embed = reinterpret_cast<uint16_t*>(take((size_t)(c->NCB - 1) * c->Vmax * H * 2));
+  if (cb_sum) c->slow_cb = reinterpret_cast<uint16_t*>(take((size_t)(c->NCB - 1) * c->Vc * H * 2));
   c->sem.w = reinterpret_cast<uint8_t*>(c->text_embed + (size_t)c->sem_base * H);
   c->sem.N = c->Vs;
   c->sem.K = c->H;
@@ -975,6 +1026,9 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       dev_alloc_t(c, &c->hist, (size_t)T * B * c->NCB) || dev_alloc_t(c, &c->st, 1) ||
       dev_alloc_t(c, &c->fb_ring, B * kRepRing * kRepIds) ||
       dev_alloc_t(c, &c->rope, (size_t)T * (c->D / 2)))
+    return bail(TF_E_NOMEM);
+  if ((qk_slow || qk_fast) &&
+      dev_alloc_t(c, &c->qk_raw, (size_t)std::max<int>(T, 2 * (int)B) * (c->Q + c->KV)))
     return bail(TF_E_NOMEM);
   // Tensor-core prompt GEMMs for bf16 weights whenever every shape tiles.
   c->prefill_tc = gemm_tc_supported(c->QKV, c->H) && gemm_tc_supported(c->H, c->Q) &&
@@ -1153,7 +1207,11 @@ tf_status tf_load_weights(tf_ctx* c, const tf_tensor* t, int32_t n) {
     } else if (name == "fast.head") {
       s = load_lin(c->fast_head, c->Vc, c->H, MAP_IDENTITY, 0);
     } else if (name == "fast.cb_embed") {
-      s = shape_is({c->NCB - 1, c->Vc, c->H}) ? copy_raw(c->cb_embed, (size_t)(c->NCB - 1) * c->Vc * H * 2)
+      s = shape_is({c->NCB - 1, c->Vmax, c->H})
+              ? copy_raw(c->cb_embed, (size_t)(c->NCB - 1) * c->Vmax * H * 2)
+              : bad_shape();
+    } else if (name == "slow.cb_embed" && c->slow_cb) {
+      s = shape_is({c->NCB - 1, c->Vc, c->H}) ? copy_raw(c->slow_cb, (size_t)(c->NCB - 1) * c->Vc * H * 2)
                                               : bad_shape();
     } else if (std::sscanf(name.c_str(), "%15[a-z].%d.%31s", part, &li, field) == 3 &&
                (std::string(part) == "slow" || std::string(part) == "fast")) {
@@ -1163,6 +1221,8 @@ tf_status tf_load_weights(tf_ctx* c, const tf_tensor* t, int32_t n) {
       const std::string f = field;
       if (f == "attn_norm" || f == "ffn_norm") {
         s = shape_is({c->H}) ? copy_raw(f[0] == 'a' ? L.attn_norm : L.ffn_norm, H * 2) : bad_shape();
+      } else if ((f == "q_norm" || f == "k_norm") && L.q_norm) {
+        s = shape_is({c->D}) ? copy_raw(f[0] == 'q' ? L.q_norm : L.k_norm, (size_t)c->D * 2) : bad_shape();
       } else if (f == "wqkv") {
         s = load_lin(L.qkv, c->QKV, c->H, MAP_QKV, 0);
       } else if (f == "wo") {
@@ -1194,7 +1254,10 @@ tf_status tf_load_weights(tf_ctx* c, const tf_tensor* t, int32_t n) {
 
 namespace {
 bool all_loaded(tf_ctx* c, std::string* missing) {
-  const size_t need = 1 + 7 * (c->slow.size() + c->fast.size()) + 4;
+  size_t need = 1 + 7 * (c->slow.size() + c->fast.size()) + 4;
+  if (c->cfg.flags & TF_FLAG_QK_NORM) need += 2 * c->slow.size();
+  if (c->cfg.flags & TF_FLAG_QK_NORM_FAST) need += 2 * c->fast.size();
+  if (c->cfg.flags & TF_FLAG_SLOW_CB_SUM) need += 1;
   if (c->loaded.size() >= need) return true;
   *missing = std::to_string(need - c->loaded.size()) + " tensor(s) not loaded";
   return false;
@@ -1266,6 +1329,7 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
       if (layer) {
         p.Kc = layer->K + kvo;
         p.Vc = layer->V + kvo;
+        if (layer->q_norm) p.qk_raw = c->qk_raw;
       }
       p.T = c->T;
       p.pos_fixed = 0;
@@ -1285,6 +1349,7 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
     for (const Layer& L : c->slow) {
       CK(launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
       CK(gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L));
+      if (L.q_norm) CK(qknorm(c, L, P, nullptr, 0, 0, kvo, c->pq, false));
       AttnParams a = {};
       a.q = c->pq;
       a.Kc = L.K + kvo;

@@ -71,7 +71,20 @@ typedef struct {
   int32_t max_batch;        /* sequences per context, 1..32 (lockstep batch)    */
   float rms_eps, rope_theta;
   int32_t weight_dtype;     /* TF_WEIGHT_BF16 or TF_WEIGHT_FP8                  */
+  int32_t flags;            /* TF_FLAG_* model options, 0 = none                */
 } tf_config;
+
+/* Model options (tf_config.flags) for checkpoints that have them:
+ * TF_FLAG_QK_NORM: every slow layer normalises each head of q and of k with
+ *   an RMSNorm over head_dim ("slow.{i}.q_norm", "slow.{i}.k_norm",
+ *   [head_dim] bf16) before RoPE.  The tuna-fish README's slowAR parameter
+ *   count ("Inference estimation") holds these 2 x head_dim per layer.
+ * TF_FLAG_QK_NORM_FAST: the same in the fast layers ("fast.{i}.q_norm", ...).
+ * TF_FLAG_SLOW_CB_SUM: the slow input of a decoded frame adds the embeddings
+ *   of the previous frame's codes 1..9 ("slow.cb_embed"
+ *   [n_codebooks-1][codebook_size][hidden] bf16, table j-1 for code j) to the
+ *   text-embedding row of its code 0. */
+enum { TF_FLAG_QK_NORM = 1, TF_FLAG_QK_NORM_FAST = 2, TF_FLAG_SLOW_CB_SUM = 4 };
 
 /* One named host (or device) tensor for tf_load_weights.
  * Names: "text_embed" [text_vocab][hidden];
@@ -83,7 +96,11 @@ typedef struct {
  *        "slow.{i}.w2" (down) [hidden][ffn];
  *        "slow.norm" [hidden];  the same for "fast.{i}.*" and "fast.norm";
  *        "fast.head" [codebook_size][hidden];
- *        "fast.cb_embed" [n_codebooks-1][codebook_size][hidden].
+ *        "fast.cb_embed" [n_codebooks-1][max(semantic_vocab, codebook_size)][hidden]
+ *            (table j-1 embeds the id fed at fast step j: code 0 at step 1,
+ *            code j-1 after);
+ *        with the TF_FLAG_* options also "slow.{i}.q_norm", "slow.{i}.k_norm",
+ *        "fast.{i}.q_norm", "fast.{i}.k_norm" [head_dim] and "slow.cb_embed".
  * Linear weights are [out][in] row-major.  Embeddings and norms are bf16.
  * In an FP8 context a linear weight is given either as bf16 (the library
  * quantises it per row, exactly as tf_op_quantize_fp8) or as

@@ -159,6 +159,14 @@ class DualAROracle:
         q = qkv[:, : d.q_dim].reshape(-1, d.n_heads, d.head_dim)
         k = qkv[:, d.q_dim: d.q_dim + d.kv_dim].reshape(-1, d.n_kv_heads, d.head_dim)
         v = qkv[:, d.q_dim + d.kv_dim:].reshape(-1, d.n_kv_heads, d.head_dim)
+        if f"{prefix}.q_norm" in self.raw:
+            # Option: per-head q/k RMSNorm before RoPE.  The tuna-fish README's
+            # slowAR count ("Inference estimation", params w/o emb) holds
+            # 2 x head_dim more parameters per layer than the linears and
+            # norms, the size of a q and a k norm weight; read as RMSNorm over
+            # each head's head_dim values with those weights (eps as elsewhere).
+            q = rmsnorm(q, bf16_bits_to_f64(self.raw[f"{prefix}.q_norm"]), d.rms_eps)
+            k = rmsnorm(k, bf16_bits_to_f64(self.raw[f"{prefix}.k_norm"]), d.rms_eps)
         for r, p in enumerate(positions):
             K[:, p] = round_to_bf16(apply_rope(k[r], p, d.rope_theta))
             V[:, p] = round_to_bf16(v[r])
@@ -291,6 +299,13 @@ class DualAROracle:
             if p >= d.max_seq_len:
                 raise ValueError("KV capacity reached")
             x = self.embed_row("text_embed", d.sem_base + int(self.feedback_c0[b]))[None, :]
+            if "slow.cb_embed" in self.raw:
+                # Option: the slow input also sums the embeddings of the previous
+                # frame's residual codes 1..9 (codebook j-1's table holds code c_j),
+                # read from the Dual-AR description: the slow AR sees each past
+                # frame, and a frame is all 10 codes.
+                for j in range(1, d.n_codebooks):
+                    x = x + self.embed_row("slow.cb_embed", j - 1, int(self.fed_hist[b][-1][j]))[None, :]
             x = self._slow(b, x, [p])
             self.pos[b] = p + 1
             f, z = self._frame_tail(b, x[-1], sampling,

@@ -9,7 +9,8 @@ Recipe (the same for every workload):
     seed ``s`` uses ``numpy.random.Generator(PCG64(SeedSequence([s, i])))`` and
     ``standard_normal(float32) * std`` (std 0.02), then is rounded to bfloat16
     (round to nearest even) and kept as its raw 16-bit pattern.
-  * RMSNorm weights are 1.0 (bf16 0x3F80) and still consume their index.
+  * RMSNorm weights are 1.0 (bf16 0x3F80) and still consume their index;
+    the optional per-head q/k norm weights are 1 + 0.1 N(0, 1).
   * Prompt ids of sequence ``b`` are ``Generator(PCG64(seed + b))``
     ``.integers(0, text_vocab)``.
 
@@ -49,6 +50,10 @@ class ModelDims:
     max_seq_len: int = 1024
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
+    # Model-fidelity options (off in every benchmark workload):
+    qk_norm: bool = False        # per-head RMSNorm of q and k before RoPE (slow decoder)
+    qk_norm_fast: bool = False   # the same in the fast decoder
+    slow_cb_sum: bool = False    # slow input adds the previous frame's codebook 1..9 embeddings
 
     @property
     def q_dim(self) -> int:
@@ -120,7 +125,8 @@ WORKLOADS = {
 def tensor_specs(d: ModelDims):
     """(name, shape, kind) in the fixed generation order.
 
-    kind is "linear" (an nn.Linear weight, [out][in]), "embed" or "norm".
+    kind is "linear" (an nn.Linear weight, [out][in]), "embed", "norm" or
+    "qknorm" (the optional per-head q/k RMSNorm weights, [head_dim]).
     Linear weights: wqkv [q_dim + 2 kv_dim][hidden] (rows: q heads, k heads,
     v heads), wo [hidden][q_dim], w1 (gate) and w3 (up) [ffn][hidden],
     w2 (down) [hidden][ffn], fast.head [codebook_size][hidden].
@@ -128,8 +134,8 @@ def tensor_specs(d: ModelDims):
     H = d.hidden
     specs = [("text_embed", (d.text_vocab, H), "embed")]
 
-    def layer(prefix):
-        return [
+    def layer(prefix, qk):
+        out = [
             (f"{prefix}.attn_norm", (H,), "norm"),
             (f"{prefix}.wqkv", (d.qkv_dim, H), "linear"),
             (f"{prefix}.wo", (H, d.q_dim), "linear"),
@@ -138,15 +144,25 @@ def tensor_specs(d: ModelDims):
             (f"{prefix}.w3", (d.ffn, H), "linear"),
             (f"{prefix}.w2", (H, d.ffn), "linear"),
         ]
+        if qk:
+            out += [(f"{prefix}.q_norm", (d.head_dim,), "qknorm"),
+                    (f"{prefix}.k_norm", (d.head_dim,), "qknorm")]
+        return out
 
     for i in range(d.slow_layers):
-        specs += layer(f"slow.{i}")
+        specs += layer(f"slow.{i}", d.qk_norm)
     specs.append(("slow.norm", (H,), "norm"))
     for i in range(d.fast_layers):
-        specs += layer(f"fast.{i}")
+        specs += layer(f"fast.{i}", d.qk_norm_fast)
     specs.append(("fast.norm", (H,), "norm"))
     specs.append(("fast.head", (d.codebook_size, H), "linear"))
-    specs.append(("fast.cb_embed", (d.n_codebooks - 1, d.codebook_size, H), "embed"))
+    # table j-1 embeds the id fed at fast step j: c0 (semantic) at step 1,
+    # c_{j-1} after; with a semantic vocabulary larger than the codebooks the
+    # tables are as tall as the larger of the two
+    specs.append(("fast.cb_embed", (d.n_codebooks - 1, max(d.semantic_vocab, d.codebook_size), H),
+                  "embed"))
+    if d.slow_cb_sum:
+        specs.append(("slow.cb_embed", (d.n_codebooks - 1, d.codebook_size, H), "embed"))
     return specs
 
 
@@ -186,6 +202,10 @@ def make_weights(d: ModelDims, seed: int = 0, std: float = 0.02,
         idx, (name, shape, kind) = item
         if kind == "norm":
             return name, np.full(shape, BF16_ONE, dtype=np.uint16)
+        if kind == "qknorm":   # 1 + N(0, 0.1): not all ones, so their indexing shows
+            g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, idx])))
+            w = 1.0 + 0.1 * g.standard_normal(shape, dtype=np.float32)
+            return name, f32_to_bf16_bits(w.astype(np.float32))
         return name, _draw(seed, idx, shape, std)
 
     n_thr = threads or min(32, max(1, __import__("os").cpu_count() or 1))

@@ -83,11 +83,15 @@ TINY_G8 = TINY.replace(hidden=256, ffn=512, n_heads=8, n_kv_heads=1, head_dim=12
                        max_seq_len=64)
 
 
+TINY_OPTS = TINY.replace(qk_norm=True, qk_norm_fast=True, slow_cb_sum=True, codebook_size=32)
+
+
 @pytest.mark.parametrize("dims,fmt,tol,B,P", [(TINY, "bf16", BF16_TOL, 3, 16),
                                               (TINY, "fp8", FP8_TOL, 2, 16),
                                               (TINY_ODD, "bf16", BF16_TOL, 5, 12),
                                               (TINY_G8, "bf16", BF16_TOL, 4, 40),
-                                              (TINY, "bf16", BF16_TOL, 32, 8)])
+                                              (TINY, "bf16", BF16_TOL, 32, 8),
+                                              (TINY_OPTS, "bf16", BF16_TOL, 3, 40)])
 def test_tiny_batched_teacher_forced(dims, fmt, tol, B, P):
     """B sequences with their own prompts; P = 40 reaches the split
     attention path (more than 32 keys) with one ticket per row."""

@@ -69,7 +69,7 @@ def test_select_bit_exact(vocab, top_k, temp, top_p, ties, window):
     frame, cb0, seq = 17, 3, 0
     penalty = 1.7 if window else 1.0
     rng = np.random.default_rng(vocab * 3 + top_k)
-    recent = rng.integers(-2, vocab, size=(n, max(window, 1))).astype(np.int32)
+    recent = rng.integers(-2, vocab, size=(n, max(window, 2))).astype(np.int32)
     for i in range(n):                      # put each row's top ids in its window
         recent[i, :2] = np.argsort(-z[i])[:2]
     rd = torch.from_numpy(recent).to(DEV)
@@ -228,8 +228,19 @@ TINY_G8 = TINY.replace(hidden=256, ffn=512, n_heads=8, n_kv_heads=1, head_dim=12
                        max_seq_len=48)
 
 
+# Model options: per-head q/k RMSNorm before RoPE (slow and fast), the slow
+# input summing the previous frame's codes 1..9, and fast codebooks smaller
+# than the semantic vocabulary (the tuna-fish fastAR count's 1024-row head).
+TINY_OPTS = TINY.replace(qk_norm=True, qk_norm_fast=True, slow_cb_sum=True)
+TINY_SMALL_CB = TINY.replace(qk_norm=True, codebook_size=16)
+
+
 @pytest.mark.parametrize("dims,fmt,tol", [(TINY, "bf16", BF16_TOL), (TINY, "fp8", FP8_TOL),
-                                          (TINY_ODD, "bf16", BF16_TOL), (TINY_G8, "bf16", BF16_TOL)])
+                                          (TINY_ODD, "bf16", BF16_TOL), (TINY_G8, "bf16", BF16_TOL),
+                                          (TINY_OPTS, "bf16", BF16_TOL), (TINY_OPTS, "fp8", FP8_TOL),
+                                          (TINY_SMALL_CB, "bf16", BF16_TOL),
+                                          (TINY_G8.replace(qk_norm=True, qk_norm_fast=True,
+                                                           slow_cb_sum=True), "bf16", BF16_TOL)])
 def test_tiny_teacher_forced(dims, fmt, tol):
     tf = TeacherForced(dims, fmt, seed=0)
     tf.prefill(make_prompt(dims, 16, seed=0))
@@ -385,4 +396,18 @@ def test_full_size_fp8_long_context_topk30(full_weights, full_fp8_codes):
     # draws the a-priori perturbation cannot move must agree exactly; the
     # rest must be members of the oracle's candidate set (checked in check)
     assert compared + skipped == 30
+    tf.dec.close()
+
+
+def test_full_size_page_shapes_qk_norm_and_1024_row_fast_head():
+    """The shapes the tuna-fish parameter counts imply ("Inference
+    estimation": slowAR with per-head q/k norms, fastAR with a 1024-row
+    head), full size in bf16: prefill 128 then 2 decode frames."""
+    d = FULL.replace(qk_norm=True, codebook_size=1024)
+    tf = TeacherForced(d, "bf16", seed=0)
+    tf.prefill(make_prompt(d, 128, seed=0))
+    tf.decode()
+    tf.decode()
+    worst, compared, skipped = tf.check(BF16_TOL)
+    assert compared >= 15
     tf.dec.close()

@@ -416,6 +416,21 @@ def test_load_formula_page_numbers():
         assert abs(row["decode_tok_s"] * gib - row["gb_s"]) <= 0.05 * gib + 0.05
 
 
+def test_fidelity_options_reproduce_the_page_counts_through_the_tensor_list():
+    """The tensors the options add: with slow q/k norms the slow decoder's
+    tensor list (linears, norms, final norm, the 4096-row semantic slice)
+    falls short of the tuna-fish slowAR count by one hidden-size vector; the
+    fast decoder with a 1024-row head and no q/k norm is the fastAR count."""
+    g = _golden("load_formula.json")
+    d = FULL.replace(qk_norm=True, codebook_size=1024)
+    from synth import tensor_specs
+    specs = tensor_specs(d)
+    slow = sum(int(np.prod(sh)) for n, sh, _ in specs if n.startswith("slow."))
+    assert slow + d.semantic_vocab * d.hidden + d.hidden == g["slow_params_wo_emb"]
+    fast = sum(int(np.prod(sh)) for n, sh, _ in specs if n.startswith("fast.") and n != "fast.cb_embed")
+    assert fast == g["fast_params_wo_emb"]
+
+
 def test_layer_shapes_reproduce_page_param_counts():
     g = _golden("load_formula.json")
     # fastAR with a 1024-row head reproduces the inference count exactly,
@@ -439,6 +454,9 @@ def _torch_decoder(prefix, x, W, d):
     q = qkv[:, : d.q_dim].view(S, d.n_heads, d.head_dim)
     k = qkv[:, d.q_dim: d.q_dim + d.kv_dim].view(S, d.n_kv_heads, d.head_dim)
     v = qkv[:, d.q_dim + d.kv_dim:].view(S, d.n_kv_heads, d.head_dim)
+    if f"{prefix}.q_norm" in W:   # per-head RMSNorm of q and k before RoPE
+        q = F.rms_norm(q, (d.head_dim,), W[f"{prefix}.q_norm"], d.rms_eps)
+        k = F.rms_norm(k, (d.head_dim,), W[f"{prefix}.k_norm"], d.rms_eps)
     q = _rope_complex(q, pos, d.rope_theta)
     # the static KV cache holds bfloat16 values
     k = _rope_complex(k, pos, d.rope_theta).to(torch.bfloat16).double()
@@ -465,6 +483,11 @@ def _recompute_frames(d, w, prompt, frames):
     W = _torch_weights(w)
     ids = list(prompt) + [d.sem_base + int(f[0]) for f in frames[:-1]]
     x = W["text_embed"][torch.tensor(ids)]
+    if "slow.cb_embed" in W:   # decoded positions add the previous frame's codes 1..9
+        P = len(prompt)
+        for t, f in enumerate(frames[:-1]):
+            for j in range(1, d.n_codebooks):
+                x[P + t] = x[P + t] + W["slow.cb_embed"][j - 1, int(f[j])]
     for i in range(d.slow_layers):
         x = _torch_decoder(f"slow.{i}", x, W, d)
     P = len(prompt)
@@ -483,7 +506,9 @@ def _recompute_frames(d, w, prompt, frames):
 
 @pytest.mark.parametrize("dims", [TINY, TINY.replace(n_kv_heads=4, hidden=192, ffn=320,
                                                      text_vocab=300, semantic_vocab=40,
-                                                     codebook_size=48, head_dim=32)])
+                                                     codebook_size=48, head_dim=32),
+                                  TINY.replace(qk_norm=True, qk_norm_fast=True, slow_cb_sum=True),
+                                  TINY.replace(qk_norm=True, codebook_size=16)])
 def test_cached_decode_equals_full_recompute(dims):
     w = make_weights(dims, seed=3)
     o = oracle.DualAROracle(dims, w)

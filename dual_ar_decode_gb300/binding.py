@@ -63,6 +63,8 @@ EXPORTS = {
     "tf_profile_kernel": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_int64)]),
+    "tf_test_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    "tf_test_fail_alloc": (None, [ctypes.c_int32]),
     "tf_op_quantize_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_select": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,

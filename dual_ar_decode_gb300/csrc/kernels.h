@@ -100,6 +100,9 @@ struct GemvParams {
   float* qk_raw;
   const uint16_t* q_norm;  // k_qknorm: per-head RMSNorm weights [head_dim]
   const uint16_t* k_norm;
+  // Failure test: CTA 0's producer arms its last stage's barrier without
+  // issuing the copy, so that stage's bounded wait expires (ERR_TIMEOUT).
+  int32_t test_skip_copy;
 };
 // Finishes q and k after a QKV GEMM that left them raw (GemvParams::qk_raw):
 // each head of each row is RMSNorm-ed with q_norm / k_norm, rotated by RoPE

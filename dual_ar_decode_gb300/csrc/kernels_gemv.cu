@@ -268,8 +268,10 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
           }
           const uint32_t bytes = static_cast<uint32_t>(n) * rowbytes;
           mbar_arrive_expect_tx(&full[slot], bytes);
-          bulk_g2s(ring + (size_t)slot * p.stb, p.W + (size_t)(r0 + b0 + i0) * rowbytes, bytes,
-                   &full[slot], pol);
+          const bool skip = p.test_skip_copy && c == 0 && b0 + i0 + n >= nrows;  // failure test
+          if (!skip)
+            bulk_g2s(ring + (size_t)slot * p.stb, p.W + (size_t)(r0 + b0 + i0) * rowbytes, bytes,
+                     &full[slot], pol);
           ++s;
         }
       }

@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -54,6 +55,8 @@ constexpr int kBatchAttnCtasPerSm = TF_BATCH_ATTN_CTAS;  // batched attention gr
 // shared-memory footprint), 0 = staged (key chunks bulk-copied to shared memory).
 constexpr bool kBatchAttnStream = TF_BATCH_ATTN_STREAM != 0;
 thread_local std::string g_create_error;
+// Failure test: the n-th following device allocation is refused (0: off).
+std::atomic<int> g_fail_alloc{0};
 
 struct Lin {
   uint8_t* w = nullptr;
@@ -154,6 +157,8 @@ struct tf_ctx {
   bool prefilled = false;
 
   cudaGraphExec_t graph[2] = {nullptr, nullptr};  // [0] greedy, [1] top-k
+  bool inject_armed = false;  // failure test: next decode frame skips one copy
+  bool inject_skip = false;   //   (consumed by the first GEMV enqueued)
   int graph_nodes = 0;
   tf_sampling graph_samp{};
 
@@ -181,6 +186,11 @@ tf_status cuda_fail(tf_ctx* c, cudaError_t e, const char* where) {
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 tf_status dev_alloc(tf_ctx* c, void** p, size_t bytes) {
+  if (g_fail_alloc.load() > 0 && g_fail_alloc.fetch_sub(1) == 1) {
+    *p = nullptr;
+    return fail(c, TF_E_NOMEM, "device allocation of " + std::to_string(bytes) +
+                                   " bytes refused (failure test)");
+  }
   cudaError_t e = cudaMalloc(p, bytes);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
@@ -304,6 +314,10 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
     p.fb = &c->st->fb[cb];
     p.forced = &c->st->forced[cb];
     p.forced_on = &c->st->forced_on;
+  }
+  if (c->inject_skip) {
+    p.test_skip_copy = 1;
+    c->inject_skip = false;
   }
   const int eb = (L.s != nullptr) ? 1 : 2;
   gemv_plan(p, eb, c->num_sms, M);
@@ -1398,13 +1412,33 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
   if (r) return r;
   CK(cudaSetDevice(c->device));
   if ((r = set_forced(c, forced, c->Bc))) return r;
-  cudaGraphExec_t g;
-  if ((r = get_graph(c, &s, &g))) return r;
-  CK(cudaGraphLaunch(g, c->stream));
+  if (c->inject_armed && c->Bc == 1) {
+    // failure test: this frame runs outside the graph, its first GEMV
+    // skipping one weight copy
+    c->inject_armed = false;
+    c->inject_skip = true;
+    cudaError_t e = enqueue_decode_frame(c, &s);
+    c->inject_skip = false;
+    CK(e);
+  } else {
+    cudaGraphExec_t g;
+    if ((r = get_graph(c, &s, &g))) return r;
+    CK(cudaGraphLaunch(g, c->stream));
+  }
   c->pos_host += 1;
   c->frame_host += 1;
   return read_frame(c, frame, logits, c->Bc);
 }
+
+tf_status tf_test_inject(tf_ctx* c, int32_t what) {
+  if (!c || what != TF_TEST_SKIP_ONE_COPY) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  if (c->Bmax != 1) return fail(c, TF_E_INVAL, "the copy-skip test needs a batch-1 context");
+  c->inject_armed = true;
+  return TF_OK;
+}
+
+void tf_test_fail_alloc(int32_t n) { g_fail_alloc.store(n > 0 ? n : 0); }
 
 tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, int32_t* frames) {
   if (!c) return TF_E_INVAL;

@@ -232,6 +232,26 @@ tf_status tf_profile_kernel(tf_ctx* ctx, int32_t which, int32_t iters,
                             float* ms_per_launch, int64_t* bytes_per_launch);
 
 /* ---------------------------------------------------------------------------
+ * Failure tests.  They make a failure happen without faulting the GPU, so
+ * that the error paths can be tested: a bounded device wait that runs out,
+ * and a device allocation that is refused.
+ * ------------------------------------------------------------------------- */
+enum { TF_TEST_SKIP_ONE_COPY = 1 };
+/* TF_TEST_SKIP_ONE_COPY: the next tf_decode_frame of this (batch-1) context
+ * runs its kernels directly instead of from the captured graph, and in its
+ * first weight-streaming GEMV one CTA arms the barrier of its last stage
+ * without issuing the copy.  That stage's bounded wait (200 ms) runs out,
+ * the call returns TF_E_TIMEOUT and the context is poisoned as for any
+ * expired wait (every later call but tf_destroy returns TF_E_STATE).
+ * Errors: TF_E_INVAL (unknown test, batched context), TF_E_STATE. */
+tf_status tf_test_inject(tf_ctx* ctx, int32_t what);
+/* The n-th device allocation the library makes from now on (any context,
+ * any thread; tf_create allocates everything) is refused as if cudaMalloc
+ * had failed: that call returns TF_E_NOMEM and frees what it had allocated.
+ * n <= 0 turns it off.  Not thread-safe with respect to which call is hit. */
+void tf_test_fail_alloc(int32_t n);
+
+/* ---------------------------------------------------------------------------
  * Single-operation entry points, for parity tests and profiling.  Each runs
  * one kernel of the decode path on caller-provided DEVICE buffers on `stream`
  * (cudaStream_t, NULL = legacy default stream) and synchronises it.

@@ -86,6 +86,7 @@ def test_op_argument_validation_is_host_side(L):
     assert L.tf_op_select(ok, 1, 64, ctypes.byref(s), 0, 0, 0, None, 3, ok, None) == 1   # window, no ids
     assert L.tf_op_select(ok, 1, 64, ctypes.byref(s), 0, 0, 0, ok, 65, ok, None) == 1    # window > 64
     assert L.tf_op_quantize_fp8(None, 1, 16, None, None, None) == 1
+    assert L.tf_test_inject(None, 1) == 1
     assert L.tf_op_gemv(None, 0, None, 1, 16, None, None, 1, None, None) == 1
     assert L.tf_op_gemm_skinny(None, None, 16, 256, 256, None, None) == 1
     assert L.tf_op_gemm_skinny(1, 1, 65, 256, 256, 1, None) == 1   # more than 64 rows

@@ -46,20 +46,27 @@ GATE_UP_TRAFFIC = {"bf16": 99_670_272 + 3_020_800, "fp8": 49_942_272 + 0}
 
 
 # ---------------------------------------------------------------- accounting
+def linear_bytes(weight_dtype: str, rows: int, cols: int) -> int:
+    """Stored bytes of one [rows][cols] linear weight: bf16; e4m3 codes plus a
+    float32 scale per row; or 4-bit rows (cols/2 code bytes, cols/16 block
+    scales) plus a float32 scale per row."""
+    if weight_dtype == "bf16":
+        return rows * cols * 2
+    if weight_dtype == "fp8":
+        return rows * cols + rows * 4
+    return rows * (cols // 2 + cols // 16) + rows * 4
+
+
 def frame_bytes(d, weight_dtype: str, pos: int, batch: int = 1) -> dict:
     """Algorithmic HBM bytes of one decode step whose slow tokens sit at
     position `pos`: every weight streamed once (slow pass + 9 fast passes),
     and for each of the `batch` sequences the valid KV rows read and the new
     KV rows written (embedding rows are part of the weights)."""
-    eb = 1 if weight_dtype == "fp8" else 2
     H, F = d.hidden, d.ffn
-    lin_rows = d.qkv_dim + H + 2 * F + H
-    lin = d.qkv_dim * H + H * d.q_dim + 2 * F * H + H * F
-    scales = lin_rows * 4 if eb == 1 else 0
-    layer = lin * eb + scales + 2 * H * 2
+    lb = lambda r, c: linear_bytes(weight_dtype, r, c)
+    layer = lb(d.qkv_dim, H) + lb(H, d.q_dim) + 2 * lb(F, H) + lb(H, F) + 2 * H * 2
     slow_w = d.slow_layers * layer + d.semantic_vocab * H * 2 + H * 2 + H * 2
-    fast_w = d.fast_layers * layer + d.codebook_size * H * eb + (d.codebook_size * 4 if eb == 1 else 0) \
-        + H * 2 + H * 2
+    fast_w = d.fast_layers * layer + lb(d.codebook_size, H) + H * 2 + H * 2
     kv_row = d.kv_dim * 2                          # one K or V row of one layer, bf16
     kv_read = d.slow_layers * 2 * kv_row * (pos + 1)
     kv_read += sum(d.fast_layers * 2 * kv_row * (j + 1) for j in range(1, d.n_codebooks))
@@ -252,6 +259,7 @@ def main():
     ap.add_argument("--rows", type=int, default=19456)
     ap.add_argument("--cols", type=int, default=2560)
     ap.add_argument("--fp8", action="store_true")
+    ap.add_argument("--nvfp4", action="store_true", help="--op gemv: 4-bit block-scaled rows")
     ap.add_argument("--m", type=int, default=None,
                     help="--op gemm: prompt rows (1024); --op skinny: activation rows (16)")
     args = ap.parse_args()
@@ -374,7 +382,7 @@ def main():
     sched_bytes = float(np.mean([frame_bytes(d, wl.weight_dtype, p, B)["total"]
                                  for p in range(wl.prefill, wl.prefill + cap)]))
     frame_gbs = bytes_avg * (value / B) / world / 1e9
-    page_gib = PAGE_LOAD_ELEMENTS * (1 if wl.weight_dtype == "fp8" else 2) / 2 ** 30
+    page_gib = PAGE_LOAD_ELEMENTS * {"bf16": 2, "fp8": 1, "nvfp4": 0.5}[wl.weight_dtype] / 2 ** 30
     cpu = oracle_sample(wl, bits, prompt) if want_cpu else None
     dec.close()
 
@@ -384,7 +392,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if wl.weight_dtype == "bf16" else "fp8-e4m3 weights, bf16 KV, f32 accumulate",
+            "dtype": {"bf16": "bf16", "fp8": "fp8-e4m3 weights, bf16 KV, f32 accumulate",
+                      "nvfp4": "e2m1 + e4m3 block-scale weights, bf16 KV, f32 accumulate"}[wl.weight_dtype],
             "data": "synthetic: seeded N(0, 0.02) random-init weights, uniform prompt ids",
             "config": workload_config(wl, world),
             "timing": {"frames_timed": args.steps, "segments": [list(x) for x in plan],
@@ -435,28 +444,29 @@ def run_gemv_case(args):
     import torch
     from dual_ar_decode_gb300 import op_gemv
     from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
+    from dual_ar_decode_gb300.binding import TF_DTYPE_NVFP4
     dev = torch.device("cuda", 0)
-    eb = 1 if args.fp8 else 2
-    mat = args.rows * args.cols * eb
+    fmt = "nvfp4" if getattr(args, "nvfp4", False) else "fp8" if args.fp8 else "bf16"
+    mat = linear_bytes(fmt, args.rows, args.cols) - (0 if fmt == "bf16" else args.rows * 4)
     reps = max(args.steps, int(2.5e9 // mat))
     g = torch.Generator(device=dev).manual_seed(args.seed)
     W = torch.randint(0, 120, (reps * mat,), dtype=torch.uint8, device=dev, generator=g)
-    if eb == 2:
+    if fmt == "bf16":
         W = (W.view(torch.int16) & 0x3FFF).view(torch.uint8)   # finite bf16
-    S = torch.rand(reps * args.rows, device=dev, generator=g) if eb == 1 else None
+    S = torch.rand(reps * args.rows, device=dev, generator=g) if fmt != "bf16" else None
     x = torch.randn(args.cols, device=dev, generator=g)
     y = torch.empty(args.rows, device=dev)
-    dt = TF_DTYPE_FP8_E4M3 if eb == 1 else TF_DTYPE_BF16
+    dt = {"bf16": TF_DTYPE_BF16, "fp8": TF_DTYPE_FP8_E4M3, "nvfp4": TF_DTYPE_NVFP4}[fmt]
     for _ in range(args.warmup):
         op_gemv(W.data_ptr(), dt, S.data_ptr() if S is not None else None, args.rows, args.cols,
                 x.data_ptr(), y.data_ptr(), reps)
     ms = op_gemv(W.data_ptr(), dt, S.data_ptr() if S is not None else None, args.rows, args.cols,
                  x.data_ptr(), y.data_ptr(), reps)
-    nbytes = mat + (args.rows * 4 if eb == 1 else 0) + args.cols * 4 + args.rows * 4
+    nbytes = linear_bytes(fmt, args.rows, args.cols) + args.cols * 4 + args.rows * 4
     peaks = measured_peaks()
     gbs = nbytes / (ms / 1e3) / 1e9
     print(json.dumps({"op": "gemv", "rows": args.rows, "cols": args.cols,
-                      "weights": "fp8" if eb == 1 else "bf16", "launches": reps,
+                      "weights": fmt, "launches": reps,
                       "us_per_launch": round(ms * 1e3, 3), "achieved_gbs": round(gbs, 1),
                       "peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
                       "peak_source": peaks["source"]}), flush=True)

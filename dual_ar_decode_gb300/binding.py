@@ -12,8 +12,8 @@ LIB_NAME = "libtf_dualar.so"
 TF_OK = 0
 STATUS = {0: "TF_OK", 1: "TF_E_INVAL", 2: "TF_E_NOMEM", 3: "TF_E_CUDA", 4: "TF_E_STATE",
           5: "TF_E_CAPACITY", 6: "TF_E_TIMEOUT", 7: "TF_E_NUMERIC"}
-TF_WEIGHT_BF16, TF_WEIGHT_FP8 = 0, 1
-TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3 = 0, 1
+TF_WEIGHT_BF16, TF_WEIGHT_FP8, TF_WEIGHT_NVFP4 = 0, 1, 2
+TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3, TF_DTYPE_NVFP4 = 0, 1, 2
 TF_FLAG_QK_NORM, TF_FLAG_QK_NORM_FAST, TF_FLAG_SLOW_CB_SUM = 1, 2, 4
 
 
@@ -67,6 +67,8 @@ EXPORTS = {
     "tf_test_fail_alloc": (None, [ctypes.c_int32]),
     "tf_op_quantize_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "tf_op_quantize_nvfp4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_select": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(TfSampling), ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
@@ -127,7 +129,7 @@ def config_from_dims(d, weight_dtype: str = "bf16", max_batch: int = 1) -> TfCon
     return TfConfig(d.slow_layers, d.fast_layers, d.hidden, d.n_heads, d.n_kv_heads, d.head_dim,
                     d.ffn, d.text_vocab, d.semantic_vocab, d.n_codebooks, d.codebook_size,
                     d.max_seq_len, max_batch, d.rms_eps, d.rope_theta,
-                    TF_WEIGHT_FP8 if weight_dtype == "fp8" else TF_WEIGHT_BF16,
+                    {"bf16": TF_WEIGHT_BF16, "fp8": TF_WEIGHT_FP8, "nvfp4": TF_WEIGHT_NVFP4}[weight_dtype],
                     (TF_FLAG_QK_NORM if getattr(d, "qk_norm", False) else 0)
                     | (TF_FLAG_QK_NORM_FAST if getattr(d, "qk_norm_fast", False) else 0)
                     | (TF_FLAG_SLOW_CB_SUM if getattr(d, "slow_cb_sum", False) else 0))
@@ -248,6 +250,10 @@ class Decoder:
 
 def op_quantize_fp8(w_dev, rows, cols, codes_dev, scale_dev, stream=0):
     _check(lib().tf_op_quantize_fp8(w_dev, rows, cols, codes_dev, scale_dev, stream))
+
+
+def op_quantize_nvfp4(w_dev, rows, cols, packed_dev, scale_dev, stream=0):
+    _check(lib().tf_op_quantize_nvfp4(w_dev, rows, cols, packed_dev, scale_dev, stream))
 
 
 def op_select(logits_dev, n, vocab, sampling, frame, codebook0, sequence, ids_dev, stream=0,

@@ -112,12 +112,13 @@ constexpr int kSsqRows = 64;   // row stride of the partial sums of squares
 
 // Shared memory bytes a launch with these params needs.
 size_t gemv_smem_bytes(const GemvParams& p, int M);
-// Fills unit/units/rs/nst/stb/ctas_per_sm for a matrix of N x K elements of
-// `eb` bytes and M activation rows.
-void gemv_plan(GemvParams& p, int eb, int num_sms, int M);
+// Fills unit/units/rs/nst/stb/ctas_per_sm for a matrix of N x K elements
+// stored as weight format wt (0 bf16, 1 e4m3 codes, 2 block-scaled 4-bit) and
+// M activation rows.
+void gemv_plan(GemvParams& p, int wt, int num_sms, int M);
 // CTAs to launch for a planned GEMV.
 int gemv_grid(const GemvParams& p, int num_sms);
-// Launch (weight type wt: 0 bf16, 1 fp8) on `grid` CTAs; pdl = allow
+// Launch (weight format wt: 0 bf16, 1 fp8, 2 block-scaled 4-bit) on `grid` CTAs; pdl = allow
 // programmatic dependent launch on the previous kernel of the stream.
 cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl,
                         cudaStream_t s);
@@ -245,7 +246,8 @@ struct PackParams {
   int64_t rows, cols;
   int32_t map;
   int32_t q_dim, kv_dim, head_dim;
-  int32_t mode;          // 0 copy bf16, 1 quantise bf16 -> fp8, 2 copy fp8 + scale
+  int32_t mode;          // 0 copy bf16, 1 quantise bf16 -> fp8, 2 copy fp8 + scale,
+                         // 4 quantise bf16 -> block-scaled 4-bit rows
   uint32_t* err;         // mode 2: ERR_BAD_CODE if a code is NaN (0x7F / 0xFF)
 };
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
@@ -277,6 +279,9 @@ cudaError_t launch_rows_prep(const float* x, int ldx, int M, int K, const uint16
                              uint16_t* hi, uint16_t* lo, float* ssq, bool pdl, cudaStream_t s);
 // e4m3 codes -> bf16 bits of the same values (n even).
 cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaStream_t s);
+// Block-scaled 4-bit rows [N][K/2 + K/16] -> bf16 bits of e2m1 x block scale
+// [N][K] (exact; the row scale is applied later, in the GEMM epilogue).
+cudaError_t launch_nvfp4_to_bf16(const uint8_t* q, uint16_t* out, int N, int K, cudaStream_t s);
 // hi = bf16(a), lo = bf16(a - hi) elementwise.
 cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s);
 // a[m] = RMSNorm(x[m]) * w for M rows (prefill prologue).

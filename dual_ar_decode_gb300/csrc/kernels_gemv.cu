@@ -84,6 +84,16 @@ constexpr float kFp8Rescale = kFp8Path == 1 ? 1.152921504606846976e18f   // 2^60
 constexpr float kFp8ActScale = kFp8Path == 1 ? 1.152921504606846976e18f : 1.0f;
 constexpr bool kFp8HalfAct = kFp8Path == 2 || kFp8Path == 3;   // activations as packed f16 pairs
 
+// Weight storage per format (WT): 0 bf16, 1 e4m3 codes, 2 block-scaled 4-bit
+// (a row is K/2 bytes of e2m1 codes, two per byte with the even element in
+// the low nibble, then K/16 bytes of e4m3 block scales, one per 16 elements).
+// A consumer chunk is EPC consecutive elements: 16 bytes of bf16 or e4m3, or
+// one 16-element block of e2m1 (8 code bytes and its scale byte).
+__host__ __device__ constexpr int row_bytes(int wt, int K) {
+  return wt == 0 ? 2 * K : wt == 1 ? K : K / 2 + K / 16;
+}
+__host__ __device__ constexpr int chunk_elems(int wt) { return wt == 0 ? 8 : 16; }
+
 // d = a * b + c with a, b the two f16 halves selected by the template and c float.
 __device__ __forceinline__ float fma_h(uint32_t w2, uint32_t a2, float c, int half) {
   float d;
@@ -158,6 +168,33 @@ __device__ __forceinline__ float2 chunk_fma(const uint4 w, const float* a, float
   return acc;
 }
 
+// One 16-element block of e2m1 codes (w: 8 bytes, element 2i in the low
+// nibble of byte i) with its e4m3 block scale sb: the codes are converted
+// exactly to f16 pairs, multiplied by the f16 activation pairs a[0..7] with
+// float32 accumulation, and the block sum is scaled by the block scale
+// (placed as float32 bits: value x 2^-120, times 2^120, both exact; block
+// scales are never negative) before it joins acc.
+__device__ __forceinline__ float e2m1_block_fma(const uint2 w, uint32_t sb, const float* a, float acc) {
+  const uint32_t v[2] = {w.x, w.y};
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t h[4];  // the word's four code pairs as f16 pairs
+    asm("{.reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+        " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+        " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3;}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(v[i]));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t ap = __float_as_uint(a[4 * i + b]);
+      s0 = fma_h(h[b], ap, s0, 0);
+      s1 = fma_h(h[b], ap, s1, 1);
+    }
+  }
+  const float scale = __uint_as_float((sb & 0x7Fu) << 20) * 1.329227995784915873e36f;  // 2^120
+  return fmaf(s0 + s1, scale, acc);
+}
+
 // f16 bits of x, round to nearest even (finite activations).
 __device__ __forceinline__ uint32_t f16_bits(float x) {
   return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x)));
@@ -171,11 +208,11 @@ __device__ __forceinline__ void fp8_prepare(float* a) {
   if constexpr (WT == 1 && kFp8Path == 1) {
 #pragma unroll
     for (int e = 0; e < EPC; ++e) a[e] *= kFp8ActScale;
-  } else if constexpr (WT == 1 && kFp8HalfAct) {
+  } else if constexpr ((WT == 1 && kFp8HalfAct) || WT == 2) {
     float pk[EPC / 2];
 #pragma unroll
     for (int i = 0; i < EPC / 4; ++i) {
-      if constexpr (kFp8Path == 2) {   // (a0, a2), (a1, a3) of each 4 codes
+      if constexpr (WT == 1 && kFp8Path == 2) {   // (a0, a2), (a1, a3) of each 4 codes
         pk[2 * i] = __uint_as_float(f16_bits(a[4 * i]) | (f16_bits(a[4 * i + 2]) << 16));
         pk[2 * i + 1] = __uint_as_float(f16_bits(a[4 * i + 1]) | (f16_bits(a[4 * i + 3]) << 16));
       } else {                         // (a0, a1), (a2, a3)
@@ -218,7 +255,7 @@ __device__ __forceinline__ float warp_reduce_many(float (&v)[V], int lane) {
 template <int WT, int M, int J>
 __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int EPC = WT ? 16 : 8;      // elements per 16-byte chunk
+  constexpr int EPC = chunk_elems(WT);  // elements per chunk
   constexpr int R = M == 1 ? 8 : 4;     // rows reduced together
   constexpr int V = R * M;              // values per butterfly (8)
   constexpr int LOGV = 3;
@@ -230,8 +267,8 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
   const int u1 = (int)((long long)p.units * (c + 1) / G);
   const int r0 = u0 * p.unit;
   const int nrows = (u1 - u0) * p.unit;
-  const uint32_t rowbytes = static_cast<uint32_t>(p.K) * (WT ? 1u : 2u);
-  const int nch = static_cast<int>(rowbytes >> 4);
+  const uint32_t rowbytes = static_cast<uint32_t>(row_bytes(WT, p.K));
+  const int nch = p.K / EPC;
 
   uint8_t* ring = smem;
   float* red = reinterpret_cast<float*>(smem + (size_t)p.nst * p.stb);  // [kRowBatch][NW][M]
@@ -401,7 +438,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
     }
   }
 
-  if constexpr (WT == 1) {
+  if constexpr (WT >= 1) {
 #pragma unroll
     for (int m = 0; m < M; ++m)
 #pragma unroll
@@ -425,14 +462,21 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
 #pragma unroll
           for (int m = 0; m < M; ++m) acc[m] = make_float2(0.f, 0.f);
           if (i + r < n) {
-            const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)(i + r) * rowbytes);
+            const uint8_t* rowp = st + (size_t)(i + r) * rowbytes;
 #pragma unroll
             for (int j = 0; j < J; ++j) {
               const int ch = tid + j * NT;
               if (ch < nch) {
-                const uint4 w = row[ch];
+                if constexpr (WT == 2) {
+                  const uint2 w = reinterpret_cast<const uint2*>(rowp)[ch];
+                  const uint32_t sb = rowp[(p.K >> 1) + ch];
 #pragma unroll
-                for (int m = 0; m < M; ++m) acc[m] = chunk_fma<WT, EPC>(w, a[m][j], acc[m]);
+                  for (int m = 0; m < M; ++m) acc[m].x = e2m1_block_fma(w, sb, a[m][j], acc[m].x);
+                } else {
+                  const uint4 w = reinterpret_cast<const uint4*>(rowp)[ch];
+#pragma unroll
+                  for (int m = 0; m < M; ++m) acc[m] = chunk_fma<WT, EPC>(w, a[m][j], acc[m]);
+                }
               }
             }
           }
@@ -464,8 +508,8 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
             v1 += red[((2 * pi + 1) * NW + w) * M + m];
           }
           if (p.scale) {
-            v0 *= __ldg(&p.scale[rg]) * kFp8Rescale;
-            v1 *= __ldg(&p.scale[rg + 1]) * kFp8Rescale;
+            v0 *= __ldg(&p.scale[rg]) * (WT == 1 ? kFp8Rescale : 1.0f);
+            v1 *= __ldg(&p.scale[rg + 1]) * (WT == 1 ? kFp8Rescale : 1.0f);
           }
           if (p.epi == EPI_SWIGLU) {
             epi_swiglu(p, m, rg >> 1, v0, v1);
@@ -483,7 +527,7 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
         for (int m = 0; m < M; ++m) {
           float v = 0.f;
           for (int w = 0; w < NW; ++w) v += red[(ri * NW + w) * M + m];
-          if (p.scale) v *= __ldg(&p.scale[rg]) * kFp8Rescale;
+          if (p.scale) v *= __ldg(&p.scale[rg]) * (WT == 1 ? kFp8Rescale : 1.0f);
           float* o = p.out + (size_t)m * p.ldo + rg;
           if (p.epi == EPI_RESID) {
             *o = ((b0 == 0 && ri == tid) ? xr0[m] : *o) + v;
@@ -582,21 +626,23 @@ size_t gemv_smem_bytes(const GemvParams& p, int M) {
 
 namespace {
 
-const void* kernel_for(int wt, int M, int J) {
-  const void* t[2][2][5] = {
-      {{(const void*)k_gemv<0, 1, 1>, (const void*)k_gemv<0, 1, 2>, (const void*)k_gemv<0, 1, 3>,
-        (const void*)k_gemv<0, 1, 4>, (const void*)k_gemv<0, 1, 5>},
-       {(const void*)k_gemv<0, 2, 1>, (const void*)k_gemv<0, 2, 2>, (const void*)k_gemv<0, 2, 3>,
-        (const void*)k_gemv<0, 2, 4>, (const void*)k_gemv<0, 2, 5>}},
-      {{(const void*)k_gemv<1, 1, 1>, (const void*)k_gemv<1, 1, 2>, (const void*)k_gemv<1, 1, 3>,
-        (const void*)k_gemv<1, 1, 4>, (const void*)k_gemv<1, 1, 5>},
-       {(const void*)k_gemv<1, 2, 1>, (const void*)k_gemv<1, 2, 2>, (const void*)k_gemv<1, 2, 3>,
-        (const void*)k_gemv<1, 2, 4>, (const void*)k_gemv<1, 2, 5>}}};
-  return t[wt][M - 1][J - 1];
+template <int WT, int M>
+const void* kernel_j(int J) {
+  switch (J) {
+    case 1: return (const void*)k_gemv<WT, M, 1>;
+    case 2: return (const void*)k_gemv<WT, M, 2>;
+    case 3: return (const void*)k_gemv<WT, M, 3>;
+    case 4: return (const void*)k_gemv<WT, M, 4>;
+    default: return (const void*)k_gemv<WT, M, 5>;
+  }
 }
 
-// Ring of `ring` bytes in stages of about min(kStageTarget, ring / 2) bytes
-// of whole rows (at least one row and two stages).
+const void* kernel_for(int wt, int M, int J) {
+  if (wt == 0) return M == 1 ? kernel_j<0, 1>(J) : kernel_j<0, 2>(J);
+  if (wt == 1) return M == 1 ? kernel_j<1, 1>(J) : kernel_j<1, 2>(J);
+  return M == 1 ? kernel_j<2, 1>(J) : kernel_j<2, 2>(J);
+}
+
 void set_ring(GemvParams& p, int rowbytes, int ring) {
   const int target = std::min(kStageTarget, ring / 2);
   p.rs = rowbytes >= target ? 1 : target / rowbytes;
@@ -615,12 +661,12 @@ int gemv_grid(const GemvParams& p, int num_sms) {
 // lets two CTAs share an SM (registers and shared memory), else the most even
 // one with a single CTA: with only one CTA's consumer warps per SM the row
 // reductions are latency-bound.
-void gemv_plan(GemvParams& p, int eb, int num_sms, int M) {
+void gemv_plan(GemvParams& p, int wt, int num_sms, int M) {
   (void)num_sms;
   p.unit = (p.epi == EPI_SWIGLU || p.epi == EPI_QKV) ? 2 : 1;
   p.units = p.N / p.unit;
-  const int rowbytes = p.K * eb;
-  const int nch = rowbytes / 16;
+  const int rowbytes = row_bytes(wt, p.K);
+  const int nch = p.K / chunk_elems(wt);
   struct Split {
     int nt, J;
     double eff;
@@ -644,7 +690,7 @@ void gemv_plan(GemvParams& p, int eb, int num_sms, int M) {
       set_ring(p, rowbytes, kRingPerSm / ctas);
       int n = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-              &n, kernel_for(eb == 1 ? 1 : 0, M, cand[i].J), cand[i].nt + 32, gemv_smem_bytes(p, M)) ==
+              &n, kernel_for(wt, M, cand[i].J), cand[i].nt + 32, gemv_smem_bytes(p, M)) ==
               cudaSuccess &&
           n >= ctas) {
         p.ctas_per_sm = ctas;
@@ -665,7 +711,8 @@ cudaError_t launch_gemv(const GemvParams& p, int wt, int M, int grid, bool pdl, 
   const int J = p.J, nt = p.nt;
   if (J < 1 || J > 5 || M < 1 || M > 2) return cudaErrorInvalidValue;
   if (wt == 0) return M == 1 ? launch_j<0, 1>(p, J, nt, grid, pdl, s) : launch_j<0, 2>(p, J, nt, grid, pdl, s);
-  return M == 1 ? launch_j<1, 1>(p, J, nt, grid, pdl, s) : launch_j<1, 2>(p, J, nt, grid, pdl, s);
+  if (wt == 1) return M == 1 ? launch_j<1, 1>(p, J, nt, grid, pdl, s) : launch_j<1, 2>(p, J, nt, grid, pdl, s);
+  return M == 1 ? launch_j<2, 1>(p, J, nt, grid, pdl, s) : launch_j<2, 2>(p, J, nt, grid, pdl, s);
 }
 
 cudaError_t gemv_set_attributes() {
@@ -675,7 +722,9 @@ cudaError_t gemv_set_attributes() {
     if ((e = set_attr_m<0, 1>())) return e;
     if ((e = set_attr_m<0, 2>())) return e;
     if ((e = set_attr_m<1, 1>())) return e;
-    return set_attr_m<1, 2>();
+    if ((e = set_attr_m<1, 2>())) return e;
+    if ((e = set_attr_m<2, 1>())) return e;
+    return set_attr_m<2, 2>();
   });
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "device_once.h"
 #include "epilogue.cuh"
@@ -437,6 +439,62 @@ __device__ __forceinline__ int64_t map_row(const PackParams& p, int64_t s) {
   return s;
 }
 
+// e2m1 code (0..15) of a float32 in [-6, 6], round to nearest with ties to
+// the even code: the magnitude code counts the midpoints 0.25, 0.75, 1.25,
+// 1.75, 2.5, 3.5, 5 that |q| passes, a tie going to the even neighbour.
+__device__ __forceinline__ uint32_t e2m1_rne(float q) {
+  const float a = fabsf(q);
+  const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                     (a >= 3.5f) + (a > 5.0f);
+  return m | ((__float_as_uint(q) >> 31) << 3);
+}
+
+// Block-scaled 4-bit row (the tuna-fish README's nvfp4 weight format, read
+// after NVIDIA's NVFP4 layout with a per-row float32 scale): s_row =
+// amax / (6 * 448) (1 for a zero row); per 16-element block s_b =
+// e4m3_RNE(min(amax_block / (6 * s_row), 448)); code = e2m1_RNE(clamp(w /
+// (value(s_b) * s_row), +-6)), 0 where s_b is 0; every step one float32
+// operation in that order.  dst row: K/2 code bytes, then K/16 scale bytes.
+__device__ void nvfp4_row(const PackParams& p, int64_t s, int64_t d, float* red) {
+  const int tid = threadIdx.x;
+  const uint16_t* w = reinterpret_cast<const uint16_t*>(p.src) + s * p.cols;
+  float amax = 0.f;
+  for (int64_t i = tid; i < p.cols; i += blockDim.x) amax = fmaxf(amax, fabsf(bf16_to_f32(w[i])));
+  amax = warp_max(amax);
+  __syncthreads();
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+  const float s_row = amax == 0.f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  const float denom = __fmul_rn(6.0f, s_row);
+  uint8_t* out = p.dst + d * (p.cols / 2 + p.cols / 16);
+  for (int64_t b = tid; b < p.cols / 16; b += blockDim.x) {
+    float v[16];
+    float bm = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      v[e] = bf16_to_f32(w[b * 16 + e]);
+      bm = fmaxf(bm, fabsf(v[e]));
+    }
+    const float bs = fminf(__fdiv_rn(bm, denom), 448.0f);
+    const uint8_t sb = static_cast<uint8_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(bs, 0.f), __NV_SATFINITE, __NV_E4M3) & 0xFF);
+    const float sbv = e4m3x2_to_f32x2(sb).x;
+    const float dd = __fmul_rn(sbv, s_row);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float q = dd == 0.f ? 0.f : __fdiv_rn(v[e], dd);
+      q = fminf(fmaxf(q, -6.0f), 6.0f);
+      packed[e >> 3] |= e2m1_rne(q) << (4 * (e & 7));
+    }
+    reinterpret_cast<uint2*>(out)[b] = make_uint2(packed[0], packed[1]);
+    out[p.cols / 2 + b] = sb;
+  }
+  if (tid == 0) p.dst_scale[d] = s_row;
+}
+
 // One CTA per source row.  mode 0: copy bf16; mode 1: quantise bf16 -> e4m3
 // with a per-row scale; mode 2: copy e4m3 codes and their scale.
 __global__ void __launch_bounds__(256) k_pack(const PackParams p) {
@@ -465,6 +523,10 @@ __global__ void __launch_bounds__(256) k_pack(const PackParams p) {
     }
     if (nan && p.err) atomicOr(p.err, ERR_BAD_CODE);
     if (tid == 0) p.dst_scale[d] = p.src_scale[s];
+    return;
+  }
+  if (p.mode == 4) {
+    nvfp4_row(p, s, d, red);
     return;
   }
   // Per-row symmetric FP8 (drbaph s2-pro-fp8 model card, "Quantization
@@ -669,6 +731,39 @@ cudaError_t launch_select(const SelectParams& p, bool pdl, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(p.n), dim3(kSelThreads), 0, pdl, s, attr);
   return cudaLaunchKernelEx(&cfg, k_select, p);
+}
+
+// Block-scaled 4-bit rows -> bf16 bits of e2m1 x block scale (exact: at
+// most 2 + 4 significant bits, within bf16's range), one thread per block.
+__global__ void k_nvfp4_to_bf16(const uint8_t* q, uint16_t* out, int N, int K) {
+  const int nb = K / 16;
+  const int rb = K / 2 + K / 16;
+  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < (size_t)N * nb;
+       t += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = t / nb, b = t - r * nb;
+    const uint8_t* row = q + r * rb;
+    const uint2 w = reinterpret_cast<const uint2*>(row)[b];
+    const float sbv = e4m3x2_to_f32x2(row[K / 2 + b]).x;
+    const uint32_t v[2] = {w.x, w.y};
+    uint16_t* o = out + r * K + b * 16;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t c = (v[e >> 3] >> (4 * (e & 7))) & 0xFu;
+      const uint32_t mag = c & 7u;
+      // e2m1 value: exponent field 0 -> m / 2, else (1 + m / 2) * 2^(e - 1)
+      const float val = (mag < 2u) ? 0.5f * static_cast<float>(mag)
+                                   : ldexpf(1.0f + 0.5f * static_cast<float>(mag & 1u),
+                                            static_cast<int>(mag >> 1) - 1);
+      o[e] = f32_to_bf16((c & 8u) ? -(val * sbv) : val * sbv);
+    }
+  }
+}
+
+cudaError_t launch_nvfp4_to_bf16(const uint8_t* q, uint16_t* out, int N, int K, cudaStream_t s) {
+  const size_t n = (size_t)N * (K / 16);
+  const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 8192));
+  k_nvfp4_to_bf16<<<grid, 256, 0, s>>>(q, out, N, K);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {

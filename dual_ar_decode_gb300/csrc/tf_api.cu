@@ -60,9 +60,14 @@ std::atomic<int> g_fail_alloc{0};
 
 struct Lin {
   uint8_t* w = nullptr;
-  float* s = nullptr;  // per-row scales (fp8)
+  float* s = nullptr;  // per-row scales (fp8, 4-bit)
   int N = 0, K = 0;
+  int wt = 0;          // storage: 0 bf16, 1 e4m3 codes, 2 block-scaled 4-bit rows
 };
+
+// Bytes of one stored row of K weights in format wt (4-bit rows: K/2 code
+// bytes, then K/16 block-scale bytes).
+size_t lin_row_bytes(int wt, size_t K) { return wt == 0 ? 2 * K : wt == 1 ? K : K / 2 + K / 16; }
 
 struct Layer {
   Lin qkv, o, w13, w2;
@@ -96,8 +101,8 @@ struct tf_ctx {
   tf_config cfg{};
   int device = 0;
   int num_sms = 0;
-  int eb = 2;        // bytes per linear weight element
-  bool fp8 = false;
+  int wt = 0;        // linear weight format: 0 bf16, 1 fp8 per row, 2 block-scaled 4-bit
+  bool fp8 = false;  // quantised linears (wt != 0): a float32 scale per row
   cudaStream_t own_stream = nullptr;
   cudaStream_t stream = nullptr;
   std::string err;
@@ -223,7 +228,7 @@ bool valid_config(const tf_config* cfg, std::string* why) {
   if (cfg->ffn < 16 || cfg->ffn % 32) return bad("ffn must be a positive multiple of 32");
   if ((cfg->n_heads * cfg->head_dim) % 32) return bad("n_heads*head_dim must be a multiple of 32");
   // GEMV activations live in registers: K * bytes / 16 chunks over 256 threads <= 5 each.
-  const int eb = cfg->weight_dtype == TF_WEIGHT_FP8 ? 1 : 2;
+  const int eb = cfg->weight_dtype == TF_WEIGHT_BF16 ? 2 : 1;
   const int kmax = std::max(std::max(cfg->hidden, cfg->ffn), cfg->n_heads * cfg->head_dim);
   if (kmax * eb / 16 > 5 * 256) return bad("hidden/ffn too large for the decode GEMV");
   if (cfg->hidden > 16384) return bad("hidden too large");
@@ -235,8 +240,12 @@ bool valid_config(const tf_config* cfg, std::string* why) {
   if (cfg->max_seq_len < 10 || cfg->max_seq_len > 65536) return bad("max_seq_len must be in [10, 65536]");
   if (cfg->max_batch < 1 || cfg->max_batch > kMaxBatch) return bad("max_batch must be in [1, 32]");
   if (!(cfg->rms_eps > 0.f) || !(cfg->rope_theta > 1.f)) return bad("rms_eps > 0 and rope_theta > 1 required");
-  if (cfg->weight_dtype != TF_WEIGHT_BF16 && cfg->weight_dtype != TF_WEIGHT_FP8)
-    return bad("weight_dtype must be TF_WEIGHT_BF16 or TF_WEIGHT_FP8");
+  if (cfg->weight_dtype != TF_WEIGHT_BF16 && cfg->weight_dtype != TF_WEIGHT_FP8 &&
+      cfg->weight_dtype != TF_WEIGHT_NVFP4)
+    return bad("weight_dtype must be TF_WEIGHT_BF16, TF_WEIGHT_FP8 or TF_WEIGHT_NVFP4");
+  if (cfg->weight_dtype == TF_WEIGHT_NVFP4 &&
+      (cfg->hidden % 256 || cfg->ffn % 256 || (cfg->n_heads * cfg->head_dim) % 256))
+    return bad("4-bit weights need hidden, ffn and n_heads*head_dim multiples of 256");
   if (cfg->flags & ~(TF_FLAG_QK_NORM | TF_FLAG_QK_NORM_FAST | TF_FLAG_SLOW_CB_SUM))
     return bad("unknown flags");
   return true;
@@ -319,24 +328,22 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
     p.test_skip_copy = 1;
     c->inject_skip = false;
   }
-  const int eb = (L.s != nullptr) ? 1 : 2;
-  gemv_plan(p, eb, c->num_sms, M);
+  gemv_plan(p, L.wt, c->num_sms, M);
   const int grid = gemv_grid(p, c->num_sms);
   if (next.L && kGemvPrefetch > 0) {
     GemvParams q = {};
     q.N = next.L->N;
     q.K = next.L->K;
     q.epi = next.epi;
-    const int neb = (next.L->s != nullptr) ? 1 : 2;
-    gemv_plan(q, neb, c->num_sms, next.M);
+    gemv_plan(q, next.L->wt, c->num_sms, next.M);
     p.pf_w = next.L->w;
     p.pf_units = q.units;
     p.pf_unit = q.unit;
-    p.pf_rowbytes = q.K * neb;
+    p.pf_rowbytes = static_cast<int32_t>(lin_row_bytes(next.L->wt, q.K));
     p.pf_grid = gemv_grid(q, c->num_sms);
     p.pf_bytes = kGemvPrefetch;
   }
-  return launch_gemv(p, eb == 1 ? 1 : 0, M, grid, pdl, c->stream);
+  return launch_gemv(p, L.wt, M, grid, pdl, c->stream);
 }
 
 // The q/k norm option: finish the q and k a QKV GEMM left raw (rows at
@@ -547,8 +554,10 @@ cudaError_t skinny(tf_ctx* c, const Lin& L, int set, int M, int epi, float* out,
   // kernel (programmatic dependent launch), which is only right for weights
   // no kernel writes: a converted fp8 weight is launched without the overlap.
   bool pdl = true;
-  if (L.s) {  // fp8: bf16 copy of the e4m3 values; the row scale stays in p.scale
-    if (cudaError_t e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream)) return e;
+  if (L.s) {  // quantised: exact bf16 copy of the values; the row scale stays in p.scale
+    if (cudaError_t e = L.wt == 2 ? launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream)
+                                  : launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))
+      return e;
     p.W = reinterpret_cast<const uint8_t*>(c->wconv);
     pdl = false;
   }
@@ -929,8 +938,8 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
     return bail(TF_E_CUDA);
   }
 
-  c->fp8 = cfg->weight_dtype == TF_WEIGHT_FP8;
-  c->eb = c->fp8 ? 1 : 2;
+  c->wt = cfg->weight_dtype;
+  c->fp8 = c->wt != TF_WEIGHT_BF16;
   c->Bmax = cfg->max_batch;
   c->H = cfg->hidden;
   c->D = cfg->head_dim;
@@ -950,9 +959,9 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   c->S_slow = std::max(1, std::min(64, 2 * c->num_sms / c->Hkv));
 
   // ---- weights: one allocation
-  const size_t eb = c->eb, H = c->H;
+  const size_t H = c->H;
   auto lin_bytes = [&](size_t n, size_t k) {
-    return align_up(n * k * eb) + (c->fp8 ? align_up(n * sizeof(float)) : 0);
+    return align_up(n * lin_row_bytes(c->wt, k)) + (c->fp8 ? align_up(n * sizeof(float)) : 0);
   };
   const size_t layer_bytes = lin_bytes(c->QKV, H) + lin_bytes(H, c->Q) + lin_bytes(2 * c->F, H) +
                              lin_bytes(H, c->F) + 2 * align_up(H * 2);
@@ -976,7 +985,8 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
     Lin L;
     L.N = n;
     L.K = k;
-    L.w = take((size_t)n * k * eb);
+    L.w = take((size_t)n * lin_row_bytes(c->wt, k));
+    L.wt = c->wt;
     if (c->fp8) L.s = reinterpret_cast<float*>(take((size_t)n * sizeof(float)));
     return L;
   };
@@ -1051,7 +1061,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       (dev_alloc_t(c, &c->a_hi, (size_t)T * std::max({c->H, c->Q, c->F})) ||
        dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F}))))
     return bail(TF_E_NOMEM);
-  if (c->fp8 && (c->prefill_tc || B > 1) &&
+  if (c->fp8 && (c->prefill_tc || B > 1 || c->wt == TF_WEIGHT_NVFP4) &&
       dev_alloc_t(c, &c->wconv,
                   std::max({(size_t)c->QKV * H, (size_t)H * c->Q, (size_t)2 * c->F * H,
                             (size_t)H * c->F, (size_t)c->Vc * H})))
@@ -1137,10 +1147,13 @@ tf_status tf_get_info(const tf_ctx* c, tf_info* info) {
   info->num_sms = c->num_sms;
   info->graph_nodes = c->graph_nodes;
   info->weight_bytes = static_cast<int64_t>(c->weight_bytes);
-  int64_t lin = (int64_t)c->QKV * c->H + (int64_t)c->H * c->Q + 2LL * c->F * c->H + (int64_t)c->H * c->F;
+  const int w = c->wt;
+  int64_t lin = (int64_t)(c->QKV * lin_row_bytes(w, c->H) + c->H * lin_row_bytes(w, c->Q) +
+                          2LL * c->F * lin_row_bytes(w, c->H) + c->H * lin_row_bytes(w, c->F));
   int64_t norms = 2LL * c->H * 2;
-  int64_t slow = c->slow.size() * (lin * c->eb + norms) + (int64_t)c->Vs * c->H * 2 + c->H * 2 + c->H * 2;
-  int64_t fast = c->fast.size() * (lin * c->eb + norms) + (int64_t)c->Vc * c->H * c->eb + c->H * 2 + c->H * 2;
+  int64_t slow = c->slow.size() * (lin + norms) + (int64_t)c->Vs * c->H * 2 + c->H * 2 + c->H * 2;
+  int64_t fast = c->fast.size() * (lin + norms) + (int64_t)(c->Vc * lin_row_bytes(w, c->H)) + c->H * 2 +
+                 c->H * 2;
   if (c->fp8) {
     slow += c->slow.size() * (int64_t)(c->QKV + c->H + 2 * c->F + c->H) * 4;
     fast += c->fast.size() * (int64_t)(c->QKV + c->H + 2 * c->F + c->H) * 4 + (int64_t)c->Vc * 4;
@@ -1181,13 +1194,13 @@ tf_status tf_load_weights(tf_ctx* c, const tf_tensor* t, int32_t n) {
       p.kv_dim = c->KV;
       p.head_dim = c->D;
       p.src = c->staging;
-      p.dst = L.w + dst_row0 * cols * c->eb;
+      p.dst = L.w + dst_row0 * lin_row_bytes(c->wt, cols);
       p.dst_scale = L.s ? L.s + dst_row0 : nullptr;
       if (x.dtype == TF_DTYPE_BF16) {
         CK(cudaMemcpyAsync(c->staging, x.data, (size_t)rows * cols * 2, cudaMemcpyDefault, c->stream));
-        p.mode = c->fp8 ? 1 : 0;
+        p.mode = c->wt == TF_WEIGHT_NVFP4 ? 4 : c->fp8 ? 1 : 0;
       } else if (x.dtype == TF_DTYPE_FP8_E4M3) {
-        if (!c->fp8) return fail(c, TF_E_INVAL, name + ": fp8 tensor in a bf16 context");
+        if (c->wt != TF_WEIGHT_FP8) return fail(c, TF_E_INVAL, name + ": fp8 tensor in a non-fp8 context");
         if (!x.row_scale) return fail(c, TF_E_INVAL, name + ": fp8 tensor without row_scale");
         CK(cudaMemcpyAsync(c->staging, x.data, (size_t)rows * cols, cudaMemcpyDefault, c->stream));
         CK(cudaMemcpyAsync(c->staging_scale, x.row_scale, (size_t)rows * 4, cudaMemcpyDefault, c->stream));
@@ -1310,7 +1323,8 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
   c->Bc = B;
   c->prefilled = false;
 
-  const int wt = c->fp8 ? 1 : 0;
+  // CUDA-core fallback prompt GEMM: bf16 or e4m3 rows (4-bit rows go through a bf16 copy)
+  const int wt = c->wt == TF_WEIGHT_FP8 ? 1 : 0;
   // Slow decoder over sequence b's prompt: row m at position m, KV caches of
   // sequence b; its last residual row goes to xs[b].
   for (int sb = 0; sb < B; ++sb) {
@@ -1349,10 +1363,14 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
       p.pos_fixed = 0;
       p.rope = c->rope;
       p.err = &c->st->err;
+      cudaError_t e;
+      if (c->wt == TF_WEIGHT_NVFP4) {  // exact bf16 copy of e2m1 x block scale; row scale in p.scale
+        if ((e = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e;
+        p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+      }
       if (c->prefill_tc) {
-        cudaError_t e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream);
-        if (e) return e;
-        if (c->fp8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
+        if ((e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream))) return e;
+        if (c->wt == TF_WEIGHT_FP8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
           if ((e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e;
           p.W = reinterpret_cast<const uint8_t*>(c->wconv);
         }
@@ -1561,7 +1579,7 @@ tf_status tf_profile_kernel(tf_ctx* c, int32_t which, int32_t iters, float* ms_p
   if (ms_per_launch) *ms_per_launch = ms / iters;
   const Layer& L0 = c->slow[0];
   const Lin& lin = kind == 0 ? L0.w13 : kind == 1 ? L0.qkv : kind == 2 ? L0.o : L0.w2;
-  int64_t bytes = (int64_t)lin.N * lin.K * c->eb + (c->fp8 ? (int64_t)lin.N * 4 : 0);
+  int64_t bytes = (int64_t)(lin.N * lin_row_bytes(c->wt, lin.K)) + (c->fp8 ? (int64_t)lin.N * 4 : 0);
   if (batched) {
     bytes += (int64_t)M * lin.K * 4;                   // activation rows in (bf16 hi + lo)
     bytes += (int64_t)M * (kind == 0 ? (int64_t)c->F * 4 : kind == 1 ? (int64_t)(c->Q * 4 + 2 * c->KV * 2)
@@ -1590,6 +1608,23 @@ tf_status tf_op_quantize_fp8(const uint16_t* w, int64_t rows, int64_t cols, uint
   p.cols = cols;
   p.map = MAP_IDENTITY;
   p.mode = 1;
+  if (launch_pack(p, s) != cudaSuccess) return TF_E_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? TF_OK : TF_E_CUDA;
+}
+
+tf_status tf_op_quantize_nvfp4(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* packed,
+                               float* row_scale, void* stream) {
+  if (!w || !packed || !row_scale || rows < 1 || cols < 256 || cols % 256 || rows > (1 << 30))
+    return TF_E_INVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PackParams p = {};
+  p.src = reinterpret_cast<const uint8_t*>(w);
+  p.dst = packed;
+  p.dst_scale = row_scale;
+  p.rows = rows;
+  p.cols = cols;
+  p.map = MAP_IDENTITY;
+  p.mode = 4;
   if (launch_pack(p, s) != cudaSuccess) return TF_E_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? TF_OK : TF_E_CUDA;
 }
@@ -1781,10 +1816,12 @@ tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64
                      int64_t cols, const float* x, float* y, int32_t repeat, float* ms,
                      void* stream) {
   if (!W || !x || !y || rows < 1 || cols < 16 || rows > (1 << 30) || repeat < 1) return TF_E_INVAL;
-  if (dtype != TF_DTYPE_BF16 && dtype != TF_DTYPE_FP8_E4M3) return TF_E_INVAL;
-  if (dtype == TF_DTYPE_FP8_E4M3 && !row_scale) return TF_E_INVAL;
-  const int eb = dtype == TF_DTYPE_FP8_E4M3 ? 1 : 2;
+  if (dtype != TF_DTYPE_BF16 && dtype != TF_DTYPE_FP8_E4M3 && dtype != TF_DTYPE_NVFP4) return TF_E_INVAL;
+  if (dtype != TF_DTYPE_BF16 && !row_scale) return TF_E_INVAL;
+  const int wt = dtype;  // TF_DTYPE_* matches the GEMV's format numbers
+  const int eb = dtype == TF_DTYPE_BF16 ? 2 : 1;
   if ((cols * eb) % 16 || cols * eb / 16 > 5 * 256) return TF_E_INVAL;
+  if (dtype == TF_DTYPE_NVFP4 && cols % 256) return TF_E_INVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -1803,7 +1840,7 @@ tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64
   p.out = y;
   p.ldo = 0;
   p.err = err;
-  gemv_plan(p, eb, sms, 1);
+  gemv_plan(p, wt, sms, 1);
   const int grid = gemv_grid(p, sms);
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   tf_status r = TF_OK;
@@ -1813,9 +1850,9 @@ tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64
     cudaEventRecord(e0, s);
   }
   for (int i = 0; i < repeat && r == TF_OK; ++i) {
-    p.W = static_cast<const uint8_t*>(W) + (size_t)i * rows * cols * eb;
+    p.W = static_cast<const uint8_t*>(W) + (size_t)i * rows * lin_row_bytes(wt, cols);
     p.scale = row_scale ? row_scale + (size_t)i * rows : nullptr;
-    if (launch_gemv(p, eb == 1 ? 1 : 0, 1, grid, i > 0, s) != cudaSuccess) r = TF_E_CUDA;
+    if (launch_gemv(p, wt, 1, grid, i > 0, s) != cudaSuccess) r = TF_E_CUDA;
   }
   if (ms) cudaEventRecord(e1, s);
   uint32_t e = 0;

@@ -51,10 +51,17 @@ typedef enum {
   TF_E_NUMERIC = 7    /* NaN logit met during selection                          */
 } tf_status;
 
-/* Weight formats of the linear layers (tf_config.weight_dtype). */
-enum { TF_WEIGHT_BF16 = 0, TF_WEIGHT_FP8 = 1 };
-/* Element types of tensors handed to tf_load_weights (tf_tensor.dtype). */
-enum { TF_DTYPE_BF16 = 0, TF_DTYPE_FP8_E4M3 = 1 };
+/* Weight formats of the linear layers (tf_config.weight_dtype).
+ * TF_WEIGHT_NVFP4: block-scaled 4-bit weights (the tuna-fish README lists
+ * nvfp4 among its formats): FP4 E2M1 codes, an e4m3 scale per 16 elements
+ * of a row and a float32 scale per row; the library quantises bf16 linears
+ * as tf_op_quantize_nvfp4 does.  Needs hidden, ffn and n_heads*head_dim
+ * multiples of 256. */
+enum { TF_WEIGHT_BF16 = 0, TF_WEIGHT_FP8 = 1, TF_WEIGHT_NVFP4 = 2 };
+/* Element types of tensors handed to tf_load_weights (tf_tensor.dtype), and
+ * of the weight given to tf_op_gemv (TF_DTYPE_NVFP4: rows as
+ * tf_op_quantize_nvfp4 writes them). */
+enum { TF_DTYPE_BF16 = 0, TF_DTYPE_FP8_E4M3 = 1, TF_DTYPE_NVFP4 = 2 };
 
 /* Model shape.  All sizes are element counts.
  * head_dim must be 64 or 128; n_heads a multiple of n_kv_heads with
@@ -266,6 +273,19 @@ void tf_test_fail_alloc(int32_t n);
 tf_status tf_op_quantize_fp8(const uint16_t* w_bf16, int64_t rows, int64_t cols,
                              uint8_t* codes, float* scale, void* stream);
 
+/* Block-scaled 4-bit quantisation of a bf16 weight [rows][cols] (cols a
+ * multiple of 256): per row s = amax / (6 * 448) (IEEE float32 division; 1
+ * for an all-zero row); per 16-element block b = e4m3 round-to-nearest-even
+ * of min(amax_block / (6 * s), 448); code = FP4 E2M1 round-to-nearest-even
+ * (ties to the even code) of clamp(w / (value(b) * s), -6, 6), 0 where b is
+ * 0 -- each step one float32 operation.  packed: [rows][cols/2 + cols/16]
+ * bytes (the codes, two per byte with the even element in the low nibble,
+ * then the block scales); row_scale: float32 [rows].  All device pointers.
+ * The value of element k is e2m1(code) * e4m3(b) * s.
+ * Errors: TF_E_INVAL, TF_E_CUDA. */
+tf_status tf_op_quantize_nvfp4(const uint16_t* w_bf16, int64_t rows, int64_t cols,
+                               uint8_t* packed, float* row_scale, void* stream);
+
 /* Codebook-id selection over float32 logits [n][vocab] (device); row i uses
  * Philox counter (frame, codebook0 + i, sequence, 0).  Writes ids [n] (device,
  * int32).  sampling as tf_sampling (top_k 0 = argmax).  vocab <= 8192.
@@ -339,7 +359,9 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
 
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
- * TF_DTYPE_BF16) or e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3);
+ * TF_DTYPE_BF16), e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3), or
+ * 4-bit rows as tf_op_quantize_nvfp4 writes them with row_scale[rows]
+ * (TF_DTYPE_NVFP4, cols a multiple of 256);
  * x, y float32 device vectors.  `repeat` > 1 launches it that many times
  * back to back (each launch with weights W + i * rows * cols elements, so the
  * caller can rotate through distinct matrices) and returns the mean device

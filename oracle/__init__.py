@@ -24,6 +24,7 @@ docstring of the function that implements it.
 """
 from .numerics import (bf16_bits_to_f64, bf16_bits_to_f32, round_to_bf16, e4m3_decode,
                        e4m3_encode_rne, fp8_quantize_rows, fp8_dequant_rows,
+                       e2m1_decode, e2m1_encode_rne, nvfp4_quantize_rows, nvfp4_dequant_rows,
                        rmsnorm, rope_angles, apply_rope, attention_row,
                        causal_attention, silu, linear)
 from .sampler import (philox4x32_10, exp_f32, argmax_lowest, topk_candidates,
@@ -32,7 +33,8 @@ from .model import DualAROracle, load_formula
 
 __all__ = [
     "bf16_bits_to_f64", "bf16_bits_to_f32", "round_to_bf16", "e4m3_decode", "e4m3_encode_rne",
-    "fp8_quantize_rows", "fp8_dequant_rows", "rmsnorm", "rope_angles",
+    "fp8_quantize_rows", "fp8_dequant_rows", "e2m1_decode", "e2m1_encode_rne",
+    "nvfp4_quantize_rows", "nvfp4_dequant_rows", "rmsnorm", "rope_angles",
     "apply_rope", "attention_row", "causal_attention", "silu", "linear", "philox4x32_10", "exp_f32",
     "argmax_lowest", "topk_candidates", "topk_sample", "uniform24",
     "apply_repetition_penalty",

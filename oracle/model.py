@@ -38,6 +38,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 from .numerics import (bf16_bits_to_f64, round_to_bf16, fp8_quantize_rows, fp8_dequant_rows,
+                       nvfp4_quantize_rows, nvfp4_dequant_rows,
                        rmsnorm, apply_rope, attention_row, causal_attention, silu, linear)
 from .sampler import argmax_lowest, apply_repetition_penalty, topk_sample
 
@@ -87,7 +88,8 @@ class DualAROracle:
     weights: name -> bf16 bit patterns (uint16), shapes as synth.tensor_specs.
     weight_format: "bf16", or "fp8" to quantise every linear weight per row
     (fp8_quantize_rows) and use the dequantised values; embeddings and norms
-    stay bf16 (drbaph s2-pro-fp8 model card, "Quantization Details").
+    stay bf16 (drbaph s2-pro-fp8 model card, "Quantization Details"); or
+    "nvfp4" for the block-scaled 4-bit format (nvfp4_quantize_rows).
     batch: number of independent sequences.
     fp8_codes: optional name -> (codes, scale) of fp8_quantize_rows already
     computed for these weights (the quantisation is then not repeated).
@@ -107,13 +109,14 @@ class DualAROracle:
         self.cache_fast = total >= 100_000_000
         self._cache = {}
         self.fp8 = {}
-        if weight_format == "fp8":
+        if weight_format in ("fp8", "nvfp4"):
             names = linear_names(dims)
+            quant = fp8_quantize_rows if weight_format == "fp8" else nvfp4_quantize_rows
             if fp8_codes is not None:
                 self.fp8 = {n: fp8_codes[n] for n in names}
             else:   # one tensor per task; NumPy releases the GIL in its loops
                 with ThreadPoolExecutor(min(32, os.cpu_count() or 1)) as ex:
-                    self.fp8 = dict(zip(names, ex.map(lambda n: fp8_quantize_rows(weights[n]), names)))
+                    self.fp8 = dict(zip(names, ex.map(lambda n: quant(weights[n]), names)))
         elif weight_format != "bf16":
             raise ValueError(weight_format)
         self.reset()
@@ -123,7 +126,7 @@ class DualAROracle:
         if name in self._cache:
             return self._cache[name]
         if name in self.fp8:
-            w = fp8_dequant_rows(*self.fp8[name])
+            w = (fp8_dequant_rows if self.fmt == "fp8" else nvfp4_dequant_rows)(*self.fp8[name])
         else:
             w = bf16_bits_to_f64(self.raw[name])
         if self.cache_f64 or (self.cache_fast and name.startswith("fast.")):

@@ -120,6 +120,87 @@ def fp8_dequant_rows(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return (np.asarray(scale, np.float32)[:, None] * v).astype(np.float32).astype(np.float64)
 
 
+def _e2m1_value(code: int) -> float:
+    """Value of one FP4 E2M1 code (OCP Microscaling formats, FP4 E2M1).
+
+    Bit 3 sign, bits 2..1 exponent with bias 1, bit 0 mantissa.  Exponent
+    field 0 is subnormal (m/2 * 2^0); there are no infinities or NaNs, so the
+    magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+    """
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * (m / 2.0)
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+_E2M1_POS = E2M1_TABLE[:8]
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    """FP4 E2M1 codes (0..15) -> float64 values."""
+    return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def e2m1_encode_rne(x: np.ndarray) -> np.ndarray:
+    """float -> FP4 E2M1 code, round to nearest, ties to the even code
+    (mantissa bit 0); inputs finite with |x| <= 6 (the quantiser clamps)."""
+    x = np.asarray(x, dtype=np.float64)
+    if np.any(~np.isfinite(x)) or np.any(np.abs(x) > 6.0):
+        raise ValueError("e2m1_encode_rne: input outside [-6, 6]")
+    a = np.abs(x)
+    hi = np.minimum(np.searchsorted(_E2M1_POS, a, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E2M1_POS[hi] - a
+    d_lo = a - _E2M1_POS[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(a == _E2M1_POS[hi], hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    return (code | np.where(np.signbit(x), 0x8, 0).astype(np.uint8)).astype(np.uint8)
+
+
+def nvfp4_quantize_rows(w_bits: np.ndarray):
+    """Block-scaled 4-bit quantisation of one [out][in] bf16 weight.
+
+    The tuna-fish README lists nvfp4 among its weight formats (intro list,
+    "Support int8/fp8/int4/nvfp4 quantization"; memory table) without the
+    details.  Reading, after NVIDIA's NVFP4 layout: FP4 E2M1 elements, one
+    E4M3 scale per 16 consecutive elements of a row, and a float32 scale per
+    output row (where NVFP4 keeps one per tensor; per row follows the fp8
+    model card).  All in float32, in this order:
+      s_row = amax(row) / (6 * 448)            (1 for an all-zero row)
+      s_b   = e4m3_RNE(min(amax(block) / f32(6 * s_row), 448))
+      code  = e2m1_RNE(clamp(w / f32(value(s_b) * s_row), -6, 6))   (0 if s_b = 0)
+    Returns (codes uint8 [out][in/16][16] (one code per byte), block scales
+    uint8 [out][in/16], row scales float32 [out]).
+    """
+    w = bf16_bits_to_f32(w_bits)
+    rows, cols = w.shape
+    blocks = w.reshape(rows, cols // 16, 16)
+    F = np.float32
+    amax = np.max(np.abs(w), axis=1).astype(F)
+    s_row = np.where(amax == 0, F(1.0), (amax / F(6.0 * 448.0)).astype(F)).astype(F)
+    denom = (F(6.0) * s_row).astype(F)
+    bs = (np.max(np.abs(blocks), axis=2).astype(F) / denom[:, None]).astype(F)
+    bs = np.minimum(bs, F(448.0))
+    sb = e4m3_encode_rne(bs)
+    d = (e4m3_decode(sb).astype(F) * s_row[:, None]).astype(F)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (blocks / d[:, :, None]).astype(F)
+    q = np.where(d[:, :, None] == 0, F(0.0), q)
+    q = np.clip(q, F(-6.0), F(6.0))
+    return e2m1_encode_rne(q), sb, s_row
+
+
+def nvfp4_dequant_rows(codes: np.ndarray, sb: np.ndarray, s_row: np.ndarray) -> np.ndarray:
+    """Dequantised weight = float32(e2m1 * e4m3(s_b) * s_row) as float64 [out][in]
+    (e2m1 * e4m3 is exact, so the one rounding is the row scale's)."""
+    v = e2m1_decode(codes) * e4m3_decode(sb)[:, :, None]
+    out = (v.astype(np.float32) * np.asarray(s_row, np.float32)[:, None, None]).astype(np.float32)
+    return out.reshape(codes.shape[0], -1).astype(np.float64)
+
+
 # --------------------------------------------------------------------------
 # Transformer pieces
 # --------------------------------------------------------------------------

@@ -95,7 +95,8 @@ class Workload:
     """A named decode workload: model, weight format and schedule."""
     name: str
     dims: ModelDims
-    weight_dtype: str          # "bf16" or "fp8"  (fp8 = e4m3 + per-row fp32 scale)
+    weight_dtype: str          # "bf16", "fp8" (e4m3 + per-row fp32 scale) or "nvfp4"
+                               # (e2m1 + e4m3 per 16 elements + per-row fp32 scale)
     batch: int
     prefill: int
     decode: int
@@ -110,6 +111,8 @@ WORKLOADS = {
                           FULL, "bf16", 1, 128, 896),
     "full_fp8": Workload("full-size fp8 per-row, prefill 128 + decode 896 (T=1024)",
                          FULL, "fp8", 1, 128, 896),
+    "full_nvfp4": Workload("full-size 4-bit block-scaled, prefill 128 + decode 896 (T=1024)",
+                           FULL, "nvfp4", 1, 128, 896),
     "full_prefill_heavy": Workload(
         "full-size bf16, prefill 1024 + decode 64 (T=2048)",
         FULL.replace(max_seq_len=2048), "bf16", 1, 1024, 64),

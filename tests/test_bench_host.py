@@ -14,32 +14,32 @@ import bench
 from synth import FULL, TINY, tensor_specs
 
 
-def _frame_weight_bytes_from_specs(d, eb_linear):
+def _frame_weight_bytes_from_specs(d, fmt):
     """Weights one decode frame reads, summed from the model's tensor list:
     every slow tensor but the text embedding, plus its semantic slice and one
     embedding row; nine passes over the fast tensors but the codebook tables,
-    plus one codebook row each."""
+    plus one codebook row each.  Quantised linears: bytes per element (1 for
+    e4m3, 1/2 + 1/16 for 4-bit codes and block scales) plus 4 per row."""
+    per = {"bf16": 2.0, "fp8": 1.0, "nvfp4": 0.5 + 1.0 / 16}[fmt]
     slow = fast = 0
     for name, shape, kind in tensor_specs(d):
         n = int(np.prod(shape))
-        eb = eb_linear if kind == "linear" else 2
+        nbytes = n * per + (shape[0] * 4 if fmt != "bf16" else 0) if kind == "linear" else n * 2
         if name.startswith("slow."):
-            slow += n * eb
+            slow += nbytes
         elif name == "fast.cb_embed":
             fast += d.hidden * 2
         elif name.startswith("fast."):
-            fast += n * eb + (shape[0] * 4 if kind == "linear" and eb_linear == 1 else 0)
-        if name.startswith("slow.") and kind == "linear" and eb_linear == 1:
-            slow += shape[0] * 4
+            fast += nbytes
     slow += d.semantic_vocab * d.hidden * 2 + d.hidden * 2
     return slow + (d.n_codebooks - 1) * fast
 
 
 @pytest.mark.parametrize("d", [TINY, FULL])
-@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("fmt", ["bf16", "fp8", "nvfp4"])
 def test_frame_weight_bytes_match_the_tensor_list(d, fmt):
     fb = bench.frame_bytes(d, fmt, 10)
-    assert fb["weights"] == _frame_weight_bytes_from_specs(d, 1 if fmt == "fp8" else 2)
+    assert fb["weights"] == _frame_weight_bytes_from_specs(d, fmt)
 
 
 def test_frame_bytes_full_size_total_and_batch_scaling():

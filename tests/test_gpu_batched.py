@@ -91,7 +91,8 @@ TINY_OPTS = TINY.replace(qk_norm=True, qk_norm_fast=True, slow_cb_sum=True, code
                                               (TINY_ODD, "bf16", BF16_TOL, 5, 12),
                                               (TINY_G8, "bf16", BF16_TOL, 4, 40),
                                               (TINY, "bf16", BF16_TOL, 32, 8),
-                                              (TINY_OPTS, "bf16", BF16_TOL, 3, 40)])
+                                              (TINY_OPTS, "bf16", BF16_TOL, 3, 40),
+                                              (TINY, "nvfp4", FP8_TOL, 4, 16)])
 def test_tiny_batched_teacher_forced(dims, fmt, tol, B, P):
     """B sequences with their own prompts; P = 40 reaches the split
     attention path (more than 32 keys) with one ticket per row."""

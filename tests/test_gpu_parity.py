@@ -11,8 +11,8 @@ import torch
 
 import oracle
 from dual_ar_decode_gb300 import (Decoder, TfError, op_attention, op_gemm, op_gemv,
-                                  op_quantize_fp8, op_select)
-from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3
+                                  op_quantize_fp8, op_quantize_nvfp4, op_select)
+from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3, TF_DTYPE_NVFP4
 from synth import FULL, TINY, make_logits, make_prompt, make_weights, f32_to_bf16_bits
 
 from gpu_helpers import BF16_TOL, FP8_TOL, TeacherForced
@@ -48,6 +48,77 @@ def test_quantize_fp8_bit_exact(rows, cols):
     rc, rs = oracle.fp8_quantize_rows(w)
     assert np.array_equal(codes.cpu().numpy(), rc)
     assert np.array_equal(scale.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+def nvfp4_pack(codes, sb):
+    """Oracle codes [rows][blocks][16] and block scales -> the stored rows:
+    two codes per byte (even element in the low nibble), then the scales."""
+    c = codes.reshape(codes.shape[0], -1)
+    return np.concatenate([(c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8), sb], axis=1)
+
+
+@pytest.mark.parametrize("rows,cols", [(37, 2560), (5, 256), (64, 9728), (3, 512)])
+def test_quantize_nvfp4_bit_exact(rows, cols):
+    rng = np.random.default_rng(rows * 5 + cols)
+    w = f32_to_bf16_bits(rng.standard_normal((rows, cols)).astype(np.float32) * 0.02)
+    w[0] = 0                                                      # all-zero row
+    w[1, 16:32] = 0                                               # all-zero block
+    w[2, 7] = f32_to_bf16_bits(np.array([4.0], np.float32))[0]    # an outlier
+    w[min(3, rows - 1), 40:48] = f32_to_bf16_bits(np.array([1e-6], np.float32))[0]  # tiny values
+    wd = dev_u16(w)
+    packed = torch.empty((rows, cols // 2 + cols // 16), dtype=torch.uint8, device=DEV)
+    scale = torch.empty(rows, dtype=torch.float32, device=DEV)
+    op_quantize_nvfp4(wd.data_ptr(), rows, cols, packed.data_ptr(), scale.data_ptr())
+    codes, sb, sr = oracle.nvfp4_quantize_rows(w)
+    assert np.array_equal(packed.cpu().numpy(), nvfp4_pack(codes, sb))
+    assert np.array_equal(scale.cpu().numpy().view(np.uint32), sr.view(np.uint32))
+
+
+def test_nvfp4_gemv_decodes_every_code_and_block_scale():
+    """Every e2m1 code under block scales 2^-9 (the smallest subnormal e4m3),
+    1, 2 and 448: row r holds one code in element 0 of its first block (zeros
+    elsewhere) and x[0] = 1, so y[r] is exactly e2m1 * e4m3 * s_row."""
+    cols = 256
+    combos = [(c, b) for b in (0x01, 0x38, 0x40, 0x7E) for c in range(16)]
+    rows = len(combos)
+    codes = np.zeros((rows, cols // 16, 16), np.uint8)
+    sb = np.full((rows, cols // 16), 0x38, np.uint8)
+    for r, (c, b) in enumerate(combos):
+        codes[r, 0, 0] = c
+        sb[r, 0] = b
+    sr = np.full(rows, 0.25, np.float32)
+    x = np.random.default_rng(3).standard_normal(cols).astype(np.float32)
+    x[0] = 1.0
+    Wd = torch.from_numpy(nvfp4_pack(codes, sb)).to(DEV)
+    sd = torch.from_numpy(sr).to(DEV)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.full((rows,), np.nan, dtype=torch.float32, device=DEV)
+    op_gemv(Wd.data_ptr(), TF_DTYPE_NVFP4, sd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr())
+    want = np.array([oracle.e2m1_decode(np.array([c]))[0] * oracle.e4m3_decode(np.array([b]))[0] * 0.25
+                     for c, b in combos])
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), want)
+
+
+@pytest.mark.parametrize("rows,cols", [(6144, 2560), (2560, 9728), (33, 256)])
+def test_nvfp4_gemv_matches_oracle_linear(rows, cols):
+    rng = np.random.default_rng(rows + 3 * cols)
+    w = f32_to_bf16_bits(rng.standard_normal((rows, cols)).astype(np.float32) * 0.02)
+    x = rng.standard_normal(cols).astype(np.float32)
+    codes, sb, sr = oracle.nvfp4_quantize_rows(w)
+    Wd = torch.from_numpy(nvfp4_pack(codes, sb)).to(DEV)
+    sd = torch.from_numpy(sr).to(DEV)
+    xd = torch.from_numpy(x).to(DEV)
+    y = torch.zeros(rows, dtype=torch.float32, device=DEV)
+    op_gemv(Wd.data_ptr(), TF_DTYPE_NVFP4, sd.data_ptr(), rows, cols, xd.data_ptr(), y.data_ptr())
+    Wf = oracle.nvfp4_dequant_rows(codes, sb, sr)
+    ref = oracle.linear(Wf, x.astype(np.float64))
+    got = y.cpu().numpy().astype(np.float64)
+    # exact e2m1 x block-scale products with f16 activations (<= 2^-11 each),
+    # float32 sums (<= K 2^-24), and the row scale applied once at the end
+    # (where the oracle rounds each weight: <= 2^-24 relative per weight)
+    absdot = np.abs(Wf) @ np.abs(x.astype(np.float64))
+    assert np.all(np.abs(got - ref) <= (2.0 ** -11 + cols * 2.0 ** -24 + 2.0 ** -23) * absdot)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-3
 
 
 @pytest.mark.parametrize("vocab", [64, 4096, 1000])
@@ -239,6 +310,7 @@ TINY_SMALL_CB = TINY.replace(qk_norm=True, codebook_size=16)
                                           (TINY_ODD, "bf16", BF16_TOL), (TINY_G8, "bf16", BF16_TOL),
                                           (TINY_OPTS, "bf16", BF16_TOL), (TINY_OPTS, "fp8", FP8_TOL),
                                           (TINY_SMALL_CB, "bf16", BF16_TOL),
+                                          (TINY, "nvfp4", FP8_TOL), (TINY_OPTS, "nvfp4", FP8_TOL),
                                           (TINY_G8.replace(qk_norm=True, qk_norm_fast=True,
                                                            slow_cb_sum=True), "bf16", BF16_TOL)])
 def test_tiny_teacher_forced(dims, fmt, tol):
@@ -354,12 +426,12 @@ def full_fp8_codes(full_weights):
     return oracle.DualAROracle(FULL, full_weights, "fp8").fp8
 
 
-@pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL)])
+@pytest.mark.parametrize("fmt,tol", [("bf16", BF16_TOL), ("fp8", FP8_TOL), ("nvfp4", FP8_TOL)])
 def test_full_size_teacher_forced_sampled_frames(full_weights, full_fp8_codes, fmt, tol):
     """Full-size model (36+4 layers, hidden 2560), prefill 128 then 2 decode
     frames, in the launch configuration the benchmark times."""
     tf = TeacherForced(FULL, fmt, weights=full_weights,
-                       fp8_codes=full_fp8_codes if fmt == "fp8" else None)
+                       fp8_codes=full_fp8_codes if fmt == "fp8" else None)   # 4-bit: quantised here
     tf.prefill(make_prompt(FULL, 128, seed=0))
     tf.decode()
     tf.decode()

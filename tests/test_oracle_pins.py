@@ -114,6 +114,64 @@ def test_fp8_row_quantiser_bounds_and_definition():
 
 # ----------------------------------------------------------------- pieces
 
+def test_e2m1_codes_equal_their_e4m3_rebiasing_under_torch():
+    """FP4 E2M1 (bias 1) and FP8 E4M3 (bias 7) share the IEEE layout, so a
+    normal e2m1 code (s, e, m) is the e4m3 code (s, e + 6, m << 2) and the
+    subnormal 0.5 is 2^-1 = e4m3 (s, 6, 0); torch's float8_e4m3fn decodes
+    those e4m3 codes, pinning every e2m1 value."""
+    for c in range(16):
+        s_, e, m = c >> 3, (c >> 1) & 3, c & 1
+        if e == 0:
+            e8 = (s_ << 7) | ((6 << 3) if m else 0)
+        else:
+            e8 = (s_ << 7) | ((e + 6) << 3) | (m << 2)
+        want = torch.tensor([e8], dtype=torch.uint8).view(torch.float8_e4m3fn).float().item()
+        assert oracle.e2m1_decode(np.array([c]))[0] == want, c
+
+
+def test_e2m1_encode_round_trip_and_ties():
+    codes = np.arange(16, dtype=np.uint8)
+    vals = oracle.e2m1_decode(codes)
+    back = oracle.e2m1_encode_rne(vals)
+    assert np.array_equal(oracle.e2m1_decode(back), vals)          # -0 and +0 alike
+    # midpoints go to the neighbour with an even code (mantissa bit 0)
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    assert oracle.e2m1_decode(oracle.e2m1_encode_rne(mids)).tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]
+    assert oracle.e2m1_decode(oracle.e2m1_encode_rne(-mids)).tolist() == [-0.0, -1.0, -1.0, -2.0, -2.0,
+                                                                        -4.0, -4.0]
+    # off the midpoints: the nearest value
+    x = np.linspace(-6, 6, 2001)
+    got = oracle.e2m1_decode(oracle.e2m1_encode_rne(x))
+    dist = np.abs(oracle.e2m1_decode(np.arange(16))[None, :] - x[:, None]).min(axis=1)
+    assert np.allclose(np.abs(got - x), dist)
+
+
+def test_nvfp4_quantiser_bounds_and_structure():
+    rng = np.random.default_rng(4)
+    w = f32_to_bf16_bits(rng.standard_normal((24, 256)).astype(np.float32) * 0.02)
+    w[0] = 0                                            # all-zero row
+    w[1, :16] = 0                                       # all-zero block
+    w[2, 5] = f32_to_bf16_bits(np.array([3.0], np.float32))[0]   # an outlier
+    codes, sb, sr = oracle.nvfp4_quantize_rows(w)
+    wf = oracle.bf16_bits_to_f64(w)
+    deq = oracle.nvfp4_dequant_rows(codes, sb, sr)
+    assert sr[0] == 1.0 and not codes[0].any() and not sb[0].any()
+    assert not sb[1, 0] and not codes[1, 0].any()
+    # the row scale maps the row maximum to 6 * 448
+    amax = np.abs(oracle.bf16_bits_to_f32(w[2:])).max(axis=1)
+    assert np.array_equal(sr[2:], (amax / np.float32(2688.0)).astype(np.float32))
+    # every element within one e2m1 step of its block (value(s_b) * s_row)
+    step = oracle.e4m3_decode(sb) * sr[:, None].astype(np.float64)
+    err = np.abs(deq - wf).reshape(24, 16, 16)
+    assert np.all(err <= step[:, :, None] * (1 + 1e-6) + 1e-30)
+    # a normal block scale puts the block's largest element at +-6
+    mags = (codes & 7).reshape(24, 16, 16)
+    bmax = np.abs(wf.reshape(24, 16, 16)).argmax(axis=2)
+    normal = oracle.e4m3_decode(sb) >= 2.0 ** -6
+    top = np.take_along_axis(mags, bmax[:, :, None], axis=2)[:, :, 0]
+    assert np.all(top[normal] == 7)
+
+
 def test_linear_matches_torch_nonsquare():
     rng = np.random.default_rng(5)
     w = rng.standard_normal((7, 13))

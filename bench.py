@@ -308,12 +308,12 @@ def main():
 
     # warm-up: prefill + W frames (captures the frame graph)
     dec.prefill(prompt, sampling)
-    dec.decode_frames(min(args.warmup, d.max_seq_len - wl.prefill), sampling)
+    dec.decode_frames(min(args.warmup, wl.decode, d.max_seq_len - wl.prefill), sampling)
 
     # Timed frames are spread evenly over the decode schedule (positions
     # prefill .. max_seq_len - 1): segment i starts at plan[i][0], reached by
     # untimed decoding after an untimed prefill, and times plan[i][1] frames.
-    cap = d.max_seq_len - wl.prefill
+    cap = min(wl.decode, d.max_seq_len - wl.prefill)   # frames of the workload's schedule
     plan = schedule_plan(wl.prefill, cap, args.steps)
     total_ms = 0.0
     clocks = ClockSampler(local)

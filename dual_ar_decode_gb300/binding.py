@@ -14,7 +14,7 @@ STATUS = {0: "TF_OK", 1: "TF_E_INVAL", 2: "TF_E_NOMEM", 3: "TF_E_CUDA", 4: "TF_E
           5: "TF_E_CAPACITY", 6: "TF_E_TIMEOUT", 7: "TF_E_NUMERIC"}
 TF_WEIGHT_BF16, TF_WEIGHT_FP8, TF_WEIGHT_NVFP4 = 0, 1, 2
 TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3, TF_DTYPE_NVFP4 = 0, 1, 2
-TF_FLAG_QK_NORM, TF_FLAG_QK_NORM_FAST, TF_FLAG_SLOW_CB_SUM = 1, 2, 4
+TF_FLAG_QK_NORM, TF_FLAG_QK_NORM_FAST, TF_FLAG_SLOW_CB_SUM, TF_FLAG_PAGED_KV = 1, 2, 4, 8
 
 
 class TfConfig(ctypes.Structure):
@@ -63,6 +63,8 @@ EXPORTS = {
     "tf_profile_kernel": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_int64)]),
+    "tf_prefill_seq": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32]),
+    "tf_release_seq": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "tf_test_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "tf_test_fail_alloc": (None, [ctypes.c_int32]),
     "tf_op_quantize_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
@@ -157,9 +159,12 @@ def _ptr(a):
 class Decoder:
     """One decode context (tf_create ... tf_destroy)."""
 
-    def __init__(self, dims, weight_dtype: str = "bf16", device: int = 0, max_batch: int = 1):
+    def __init__(self, dims, weight_dtype: str = "bf16", device: int = 0, max_batch: int = 1,
+                 paged: bool = False):
         self.dims = dims
         self.cfg = config_from_dims(dims, weight_dtype, max_batch)
+        if paged:
+            self.cfg.flags |= TF_FLAG_PAGED_KV
         self.batch = 1  # sequences of the last prefill
         h = ctypes.c_void_p()
         _check(lib().tf_create(ctypes.byref(self.cfg), device, ctypes.byref(h)), None)
@@ -210,7 +215,22 @@ class Decoder:
         _check(lib().tf_prefill(self.h, _ptr(tok), tok.shape[0], tok.shape[1], ctypes.byref(s),
                                 _ptr(fo), _ptr(frame), _ptr(lg)), self.h)
         self.batch = tok.shape[0]
+        self.active = set(range(tok.shape[0]))
         return frame, lg
+
+    def prefill_seq(self, slot: int, tokens):
+        """Start a sequence in `slot` (continuous batching); its frame 0 comes
+        from the next decode call.  The batch becomes the slots up to the last
+        active one."""
+        tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+        _check(lib().tf_prefill_seq(self.h, slot, _ptr(tok), tok.size), self.h)
+        self.active = getattr(self, "active", set()) | {slot}
+        self.batch = max(self.active) + 1
+
+    def release_seq(self, slot: int):
+        _check(lib().tf_release_seq(self.h, slot), self.h)
+        self.active = getattr(self, "active", set()) - {slot}
+        self.batch = max(self.active) + 1 if self.active else 1
 
     def decode_frame(self, sampling=None, forced=None, logits=False):
         B = self.batch

@@ -6,15 +6,28 @@
 
 namespace tf {
 
-// Position of activation row m: rows are grouped by sequence (p.rps rows
-// each, consecutive positions from the shared base) or all belong to one.
-__device__ __forceinline__ int row_pos(const GemvParams& p, int m) {
-  return (p.pos_ptr ? __ldg(p.pos_ptr) : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
+// Sequence of activation row m: rows are grouped by sequence (p.rps rows
+// each) from sequence seq_base, or all belong to sequence seq_base.
+__device__ __forceinline__ int row_seq(const GemvParams& p, int m) {
+  return p.seq_base + (p.rps > 0 ? m / p.rps : 0);
 }
 
-// Offset of row m's sequence in the KV caches.
-__device__ __forceinline__ size_t row_kv_offset(const GemvParams& p, int m) {
-  return p.rps > 0 ? static_cast<size_t>(m / p.rps) * static_cast<size_t>(p.kv_seq) : 0;
+// Position of activation row m: its sequence's position plus its index among
+// the sequence's rows, or pos_fixed plus the row index.
+__device__ __forceinline__ int row_pos(const GemvParams& p, int m) {
+  return (p.pos_ptr ? __ldg(p.pos_ptr + row_seq(p, m)) : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
+}
+
+// Element offset of the cached K (or V) row of (sequence, KV head g,
+// position): dense caches [sequence][Hkv][T][D], or pages
+// [page][Hkv][kKvPage][D] found in the block table.
+__device__ __forceinline__ size_t kv_index(const int32_t* tbl, int npp, int hkv, int T, int64_t kv_seq,
+                                           int seq, int g, int pos, int D) {
+  if (tbl) {
+    const int page = __ldg(tbl + (size_t)seq * npp + pos / kKvPage);
+    return (((size_t)page * hkv + g) * kKvPage + pos % kKvPage) * D;
+  }
+  return (size_t)seq * (size_t)kv_seq + ((size_t)g * T + pos) * D;
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -87,14 +100,16 @@ __device__ __forceinline__ void epi_qkv_pair_at(const GemvParams& p, int m, int 
       q[i] = r0;
       q[i + half] = r1;
     } else {
-      uint16_t* k = p.Kc + row_kv_offset(p, m) + ((size_t)h * p.T + pos) * p.head_dim;
+      uint16_t* k = p.Kc + kv_index(p.kv_tbl, p.kv_npp, p.kv_dim / p.head_dim, p.T, p.kv_seq,
+                                    row_seq(p, m), h, pos, p.head_dim);
       k[i] = f32_to_bf16(r0);
       k[i + half] = f32_to_bf16(r1);
     }
   } else {
     const int d0 = 2 * (pair - qp - kp);
     const int g = d0 / p.head_dim, d = d0 - g * p.head_dim;
-    uint16_t* v = p.Vc + row_kv_offset(p, m) + ((size_t)g * p.T + pos) * p.head_dim + d;
+    uint16_t* v = p.Vc + kv_index(p.kv_tbl, p.kv_npp, p.kv_dim / p.head_dim, p.T, p.kv_seq, row_seq(p, m),
+                                  g, pos, p.head_dim) + d;
     v[0] = f32_to_bf16(v0);
     v[1] = f32_to_bf16(v1);
   }

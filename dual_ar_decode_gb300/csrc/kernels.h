@@ -62,9 +62,13 @@ struct GemvParams {
   const int32_t* pos_ptr;  // row m sits at position pos_ptr[0] + m, or
   int32_t pos_fixed;       // pos_fixed + m when pos_ptr is null
   int32_t rps;           // rows per sequence: > 0 -> row m is row m % rps of
-                         // sequence m / rps (position base + m % rps, KV cache
-                         // Kc/Vc + (m / rps) * kv_seq); 0 -> one sequence
-  int64_t kv_seq;        // elements between two sequences' caches
+                         // sequence seq_base + m / rps (position pos_ptr[seq] +
+                         // m % rps); 0 -> every row belongs to sequence seq_base
+  int32_t seq_base;
+  int64_t kv_seq;        // elements between two sequences' caches (dense caches)
+  const int32_t* kv_tbl; // paged caches: page of (sequence, position / kKvPage) at
+  int32_t kv_npp;        // kv_tbl[seq * kv_npp + position / kKvPage]; null: dense
+  int32_t pos_uniform;   // every sequence sits at the same position (lockstep)
   const float2* rope;    // [T][head_dim/2] (cos, sin)
   // EPI_LOGITS
   int32_t select;        // 1: argmax -> sel[cb], fb[cb]
@@ -109,6 +113,9 @@ struct GemvParams {
 // at the row's position, q stored to qout and k appended to the KV cache.
 cudaError_t launch_qknorm(const GemvParams& p, int M, bool pdl, cudaStream_t s);
 constexpr int kSsqRows = 64;   // row stride of the partial sums of squares
+// Paged KV caches: a page holds kKvPage positions of every KV head of one
+// layer, laid out [page][Hkv][kKvPage][D]; page 0 is a scratch page.
+constexpr int kKvPage = 32;
 
 // Shared memory bytes a launch with these params needs.
 size_t gemv_smem_bytes(const GemvParams& p, int M);
@@ -127,13 +134,16 @@ cudaError_t gemv_set_attributes();
 // ----------------------------------------------------------------- attention
 struct AttnParams {
   const float* q;        // [M][Hq*D] rotated queries
-  const uint16_t* Kc;    // [Hkv][T][D]
+  const uint16_t* Kc;    // [Hkv][T][D] per sequence, or the page pool
   const uint16_t* Vc;
   int32_t T, Hq, Hkv, D;
-  const int32_t* pos_ptr;
+  const int32_t* pos_ptr;  // per-sequence positions, or null: pos_fixed
   int32_t pos_fixed;
   int32_t rps;           // rows per sequence (as GemvParams::rps)
-  int64_t kv_seq;        // elements between two sequences' caches
+  int32_t seq_base;
+  int64_t kv_seq;        // elements between two sequences' caches (dense)
+  const int32_t* kv_tbl; // paged caches (as GemvParams::kv_tbl)
+  int32_t kv_npp;
   int32_t S;             // splits over the key range (grid.x)
   float* part;           // [M][Hq][S][D + 2] partial (m, l, acc)
   uint32_t* counters;    // [M][Hkv], zero between launches
@@ -157,6 +167,11 @@ enum BuildMode : int32_t {
 };
 struct BuildParams {
   int32_t mode, j, H, M;
+  // BUILD_SLOW: a sequence with pending[b] >= 0 still has that prompt id to
+  // feed (it joined with its prompt pass done but for its last id): its row
+  // is text_embed[pending[b]] (table + 0, text_rows ids) instead
+  const int32_t* pending;
+  int32_t text_rows;
   const uint16_t* table;   // embedding table base (text_embed or cb_embed[j-1])
   int32_t table_rows;      // rows the id may address
   int32_t row_base;        // added to the id (sem_base for BUILD_SLOW)
@@ -183,9 +198,11 @@ cudaError_t launch_build(const BuildParams& p, bool pdl, cudaStream_t s);
 // Per-frame bookkeeping after the last codebook: pos += advance,
 // frame_index += 1, history[hist_idx++] = sel of every sequence.
 struct FrameEndParams {
-  int32_t* pos;
+  int32_t* pos;          // per sequence
   int32_t advance;
-  int32_t* frame_index;
+  int32_t* frame_index;  // per sequence
+  const int32_t* active; // null: every sequence; else only those with active[b]
+  int32_t* pending;      // null, or cleared to -1 for the sequences that advance
   const int32_t* sel;    // sequence b's ids at sel[b * sel_stride]
   int32_t sel_stride;
   int32_t nseq;          // history row = [nseq][ncb]
@@ -209,7 +226,7 @@ struct SelectParams {
   int32_t top_k;
   float temperature;
   uint32_t key0, key1;   // Philox key (seed low / high)
-  const int32_t* frame_ptr;  // frame index from device (or null -> frame)
+  const int32_t* frame_ptr;  // per-sequence frame indices on the device (or null -> frame)
   int32_t frame;
   int32_t codebook0;     // row i uses codebook0 + i (seq_rows = 0)
   int32_t sequence;

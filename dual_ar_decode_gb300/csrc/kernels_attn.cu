@@ -94,20 +94,24 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnParams p) {
 
   pdl_launch_dependents();
   pdl_wait();
-  // Row m is row m % rps of sequence m / rps (rps = 0: one sequence).
-  const int pos = (p.pos_ptr ? p.pos_ptr[0] : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
-  const size_t kvo = p.rps > 0 ? static_cast<size_t>(m / p.rps) * static_cast<size_t>(p.kv_seq) : 0;
+  // Row m is row m % rps of sequence seq_base + m / rps (rps = 0: every row
+  // belongs to sequence seq_base).
+  const int seq = p.seq_base + (p.rps > 0 ? m / p.rps : 0);
+  const int pos = (p.pos_ptr ? p.pos_ptr[seq] : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
   if (pos < 0 || pos >= p.T) {
     if (tid == 0 && s == 0) atomicOr(p.err, ERR_BAD_POS);
     return;
   }
   const int n = pos + 1;
-  // At least kMinKeys keys per slice: short contexts use fewer CTAs.
-  const int L = max((n + p.S - 1) / p.S, kMinKeys);
+  // At least kMinKeys keys per slice: short contexts use fewer CTAs.  Paged
+  // caches: slices start on page boundaries, so a 64-key chunk is two pages.
+  int L = max((n + p.S - 1) / p.S, kMinKeys);
+  if (p.kv_tbl) L = (L + kKvPage - 1) / kKvPage * kKvPage;
   const int sact = (n + L - 1) / L;
   if (s >= sact) return;
   const int k0 = s * L, nk = min(n, k0 + L) - k0;
   const int nch = (nk + kChunk - 1) / kChunk;
+  const size_t kvo = (size_t)seq * (size_t)p.kv_seq;
   const uint16_t* Kg = p.Kc + kvo + ((size_t)g * p.T + k0) * D;
   const uint16_t* Vg = p.Vc + kvo + ((size_t)g * p.T + k0) * D;
 
@@ -116,9 +120,21 @@ __global__ void __launch_bounds__(kThreads) k_attn(const AttnParams p) {
     const int rows = min(kChunk, nk - ch * kChunk);
     const uint32_t bytes = static_cast<uint32_t>(rows * SL::kRow);
     mbar_arrive_expect_tx(&bar[b], 2 * bytes);
-    bulk_g2s_plain(kv + (size_t)(2 * b) * kChunk * D, Kg + (size_t)ch * kChunk * D, bytes, &bar[b]);
-    bulk_g2s_plain(kv + (size_t)(2 * b + 1) * kChunk * D, Vg + (size_t)ch * kChunk * D, bytes,
-                   &bar[b]);
+    uint16_t* kd = kv + (size_t)(2 * b) * kChunk * D;
+    uint16_t* vd = kv + (size_t)(2 * b + 1) * kChunk * D;
+    if (p.kv_tbl) {  // one copy per page run of the chunk
+      for (int r0 = 0; r0 < rows; r0 += kKvPage) {
+        const int kpos = k0 + ch * kChunk + r0;
+        const int page = p.kv_tbl[(size_t)seq * p.kv_npp + kpos / kKvPage];
+        const size_t src = (((size_t)page * p.Hkv + g) * kKvPage) * D;
+        const uint32_t rb = static_cast<uint32_t>(min(kKvPage, rows - r0) * SL::kRow);
+        bulk_g2s_plain(kd + (size_t)r0 * D, p.Kc + src, rb, &bar[b]);
+        bulk_g2s_plain(vd + (size_t)r0 * D, p.Vc + src, rb, &bar[b]);
+      }
+    } else {
+      bulk_g2s_plain(kd, Kg + (size_t)ch * kChunk * D, bytes, &bar[b]);
+      bulk_g2s_plain(vd, Vg + (size_t)ch * kChunk * D, bytes, &bar[b]);
+    }
   };
   if (tid == 0) {
     mbar_init(&bar[0], 1);
@@ -349,9 +365,11 @@ __global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p
 
   pdl_launch_dependents();
   pdl_wait();
-  // Row m is row m % rps of sequence m / rps (rps = 0: one sequence).
-  const int pos = (p.pos_ptr ? p.pos_ptr[0] : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
-  const size_t kvo = p.rps > 0 ? static_cast<size_t>(m / p.rps) * static_cast<size_t>(p.kv_seq) : 0;
+  // Row m is row m % rps of sequence seq_base + m / rps (rps = 0: every row
+  // belongs to sequence seq_base).
+  const int seq = p.seq_base + (p.rps > 0 ? m / p.rps : 0);
+  const int pos = (p.pos_ptr ? p.pos_ptr[seq] : p.pos_fixed) + (p.rps > 0 ? m % p.rps : m);
+  const size_t kvo = (size_t)seq * (size_t)p.kv_seq;
   if (pos < 0 || pos >= p.T) {
     if (tid == 0 && s == 0) atomicOr(p.err, ERR_BAD_POS);
     return;
@@ -382,8 +400,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p
     for (int d = 0; d < DL; ++d) acc[h][d] = 0.f;
   }
 
-  const uint16_t* Kg = p.Kc + kvo + (size_t)g * p.T * D + lane * DL;
-  const uint16_t* Vg = p.Vc + kvo + (size_t)g * p.T * D + lane * DL;
+  const uint16_t* Kg = p.Kc + lane * DL;
+  const uint16_t* Vg = p.Vc + lane * DL;
+  // element offset of key t's row in the caches: dense, or through the block table
+  auto key_off = [&](int t) -> size_t {
+    if (!p.kv_tbl) return kvo + ((size_t)g * p.T + t) * D;
+    const int page = __ldg(p.kv_tbl + (size_t)seq * p.kv_npp + t / kKvPage);
+    return (((size_t)page * p.Hkv + g) * kKvPage + t % kKvPage) * D;
+  };
   for (int t0 = k0 + warp * kRowUnroll; t0 < k1; t0 += kRowWarps * kRowUnroll) {
     // Load up to kRowUnroll rows of K and V (DL bf16 per lane).
     uint32_t kr[kRowUnroll][DL / 2], vr[kRowUnroll][DL / 2];
@@ -391,14 +415,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p
     for (int u = 0; u < kRowUnroll; ++u) {
       const int t = t0 + u;
       if (t < k1) {
+        const size_t o = key_off(t);
         if constexpr (DL == 4) {
-          const uint2 kk = *reinterpret_cast<const uint2*>(Kg + (size_t)t * D);
-          const uint2 vv = *reinterpret_cast<const uint2*>(Vg + (size_t)t * D);
+          const uint2 kk = *reinterpret_cast<const uint2*>(Kg + o);
+          const uint2 vv = *reinterpret_cast<const uint2*>(Vg + o);
           kr[u][0] = kk.x; kr[u][1] = kk.y;
           vr[u][0] = vv.x; vr[u][1] = vv.y;
         } else {
-          kr[u][0] = *reinterpret_cast<const uint32_t*>(Kg + (size_t)t * D);
-          vr[u][0] = *reinterpret_cast<const uint32_t*>(Vg + (size_t)t * D);
+          kr[u][0] = *reinterpret_cast<const uint32_t*>(Kg + o);
+          vr[u][0] = *reinterpret_cast<const uint32_t*>(Vg + o);
         }
       }
     }

@@ -90,6 +90,14 @@ __global__ void __launch_bounds__(256) k_build(const BuildParams p) {
   } else {
     id = p.ids[(size_t)m * p.id_stride];
   }
+  const int pend = (p.mode == BUILD_SLOW && p.pending) ? p.pending[m] : -1;
+  if (pend >= 0) {  // the sequence's last prompt id, a text token
+    const uint16_t* row = p.table + (size_t)(pend < p.text_rows ? pend : 0) * p.H;
+    if (pend >= p.text_rows && tid == 0) atomicOr(p.err, ERR_BAD_ID);
+    for (int k = tid; k < p.H; k += blockDim.x) xo[k] = bf16_to_f32(row[k]);
+    if (p.nx_hi) build_norm_out(p, m, xo, red);
+    return;
+  }
   if (id < 0 || id >= p.table_rows) {
     if (tid == 0) atomicOr(p.err, ERR_BAD_ID);
     id = 0;
@@ -155,7 +163,8 @@ __global__ void __launch_bounds__(64) k_qknorm(const GemvParams p) {
     q[i] = r0;
     q[i + half] = r1;
   } else {
-    uint16_t* k = p.Kc + row_kv_offset(p, m) + ((size_t)hh * p.T + pos) * p.head_dim;
+    uint16_t* k = p.Kc + kv_index(p.kv_tbl, p.kv_npp, p.kv_dim / p.head_dim, p.T, p.kv_seq, row_seq(p, m),
+                                  hh, pos, p.head_dim);
     k[i] = f32_to_bf16(r0);
     k[i + half] = f32_to_bf16(r1);
   }
@@ -166,14 +175,17 @@ __global__ void k_frame_end(const FrameEndParams p) {
   pdl_launch_dependents();
   pdl_wait();
   if (threadIdx.x == 0) {
-    if (p.fb_ring) {  // the ids fed back this frame, for later repetition windows
-      const int slot = *p.frame_index % kRepRing;
-      for (int b = 0; b < p.nseq; ++b)
+    for (int b = 0; b < p.nseq; ++b) {
+      if (p.active && !p.active[b]) continue;  // an idle slot stays where it is
+      if (p.fb_ring) {  // the ids fed back this frame, for later repetition windows
+        const int slot = p.frame_index[b] % kRepRing;
         for (int c = 0; c < p.ncb; ++c)
           p.fb_ring[((size_t)b * kRepRing + slot) * kRepIds + c] = p.fb[(size_t)b * p.sel_stride + c];
+      }
+      p.pos[b] += p.advance;
+      p.frame_index[b] += 1;
+      if (p.pending) p.pending[b] = -1;
     }
-    *p.pos += p.advance;
-    *p.frame_index += 1;
     if (p.hist) {
       const int i = *p.hist_idx;
       if (i < p.hist_cap) {
@@ -259,9 +271,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(const SelectParams p) {
   const int row = blockIdx.x;
   const float* z = p.logits + (size_t)row * p.ld;
   const int V = p.vocab;
-  const int frame = p.frame_ptr ? *p.frame_ptr : p.frame;
   const uint32_t cb = static_cast<uint32_t>(p.seq_rows ? p.codebook0 : p.codebook0 + row);
   const uint32_t sq = static_cast<uint32_t>(p.seq_rows ? p.sequence + row : p.sequence);
+  const int frame = p.frame_ptr ? p.frame_ptr[sq] : p.frame;
 
   // Repetition window: the ids this codebook fed back in the previous
   // rep_window frames of the sequence (or the explicit list), as a bitmap.

@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
       // pair (et & 63) of the tile, rows of parity et >> 6: with one or two
       // rows per sequence they all sit at one position
       pos0 = p.pos_ptr ? *p.pos_ptr : p.pos_fixed;
-      if (p.rps == 1 || p.rps == 2)
+      if ((p.rps == 1 || p.rps == 2) && (!p.pos_ptr || p.pos_uniform))
         cs_t = qkv_pair_rope(p, (n0 >> 1) + (et & 63), pos0 + (p.rps == 2 ? (et >> 6) : 0));
     }
     const bool wok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
@@ -574,8 +574,9 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
           for (int c = par; c < M; c += 2) {
             const float v0 = vs[c * 128 + 2 * pl], v1 = vs[c * 128 + 2 * pl + 1];
             if (p.epi == EPI_QKV) {
-              const int pos = pos0 + (p.rps > 0 ? c % p.rps : c);
-              const bool pre = p.rps == 1 || p.rps == 2;  // position fixed by parity
+              // with one position for every sequence, parity fixes a row's position
+              const bool pre = (p.rps == 1 || p.rps == 2) && (!p.pos_ptr || p.pos_uniform);
+              const int pos = pre ? pos0 + (p.rps > 0 ? c % p.rps : c) : row_pos(p, c);
               epi_qkv_pair_at(p, c, pair, v0, v1, pos, pre ? cs_t : qkv_pair_rope(p, pair, pos));
             } else {
               epi_swiglu(p, c, pair, v0, v1);

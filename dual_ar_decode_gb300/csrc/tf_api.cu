@@ -75,15 +75,20 @@ struct Layer {
   uint16_t* ffn_norm = nullptr;
   uint16_t* q_norm = nullptr;  // per-head q/k RMSNorm weights [D] (TF_FLAG_QK_NORM*)
   uint16_t* k_norm = nullptr;
+  bool paged = false;          // K/V are page pools addressed through the block table
   uint16_t* K = nullptr;  // [Hkv][T][D]
   uint16_t* V = nullptr;
 };
 
-// Device-resident frame state.  Sequences advance in lockstep (one shared
-// position); sequence b's ids sit at [b * kIdStride + codebook].
+// Device-resident frame state, per sequence slot: the next slow position,
+// the frames emitted since the sequence started, whether the slot decodes,
+// and a prompt id still to feed (a sequence that joined with
+// tf_prefill_seq); sequence b's ids sit at [b * kIdStride + codebook].
 struct DevState {
-  int32_t pos;
-  int32_t frame_index;
+  int32_t pos[kMaxBatch];
+  int32_t frame_index[kMaxBatch];
+  int32_t active[kMaxBatch];
+  int32_t pending[kMaxBatch];
   int32_t forced_on;
   int32_t hist_idx;
   uint32_t err;
@@ -150,16 +155,28 @@ struct tf_ctx {
   float* sk_part = nullptr;   // split-K partials
   float* ssq = nullptr;       // deferred RMSNorm: partial sums of squares [tile][kSsqRows]
   uint32_t* sk_tickets = nullptr;
-  int graph_B = 1;            // batch the captured graphs were built for
+  int graph_B = 1;            // slots the captured graphs were built for
   int32_t* hist = nullptr;
   int32_t* fb_ring = nullptr;  // [Bmax][kRepRing][kRepIds] fed-back ids (repetition window)
   DevState* st = nullptr;
   int S_slow = 1;
 
-  // host mirrors
-  int pos_host = 0;
-  int frame_host = 0;
+  // host mirrors of the per-slot state (DevState) and the batch shape
+  int32_t pos_host[kMaxBatch] = {};
+  int32_t frame_host[kMaxBatch] = {};
+  int32_t active_host[kMaxBatch] = {};
+  int32_t pending_host[kMaxBatch] = {};
   bool prefilled = false;
+  bool uniform = true;        // every slot at one position (lockstep batch)
+  bool graph_uniform = true;  // the captured graphs' assumption
+  // paged KV caches (TF_FLAG_PAGED_KV): block table [Bmax][npp] on the
+  // device and its host mirror, free pages, each slot's pages in order
+  bool paged = false;
+  int npp = 0;
+  int32_t* kv_tbl = nullptr;
+  std::vector<int32_t> tbl_host;
+  std::vector<int32_t> free_pages;
+  std::vector<int32_t> seq_pages[kMaxBatch];
 
   cudaGraphExec_t graph[2] = {nullptr, nullptr};  // [0] greedy, [1] top-k
   bool inject_armed = false;  // failure test: next decode frame skips one copy
@@ -246,7 +263,7 @@ bool valid_config(const tf_config* cfg, std::string* why) {
   if (cfg->weight_dtype == TF_WEIGHT_NVFP4 &&
       (cfg->hidden % 256 || cfg->ffn % 256 || (cfg->n_heads * cfg->head_dim) % 256))
     return bad("4-bit weights need hidden, ffn and n_heads*head_dim multiples of 256");
-  if (cfg->flags & ~(TF_FLAG_QK_NORM | TF_FLAG_QK_NORM_FAST | TF_FLAG_SLOW_CB_SUM))
+  if (cfg->flags & ~(TF_FLAG_QK_NORM | TF_FLAG_QK_NORM_FAST | TF_FLAG_SLOW_CB_SUM | TF_FLAG_PAGED_KV))
     return bad("unknown flags");
   return true;
 }
@@ -265,6 +282,64 @@ tf_status check_kernel_errors(tf_ctx* c) {
   if (e & ERR_NAN) return fail(c, TF_E_NUMERIC, "NaN logit met during selection");
   c->poisoned = true;
   return fail(c, TF_E_STATE, "device reported an id or position out of range");
+}
+
+// Uploads the host mirrors of the per-slot state (positions, frame indices,
+// active flags, pending prompt ids) to DevState.
+tf_status upload_slots(tf_ctx* c) {
+  CK(cudaMemcpyAsync(c->st->pos, c->pos_host, sizeof(c->pos_host), cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->st->frame_index, c->frame_host, sizeof(c->frame_host), cudaMemcpyHostToDevice,
+                     c->stream));
+  CK(cudaMemcpyAsync(c->st->active, c->active_host, sizeof(c->active_host), cudaMemcpyHostToDevice,
+                     c->stream));
+  CK(cudaMemcpyAsync(c->st->pending, c->pending_host, sizeof(c->pending_host), cudaMemcpyHostToDevice,
+                     c->stream));
+  return TF_OK;
+}
+
+// Paged caches: gives slot `slot` pages for positions 0..last (in order,
+// from the free list) and uploads its block-table row if it changed.
+tf_status ensure_pages(tf_ctx* c, int slot, int last) {
+  if (!c->paged) return TF_OK;
+  std::vector<int32_t>& mine = c->seq_pages[slot];
+  const size_t need = (size_t)last / kKvPage + 1;
+  if (mine.size() >= need) return TF_OK;
+  while (mine.size() < need) {
+    if (c->free_pages.empty()) return fail(c, TF_E_CAPACITY, "no free KV page");
+    const int32_t pg = c->free_pages.back();
+    c->free_pages.pop_back();
+    c->tbl_host[(size_t)slot * c->npp + mine.size()] = pg;
+    mine.push_back(pg);
+  }
+  CK(cudaMemcpyAsync(c->kv_tbl + (size_t)slot * c->npp, c->tbl_host.data() + (size_t)slot * c->npp,
+                     sizeof(int32_t) * c->npp, cudaMemcpyHostToDevice, c->stream));
+  return TF_OK;
+}
+
+// Frees slot `slot`: its pages go back to the free list (its block-table row
+// points at the scratch page 0 again) and its state is cleared on the host.
+tf_status release_slot(tf_ctx* c, int slot) {
+  c->active_host[slot] = 0;
+  c->pos_host[slot] = 0;
+  c->frame_host[slot] = 0;
+  c->pending_host[slot] = -1;
+  if (!c->paged) return TF_OK;
+  std::vector<int32_t>& mine = c->seq_pages[slot];
+  if (mine.empty()) return TF_OK;
+  for (size_t i = mine.size(); i-- > 0;) c->free_pages.push_back(mine[i]);
+  mine.clear();
+  std::fill(c->tbl_host.begin() + (size_t)slot * c->npp, c->tbl_host.begin() + (size_t)(slot + 1) * c->npp, 0);
+  CK(cudaMemcpyAsync(c->kv_tbl + (size_t)slot * c->npp, c->tbl_host.data() + (size_t)slot * c->npp,
+                     sizeof(int32_t) * c->npp, cudaMemcpyHostToDevice, c->stream));
+  return TF_OK;
+}
+
+// Slots a decode step runs: up to the last active one.
+int slots_in_use(const tf_ctx* c) {
+  int n = 0;
+  for (int b = 0; b < c->Bmax; ++b)
+    if (c->active_host[b]) n = b + 1;
+  return n;
 }
 
 // Sampling that needs the selection kernel (a draw or a repetition window);
@@ -309,7 +384,12 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
     p.Kc = layer->K;
     p.Vc = layer->V;
     if (layer->q_norm && epi == EPI_QKV) p.qk_raw = c->qk_raw;
+    if (layer->paged) {
+      p.kv_tbl = c->kv_tbl;
+      p.kv_npp = c->npp;
+    }
   }
+  p.kv_seq = c->kv_seq;
   p.T = c->T;
   p.pos_ptr = pos_ptr;
   p.pos_fixed = pos_fixed;
@@ -347,9 +427,10 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
 }
 
 // The q/k norm option: finish the q and k a QKV GEMM left raw (rows at
-// pos_ptr / pos_fixed, rps rows per sequence, caches of `L` + kv_off).
+// pos_ptr / pos_fixed, rps rows per sequence from sequence seq_base, the
+// caches of `L`).
 cudaError_t qknorm(tf_ctx* c, const Layer& L, int M, const int32_t* pos_ptr, int pos_fixed, int rps,
-                   size_t kv_off, float* qout, bool pdl) {
+                   int seq_base, float* qout, bool pdl) {
   GemvParams p = {};
   p.q_dim = c->Q;
   p.kv_dim = c->KV;
@@ -359,12 +440,17 @@ cudaError_t qknorm(tf_ctx* c, const Layer& L, int M, const int32_t* pos_ptr, int
   p.k_norm = L.k_norm;
   p.eps = c->cfg.rms_eps;
   p.qout = qout;
-  p.Kc = L.K + kv_off;
-  p.Vc = L.V + kv_off;
+  p.Kc = L.K;
+  p.Vc = L.V;
+  if (L.paged) {
+    p.kv_tbl = c->kv_tbl;
+    p.kv_npp = c->npp;
+  }
   p.T = c->T;
   p.pos_ptr = pos_ptr;
   p.pos_fixed = pos_fixed;
   p.rps = rps;
+  p.seq_base = seq_base;
   p.kv_seq = c->kv_seq;
   p.rope = c->rope;
   p.err = &c->st->err;
@@ -388,6 +474,11 @@ cudaError_t layer_decode(tf_ctx* c, const Layer& L, float* x, int M, const int32
   a.D = c->D;
   a.pos_ptr = pos_ptr;
   a.pos_fixed = pos_fixed;
+  a.kv_seq = c->kv_seq;
+  if (L.paged) {
+    a.kv_tbl = c->kv_tbl;
+    a.kv_npp = c->npp;
+  }
   a.S = S;
   a.part = c->part;
   a.counters = c->counters;
@@ -418,7 +509,7 @@ cudaError_t enqueue_select(tf_ctx* c, int cb, const tf_sampling* s) {
   q.rep_penalty = s->rep_penalty;
   q.rep_window = s->rep_window;
   q.fb_ring = c->fb_ring;
-  q.frame_ptr = &c->st->frame_index;
+  q.frame_ptr = c->st->frame_index;
   q.codebook0 = cb;
   q.sequence = 0;
   q.sel = &c->st->sel[cb];
@@ -471,9 +562,11 @@ cudaError_t enqueue_tail(tf_ctx* c, const tf_sampling* s, int advance, bool pdl_
     if (topk && (e = enqueue_select(c, j, s))) return e;
   }
   FrameEndParams f = {};
-  f.pos = &c->st->pos;
+  f.pos = c->st->pos;
   f.advance = advance;
-  f.frame_index = &c->st->frame_index;
+  f.frame_index = c->st->frame_index;
+  f.active = c->st->active;
+  f.pending = c->st->pending;
   f.sel = c->st->sel;
   f.sel_stride = kIdStride;
   f.nseq = 1;
@@ -530,7 +623,12 @@ cudaError_t skinny(tf_ctx* c, const Lin& L, int set, int M, int epi, float* out,
     p.Kc = o.layer->K;
     p.Vc = o.layer->V;
     if (o.layer->q_norm && epi == EPI_QKV) p.qk_raw = c->qk_raw;
+    if (o.layer->paged) {
+      p.kv_tbl = c->kv_tbl;
+      p.kv_npp = c->npp;
+    }
   }
+  p.pos_uniform = c->uniform ? 1 : 0;
   p.T = c->T;
   p.pos_ptr = o.pos_ptr;
   p.pos_fixed = o.pos_fixed;
@@ -592,6 +690,10 @@ cudaError_t layer_batched(tf_ctx* c, const Layer& L, float* x, int M, int rps,
   a.pos_fixed = pos_fixed;
   a.rps = rps;
   a.kv_seq = c->kv_seq;
+  if (L.paged) {
+    a.kv_tbl = c->kv_tbl;
+    a.kv_npp = c->npp;
+  }
   a.S = S;
   a.part = c->part;
   a.counters = c->counters;
@@ -627,7 +729,7 @@ cudaError_t select_batched(tf_ctx* c, int cb, int B, const tf_sampling* s) {
   q.rep_penalty = s->rep_penalty;
   q.rep_window = s->rep_window;
   q.fb_ring = c->fb_ring;
-  q.frame_ptr = &c->st->frame_index;
+  q.frame_ptr = c->st->frame_index;
   q.codebook0 = cb;
   q.sequence = 0;
   q.seq_rows = 1;
@@ -697,9 +799,11 @@ cudaError_t enqueue_tail_batched(tf_ctx* c, const tf_sampling* s, int B, int adv
     if ((e = select_batched(c, j, B, s))) return e;
   }
   FrameEndParams f = {};
-  f.pos = &c->st->pos;
+  f.pos = c->st->pos;
   f.advance = advance;
-  f.frame_index = &c->st->frame_index;
+  f.frame_index = c->st->frame_index;
+  f.active = c->st->active;
+  f.pending = c->st->pending;
   f.sel = c->st->sel;
   f.sel_stride = kIdStride;
   f.nseq = B;
@@ -726,6 +830,8 @@ cudaError_t enqueue_decode_batched(tf_ctx* c, const tf_sampling* s, int B) {
   b.cb_sum = c->slow_cb;
   b.cb_rows = c->Vc;
   b.ncb = c->NCB;
+  b.pending = c->st->pending;
+  b.text_rows = c->Vt;
   b.x = c->xs;
   b.err = &c->st->err;
   b.nw_next = c->slow[0].attn_norm;
@@ -738,7 +844,7 @@ cudaError_t enqueue_decode_batched(tf_ctx* c, const tf_sampling* s, int B) {
   const int S = std::max(1, std::min(c->S_slow, kBatchAttnCtasPerSm * c->num_sms / (B * c->Hkv)));
   const int Ls = static_cast<int>(c->slow.size());
   for (int i = 0; i < Ls; ++i)
-    if ((e = layer_batched(c, c->slow[i], c->xs, B, 1, &c->st->pos, 0, S,
+    if ((e = layer_batched(c, c->slow[i], c->xs, B, 1, c->st->pos, 0, S,
                            i == 0 ? 1 : hidden_tiles(c),
                            i + 1 < Ls ? c->slow[i + 1].attn_norm : c->slow_norm)))
       return e;
@@ -759,6 +865,8 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
   b.cb_sum = c->slow_cb;
   b.cb_rows = c->Vc;
   b.ncb = c->NCB;
+  b.pending = c->st->pending;
+  b.text_rows = c->Vt;
   b.x = c->xs;
   b.err = &c->st->err;
   if ((e = launch_build(b, false, c->stream))) return e;
@@ -766,10 +874,107 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
   for (int i = 0; i < Ls; ++i) {
     const NextGemv after = i + 1 < Ls ? NextGemv{&c->slow[i + 1].qkv, EPI_QKV, 1}
                                       : NextGemv{&c->sem, EPI_LOGITS, 1};
-    if ((e = layer_decode(c, c->slow[i], c->xs, 1, &c->st->pos, 0, c->S_slow, true, after)))
+    if ((e = layer_decode(c, c->slow[i], c->xs, 1, c->st->pos, 0, c->S_slow, true, after)))
       return e;
   }
   return enqueue_tail(c, s, 1, true);
+}
+
+// Prompt pass of one sequence: the P ids at tokens_dev (device) at positions
+// 0..P-1 through the slow decoder into slot `slot`'s KV caches (tensor-core
+// GEMMs with the decode path's epilogues, causal attention over the rows);
+// the last row's residual goes to xs[slot].
+cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
+  cudaError_t e;
+  BuildParams b = {};
+  b.mode = BUILD_TOKENS;
+  b.H = c->H;
+  b.M = P;
+  b.table = c->text_embed;
+  b.table_rows = c->Vt;
+  b.ids = tokens_dev;
+  b.x = c->px;
+  b.err = &c->st->err;
+  if ((e = launch_build(b, false, c->stream))) return e;
+  // CUDA-core fallback prompt GEMM: bf16 or e4m3 rows (4-bit rows go through a bf16 copy)
+  const int wt = c->wt == TF_WEIGHT_FP8 ? 1 : 0;
+  auto gemm = [&](const Lin& L, const float* A, int epi, float* out, int ldo, const Layer* layer) {
+    GemvParams p = {};
+    p.W = L.w;
+    p.scale = L.s;
+    p.N = L.N;
+    p.K = L.K;
+    p.x = A;
+    p.ldx = L.K;
+    p.epi = epi;
+    p.out = out;
+    p.ldo = ldo;
+    p.q_dim = c->Q;
+    p.kv_dim = c->KV;
+    p.head_dim = c->D;
+    p.qout = c->pq;
+    if (layer) {
+      p.Kc = layer->K;
+      p.Vc = layer->V;
+      p.seq_base = slot;
+      p.kv_seq = c->kv_seq;
+      if (layer->paged) {
+        p.kv_tbl = c->kv_tbl;
+        p.kv_npp = c->npp;
+      }
+      if (layer->q_norm) p.qk_raw = c->qk_raw;
+    }
+    p.T = c->T;
+    p.pos_fixed = 0;
+    p.rope = c->rope;
+    p.err = &c->st->err;
+    cudaError_t e2;
+    if (c->wt == TF_WEIGHT_NVFP4) {  // exact bf16 copy of e2m1 x block scale; row scale in p.scale
+      if ((e2 = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e2;
+      p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+    }
+    if (c->prefill_tc) {
+      if ((e2 = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream))) return e2;
+      if (c->wt == TF_WEIGHT_FP8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
+        if ((e2 = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e2;
+        p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+      }
+      return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
+    }
+    return launch_gemm_rows(p, wt, P, c->stream);
+  };
+  for (const Layer& L : c->slow) {
+    if ((e = launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream))) return e;
+    if ((e = gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L))) return e;
+    if (L.q_norm && (e = qknorm(c, L, P, nullptr, 0, 0, slot, c->pq, false))) return e;
+    AttnParams a = {};
+    a.q = c->pq;
+    a.Kc = L.K;
+    a.Vc = L.V;
+    a.T = c->T;
+    a.Hq = c->Hq;
+    a.Hkv = c->Hkv;
+    a.D = c->D;
+    a.pos_fixed = 0;
+    a.seq_base = slot;
+    a.kv_seq = c->kv_seq;
+    if (L.paged) {
+      a.kv_tbl = c->kv_tbl;
+      a.kv_npp = c->npp;
+    }
+    a.S = 1;
+    a.part = c->part;
+    a.counters = c->counters;
+    a.out = c->po;
+    a.err = &c->st->err;
+    if ((e = launch_attention_rows(a, P, false, c->stream))) return e;
+    if ((e = gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr))) return e;
+    if ((e = launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream))) return e;
+    if ((e = gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr))) return e;
+    if ((e = gemm(L.w2, c->pu, EPI_RESID, c->px, c->H, nullptr))) return e;
+  }
+  return cudaMemcpyAsync(c->xs + (size_t)slot * c->H, c->px + (size_t)(P - 1) * c->H, sizeof(float) * c->H,
+                         cudaMemcpyDeviceToDevice, c->stream);
 }
 
 bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
@@ -778,13 +983,14 @@ bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
 }
 
 tf_status get_graph(tf_ctx* c, const tf_sampling* s, cudaGraphExec_t* out) {
-  if (c->graph_B != c->Bc) {  // graphs are per batch size
+  if (c->graph_B != c->Bc || c->graph_uniform != c->uniform) {  // graphs are per batch shape
     for (auto& g : c->graph)
       if (g) {
         cudaGraphExecDestroy(g);
         g = nullptr;
       }
     c->graph_B = c->Bc;
+    c->graph_uniform = c->uniform;
   }
   const int gi = uses_select(s) ? 1 : 0;
   if (c->graph[gi] && (gi == 0 || same_sampling(c->graph_samp, *s))) {
@@ -876,7 +1082,7 @@ tf_status read_frame(tf_ctx* c, int32_t* frame, float* logits, int B) {
   if (frame)
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < c->NCB; ++j)
-        frame[(size_t)b * c->NCB + j] = slots[(size_t)b * kIdStride + j];
+        frame[(size_t)b * c->NCB + j] = c->active_host[b] ? slots[(size_t)b * kIdStride + j] : -1;
   return r;
 }
 
@@ -1017,13 +1223,24 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   c->sem.N = c->Vs;
   c->sem.K = c->H;
 
-  // ---- KV caches: [sequence][Hkv][T][D] per layer
+  // ---- KV caches: [sequence][Hkv][T][D] per layer, or (paged) page pools
+  // [page][Hkv][kKvPage][D] with one page per kKvPage positions of every
+  // slot plus the scratch page 0, addressed through a block table
   const size_t kv_elems = (size_t)c->Hkv * c->T * c->D;
   c->kv_seq = static_cast<int64_t>(kv_elems);
   const size_t B = c->Bmax;
+  c->paged = cfg->flags & TF_FLAG_PAGED_KV;
+  c->npp = (c->T + kKvPage - 1) / kKvPage;
+  const size_t n_pages = B * c->npp + 1;
+  const size_t slow_kv = c->paged ? n_pages * c->Hkv * kKvPage * c->D : B * kv_elems;
   for (Layer& L : c->slow) {
-    if (dev_alloc_t(c, &L.K, B * kv_elems) || dev_alloc_t(c, &L.V, B * kv_elems))
-      return bail(TF_E_NOMEM);
+    L.paged = c->paged;
+    if (dev_alloc_t(c, &L.K, slow_kv) || dev_alloc_t(c, &L.V, slow_kv)) return bail(TF_E_NOMEM);
+  }
+  if (c->paged) {
+    if (dev_alloc_t(c, &c->kv_tbl, B * c->npp)) return bail(TF_E_NOMEM);
+    c->tbl_host.assign(B * c->npp, 0);
+    for (size_t pg = n_pages - 1; pg >= 1; --pg) c->free_pages.push_back(static_cast<int32_t>(pg));
   }
   const size_t fkv = B * kv_elems;  // fast uses positions 0..9 of a T-slot cache
   for (Layer& L : c->fast) {
@@ -1099,10 +1316,13 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       return bail(TF_E_CUDA);
     }
   }
-  if (cudaMemset(c->st, 0, sizeof(DevState)) || cudaMemset(c->counters, 0, 2 * B * c->Hkv * 4)) {
+  if (cudaMemset(c->st, 0, sizeof(DevState)) || cudaMemset(c->counters, 0, 2 * B * c->Hkv * 4) ||
+      (c->kv_tbl && cudaMemset(c->kv_tbl, 0, B * c->npp * 4))) {
     c->err = "state init failed";
     return bail(TF_E_CUDA);
   }
+  for (int b = 0; b < kMaxBatch; ++b) c->pending_host[b] = -1;
+  if (upload_slots(c) != TF_OK) return bail(TF_E_CUDA);
   for (const Layer& L : c->fast) {
     cudaMemset(L.K, 0, fkv * 2);
     cudaMemset(L.V, 0, fkv * 2);
@@ -1142,8 +1362,8 @@ void* tf_get_stream(const tf_ctx* c) { return c ? static_cast<void*>(c->stream) 
 
 tf_status tf_get_info(const tf_ctx* c, tf_info* info) {
   if (!c || !info) return TF_E_INVAL;
-  info->position = c->pos_host;
-  info->frame_index = c->frame_host;
+  info->position = c->pos_host[0];
+  info->frame_index = c->frame_host[0];
   info->num_sms = c->num_sms;
   info->graph_nodes = c->graph_nodes;
   info->weight_bytes = static_cast<int64_t>(c->weight_bytes);
@@ -1310,112 +1530,99 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
   if (r) return r;
   CK(cudaSetDevice(c->device));
   if ((r = set_forced(c, forced, B))) return r;
+  // every slot starts over: B sequences at position P, the others idle
+  for (int b = 0; b < c->Bmax; ++b)
+    if ((r = release_slot(c, b))) return r;
+  for (int b = 0; b < B; ++b) {
+    if ((r = ensure_pages(c, b, P - 1))) return r;
+    c->pos_host[b] = P;
+    c->active_host[b] = 1;
+  }
+  if ((r = upload_slots(c))) return r;
   CK(cudaMemcpyAsync(c->tokens, tokens, sizeof(int32_t) * B * P, cudaMemcpyHostToDevice, c->stream));
-  const int32_t zero4[4] = {0, 0, 0, 0};  // pos, frame_index, forced_on kept, hist_idx
-  CK(cudaMemcpyAsync(&c->st->pos, &zero4[0], 4, cudaMemcpyHostToDevice, c->stream));
-  CK(cudaMemcpyAsync(&c->st->frame_index, &zero4[1], 4, cudaMemcpyHostToDevice, c->stream));
-  CK(cudaMemcpyAsync(&c->st->hist_idx, &zero4[3], 4, cudaMemcpyHostToDevice, c->stream));
-  if (s.top_k > 0) {
-    const uint32_t samp[3] = {(uint32_t)(s.seed & 0xFFFFFFFFu), (uint32_t)(s.seed >> 32), 0};
-    CK(cudaMemcpyAsync(c->st->samp, samp, sizeof(samp), cudaMemcpyHostToDevice, c->stream));
-  }
-  CK(cudaStreamSynchronize(c->stream));  // the host copies above read stack memory
+  const int32_t zero = 0;
+  CK(cudaMemcpyAsync(&c->st->hist_idx, &zero, 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaStreamSynchronize(c->stream));  // the host copies above read host memory
   c->Bc = B;
+  c->uniform = true;
   c->prefilled = false;
-
-  // CUDA-core fallback prompt GEMM: bf16 or e4m3 rows (4-bit rows go through a bf16 copy)
-  const int wt = c->wt == TF_WEIGHT_FP8 ? 1 : 0;
-  // Slow decoder over sequence b's prompt: row m at position m, KV caches of
-  // sequence b; its last residual row goes to xs[b].
-  for (int sb = 0; sb < B; ++sb) {
-    BuildParams b = {};
-    b.mode = BUILD_TOKENS;
-    b.H = c->H;
-    b.M = P;
-    b.table = c->text_embed;
-    b.table_rows = c->Vt;
-    b.ids = c->tokens + (size_t)sb * P;
-    b.x = c->px;
-    b.err = &c->st->err;
-    CK(launch_build(b, false, c->stream));
-    const size_t kvo = (size_t)sb * c->kv_seq;
-    auto gemm = [&](const Lin& L, const float* A, int epi, float* out, int ldo, const Layer* layer) {
-      GemvParams p = {};
-      p.W = L.w;
-      p.scale = L.s;
-      p.N = L.N;
-      p.K = L.K;
-      p.x = A;
-      p.ldx = L.K;
-      p.epi = epi;
-      p.out = out;
-      p.ldo = ldo;
-      p.q_dim = c->Q;
-      p.kv_dim = c->KV;
-      p.head_dim = c->D;
-      p.qout = c->pq;
-      if (layer) {
-        p.Kc = layer->K + kvo;
-        p.Vc = layer->V + kvo;
-        if (layer->q_norm) p.qk_raw = c->qk_raw;
-      }
-      p.T = c->T;
-      p.pos_fixed = 0;
-      p.rope = c->rope;
-      p.err = &c->st->err;
-      cudaError_t e;
-      if (c->wt == TF_WEIGHT_NVFP4) {  // exact bf16 copy of e2m1 x block scale; row scale in p.scale
-        if ((e = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e;
-        p.W = reinterpret_cast<const uint8_t*>(c->wconv);
-      }
-      if (c->prefill_tc) {
-        if ((e = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream))) return e;
-        if (c->wt == TF_WEIGHT_FP8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
-          if ((e = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e;
-          p.W = reinterpret_cast<const uint8_t*>(c->wconv);
-        }
-        return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
-      }
-      return launch_gemm_rows(p, wt, P, c->stream);
-    };
-    for (const Layer& L : c->slow) {
-      CK(launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
-      CK(gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L));
-      if (L.q_norm) CK(qknorm(c, L, P, nullptr, 0, 0, kvo, c->pq, false));
-      AttnParams a = {};
-      a.q = c->pq;
-      a.Kc = L.K + kvo;
-      a.Vc = L.V + kvo;
-      a.T = c->T;
-      a.Hq = c->Hq;
-      a.Hkv = c->Hkv;
-      a.D = c->D;
-      a.pos_fixed = 0;
-      a.S = 1;
-      a.part = c->part;
-      a.counters = c->counters;
-      a.out = c->po;
-      a.err = &c->st->err;
-      CK(launch_attention_rows(a, P, false, c->stream));
-      CK(gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr));
-      CK(launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream));
-      CK(gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr));
-      CK(gemm(L.w2, c->pu, EPI_RESID, c->px, c->H, nullptr));
-    }
-    CK(cudaMemcpyAsync(c->xs + (size_t)sb * c->H, c->px + (size_t)(P - 1) * c->H,
-                       sizeof(float) * c->H, cudaMemcpyDeviceToDevice, c->stream));
-  }
-  const int32_t posP = P;
-  CK(cudaMemcpyAsync(&c->st->pos, &posP, 4, cudaMemcpyHostToDevice, c->stream));
+  for (int sb = 0; sb < B; ++sb) CK(prompt_pass(c, sb, c->tokens + (size_t)sb * P, P));
   if (B > 1) {
     CK(enqueue_tail_batched(c, &s, B, 0, true));
   } else {
     CK(enqueue_tail(c, &s, 0, false));
   }
-  c->pos_host = P;
-  c->frame_host = 1;
+  for (int b = 0; b < B; ++b) c->frame_host[b] = 1;
   c->prefilled = true;
   return read_frame(c, frame0, logits, B);
+}
+
+tf_status tf_prefill_seq(tf_ctx* c, int32_t slot, const int32_t* tokens, int32_t P) {
+  if (!c) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  if (!tokens) return fail(c, TF_E_INVAL, "tokens are required");
+  if (slot < 0 || slot >= c->Bmax) return fail(c, TF_E_INVAL, "slot must be in [0, max_batch)");
+  if (P < 1 || P > c->T) return fail(c, TF_E_INVAL, "P must be in [1, max_seq_len]");
+  std::string missing;
+  if (!all_loaded(c, &missing)) return fail(c, TF_E_STATE, missing);
+  for (int32_t i = 0; i < P; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c->Vt) return fail(c, TF_E_INVAL, "prompt id out of range");
+  CK(cudaSetDevice(c->device));
+  tf_status r;
+  if ((r = release_slot(c, slot))) return r;
+  if ((r = ensure_pages(c, slot, P - 1))) return r;
+  if (P > 1) {  // every prompt id but the last through the prompt pass
+    CK(cudaMemcpyAsync(c->tokens, tokens, sizeof(int32_t) * (P - 1), cudaMemcpyHostToDevice, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    CK(prompt_pass(c, slot, c->tokens, P - 1));
+  }
+  // the last prompt id is fed by the next decode step, which emits frame 0
+  c->pos_host[slot] = P - 1;
+  c->frame_host[slot] = 0;
+  c->active_host[slot] = 1;
+  c->pending_host[slot] = tokens[P - 1];
+  if ((r = upload_slots(c))) return r;
+  CK(cudaStreamSynchronize(c->stream));
+  c->Bc = slots_in_use(c);
+  c->uniform = false;
+  c->prefilled = true;
+  return TF_OK;
+}
+
+tf_status tf_release_seq(tf_ctx* c, int32_t slot) {
+  if (!c) return TF_E_INVAL;
+  if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
+  if (slot < 0 || slot >= c->Bmax) return fail(c, TF_E_INVAL, "slot must be in [0, max_batch)");
+  CK(cudaSetDevice(c->device));
+  tf_status r;
+  if ((r = release_slot(c, slot))) return r;
+  if ((r = upload_slots(c))) return r;
+  CK(cudaStreamSynchronize(c->stream));
+  c->Bc = std::max(1, slots_in_use(c));
+  return TF_OK;
+}
+
+// Checks that every active slot can take n more frames and gives the paged
+// caches the pages they will write.
+static tf_status reserve_frames(tf_ctx* c, int n) {
+  if (!slots_in_use(c)) return fail(c, TF_E_STATE, "no active sequence");
+  for (int b = 0; b < c->Bc; ++b)
+    if (c->active_host[b] && c->pos_host[b] + n > c->T)
+      return fail(c, TF_E_CAPACITY, "KV cache full (slot " + std::to_string(b) + ")");
+  for (int b = 0; b < c->Bc; ++b)
+    if (c->active_host[b])
+      if (tf_status r = ensure_pages(c, b, c->pos_host[b] + n - 1)) return r;
+  return TF_OK;
+}
+
+// Host mirrors after n decode frames: every active slot advanced.
+static void advance_slots(tf_ctx* c, int n) {
+  for (int b = 0; b < c->Bc; ++b)
+    if (c->active_host[b]) {
+      c->pos_host[b] += n;
+      c->frame_host[b] += n;
+      c->pending_host[b] = -1;
+    }
 }
 
 tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t* forced,
@@ -1424,11 +1631,11 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
   if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
   if (!frame) return fail(c, TF_E_INVAL, "frame is required");
   if (!c->prefilled) return fail(c, TF_E_STATE, "tf_prefill must come first");
-  if (c->pos_host >= c->T) return fail(c, TF_E_CAPACITY, "KV cache full");
   tf_sampling s;
   tf_status r = check_sampling(c, sampling, &s);
   if (r) return r;
   CK(cudaSetDevice(c->device));
+  if ((r = reserve_frames(c, 1))) return r;
   if ((r = set_forced(c, forced, c->Bc))) return r;
   if (c->inject_armed && c->Bc == 1) {
     // failure test: this frame runs outside the graph, its first GEMV
@@ -1443,8 +1650,7 @@ tf_status tf_decode_frame(tf_ctx* c, const tf_sampling* sampling, const int32_t*
     if ((r = get_graph(c, &s, &g))) return r;
     CK(cudaGraphLaunch(g, c->stream));
   }
-  c->pos_host += 1;
-  c->frame_host += 1;
+  advance_slots(c, 1);
   return read_frame(c, frame, logits, c->Bc);
 }
 
@@ -1463,23 +1669,27 @@ tf_status tf_decode_frames(tf_ctx* c, const tf_sampling* sampling, int32_t n, in
   if (c->poisoned) return fail(c, TF_E_STATE, "context poisoned by an earlier error");
   if (n < 0 || (n > 0 && !frames)) return fail(c, TF_E_INVAL, "bad n or frames");
   if (!c->prefilled) return fail(c, TF_E_STATE, "tf_prefill must come first");
-  if (c->pos_host + n > c->T) return fail(c, TF_E_CAPACITY, "KV cache cannot hold n more frames");
   if (n == 0) return TF_OK;
   tf_sampling s;
   tf_status r = check_sampling(c, sampling, &s);
   if (r) return r;
   CK(cudaSetDevice(c->device));
+  if ((r = reserve_frames(c, n))) return r;
   if ((r = set_forced(c, nullptr, c->Bc))) return r;
   const int32_t zero = 0;
   CK(cudaMemcpyAsync(&c->st->hist_idx, &zero, 4, cudaMemcpyHostToDevice, c->stream));
   cudaGraphExec_t g;
   if ((r = get_graph(c, &s, &g))) return r;
   for (int i = 0; i < n; ++i) CK(cudaGraphLaunch(g, c->stream));
-  c->pos_host += n;
-  c->frame_host += n;
   CK(cudaMemcpyAsync(frames, c->hist, sizeof(int32_t) * c->NCB * c->Bc * n, cudaMemcpyDeviceToHost,
                      c->stream));
-  return check_kernel_errors(c);
+  r = check_kernel_errors(c);  // synchronises the stream
+  for (int i = 0; i < n; ++i)   // idle slots report -1
+    for (int b = 0; b < c->Bc; ++b)
+      if (!c->active_host[b])
+        for (int j = 0; j < c->NCB; ++j) frames[((size_t)i * c->Bc + b) * c->NCB + j] = -1;
+  advance_slots(c, n);
+  return r;
 }
 
 tf_status tf_profile_kernel(tf_ctx* c, int32_t which, int32_t iters, float* ms_per_launch,

@@ -91,7 +91,13 @@ typedef struct {
  *   of the previous frame's codes 1..9 ("slow.cb_embed"
  *   [n_codebooks-1][codebook_size][hidden] bf16, table j-1 for code j) to the
  *   text-embedding row of its code 0. */
-enum { TF_FLAG_QK_NORM = 1, TF_FLAG_QK_NORM_FAST = 2, TF_FLAG_SLOW_CB_SUM = 4 };
+enum { TF_FLAG_QK_NORM = 1, TF_FLAG_QK_NORM_FAST = 2, TF_FLAG_SLOW_CB_SUM = 4, TF_FLAG_PAGED_KV = 8 };
+/* TF_FLAG_PAGED_KV: the slow KV caches are pools of pages of 32 positions
+ * shared by the sequence slots, found through a block table; a slot holds
+ * pages only for the positions it has reached (the fish-s2-pro-mlx-local-
+ * deploy README's architecture paragraph and the drbaph s2-pro-fp8 card's
+ * "Architecture" name continuous batching with a paged KV cache for
+ * serving).  Results equal the dense caches'. */
 
 /* One named host (or device) tensor for tf_load_weights.
  * Names: "text_embed" [text_vocab][hidden];
@@ -191,16 +197,34 @@ tf_status tf_prefill(tf_ctx* ctx, const int32_t* tokens, int32_t B, int32_t P,
                      const tf_sampling* sampling, const int32_t* forced,
                      int32_t* frame0, float* logits);
 
-/* One decode frame: feeds each sequence's last codebook-0 id at its next
- * position, emits the next frame of every sequence of the last prefill.
- * Arguments as tf_prefill (B = that prefill's B).  At position ==
- * max_seq_len returns TF_E_CAPACITY and changes nothing. */
+/* Continuous batching: starts a sequence in slot `slot` (0 <= slot <
+ * max_batch) while the other slots keep their state.  tokens: host int32
+ * [P], ids in [0, text_vocab), 1 <= P <= max_seq_len.  Ids 0..P-2 run
+ * through the prompt pass into the slot's KV caches; the last id is fed by
+ * the next decode call, whose frame for this slot is the sequence's frame 0
+ * (sampling counters restart: its frame index is 0).  A sequence already in
+ * the slot is released first.  Prompt lengths may differ between slots: each
+ * slot has its own position.  Errors: TF_E_INVAL, TF_E_STATE (weights
+ * missing), TF_E_CAPACITY (no free KV page), TF_E_CUDA. */
+tf_status tf_prefill_seq(tf_ctx* ctx, int32_t slot, const int32_t* tokens, int32_t P);
+
+/* Ends the sequence in slot `slot`: the slot goes idle (its frames read -1)
+ * and, with paged caches, its pages return to the pool.  Errors: TF_E_INVAL. */
+tf_status tf_release_seq(tf_ctx* ctx, int32_t slot);
+
+/* One decode frame: feeds each active sequence's last codebook-0 id (or the
+ * last id of a prompt started with tf_prefill_seq) at its own next position
+ * and emits the next frame of every slot up to the last active one (B =
+ * that count; idle slots read -1).  forced, frame and logits as tf_prefill.
+ * When an active slot is at position == max_seq_len returns TF_E_CAPACITY
+ * and changes nothing; TF_E_STATE when no sequence is active. */
 tf_status tf_decode_frame(tf_ctx* ctx, const tf_sampling* sampling,
                           const int32_t* forced, int32_t* frame, float* logits);
 
 /* n decode frames back to back on the device (no host round trip between
- * frames); frames: host int32 [n][B][n_codebooks].  Fails with TF_E_CAPACITY
- * before running anything if the n frames do not fit. */
+ * frames); frames: host int32 [n][B][n_codebooks] (B and idle slots as
+ * tf_decode_frame).  Fails with TF_E_CAPACITY before running anything if
+ * the n frames do not fit. */
 tf_status tf_decode_frames(tf_ctx* ctx, const tf_sampling* sampling, int32_t n,
                            int32_t* frames);
 

@@ -91,13 +91,17 @@ class DualAROracle:
     stay bf16 (drbaph s2-pro-fp8 model card, "Quantization Details"); or
     "nvfp4" for the block-scaled 4-bit format (nvfp4_quantize_rows).
     batch: number of independent sequences.
+    seq_offset: added to the sequence index in the sampling counter (a
+    sequence run on its own that sits in batch slot seq_offset elsewhere).
     fp8_codes: optional name -> (codes, scale) of fp8_quantize_rows already
     computed for these weights (the quantisation is then not repeated).
     """
 
     def __init__(self, dims, weights: dict, weight_format: str = "bf16",
-                 batch: int = 1, cache_f64: bool | None = None, fp8_codes: dict | None = None):
+                 batch: int = 1, cache_f64: bool | None = None, fp8_codes: dict | None = None,
+                 seq_offset: int = 0):
         self.d = dims
+        self.seq_offset = seq_offset   # sequence b draws with Philox sequence word b + seq_offset
         self.raw = weights
         self.fmt = weight_format
         self.batch = batch
@@ -245,7 +249,7 @@ class DualAROracle:
             if window > 0:
                 z32 = apply_repetition_penalty(z32, [f[j] for f in past], penalty)
             if top_k > 1:
-                chosen, _ = topk_sample(z32, top_k, seed, frame, j, b, temp, top_p)
+                chosen, _ = topk_sample(z32, top_k, seed, frame, j, b + self.seq_offset, temp, top_p)
             else:
                 chosen = argmax_lowest(z32)
             fed = chosen if forced_row is None else int(forced_row[j])

@@ -156,3 +156,53 @@ class TeacherForced:
                         cand = oracle.topk_candidates(o.astype(np.float32), k + 2)
                         assert gf[j] in set(int(c) for c in cand), (t, b, j, gf[j])
         return worst, compared, skipped
+
+
+class ContinuousForced:
+    """Continuous batching under teacher forcing: sequences join slots of one
+    decoder (tf_prefill_seq) and leave them (tf_release_seq) while the others
+    decode; every sequence is also run by its own oracle (Philox sequence word
+    = its slot).  A sequence's frame 0 is the decode call right after it
+    joined.  Records (slot, frame t, oracle ids, oracle logits, gpu ids, gpu
+    logits) for check(); idle slots must read -1."""
+
+    def __init__(self, dims, dec, weights, fmt="bf16"):
+        self.d, self.dec, self.w, self.fmt = dims, dec, weights, fmt
+        self.seqs = {}      # slot -> [oracle, prompt, frames decoded]
+        self.frames = []
+        self.idle_ok = True
+
+    def join(self, slot, prompt):
+        self.dec.prefill_seq(slot, prompt)
+        self.seqs[slot] = [oracle.DualAROracle(self.d, self.w, self.fmt, seq_offset=slot),
+                           np.asarray(prompt, np.int32)[None], 0]
+
+    def leave(self, slot):
+        self.dec.release_seq(slot)
+        del self.seqs[slot]
+
+    def decode(self, sampling=None):
+        B = self.dec.batch
+        forced = np.zeros((B, self.d.n_codebooks), np.int32)
+        want = {}
+        for slot, st in self.seqs.items():
+            o, prompt, t = st
+            rf, rz = (o.prefill(prompt, sampling) if t == 0 else o.decode_frame(sampling))
+            forced[slot] = rf[0]
+            want[slot] = (t, rf[0], rz[0])
+            st[2] = t + 1
+        gf, gz = self.dec.decode_frame(sampling, forced=forced, logits=True)
+        for slot in range(B):
+            if slot in want:
+                t, rf, rz = want[slot]
+                self.frames.append((t, slot, rf, rz, gf[slot], gz[slot]))
+            else:
+                self.idle_ok &= bool((gf[slot] == -1).all())
+
+    def check(self, tol, sampling=None):
+        """The gates of TeacherForced.check on every recorded (slot, frame)."""
+        assert self.idle_ok, "an idle slot did not read -1"
+        tf = TeacherForced.__new__(TeacherForced)
+        tf.d = self.d
+        tf.frames = [(t, slot, rf, rz, gf, gz) for t, slot, rf, rz, gf, gz in self.frames]
+        return TeacherForced.check(tf, tol, sampling)

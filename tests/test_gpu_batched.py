@@ -14,7 +14,7 @@ import oracle
 from dual_ar_decode_gb300 import Decoder, TfError, op_gemm_skinny
 from synth import FULL, TINY, make_prompt, make_weights, f32_to_bf16_bits
 
-from gpu_helpers import BF16_TOL, FP8_TOL, TeacherForced, rel_l2, vocab_of
+from gpu_helpers import BF16_TOL, FP8_TOL, ContinuousForced, TeacherForced, rel_l2, vocab_of
 
 pytestmark = pytest.mark.gpu
 
@@ -165,6 +165,96 @@ def test_batch_size_changes_and_errors():
     dec.close()
 
 
+# ------------------------------------------------------------------ continuous batching
+
+def _continuous_schedule(cf, d, sampling=None):
+    """Joins, decodes and releases with prompts of different lengths; the
+    first phase has slot 0 alone (the batch-1 kernels), later ones the
+    batched kernels with idle slots inside the batch."""
+    P = lambda n, seed: make_prompt(d, n, seed=seed)[0]
+    cf.join(0, P(10, 1))
+    for _ in range(3):
+        cf.decode(sampling)
+    cf.join(2, P(5, 2))                      # slot 1 idle inside the batch
+    for _ in range(3):
+        cf.decode(sampling)
+    cf.leave(0)
+    cf.join(1, P(40, 3))                     # more than one 32-position page
+    for _ in range(3):
+        cf.decode(sampling)
+    cf.join(0, P(1, 4))                      # a one-id prompt: no prompt pass
+    cf.leave(2)
+    for _ in range(2):
+        cf.decode(sampling)
+
+
+@pytest.mark.parametrize("dims,fmt,tol,paged", [(TINY, "bf16", BF16_TOL, False),
+                                                (TINY, "bf16", BF16_TOL, True),
+                                                (TINY_OPTS, "bf16", BF16_TOL, True),
+                                                (TINY, "fp8", FP8_TOL, True)])
+def test_continuous_batching_ragged_prompts(dims, fmt, tol, paged):
+    """Sequences join and leave slots while others decode, each at its own
+    position, with dense or paged KV caches; every sequence matches its own
+    oracle run."""
+    w = make_weights(dims, seed=31)
+    dec = Decoder(dims, fmt, max_batch=4, paged=paged)
+    dec.load_weights(w)
+    cf = ContinuousForced(dims, dec, w, fmt)
+    _continuous_schedule(cf, dims)
+    worst, compared, skipped = cf.check(tol)
+    assert compared > 0.5 * (compared + skipped)
+    dec.close()
+
+
+def test_continuous_batching_topk_uses_the_slot_as_sequence():
+    s = {"top_k": 4, "seed": 5}
+    w = make_weights(TINY, seed=32)
+    dec = Decoder(TINY, "bf16", max_batch=4, paged=True)
+    dec.load_weights(w)
+    cf = ContinuousForced(TINY, dec, w)
+    _continuous_schedule(cf, TINY, s)
+    worst, compared, skipped = cf.check(BF16_TOL, s)
+    assert compared >= 40
+    dec.close()
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_lockstep_batch_on_paged_caches(paged):
+    tf = TeacherForced(TINY, "bf16", seed=0, batch=3,
+                       dec=Decoder(TINY, "bf16", max_batch=3, paged=paged))
+    tf.dec.load_weights(tf.w)
+    tf.prefill(make_prompt(TINY, 37, seed=10, batch=3))
+    for _ in range(4):
+        tf.decode()
+    worst, compared, skipped = tf.check(BF16_TOL)
+    assert compared > 0.5 * (compared + skipped)
+    tf.dec.close()
+
+
+def test_continuous_batching_errors():
+    d = TINY.replace(max_seq_len=24)
+    w = make_weights(d, seed=33)
+    dec = Decoder(d, "bf16", max_batch=2, paged=True)
+    dec.load_weights(w)
+    with pytest.raises(TfError, match="INVAL"):
+        dec.prefill_seq(2, make_prompt(d, 4)[0])                 # no such slot
+    with pytest.raises(TfError, match="INVAL"):
+        dec.prefill_seq(0, np.array([0, d.text_vocab], np.int32))  # id out of range
+    with pytest.raises(TfError, match="STATE"):
+        dec.decode_frame()                                        # nothing active
+    dec.prefill_seq(1, make_prompt(d, 22, seed=1)[0])             # positions 0..21
+    dec.decode_frame()                                            # frame 0 at 21
+    dec.decode_frame()                                            # frame 1 at 22
+    dec.decode_frame()                                            # frame 2 at 23
+    with pytest.raises(TfError, match="CAPACITY"):
+        dec.decode_frame()
+    dec.release_seq(1)
+    dec.prefill_seq(0, make_prompt(d, 3, seed=2)[0])              # the pages came back
+    f, _ = dec.decode_frame()
+    assert f.shape == (1, 10) and (f >= 0).all()
+    dec.close()
+
+
 # ------------------------------------------------------------------ full size
 
 def test_full_size_batched16_sampled_sequences():
@@ -206,4 +296,26 @@ def test_full_size_batched16_sampled_sequences():
                     compared += 1
                     assert gf[b, j] == rf[j], (t, b, j)
     assert compared >= 30
+    dec.close()
+
+
+def test_full_size_continuous_batching_paged():
+    """Full-size bf16 with paged caches: sequences with 37-, 130- and 513-id
+    prompts join four slots at different times (split attention over many
+    pages); two of them are checked against their own oracle runs, the
+    third is teacher-forced with its oracle too but only for 1 frame."""
+    d = FULL.replace(max_seq_len=1024)
+    w = make_weights(d, seed=0)
+    dec = Decoder(d, "bf16", max_batch=4, paged=True)
+    dec.load_weights(w)
+    cf = ContinuousForced(d, dec, w)
+    cf.join(3, make_prompt(d, 513, seed=41)[0])
+    cf.decode()
+    cf.join(0, make_prompt(d, 37, seed=42)[0])
+    cf.decode()
+    cf.leave(3)
+    cf.join(1, make_prompt(d, 130, seed=43)[0])
+    cf.decode()
+    worst, compared, skipped = cf.check(BF16_TOL)
+    assert compared >= 20
     dec.close()

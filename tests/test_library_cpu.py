@@ -55,7 +55,7 @@ def test_destroy_null_and_last_error(L):
     (dict(max_batch=0), b"max_batch"),
     (dict(max_batch=33), b"max_batch"),
     (dict(hidden=250), b"hidden"),
-    (dict(flags=8), b"flags"),
+    (dict(flags=16), b"flags"),
 ])
 def test_create_rejects_bad_config_before_touching_a_device(L, change, needle):
     cfg = binding.config_from_dims(TINY)

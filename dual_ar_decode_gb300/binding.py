@@ -82,6 +82,10 @@ EXPORTS = {
                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
+    "tf_op_attention_prompt": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_gemm": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_gemm_skinny": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
@@ -286,6 +290,11 @@ def op_select(logits_dev, n, vocab, sampling, frame, codebook0, sequence, ids_de
 def op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev, stream=0):
     _check(lib().tf_op_attention(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, splits, out_dev,
                                  stream))
+
+
+def op_attention_prompt(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, out_dev, stream=0):
+    _check(lib().tf_op_attention_prompt(q_dev, K_dev, V_dev, T, Hq, Hkv, D, rows, pos0, out_dev,
+                                        stream))
 
 
 def op_gemm(A_dev, W_dev, M, N, K, C_dev, stream=0):

@@ -155,6 +155,26 @@ struct AttnParams {
 cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t s);
 // The same attention for prompt rows (many rows, one long key slice each).
 cudaError_t launch_attention_rows(const AttnParams& p, int M, bool pdl, cudaStream_t s);
+// Causal attention of P prompt rows on the tensor cores: row m sits at
+// position pos0 + m and attends to keys 0..pos0 + m of its sequence.  The
+// queries come as bf16 hi / lo parts [P][Hq*D]; Kc / Vc are the sequence's
+// dense cache [Hkv][T][D] (kv_rows = Hkv*T), or with kv_tbl the page pool
+// [pages][Hkv][kKvPage][D] (kv_rows = pages*Hkv*kKvPage).  D = 64 or 128.
+struct PromptAttnArgs {
+  int32_t P, pos0, Hq, Hkv, T;
+  int32_t seq;             // the sequence's slot (paged caches)
+  const int32_t* kv_tbl;   // paged: block table [slots][npp]; null: dense
+  int32_t kv_npp;
+  float scale_log2;        // log2(e) / sqrt(D)
+  float* out;              // [P][Hq*D] fp32, or
+  uint16_t* out_hi;        // bf16 hi / lo parts
+  uint16_t* out_lo;
+  uint32_t* err;
+};
+bool prompt_attention_tc_supported(int D, int Hq, int Hkv);
+cudaError_t launch_prompt_attention_tc(const uint16_t* q_hi, const uint16_t* q_lo, const uint16_t* Kc,
+                                       const uint16_t* Vc, int64_t kv_rows, int D,
+                                       const PromptAttnArgs& a, cudaStream_t s);
 
 // ----------------------------------------------------------------- misc
 // Builds the input rows of a decoder pass.  Sequence b's ids sit at
@@ -275,10 +295,15 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
 cudaError_t launch_gemm_rows(const GemvParams& p, int wt, int M, cudaStream_t s);
 // Tensor-core (tcgen05) GEMM for prompts, bf16 weights:
 // out = epi(A[M][K] * W[N][K]^T) with A given as bf16 hi/lo parts [M][K].
+// K is split when the tiles alone would not fill the SMs (gemm_tc_splits);
+// then part holds gemm_tc_part_floats() floats and tickets one zeroed word per
+// output tile (returned to zero by the launch).
 bool gemm_tc_supported(int N, int K);
 size_t gemm_tc_smem_bytes();
+int gemm_tc_splits(int M, int N, int K, int num_sms);
+size_t gemm_tc_part_floats(int M, int N, int K, int num_sms);
 cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
-                           cudaStream_t s);
+                           float* part, uint32_t* tickets, int num_sms, cudaStream_t s);
 // Skinny tensor-core GEMM for batched decode (M <= 64 activation rows):
 // out = epi(A[M][K] * W[N][K]^T), the weight rows on the MMA's 128-row side,
 // the activation rows (bf16 hi / lo parts, [M][K]) on its N side, split over K
@@ -304,5 +329,8 @@ cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t
 // a[m] = RMSNorm(x[m]) * w for M rows (prefill prologue).
 cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int M, int H,
                                 float eps, cudaStream_t s);
+// The same rows as bf16 hi / lo parts (the tensor-core prompt GEMM's input).
+cudaError_t launch_rmsnorm_split(const float* x, const uint16_t* w, uint16_t* hi, uint16_t* lo,
+                                 int M, int H, float eps, cudaStream_t s);
 
 }  // namespace tf

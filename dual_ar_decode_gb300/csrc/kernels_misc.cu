@@ -581,6 +581,26 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* x, const uint
     a[(size_t)m * H + k] = xm[k] * rstd * bf16_to_f32(w[k]);
 }
 
+// RMSNorm rows straight into the bf16 hi / lo parts a tensor-core prompt GEMM
+// reads: a = x * rstd * w (the same float operations as k_rmsnorm_rows), hi =
+// bf16(a), lo = bf16(a - hi); one CTA per row.
+__global__ void __launch_bounds__(256) k_rmsnorm_split(const float* x, const uint16_t* w,
+                                                       uint16_t* hi, uint16_t* lo, int H, float eps) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  const float* xm = x + (size_t)m * H;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < H; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
+  ss = block_sum_256(ss, red);
+  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
+  for (int k = threadIdx.x; k < H; k += blockDim.x) {
+    const float a = xm[k] * rstd * bf16_to_f32(w[k]);
+    const uint16_t h = f32_to_bf16(a);
+    hi[(size_t)m * H + k] = h;
+    lo[(size_t)m * H + k] = f32_to_bf16(a - bf16_to_f32(h));
+  }
+}
+
 // Rows for a skinny GEMM with a deferred RMSNorm: x[m] * w as bf16 hi / lo
 // parts and the row's sum of squares; one CTA per row.
 __global__ void __launch_bounds__(256) k_rows_prep(const float* x, int ldx, int K,
@@ -787,6 +807,13 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
 cudaError_t launch_rmsnorm_rows(const float* x, const uint16_t* w, float* a, int M, int H,
                                 float eps, cudaStream_t s) {
   k_rmsnorm_rows<<<M, 256, 0, s>>>(x, w, a, H, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_split(const float* x, const uint16_t* w, uint16_t* hi, uint16_t* lo,
+                                 int M, int H, float eps, cudaStream_t s) {
+  if (M < 1) return cudaSuccess;
+  k_rmsnorm_split<<<M, 256, 0, s>>>(x, w, hi, lo, H, eps);
   return cudaGetLastError();
 }
 

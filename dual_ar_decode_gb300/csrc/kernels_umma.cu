@@ -4,10 +4,10 @@
 // "Inference speedtest": prefill is reported separately in tokens/s); its
 // linear layers are dense contractions C[m][n] = sum_k A[m][k] W[n][k] with
 // m over prompt tokens, so they belong on the 5th-generation tensor cores:
-//   * one CTA per 128 x 128 output tile; warp 0 streams 64-wide K slices of
-//     the activation tile and the weight tile into a 4-stage shared-memory
-//     ring with TMA tensor copies (128-byte swizzle), completion counted on
-//     mbarriers;
+//   * one CTA per 128 x 128 output tile and slice of K; warp 0 streams
+//     64-wide K slices of the activation tile and the weight tile into a
+//     4-stage shared-memory ring with TMA tensor copies (128-byte swizzle),
+//     completion counted on mbarriers;
 //   * warp 1 owns 128 TMEM columns (the fp32 accumulator) and issues
 //     tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), four K=16 steps per slice;
 //     tcgen05.commit frees a stage once the MMAs reading it are done;
@@ -17,7 +17,12 @@
 //   * warps 2-5 wait for the final commit, read the accumulator with
 //     tcgen05.ld (each warp its 32-lane quarter, one row per thread) and run
 //     the decode path's fused epilogues (RoPE + KV append, residual add,
-//     SwiGLU, store).
+//     SwiGLU, store);
+//   * few tiles (short prompts, or the 2560-wide O and down projections)
+//     would leave most SMs idle, so K is split until the grid fills whole
+//     waves: each split stores its partial tile and takes a ticket, and the
+//     tile's last CTA adds the partials in split order (deterministic) before
+//     the epilogue.
 // Every wait is bounded; the TMEM columns are always released.
 //
 // Batched decode (several sequences in lockstep, one row each per step) turns
@@ -104,10 +109,135 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+}
+
+// Ticket of a split-K tile: the add releases this CTA's partial (stored by
+// the four epilogue warps before the barrier that precedes it) and acquires
+// the partials of the CTAs that came earlier.
+__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* t) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
+
+// Epilogue of 16 consecutive output columns n..n+15 of prompt row m (n a
+// multiple of 16), with vector loads and stores: the row's columns are
+// contiguous in every output, so each chunk costs a few wide accesses
+// instead of one dependent round trip per element.  xr: the residual of
+// the same columns (EPI_RESID), loaded ahead by the caller.
+__device__ __forceinline__ void store4(float* dst, const float* v) {
+  *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = static_cast<uint32_t>(f32_to_bf16(v[2 * i])) |
+           (static_cast<uint32_t>(f32_to_bf16(v[2 * i + 1])) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void gemm_epi_chunk(const GemvParams& p, int m, int n, float (&v)[16],
+                                               const float (&xr)[16]) {
+  if (p.scale) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      const float4 sc = __ldg(reinterpret_cast<const float4*>(p.scale + n + i));
+      v[i] *= sc.x;
+      v[i + 1] *= sc.y;
+      v[i + 2] *= sc.z;
+      v[i + 3] *= sc.w;
+    }
+  }
+  if (p.epi == EPI_RESID) {
+    float* o = p.out + (size_t)m * p.ldo + n;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = xr[i] + v[i];
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) store4(o + i, v + i);
+  } else if (p.epi == EPI_SWIGLU) {
+    float u[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = silu(v[2 * i]) * v[2 * i + 1];
+    const size_t o = (size_t)m * p.ldo + (n >> 1);
+    if (p.out_hi) {
+      float hv[8], lv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        hv[i] = bf16_to_f32(f32_to_bf16(u[i]));
+        lv[i] = u[i] - hv[i];
+      }
+      *reinterpret_cast<uint4*>(p.out_hi + o) = pack_bf16x8(hv);
+      *reinterpret_cast<uint4*>(p.out_lo + o) = pack_bf16x8(lv);
+    } else {
+      store4(p.out + o, u);
+      store4(p.out + o + 4, u + 4);
+    }
+  } else if (p.epi == EPI_QKV) {
+    const int pos = row_pos(p, m);
+    if (pos < 0 || pos >= p.T) {
+      atomicOr(p.err, ERR_BAD_POS);
+      return;
+    }
+    const int half = p.head_dim >> 1;
+    const int qp = p.q_dim >> 1, kp = p.kv_dim >> 1;
+    const int pair = n >> 1;  // the chunk's 8 pairs lie in one head
+    if (pair < qp + kp && p.qk_raw) {  // q/k norm follows in k_qknorm
+      float* r = p.qk_raw + (size_t)m * (p.q_dim + p.kv_dim) + n;
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) store4(r + i, v + i);
+      return;
+    }
+    if (pair < qp + kp) {
+      const bool isq = pair < qp;
+      const int pr = isq ? pair : pair - qp;
+      const int h = pr / half, i0 = pr - h * half;
+      const float4* rp = reinterpret_cast<const float4*>(p.rope + (size_t)pos * half + i0);
+      float r0[8], r1[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 cs = __ldg(rp + j);  // (cos, sin) of pairs 2j and 2j + 1
+        const float a0 = v[4 * j], b0 = v[4 * j + 1], a1 = v[4 * j + 2], b1 = v[4 * j + 3];
+        r0[2 * j] = a0 * cs.x - b0 * cs.y;
+        r1[2 * j] = b0 * cs.x + a0 * cs.y;
+        r0[2 * j + 1] = a1 * cs.z - b1 * cs.w;
+        r1[2 * j + 1] = b1 * cs.z + a1 * cs.w;
+      }
+      if (isq) {
+        float* q = p.qout + (size_t)m * p.q_dim + h * p.head_dim + i0;
+        store4(q, r0);
+        store4(q + 4, r0 + 4);
+        store4(q + half, r1);
+        store4(q + half + 4, r1 + 4);
+      } else {
+        uint16_t* k = p.Kc + kv_index(p.kv_tbl, p.kv_npp, p.kv_dim / p.head_dim, p.T, p.kv_seq,
+                                      row_seq(p, m), h, pos, p.head_dim) + i0;
+        *reinterpret_cast<uint4*>(k) = pack_bf16x8(r0);
+        *reinterpret_cast<uint4*>(k + half) = pack_bf16x8(r1);
+      }
+    } else {
+      const int d0 = 2 * (pair - qp - kp);
+      const int g = d0 / p.head_dim, d = d0 - g * p.head_dim;
+      uint16_t* vv = p.Vc + kv_index(p.kv_tbl, p.kv_npp, p.kv_dim / p.head_dim, p.T, p.kv_seq,
+                                     row_seq(p, m), g, pos, p.head_dim) + d;
+      *reinterpret_cast<uint4*>(vv) = pack_bf16x8(v);
+      *reinterpret_cast<uint4*>(vv + 8) = pack_bf16x8(v + 8);
+    }
+  } else {
+    float* o = p.out + (size_t)m * p.ldo + n;
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) store4(o + i, v + i);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap map_ahi,
                 const __grid_constant__ CUtensorMap map_alo,
-                const __grid_constant__ CUtensorMap map_w, const GemvParams p, int M) {
+                const __grid_constant__ CUtensorMap map_w, const GemvParams p, int M, int S,
+                float* part, uint32_t* tickets) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -118,10 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* consumed = tmem_slot + 2;  // K slices the MMA warp took
+  volatile uint32_t* okv = tmem_slot + 4;       // [4] epilogue warps' wait outcomes
+  volatile uint32_t* last_flag = tmem_slot + 8;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-  const int nk = p.K / BK;
+  const int split = blockIdx.z;
+  const int nkt = p.K / BK;
+  const int kb0 = static_cast<int>((int64_t)split * nkt / S);
+  const int nk = static_cast<int>((int64_t)(split + 1) * nkt / S) - kb0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -157,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* st = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(st, &map_ahi, k * BK, m0, &full[s]);
-        tma_load_2d(st + kTileA, &map_alo, k * BK, m0, &full[s]);
-        tma_load_2d(st + 2 * kTileA, &map_w, k * BK, n0, &full[s]);
+        tma_load_2d(st, &map_ahi, (kb0 + k) * BK, m0, &full[s]);
+        tma_load_2d(st + kTileA, &map_alo, (kb0 + k) * BK, m0, &full[s]);
+        tma_load_2d(st + 2 * kTileA, &map_w, (kb0 + k) * BK, n0, &full[s]);
         issued = k + 1;
       }
       // After an abort, let the copies still in flight land before the CTA
@@ -199,35 +334,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int m = m0 + row;
-    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
+    // the first chunk's residual is loaded while the MMAs run
+    const bool resid = p.epi == EPI_RESID && m < M;
+    const float* xrow = p.out + (size_t)m * p.ldo + n0;
+    float xr[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) xr[i] = 0.f;
+    if (resid) {
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(xrow + i);
+        xr[i] = t.x;
+        xr[i + 1] = t.y;
+        xr[i + 2] = t.z;
+        xr[i + 3] = t.w;
+      }
+    }
+    const bool wok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
+    if (lane == 0) okv[q] = wok ? 1u : 0u;
+    epi_bar_sync();
+    const bool ok = okv[0] && okv[1] && okv[2] && okv[3];  // CTA-uniform
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok) {
+    bool run = ok;
+    const size_t tile_id = (size_t)blockIdx.x * gridDim.y + blockIdx.y;
+    const size_t tile_stride = (size_t)gridDim.x * gridDim.y * (BM * BN);
+    if (S > 1) {
+      // this split's partial tile [128 rows][128 columns], then a ticket
+      float* mine = part + split * tile_stride + tile_id * (BM * BN) + (size_t)row * BN;
+      if (ok) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            __stcg(reinterpret_cast<float4*>(mine + c + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+        }
+      }
+      epi_bar_sync();
+      if (threadIdx.x == 64) {
+        const uint32_t t = ticket_acq_rel(&tickets[tile_id]);
+        *last_flag = (t == static_cast<uint32_t>(S) - 1u) ? 1u : 0u;
+      }
+      epi_bar_sync();
+      run = ok && *last_flag != 0;
+    }
+    if (run) {
 #pragma unroll 1
       for (int c = 0; c < BN; c += 16) {
         float v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
-        if (m >= M) continue;
+        if (S > 1) {
+          // the splits' partials, added in split order
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const int n = n0 + c + i;
-          float v0 = v[i], v1 = v[i + 1];
-          if (p.scale) {
-            v0 *= __ldg(&p.scale[n]);
-            v1 *= __ldg(&p.scale[n + 1]);
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          const float* src = part + tile_id * (BM * BN) + (size_t)row * BN + c;
+          for (int j = 0; j < S; ++j, src += tile_stride) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 t = __ldcg(reinterpret_cast<const float4*>(src + i));
+              v[i] += t.x;
+              v[i + 1] += t.y;
+              v[i + 2] += t.z;
+              v[i + 3] += t.w;
+            }
           }
-          if (p.epi == EPI_QKV) {
-            epi_qkv_pair(p, m, n >> 1, v0, v1);
-          } else if (p.epi == EPI_SWIGLU) {
-            epi_swiglu(p, m, n >> 1, v0, v1);
-          } else if (p.epi == EPI_RESID) {
-            p.out[(size_t)m * p.ldo + n] += v0;
-            p.out[(size_t)m * p.ldo + n + 1] += v1;
-          } else {
-            p.out[(size_t)m * p.ldo + n] = v0;
-            p.out[(size_t)m * p.ldo + n + 1] = v1;
+        } else {
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+        }
+        if (m >= M) continue;
+        float xc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xc[i] = xr[i];
+        if (resid && c + 16 < BN) {  // the next chunk's residual, ahead of this chunk's stores
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(xrow + c + 16 + i);
+            xr[i] = t.x;
+            xr[i + 1] = t.y;
+            xr[i + 2] = t.z;
+            xr[i + 3] = t.w;
           }
         }
+        gemm_epi_chunk(p, m, n0 + c, v, xc);
       }
+      if (S > 1 && threadIdx.x == 64) tickets[tile_id] = 0u;
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -258,9 +448,6 @@ __device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint3
       : "memory");
 }
 
-__device__ __forceinline__ void epi_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
-}
 
 // ---------------------------------------------------------------- skinny GEMM
 // D[n][m] = sum_k W[n][k] a[m][k] for one 128-row weight tile and one slice of
@@ -297,15 +484,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 constexpr int kSkStages = TF_SKINNY_STAGES;
 constexpr int kSkThreads = 6 * 32;
-
-// Ticket of a split-K tile: the add releases this CTA's partial (stored by
-// the four epilogue warps before the barrier that precedes it) and acquires
-// the partials of the CTAs that came earlier.
-__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* t) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
-  return old;
-}
 
 template <int NB>
 struct Skinny {
@@ -354,7 +532,6 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
   const int kb0 = static_cast<int>((int64_t)split * nk / S);
   const int kb1 = static_cast<int>((int64_t)(split + 1) * nk / S);
   const int nkb = kb1 - kb0;
-  const size_t Np = (size_t)gridDim.x * 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSkStages; ++s) {
@@ -631,6 +808,368 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
   }
 }
 
+// ---------------------------------------------------------------- prompt attention
+// Causal attention of P prompt rows on the tensor cores ("Fish Speech" tour,
+// "Why You Need This": grouped-query attention; the tuna-fish README's
+// prefill tokens/s).  One CTA per (block of 128 query rows, query head); the
+// keys 0..pos of every row are visited in tiles of 128:
+//   * warp 0 loads the block's queries once (bf16 hi and lo parts) and the
+//     K and V tiles of the head's KV group into a two-stage ring (TMA,
+//     128-byte swizzle; paged caches: one box per 32-position page);
+//   * warp 1 issues S = Q K^T (hi and lo parts, fp32 in TMEM columns 0..127)
+//     and, once the probabilities are in shared memory, O += P V (TMEM
+//     columns 128..; V is read in its cache layout, an MN-major operand);
+//   * warps 2-5 own one query row each (its TMEM lane): they read the row's
+//     128 scores, apply the 1/sqrt(D) scale and the causal mask, keep the
+//     running maximum m and the sum l of the bf16 weights, and write
+//     p = 2^(s - m) as bf16 (so O / l is a convex combination of V rows).  O is
+//     rescaled (read, scaled, written back in TMEM) only when the maximum
+//     grows by more than 2^8, so p <= 256 and nothing overflows; the same m
+//     scales l, so the result is exact up to rounding.
+// V rows past the block's last key are zeroed in shared memory before the
+// product (the cache holds stale rows there; their p is 0, but 0 x NaN is
+// not).  Bounded waits; TMEM always released.
+template <int D>
+struct PAttn {
+  static constexpr int kBoxes = D / 64;            // 64-column boxes per row
+  static constexpr int kQ = 128 * D * 2;           // one query part, bytes
+  static constexpr int kKV = 128 * D * 2;          // one K or V tile
+  static constexpr int kP = 128 * 128 * 2;         // probabilities (bf16)
+  static constexpr int kStages = 2;
+  static constexpr size_t kOffKV = 2 * (size_t)kQ;
+  static constexpr size_t kOffP = kOffKV + (size_t)kStages * 2 * kKV;
+  static constexpr size_t kOffBar = kOffP + kP;
+  static constexpr size_t kSmem = 1024 + kOffBar + 128;
+  static constexpr uint32_t kCols = 256;           // S: 0..127, O: 128..
+  // kind::f16, fp32 accumulate, bf16 operands, M = 128.  S: B (keys x D)
+  // K-major, N = 128.  O: B (keys x D) MN-major (bit 16), N = D.
+  static constexpr uint32_t kIdescS =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+  static constexpr uint32_t kIdescO = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                      ((uint32_t)(D >> 3) << 17) | ((128u >> 4) << 24);
+};
+
+// Descriptor of an MN-major operand in the 128-byte swizzle layout TMA
+// writes for [rows = K][64 elements along N] boxes: 8-row groups 1024 bytes
+// apart (stride), 64-element column blocks `lbo` bytes apart (leading).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    k_umma_attn(const __grid_constant__ CUtensorMap map_qhi, const __grid_constant__ CUtensorMap map_qlo,
+                const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                const PromptAttnArgs a) {
+  using C = PAttn<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sq = smem;                    // [hi, lo][boxes][128 rows][128 B]
+  uint8_t* skv = smem + C::kOffKV;       // [stage][K, V][boxes][128 rows][128 B]
+  uint8_t* sp = smem + C::kOffP;         // [2 key halves][128 rows][128 B]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bar;
+  uint64_t* kv_full = bar + 1;           // [2]
+  uint64_t* kv_empty = bar + 3;          // [2]
+  uint64_t* s_full = bar + 5;
+  uint64_t* p_full = bar + 6;
+  uint64_t* o_full = bar + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 8);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  volatile uint32_t* issued_tiles = tmem_slot + 2;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = (a.P + 127) / 128;
+  const int blk = nblk - 1 - static_cast<int>(blockIdx.x);   // longest rows first
+  const int h = blockIdx.y;
+  const int g = h / (a.Hq / a.Hkv);
+  const int q0 = blk * 128;                                  // first query row
+  const int rows = min(128, a.P - q0);
+  const int last_key = a.pos0 + q0 + rows - 1;               // the block's last key
+  const int nt = last_key / 128 + 1;                         // key tiles
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_full, 1);
+    *abort_flag = 0;
+    *issued_tiles = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_qhi);
+      prefetch_tensormap(&map_qlo);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      mbar_arrive_expect_tx(q_full, 2 * C::kQ);
+      for (int b = 0; b < C::kBoxes; ++b) {
+        tma_load_2d(sq + b * 16384, &map_qhi, h * D + b * 64, q0, q_full);
+        tma_load_2d(sq + C::kQ + b * 16384, &map_qlo, h * D + b * 64, q0, q_full);
+      }
+      int j = 0;
+      for (; j < nt; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(&kv_empty[st], ((j >> 1) - 1) & 1, a.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* kdst = skv + (size_t)st * 2 * C::kKV;
+        uint8_t* vdst = kdst + C::kKV;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kKV);
+        if (a.kv_tbl) {
+          for (int pg = 0; pg < 4; ++pg) {
+            const int pi = (j * 128) / kKvPage + pg;
+            const int page = pi < a.kv_npp ? __ldg(a.kv_tbl + (size_t)a.seq * a.kv_npp + pi) : 0;
+            const int y = (page * a.Hkv + g) * kKvPage;
+            for (int b = 0; b < C::kBoxes; ++b) {
+              tma_load_2d(kdst + b * 16384 + pg * 4096, &map_k, b * 64, y, &kv_full[st]);
+              tma_load_2d(vdst + b * 16384 + pg * 4096, &map_v, b * 64, y, &kv_full[st]);
+            }
+          }
+        } else {
+          const int y = g * a.T + j * 128;
+          for (int b = 0; b < C::kBoxes; ++b) {
+            tma_load_2d(kdst + b * 16384, &map_k, b * 64, y, &kv_full[st]);
+            tma_load_2d(vdst + b * 16384, &map_v, b * 64, y, &kv_full[st]);
+          }
+        }
+        *issued_tiles = static_cast<uint32_t>(j + 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(q_full, 0, a.err);
+      const uint32_t qb = smem_u32(sq);
+      const uint32_t pb = smem_u32(sp);
+      for (int j = 0; ok && j < nt; ++j) {
+        const int st = j & 1;
+        if (*abort_flag || !mbar_wait(&kv_full[st], (j >> 1) & 1, a.err)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t kb = smem_u32(skv + (size_t)st * 2 * C::kKV);
+        const uint32_t vb = kb + C::kKV;
+#pragma unroll
+        for (int prt = 0; prt < 2; ++prt)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16(tmem_s, smem_desc_sw128(qb + prt * C::kQ + off), smem_desc_sw128(kb + off),
+                    C::kIdescS, (prt > 0 || kk > 0) ? 1u : 0u);
+          }
+        mma_commit(s_full);
+        if (!mbar_wait(p_full, j & 1, a.err)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_f16(tmem_o, smem_desc_sw128(pb + aoff), smem_desc_sw128_mn(vb + kk * 2048, 16384),
+                  C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&kv_empty[st]);
+        mma_commit(o_full);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;                 // query row in the block (TMEM lane)
+    const int qpos = a.pos0 + q0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      // waits are made warp-uniform: tcgen05.ld is a warp-collective
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(s_full, j & 1, a.err) ? 1 : 0)) {
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 16) {
+        float t[16];
+        tmem_ld16(tmem_s + lane_base + c, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) s[c + i] = t[i];
+      }
+      const int kbase = j * 128;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = (kbase + i <= qpos) ? s[i] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      // The previous product must be done before O is rescaled or the
+      // probability tile is overwritten.
+      if (j > 0) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(o_full, (j - 1) & 1, a.err) ? 1 : 0)) {
+          ok = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      }
+      // A new reference maximum (always on tile 0).  The rescale of O is
+      // decided per warp: tcgen05.ld / st are warp-collective, so every lane
+      // takes part (alpha = 1 for rows that keep their maximum).
+      const bool grow = mx > m_used + 8.0f;
+      const float alpha = grow ? exp2f(m_used - mx) : 1.0f;
+      if (grow) {
+        l *= alpha;
+        m_used = mx;
+      }
+      if (j > 0 && __any_sync(0xFFFFFFFFu, grow)) {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 16) {
+          float t[16];
+          tmem_ld16(tmem_o + lane_base + c, t);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t[i] *= alpha;
+          tmem_st16(tmem_o + lane_base + c, t);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      // p = 2^(s - m) as bf16, the row's 128 keys in two 64-key halves of the
+      // 128-byte swizzle layout (16-byte chunk c of row r at c ^ (r & 7))
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint8_t* rowp = sp + half * 16384 + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint16_t b0 = f32_to_bf16(exp2f(s[half * 64 + c * 8 + 2 * e] - m_used));
+            const uint16_t b1 = f32_to_bf16(exp2f(s[half * 64 + c * 8 + 2 * e + 1] - m_used));
+            l += bf16_to_f32(b0);  // the weights the product uses: O / l stays a convex combination
+            l += bf16_to_f32(b1);
+            w[e] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+          }
+          *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      if (j == nt - 1) {
+        // V rows past the block's last key: zero (this thread's row r of the
+        // tile, every column box), after the tile has landed
+        const int st = j & 1;
+        if (kbase + r > last_key) {
+          if (!mbar_wait(&kv_full[st], (j >> 1) & 1, a.err)) {
+            ok = false;
+          } else {
+            uint8_t* vrow = skv + (size_t)st * 2 * C::kKV + C::kKV + r * 128;
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(vrow + b * 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(p_full);
+      if (!ok) break;
+    }
+    if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(o_full, (nt - 1) & 1, a.err) ? 1 : 0)) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const float inv = 1.0f / l;
+      const int m = q0 + r;
+      const size_t o = (size_t)m * a.Hq * D + (size_t)h * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 16) {
+        float t[16];
+        tmem_ld16(tmem_o + lane_base + c, t);
+        if (m < a.P) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t[i] *= inv;
+          if (a.out_hi) {
+            float hv[16], lv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              hv[i] = bf16_to_f32(f32_to_bf16(t[i]));
+              lv[i] = t[i] - hv[i];
+            }
+            *reinterpret_cast<uint4*>(a.out_hi + o + c) = pack_bf16x8(hv);
+            *reinterpret_cast<uint4*>(a.out_hi + o + c + 8) = pack_bf16x8(hv + 8);
+            *reinterpret_cast<uint4*>(a.out_lo + o + c) = pack_bf16x8(lv);
+            *reinterpret_cast<uint4*>(a.out_lo + o + c + 8) = pack_bf16x8(lv + 8);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) store4(a.out + o + c + i, t + i);
+          }
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    // Copies still in flight (a tile abandoned after an expired wait) land
+    // before the CTA leaves: the last fill of each stage, bounded.
+    const int n = static_cast<int>(*issued_tiles);
+    for (int j = n > 2 ? n - 2 : 0; j < n; ++j)
+      if (!mbar_wait(&kv_full[j & 1], (j >> 1) & 1, a.err)) break;
+    mbar_wait(q_full, 0, a.err);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kCols)
+                 : "memory");
+  }
+}
+
 // e4m3 codes -> bf16 bits of the same values (exact: every e4m3 value is a
 // bf16 value); the per-row scale is applied later, in the GEMM epilogue.
 __global__ void k_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n2) {
@@ -750,9 +1289,67 @@ cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const 
   }
 }
 
+template <int D>
+cudaError_t launch_prompt_attn_d(const CUtensorMap& mqh, const CUtensorMap& mql, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, const PromptAttnArgs& a, cudaStream_t s) {
+  static DeviceOnce once;
+  cudaError_t ea = device_once(once, [] {
+    return cudaFuncSetAttribute(k_umma_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)PAttn<D>::kSmem);
+  });
+  if (ea) return ea;
+  const dim3 grid((a.P + 127) / 128, a.Hq);
+  k_umma_attn<D><<<grid, 192, PAttn<D>::kSmem, s>>>(mqh, mql, mk, mv, a);
+  return cudaGetLastError();
+}
+
+bool prompt_attention_tc_supported(int D, int Hq, int Hkv) {
+  return (D == 64 || D == 128) && Hkv > 0 && Hq % Hkv == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_prompt_attention_tc(const uint16_t* q_hi, const uint16_t* q_lo, const uint16_t* Kc,
+                                       const uint16_t* Vc, int64_t kv_rows, int D,
+                                       const PromptAttnArgs& a, cudaStream_t s) {
+  if (!prompt_attention_tc_supported(D, a.Hq, a.Hkv) || a.P < 1 || a.pos0 < 0 || a.pos0 + a.P > a.T)
+    return cudaErrorInvalidValue;
+  const uint32_t box = a.kv_tbl ? static_cast<uint32_t>(kKvPage) : 128u;
+  CUtensorMap mqh, mql, mk, mv;
+  if (!make_map(&mqh, q_hi, a.P, (uint64_t)a.Hq * D, 128) || !make_map(&mql, q_lo, a.P, (uint64_t)a.Hq * D, 128) ||
+      !make_map(&mk, Kc, kv_rows, D, box) || !make_map(&mv, Vc, kv_rows, D, box))
+    return cudaErrorInvalidValue;
+  return D == 64 ? launch_prompt_attn_d<64>(mqh, mql, mk, mv, a, s)
+                 : launch_prompt_attn_d<128>(mqh, mql, mk, mv, a, s);
+}
+
 bool gemm_tc_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && encode_fn() != nullptr; }
 
-size_t gemm_tc_smem_bytes() { return 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 16; }
+// K splits of a prompt GEMM: the fewest that fill at least 80% of the last
+// wave of CTAs (one CTA per SM), keeping >= 4 K slices per split; else the
+// best fill found.
+int gemm_tc_splits(int M, int N, int K, int num_sms) {
+  const int tiles = ((M + BM - 1) / BM) * (N / BN);
+  const int smax = std::max(1, std::min(16, (K / BK) / 4));
+  int best = 1;
+  double best_fill = 0.0;
+  for (int S = 1; S <= smax; ++S) {
+    const long ctas = (long)tiles * S;
+    const long waves = (ctas + num_sms - 1) / num_sms;
+    const double fill = (double)ctas / ((double)waves * num_sms);
+    if (fill >= 0.8) return S;
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = S;
+    }
+  }
+  return best;
+}
+
+size_t gemm_tc_part_floats(int M, int N, int K, int num_sms) {
+  const int S = gemm_tc_splits(M, N, K, num_sms);
+  return S > 1 ? (size_t)S * ((M + BM - 1) / BM) * (N / BN) * BM * BN : 0;
+}
+
+size_t gemm_tc_smem_bytes() { return 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 64; }
 
 cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s) {
   const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
@@ -767,7 +1364,7 @@ cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaS
 }
 
 cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
-                           cudaStream_t s) {
+                           float* part, uint32_t* tickets, int num_sms, cudaStream_t s) {
   static DeviceOnce once;
   cudaError_t ea = device_once(once, [] {
     return cudaFuncSetAttribute(k_umma_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -779,8 +1376,10 @@ cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint
   if (!make_map(&ma_hi, a_hi, M, p.K, BM) || !make_map(&ma_lo, a_lo, M, p.K, BM) ||
       !make_map(&mw, p.W, p.N, p.K, BN))
     return cudaErrorInvalidValue;
-  dim3 grid((M + BM - 1) / BM, p.N / BN);
-  k_umma_gemm<<<grid, kThreads, gemm_tc_smem_bytes(), s>>>(ma_hi, ma_lo, mw, p, M);
+  const int S = gemm_tc_splits(M, p.N, p.K, num_sms);
+  if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
+  dim3 grid((M + BM - 1) / BM, p.N / BN, S);
+  k_umma_gemm<<<grid, kThreads, gemm_tc_smem_bytes(), s>>>(ma_hi, ma_lo, mw, p, M, S, part, tickets);
   return cudaGetLastError();
 }
 

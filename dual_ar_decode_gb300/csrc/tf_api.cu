@@ -144,8 +144,13 @@ struct tf_ctx {
   float *px = nullptr, *pa = nullptr, *pq = nullptr, *po = nullptr, *pu = nullptr;
   int32_t* tokens = nullptr;
   uint16_t *a_hi = nullptr, *a_lo = nullptr;  // prompt GEMM inputs as bf16 hi / lo parts
+  uint16_t *u_hi = nullptr, *u_lo = nullptr;  // the SwiGLU output as parts (down GEMM input)
+  float* g_part = nullptr;                    // prompt GEMM split-K partials
+  uint32_t* g_tickets = nullptr;              // one per output tile
+  size_t g_part_floats = 0, g_tiles = 0;
   uint16_t* wconv = nullptr;  // fp8 weight converted to bf16 for one tensor-core GEMM
   bool prefill_tc = false;
+  bool attn_tc = false;        // prompt attention on the tensor cores
   // batched decode
   int Bmax = 1;               // sequences the context holds
   int Bc = 1;                 // sequences of the current prefill
@@ -896,9 +901,14 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
   b.x = c->px;
   b.err = &c->st->err;
   if ((e = launch_build(b, false, c->stream))) return e;
-  // CUDA-core fallback prompt GEMM: bf16 or e4m3 rows (4-bit rows go through a bf16 copy)
+  // Tensor-core GEMMs take their input as bf16 hi / lo parts: written by the
+  // fused RMSNorm, by the SwiGLU epilogue, or split from the attention output.
+  // The CUDA-core fallback takes fp32 rows (e4m3 rows as they are; 4-bit rows
+  // go through a bf16 copy).
+  const bool tc = c->prefill_tc;
   const int wt = c->wt == TF_WEIGHT_FP8 ? 1 : 0;
-  auto gemm = [&](const Lin& L, const float* A, int epi, float* out, int ldo, const Layer* layer) {
+  auto gemm = [&](const Lin& L, const float* A, const uint16_t* hi, const uint16_t* lo, int epi,
+                  float* out, int ldo, const Layer* layer) {
     GemvParams p = {};
     p.W = L.w;
     p.scale = L.s;
@@ -924,6 +934,10 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
       }
       if (layer->q_norm) p.qk_raw = c->qk_raw;
     }
+    if (epi == EPI_SWIGLU && tc) {  // the down GEMM's input parts, no fp32 rows
+      p.out_hi = c->u_hi;
+      p.out_lo = c->u_lo;
+    }
     p.T = c->T;
     p.pos_fixed = 0;
     p.rope = c->rope;
@@ -933,19 +947,22 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
       if ((e2 = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e2;
       p.W = reinterpret_cast<const uint8_t*>(c->wconv);
     }
-    if (c->prefill_tc) {
-      if ((e2 = launch_split_bf16(A, c->a_hi, c->a_lo, (size_t)P * L.K, c->stream))) return e2;
+    if (tc) {
       if (c->wt == TF_WEIGHT_FP8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
         if ((e2 = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e2;
         p.W = reinterpret_cast<const uint8_t*>(c->wconv);
       }
-      return launch_gemm_tc(p, c->a_hi, c->a_lo, P, c->stream);
+      return launch_gemm_tc(p, hi, lo, P, c->g_part, c->g_tickets, c->num_sms, c->stream);
     }
     return launch_gemm_rows(p, wt, P, c->stream);
   };
+  auto norm = [&](const uint16_t* w) {
+    return tc ? launch_rmsnorm_split(c->px, w, c->a_hi, c->a_lo, P, c->H, c->cfg.rms_eps, c->stream)
+              : launch_rmsnorm_rows(c->px, w, c->pa, P, c->H, c->cfg.rms_eps, c->stream);
+  };
   for (const Layer& L : c->slow) {
-    if ((e = launch_rmsnorm_rows(c->px, L.attn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream))) return e;
-    if ((e = gemm(L.qkv, c->pa, EPI_QKV, nullptr, 0, &L))) return e;
+    if ((e = norm(L.attn_norm))) return e;
+    if ((e = gemm(L.qkv, c->pa, c->a_hi, c->a_lo, EPI_QKV, nullptr, 0, &L))) return e;
     if (L.q_norm && (e = qknorm(c, L, P, nullptr, 0, 0, slot, c->pq, false))) return e;
     AttnParams a = {};
     a.q = c->pq;
@@ -966,12 +983,46 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
     a.part = c->part;
     a.counters = c->counters;
     a.out = c->po;
+    if (tc) {  // the O GEMM's input parts
+      a.out_hi = c->a_hi;
+      a.out_lo = c->a_lo;
+    }
     a.err = &c->st->err;
-    if ((e = launch_attention_rows(a, P, false, c->stream))) return e;
-    if ((e = gemm(L.o, c->po, EPI_RESID, c->px, c->H, nullptr))) return e;
-    if ((e = launch_rmsnorm_rows(c->px, L.ffn_norm, c->pa, P, c->H, c->cfg.rms_eps, c->stream))) return e;
-    if ((e = gemm(L.w13, c->pa, EPI_SWIGLU, c->pu, c->F, nullptr))) return e;
-    if ((e = gemm(L.w2, c->pu, EPI_RESID, c->px, c->H, nullptr))) return e;
+    if (c->attn_tc) {
+      // tensor-core causal attention; the queries as bf16 parts in the
+      // (idle) SwiGLU part buffers
+      if ((e = launch_split_bf16(c->pq, c->u_hi, c->u_lo, (size_t)P * c->Q, c->stream))) return e;
+      PromptAttnArgs t = {};
+      t.P = P;
+      t.pos0 = 0;
+      t.Hq = c->Hq;
+      t.Hkv = c->Hkv;
+      t.T = c->T;
+      t.seq = slot;
+      t.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt((double)c->D));
+      t.out = c->po;
+      t.out_hi = a.out_hi;
+      t.out_lo = a.out_lo;
+      t.err = &c->st->err;
+      const uint16_t* Kc = L.K;
+      const uint16_t* Vc = L.V;
+      int64_t rows = (int64_t)c->Hkv * c->T;
+      if (L.paged) {
+        t.kv_tbl = c->kv_tbl;
+        t.kv_npp = c->npp;
+        rows = (int64_t)(c->Bmax * c->npp + 1) * c->Hkv * kKvPage;
+      } else {
+        Kc += (size_t)slot * c->kv_seq;
+        Vc += (size_t)slot * c->kv_seq;
+      }
+      if ((e = launch_prompt_attention_tc(c->u_hi, c->u_lo, Kc, Vc, rows, c->D, t, c->stream))) return e;
+    } else if ((e = launch_attention_rows(a, P, false, c->stream))) {
+      return e;
+    }
+    if ((e = gemm(L.o, c->po, c->a_hi, c->a_lo, EPI_RESID, c->px, c->H, nullptr))) return e;
+    if ((e = norm(L.ffn_norm))) return e;
+    if ((e = gemm(L.w13, c->pa, c->a_hi, c->a_lo, EPI_SWIGLU, c->pu, c->F, nullptr))) return e;
+    if ((e = gemm(L.w2, c->pu, c->u_hi, c->u_lo, EPI_RESID, c->px, c->H, nullptr))) return e;
   }
   return cudaMemcpyAsync(c->xs + (size_t)slot * c->H, c->px + (size_t)(P - 1) * c->H, sizeof(float) * c->H,
                          cudaMemcpyDeviceToDevice, c->stream);
@@ -1274,10 +1325,25 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
   // Tensor-core prompt GEMMs for bf16 weights whenever every shape tiles.
   c->prefill_tc = gemm_tc_supported(c->QKV, c->H) && gemm_tc_supported(c->H, c->Q) &&
                   gemm_tc_supported(2 * c->F, c->H) && gemm_tc_supported(c->H, c->F);
-  if (c->prefill_tc &&
-      (dev_alloc_t(c, &c->a_hi, (size_t)T * std::max({c->H, c->Q, c->F})) ||
-       dev_alloc_t(c, &c->a_lo, (size_t)T * std::max({c->H, c->Q, c->F}))))
-    return bail(TF_E_NOMEM);
+  if (c->prefill_tc) {
+    // split-K scratch for the largest partial set of any prompt length
+    const int shapes[4][2] = {{c->QKV, c->H}, {c->H, c->Q}, {2 * c->F, c->H}, {c->H, c->F}};
+    for (int m = 128; m < T + 128; m += 128)
+      for (auto& sh : shapes) {
+        const int M = std::min(m, T);
+        c->g_part_floats = std::max(c->g_part_floats, gemm_tc_part_floats(M, sh[0], sh[1], c->num_sms));
+        if (gemm_tc_splits(M, sh[0], sh[1], c->num_sms) > 1)
+          c->g_tiles = std::max(c->g_tiles, (size_t)((M + 127) / 128) * (sh[0] / 128));
+      }
+    c->attn_tc = prompt_attention_tc_supported(c->D, c->Hq, c->Hkv) && c->F >= c->Q;
+    if (dev_alloc_t(c, &c->a_hi, (size_t)T * std::max(c->H, c->Q)) ||
+        dev_alloc_t(c, &c->a_lo, (size_t)T * std::max(c->H, c->Q)) ||
+        dev_alloc_t(c, &c->u_hi, (size_t)T * c->F) || dev_alloc_t(c, &c->u_lo, (size_t)T * c->F) ||
+        dev_alloc_t(c, &c->g_part, std::max<size_t>(c->g_part_floats, 4)) ||
+        dev_alloc_t(c, &c->g_tickets, std::max<size_t>(c->g_tiles, 1)) ||
+        cudaMemset(c->g_tickets, 0, std::max<size_t>(c->g_tiles, 1) * 4))
+      return bail(TF_E_NOMEM);
+  }
   if (c->fp8 && (c->prefill_tc || B > 1 || c->wt == TF_WEIGHT_NVFP4) &&
       dev_alloc_t(c, &c->wconv,
                   std::max({(size_t)c->QKV * H, (size_t)H * c->Q, (size_t)2 * c->F * H,
@@ -1933,19 +1999,73 @@ tf_status tf_op_attention(const float* q, const uint16_t* K, const uint16_t* V, 
   return r;
 }
 
-tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
-                     void* stream) {
-  if (!A || !W || !C || M < 1 || N < 1 || K < 1 || !gemm_tc_supported(N, K)) return TF_E_INVAL;
+tf_status tf_op_attention_prompt(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
+                                 int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
+                                 float* out, void* stream) {
+  if (!q || !K || !V || !out || T < 1 || Hq < 1 || Hkv < 1 || rows < 1 || pos0 < 0 ||
+      (int64_t)pos0 + rows > T || !prompt_attention_tc_supported(D, Hq, Hkv) ||
+      (int64_t)Hkv * T * D >= (1ll << 40))
+    return TF_E_INVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = (size_t)rows * Hq * D;
   uint16_t *hi = nullptr, *lo = nullptr;
   uint32_t* err = nullptr;
-  const size_t n = (size_t)M * K;
   if (cudaMalloc(&hi, n * 2) != cudaSuccess || cudaMalloc(&lo, n * 2) != cudaSuccess ||
       cudaMalloc(&err, 4) != cudaSuccess) {
     (void)cudaGetLastError();
     cudaFree(hi);
     cudaFree(lo);
     cudaFree(err);
+    return TF_E_NOMEM;
+  }
+  PromptAttnArgs a = {};
+  a.P = rows;
+  a.pos0 = pos0;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.T = T;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt((double)D));
+  a.out = out;
+  a.err = err;
+  tf_status r = TF_OK;
+  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || launch_split_bf16(q, hi, lo, n, s) != cudaSuccess ||
+      launch_prompt_attention_tc(hi, lo, K, V, (int64_t)Hkv * T, D, a, s) != cudaSuccess)
+    r = TF_E_CUDA;
+  uint32_t e = 0;
+  if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                     cudaStreamSynchronize(s) != cudaSuccess))
+    r = TF_E_CUDA;
+  cudaFree(hi);
+  cudaFree(lo);
+  cudaFree(err);
+  if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
+  else if (r == TF_OK && e) r = TF_E_INVAL;
+  return r;
+}
+
+tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
+                     void* stream) {
+  if (!A || !W || !C || M < 1 || N < 1 || K < 1 || !gemm_tc_supported(N, K)) return TF_E_INVAL;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return TF_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint16_t *hi = nullptr, *lo = nullptr;
+  uint32_t *err = nullptr, *tickets = nullptr;
+  float* part = nullptr;
+  const size_t n = (size_t)M * K;
+  const size_t pf = std::max<size_t>(gemm_tc_part_floats(M, N, K, sms), 4);
+  const size_t nt = (size_t)((M + 127) / 128) * (N / 128);
+  if (cudaMalloc(&hi, n * 2) != cudaSuccess || cudaMalloc(&lo, n * 2) != cudaSuccess ||
+      cudaMalloc(&err, 4) != cudaSuccess || cudaMalloc(&tickets, nt * 4) != cudaSuccess ||
+      cudaMalloc(&part, pf * 4) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFree(hi);
+    cudaFree(lo);
+    cudaFree(err);
+    cudaFree(tickets);
+    cudaFree(part);
     return TF_E_NOMEM;
   }
   tf_status r = TF_OK;
@@ -1957,8 +2077,9 @@ tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, in
   p.out = C;
   p.ldo = N;
   p.err = err;
-  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || launch_split_bf16(A, hi, lo, n, s) != cudaSuccess ||
-      launch_gemm_tc(p, hi, lo, M, s) != cudaSuccess)
+  if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || cudaMemsetAsync(tickets, 0, nt * 4, s) != cudaSuccess ||
+      launch_split_bf16(A, hi, lo, n, s) != cudaSuccess ||
+      launch_gemm_tc(p, hi, lo, M, part, tickets, sms, s) != cudaSuccess)
     r = TF_E_CUDA;
   uint32_t e = 0;
   if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -1967,6 +2088,8 @@ tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, in
   cudaFree(hi);
   cudaFree(lo);
   cudaFree(err);
+  cudaFree(tickets);
+  cudaFree(part);
   if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
   return r;
 }

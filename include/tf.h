@@ -356,13 +356,29 @@ tf_status tf_op_attention_noalloc(const float* q, const uint16_t* K, const uint1
                                   int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
                                   int32_t splits, float* out, void* stream);
 
+/* Causal attention of prompt rows on the tensor cores (tcgen05), the
+ * prefill's attention kernel ("Fish Speech" tour, "Why You Need This":
+ * grouped-query attention).  Same arguments and results as tf_op_attention
+ * without `splits`: row m (position pos0 + m) attends to keys 0..pos0 + m of
+ * the dense cache K, V [Hkv][T][D] (bf16, device), scores scaled by
+ * 1/sqrt(D), softmax with max subtraction.  The queries are split into bf16
+ * hi and lo parts (about 16 significant bits); the probabilities enter the
+ * second product as bf16; accumulation is fp32.  D must be 64 or 128 and Hq
+ * a multiple of Hkv.  Allocates and frees its scratch.  Errors: TF_E_INVAL,
+ * TF_E_NOMEM, TF_E_CUDA, TF_E_TIMEOUT. */
+tf_status tf_op_attention_prompt(const float* q, const uint16_t* K, const uint16_t* V, int32_t T,
+                                 int32_t Hq, int32_t Hkv, int32_t D, int32_t rows, int32_t pos0,
+                                 float* out, void* stream);
+
 /* Prompt GEMM on the tensor cores (tcgen05, fp32 accumulation in TMEM), the
  * prefill's matrix kernel: C[m][n] = sum_k A[m][k] W[n][k] for the prompt
  * rows m.  A: float32 [M][K] device; W: bf16 bits [N][K] device; C: float32
  * [M][N] device.  A is split into bf16 hi and lo parts that are both
  * multiplied with W, so the result carries about 16 significant bits of A.
- * N must be a multiple of 128 and K of 64.  Allocates and frees its scratch.
- * Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA. */
+ * N must be a multiple of 128 and K of 64.  When the 128 x 128 output tiles
+ * would not fill the GPU, K is split and the splits' partials are added in
+ * split order (results do not depend on timing).  Allocates and frees its
+ * scratch.  Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA, TF_E_TIMEOUT. */
 tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
                      void* stream);
 

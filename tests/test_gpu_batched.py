@@ -231,6 +231,28 @@ def test_lockstep_batch_on_paged_caches(paged):
     tf.dec.close()
 
 
+def test_paged_kv_matches_dense_bit_for_bit_in_the_batched_step():
+    """The batched step reads and writes the paged caches through the block
+    table in the same order as the dense caches: with the same forced ids the
+    logits agree bit for bit (prompt pass and batched step both use the
+    row-streaming attention)."""
+    w = make_weights(TINY, seed=34)
+    prompts = make_prompt(TINY, 45, seed=11, batch=3)     # 2 pages, a ragged third
+    decs = [Decoder(TINY, "bf16", max_batch=3, paged=pg) for pg in (False, True)]
+    forced = np.random.default_rng(3).integers(0, TINY.codebook_size, (6, 3, 10)).astype(np.int32)
+    outs = []
+    for dec in decs:
+        dec.load_weights(w)
+        f0, z0 = dec.prefill(prompts, forced=forced[0], logits=True)
+        zs = [z0]
+        for t in range(1, 6):
+            zs.append(dec.decode_frame(forced=forced[t], logits=True)[1])
+        outs.append(np.stack(zs))
+        dec.close()
+    assert np.isfinite(outs[0]).all()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
 def test_continuous_batching_errors():
     d = TINY.replace(max_seq_len=24)
     w = make_weights(d, seed=33)

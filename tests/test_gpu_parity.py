@@ -270,8 +270,49 @@ def test_attention_matches_oracle(Hq, Hkv, D, rows, pos0, splits):
         assert np.allclose(got[m].reshape(Hq, D), ref, rtol=1e-4, atol=1e-5)
 
 
+@pytest.mark.parametrize("Hq,Hkv,D,T,rows,pos0,spike", [
+    (32, 8, 128, 1024, 300, 0, -1),      # three query blocks, a ragged last one
+    (32, 8, 128, 512, 200, 100, -1),     # rows start inside a key tile
+    (4, 2, 64, 200, 130, 5, -1),         # D = 64
+    (8, 1, 128, 300, 1, 250, -1),        # one row, eight heads per KV head
+    (4, 4, 64, 64, 64, 0, -1),           # T below one key tile
+    (32, 8, 128, 2048, 1024, 1024, -1),  # long rows: 16 key tiles
+    (32, 8, 128, 1024, 512, 0, 300),     # a key whose scores jump: O rescaled for some rows of a warp
+])
+def test_prompt_attention_matches_oracle(Hq, Hkv, D, T, rows, pos0, spike):
+    """Causal attention of prompt rows on the tensor cores against the
+    oracle's single-row attention in float64.  The keys past the rows'
+    positions hold NaN: the kernel must never let them reach a result."""
+    from dual_ar_decode_gb300 import op_attention_prompt
+    rng = np.random.default_rng(rows * 31 + T + D)
+    q = (rng.standard_normal((rows, Hq * D)) * 2.0).astype(np.float32)
+    Kf32 = rng.standard_normal((Hkv, T, D)).astype(np.float32)
+    if spike >= 0:   # scores of this key 8x larger: the rows' maximum grows by far more than 2^8
+        Kf32[:, spike, :] *= 8.0
+    K = f32_to_bf16_bits(Kf32)
+    V = f32_to_bf16_bits(rng.standard_normal((Hkv, T, D)).astype(np.float32))
+    K[:, pos0 + rows:, :] = 0x7FC0   # bf16 NaN beyond the last key
+    V[:, pos0 + rows:, :] = 0x7FC0
+    qd = torch.from_numpy(q).to(DEV)
+    Kd, Vd = dev_u16(K), dev_u16(V)
+    out = torch.full((rows, Hq * D), np.nan, dtype=torch.float32, device=DEV)
+    op_attention_prompt(qd.data_ptr(), Kd.data_ptr(), Vd.data_ptr(), T, Hq, Hkv, D, rows, pos0,
+                        out.data_ptr())
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    Kf, Vf = oracle.bf16_bits_to_f64(K), oracle.bf16_bits_to_f64(V)
+    ref = np.stack([oracle.attention_row(q[m].reshape(Hq, D).astype(np.float64), Kf, Vf,
+                                         pos0 + m + 1).reshape(-1) for m in range(rows)])
+    # queries carry ~2^-16 relative (bf16 hi + lo); each weight enters the
+    # second product as bf16 (2^-9 relative), which moves an output by at
+    # most 2^-9 of its spread of V values
+    assert np.max(np.abs(got - ref)) <= 2.0 ** -8 * np.max(np.abs(Vf[np.isfinite(Vf)]))
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2.0 ** -9
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (200, 6144, 2560), (77, 2560, 9728),
-                                   (1, 256, 128), (300, 19456, 2560), (129, 2560, 4096)])
+                                   (1, 256, 128), (300, 19456, 2560), (129, 2560, 4096),
+                                   (1024, 2560, 9728)])
 def test_tensor_core_gemm_matches_oracle(M, N, K):
     """The prompt GEMM (tcgen05 / TMEM) against A @ W^T in float64."""
     rng = np.random.default_rng(M * 7 + N + K)
@@ -283,6 +324,10 @@ def test_tensor_core_gemm_matches_oracle(M, N, K):
     op_gemm(Ad.data_ptr(), Wd.data_ptr(), M, N, K, C.data_ptr())
     ref = oracle.linear(oracle.bf16_bits_to_f64(Wb), A.astype(np.float64))
     got = C.cpu().numpy().astype(np.float64)
+    # split-K partials meet in split order: a second call is bitwise equal
+    C2 = torch.full((M, N), np.nan, dtype=torch.float32, device=DEV)
+    op_gemm(Ad.data_ptr(), Wd.data_ptr(), M, N, K, C2.data_ptr())
+    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.isfinite(got).all()
     # hi + lo bf16 parts carry A to ~2^-17 relative; fp32 tensor-core

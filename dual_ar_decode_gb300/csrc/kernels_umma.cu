@@ -813,19 +813,20 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
 // "Why You Need This": grouped-query attention; the tuna-fish README's
 // prefill tokens/s).  One CTA per (block of 128 query rows, query head); the
 // keys 0..pos of every row are visited in tiles of 128:
-//   * warp 0 loads the block's queries once (bf16 hi and lo parts) and the
-//     K and V tiles of the head's KV group into a two-stage ring (TMA,
-//     128-byte swizzle; paged caches: one box per 32-position page);
+//   * warp 0 loads the block's queries once (bf16 hi and lo parts), the K
+//     tiles of the head's KV group into two stages and the V tiles into one
+//     (TMA, 128-byte swizzle; paged caches: one box per 32-position page);
 //   * warp 1 issues S = Q K^T (hi and lo parts, fp32 in TMEM columns 0..127)
-//     and, once the probabilities are in shared memory, O += P V (TMEM
-//     columns 128..; V is read in its cache layout, an MN-major operand);
+//     and, once the probabilities are in shared memory, O += P V (hi and lo
+//     parts of P; TMEM columns 128..; V is read in its cache layout, an
+//     MN-major operand);
 //   * warps 2-5 own one query row each (its TMEM lane): they read the row's
 //     128 scores, apply the 1/sqrt(D) scale and the causal mask, keep the
-//     running maximum m and the sum l of the bf16 weights, and write
-//     p = 2^(s - m) as bf16 (so O / l is a convex combination of V rows).  O is
-//     rescaled (read, scaled, written back in TMEM) only when the maximum
-//     grows by more than 2^8, so p <= 256 and nothing overflows; the same m
-//     scales l, so the result is exact up to rounding.
+//     running maximum m and sum l, and write p = 2^(s - m) as bf16 hi and lo
+//     parts (about 16 significant bits, like the activations of the prompt
+//     GEMMs).  O is rescaled (read, scaled, written back in TMEM) only when
+//     the maximum grows by more than 2^8, so p <= 256 and nothing overflows;
+//     the same m scales l, so the result is exact up to rounding.
 // V rows past the block's last key are zeroed in shared memory before the
 // product (the cache holds stale rows there; their p is 0, but 0 x NaN is
 // not).  Bounded waits; TMEM always released.
@@ -834,11 +835,11 @@ struct PAttn {
   static constexpr int kBoxes = D / 64;            // 64-column boxes per row
   static constexpr int kQ = 128 * D * 2;           // one query part, bytes
   static constexpr int kKV = 128 * D * 2;          // one K or V tile
-  static constexpr int kP = 128 * 128 * 2;         // probabilities (bf16)
-  static constexpr int kStages = 2;
-  static constexpr size_t kOffKV = 2 * (size_t)kQ;
-  static constexpr size_t kOffP = kOffKV + (size_t)kStages * 2 * kKV;
-  static constexpr size_t kOffBar = kOffP + kP;
+  static constexpr int kP = 128 * 128 * 2;         // one part of the probabilities
+  static constexpr size_t kOffK = 2 * (size_t)kQ;  // [2 stages]
+  static constexpr size_t kOffV = kOffK + 2 * (size_t)kKV;
+  static constexpr size_t kOffP = kOffV + kKV;     // [hi, lo]
+  static constexpr size_t kOffBar = kOffP + 2 * (size_t)kP;
   static constexpr size_t kSmem = 1024 + kOffBar + 128;
   static constexpr uint32_t kCols = 256;           // S: 0..127, O: 128..
   // kind::f16, fp32 accumulate, bf16 operands, M = 128.  S: B (keys x D)
@@ -896,18 +897,22 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sq = smem;                    // [hi, lo][boxes][128 rows][128 B]
-  uint8_t* skv = smem + C::kOffKV;       // [stage][K, V][boxes][128 rows][128 B]
-  uint8_t* sp = smem + C::kOffP;         // [2 key halves][128 rows][128 B]
+  uint8_t* sk = smem + C::kOffK;         // [stage][boxes][128 rows][128 B]
+  uint8_t* sv = smem + C::kOffV;         // [boxes][128 rows][128 B]
+  uint8_t* sp = smem + C::kOffP;         // [hi, lo][2 key halves][128 rows][128 B]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bar;
-  uint64_t* kv_full = bar + 1;           // [2]
-  uint64_t* kv_empty = bar + 3;          // [2]
-  uint64_t* s_full = bar + 5;
-  uint64_t* p_full = bar + 6;
-  uint64_t* o_full = bar + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 8);
+  uint64_t* k_full = bar + 1;            // [2]
+  uint64_t* k_empty = bar + 3;           // [2]
+  uint64_t* v_full = bar + 5;
+  uint64_t* v_empty = bar + 6;
+  uint64_t* s_full = bar + 7;
+  uint64_t* p_full = bar + 8;
+  uint64_t* o_full = bar + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 10);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  volatile uint32_t* issued_tiles = tmem_slot + 2;
+  volatile uint32_t* issued_k = tmem_slot + 2;
+  volatile uint32_t* issued_v = tmem_slot + 3;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = (a.P + 127) / 128;
@@ -922,14 +927,17 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(p_full, 128);
     mbar_init(o_full, 1);
     *abort_flag = 0;
-    *issued_tiles = 0;
+    *issued_k = 0;
+    *issued_v = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -957,34 +965,36 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(sq + b * 16384, &map_qhi, h * D + b * 64, q0, q_full);
         tma_load_2d(sq + C::kQ + b * 16384, &map_qlo, h * D + b * 64, q0, q_full);
       }
-      int j = 0;
-      for (; j < nt; ++j) {
+      // one tile of K or V rows (128 keys from kbase) into dst
+      auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, int kbase, uint64_t* b_) {
+        if (a.kv_tbl) {
+          for (int pg = 0; pg < 128 / kKvPage; ++pg) {
+            const int pi = kbase / kKvPage + pg;
+            const int page = pi < a.kv_npp ? __ldg(a.kv_tbl + (size_t)a.seq * a.kv_npp + pi) : 0;
+            const int y = (page * a.Hkv + g) * kKvPage;
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_2d(dst + b * 16384 + pg * (kKvPage * 128), map, b * 64, y, b_);
+          }
+        } else {
+          for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(dst + b * 16384, map, b * 64, g * a.T + kbase, b_);
+        }
+      };
+      for (int j = 0; j < nt; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&kv_empty[st], ((j >> 1) - 1) & 1, a.err)) {
+        if (j >= 2 && !mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, a.err)) {
           *abort_flag = 1;
           break;
         }
-        uint8_t* kdst = skv + (size_t)st * 2 * C::kKV;
-        uint8_t* vdst = kdst + C::kKV;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kKV);
-        if (a.kv_tbl) {
-          for (int pg = 0; pg < 4; ++pg) {
-            const int pi = (j * 128) / kKvPage + pg;
-            const int page = pi < a.kv_npp ? __ldg(a.kv_tbl + (size_t)a.seq * a.kv_npp + pi) : 0;
-            const int y = (page * a.Hkv + g) * kKvPage;
-            for (int b = 0; b < C::kBoxes; ++b) {
-              tma_load_2d(kdst + b * 16384 + pg * 4096, &map_k, b * 64, y, &kv_full[st]);
-              tma_load_2d(vdst + b * 16384 + pg * 4096, &map_v, b * 64, y, &kv_full[st]);
-            }
-          }
-        } else {
-          const int y = g * a.T + j * 128;
-          for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_2d(kdst + b * 16384, &map_k, b * 64, y, &kv_full[st]);
-            tma_load_2d(vdst + b * 16384, &map_v, b * 64, y, &kv_full[st]);
-          }
+        mbar_arrive_expect_tx(&k_full[st], C::kKV);
+        load_tile(&map_k, sk + (size_t)st * C::kKV, j * 128, &k_full[st]);
+        *issued_k = static_cast<uint32_t>(j + 1);
+        if (j >= 1 && !mbar_wait(v_empty, (j - 1) & 1, a.err)) {
+          *abort_flag = 1;
+          break;
         }
-        *issued_tiles = static_cast<uint32_t>(j + 1);
+        mbar_arrive_expect_tx(v_full, C::kKV);
+        load_tile(&map_v, sv, j * 128, v_full);
+        *issued_v = static_cast<uint32_t>(j + 1);
       }
     }
   } else if (warp == 1) {
@@ -993,12 +1003,12 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = mbar_wait(q_full, 0, a.err);
       const uint32_t qb = smem_u32(sq);
       const uint32_t pb = smem_u32(sp);
+      const uint32_t vb = smem_u32(sv);
       for (int j = 0; ok && j < nt; ++j) {
         const int st = j & 1;
-        if (*abort_flag || !mbar_wait(&kv_full[st], (j >> 1) & 1, a.err)) break;
+        if (*abort_flag || !mbar_wait(&k_full[st], (j >> 1) & 1, a.err)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t kb = smem_u32(skv + (size_t)st * 2 * C::kKV);
-        const uint32_t vb = kb + C::kKV;
+        const uint32_t kb = smem_u32(sk + (size_t)st * C::kKV);
 #pragma unroll
         for (int prt = 0; prt < 2; ++prt)
 #pragma unroll
@@ -1007,16 +1017,19 @@ __global__ void __launch_bounds__(192, 1)
             mma_f16(tmem_s, smem_desc_sw128(qb + prt * C::kQ + off), smem_desc_sw128(kb + off),
                     C::kIdescS, (prt > 0 || kk > 0) ? 1u : 0u);
           }
+        mma_commit(&k_empty[st]);
         mma_commit(s_full);
-        if (!mbar_wait(p_full, j & 1, a.err)) break;
+        if (!mbar_wait(p_full, j & 1, a.err) || !mbar_wait(v_full, j & 1, a.err)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_f16(tmem_o, smem_desc_sw128(pb + aoff), smem_desc_sw128_mn(vb + kk * 2048, 16384),
-                  C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&kv_empty[st]);
+        for (int prt = 0; prt < 2; ++prt)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = prt * C::kP + (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16(tmem_o, smem_desc_sw128(pb + aoff), smem_desc_sw128_mn(vb + kk * 2048, 16384),
+                    C::kIdescO, (j > 0 || prt > 0 || kk > 0) ? 1u : 0u);
+          }
+        mma_commit(v_empty);
         mma_commit(o_full);
       }
     }
@@ -1051,7 +1064,7 @@ __global__ void __launch_bounds__(192, 1)
         mx = fmaxf(mx, s[i]);
       }
       // The previous product must be done before O is rescaled or the
-      // probability tile is overwritten.
+      // probability tiles are overwritten.
       if (j > 0) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(o_full, (j - 1) & 1, a.err) ? 1 : 0)) {
           ok = false;
@@ -1079,40 +1092,46 @@ __global__ void __launch_bounds__(192, 1)
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      // p = 2^(s - m) as bf16, the row's 128 keys in two 64-key halves of the
-      // 128-byte swizzle layout (16-byte chunk c of row r at c ^ (r & 7))
+      // p = 2^(s - m) as bf16 hi and lo parts, the row's 128 keys in two
+      // 64-key halves of the 128-byte swizzle layout (16-byte chunk c of row
+      // r at c ^ (r & 7))
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = exp2f(s[i] - m_used);
+        l += s[i];
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint8_t* rowp = sp + half * 16384 + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
+          uint32_t wh[4], wl[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint16_t b0 = f32_to_bf16(exp2f(s[half * 64 + c * 8 + 2 * e] - m_used));
-            const uint16_t b1 = f32_to_bf16(exp2f(s[half * 64 + c * 8 + 2 * e + 1] - m_used));
-            l += bf16_to_f32(b0);  // the weights the product uses: O / l stays a convex combination
-            l += bf16_to_f32(b1);
-            w[e] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+            const float p0 = s[half * 64 + c * 8 + 2 * e];
+            const float p1 = s[half * 64 + c * 8 + 2 * e + 1];
+            const uint16_t h0 = f32_to_bf16(p0), h1 = f32_to_bf16(p1);
+            wh[e] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+            wl[e] = static_cast<uint32_t>(f32_to_bf16(p0 - bf16_to_f32(h0))) |
+                    (static_cast<uint32_t>(f32_to_bf16(p1 - bf16_to_f32(h1))) << 16);
           }
-          *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          const int cs = (c ^ (r & 7)) << 4;
+          *reinterpret_cast<uint4*>(rowp + cs) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+          *reinterpret_cast<uint4*>(rowp + C::kP + cs) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
       }
-      if (j == nt - 1) {
+      if (j == nt - 1 && kbase + r > last_key) {
         // V rows past the block's last key: zero (this thread's row r of the
         // tile, every column box), after the tile has landed
-        const int st = j & 1;
-        if (kbase + r > last_key) {
-          if (!mbar_wait(&kv_full[st], (j >> 1) & 1, a.err)) {
-            ok = false;
-          } else {
-            uint8_t* vrow = skv + (size_t)st * 2 * C::kKV + C::kKV + r * 128;
+        if (!mbar_wait(v_full, j & 1, a.err)) {
+          ok = false;
+        } else {
+          uint8_t* vrow = sv + r * 128;
 #pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b)
+          for (int b = 0; b < C::kBoxes; ++b)
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(vrow + b * 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(vrow + b * 16384 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
@@ -1156,10 +1175,11 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 0 && lane == 0) {
     // Copies still in flight (a tile abandoned after an expired wait) land
-    // before the CTA leaves: the last fill of each stage, bounded.
-    const int n = static_cast<int>(*issued_tiles);
-    for (int j = n > 2 ? n - 2 : 0; j < n; ++j)
-      if (!mbar_wait(&kv_full[j & 1], (j >> 1) & 1, a.err)) break;
+    // before the CTA leaves: the last fill of each buffer, bounded.
+    const int nk = static_cast<int>(*issued_k), nv = static_cast<int>(*issued_v);
+    for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j)
+      if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, a.err)) break;
+    if (nv > 0) mbar_wait(v_full, (nv - 1) & 1, a.err);
     mbar_wait(q_full, 0, a.err);
   }
   if (warp == 1) {

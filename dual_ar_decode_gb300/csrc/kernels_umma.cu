@@ -863,6 +863,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t l
   return d;
 }
 
+// Two floats -> two bf16 (round to nearest even) in one word, the first in
+// the low half (the hardware conversion; inputs here are finite).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// 2^x with the SFU's approximate base-2 exponential (relative error about
+// 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -1058,11 +1074,17 @@ __global__ void __launch_bounds__(192, 1)
       }
       const int kbase = j * 128;
       float mx = -INFINITY;
+      if (kbase + 127 <= a.pos0 + q0) {  // a tile below the block's diagonal: no mask
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = (kbase + i <= qpos) ? s[i] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          s[i] = (kbase + i <= qpos) ? s[i] : -INFINITY;
+          mx = fmaxf(mx, s[i]);
+        }
       }
+      mx *= a.scale_log2;  // the scale is positive: max(s) * c = max(s * c)
       // The previous product must be done before O is rescaled or the
       // probability tiles are overwritten.
       if (j > 0) {
@@ -1076,7 +1098,7 @@ __global__ void __launch_bounds__(192, 1)
       // decided per warp: tcgen05.ld / st are warp-collective, so every lane
       // takes part (alpha = 1 for rows that keep their maximum).
       const bool grow = mx > m_used + 8.0f;
-      const float alpha = grow ? exp2f(m_used - mx) : 1.0f;
+      const float alpha = grow ? ex2_approx(m_used - mx) : 1.0f;
       if (grow) {
         l *= alpha;
         m_used = mx;
@@ -1095,9 +1117,11 @@ __global__ void __launch_bounds__(192, 1)
       // p = 2^(s - m) as bf16 hi and lo parts, the row's 128 keys in two
       // 64-key halves of the 128-byte swizzle layout (16-byte chunk c of row
       // r at c ^ (r & 7))
+      // p = 2^(s * c - m): one FMA and one ex2 per key (masked keys: 2^-inf = 0)
+      const float nm = -m_used;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        s[i] = exp2f(s[i] - m_used);
+        s[i] = ex2_approx(fmaf(s[i], a.scale_log2, nm));
         l += s[i];
       }
 #pragma unroll
@@ -1110,10 +1134,8 @@ __global__ void __launch_bounds__(192, 1)
           for (int e = 0; e < 4; ++e) {
             const float p0 = s[half * 64 + c * 8 + 2 * e];
             const float p1 = s[half * 64 + c * 8 + 2 * e + 1];
-            const uint16_t h0 = f32_to_bf16(p0), h1 = f32_to_bf16(p1);
-            wh[e] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-            wl[e] = static_cast<uint32_t>(f32_to_bf16(p0 - bf16_to_f32(h0))) |
-                    (static_cast<uint32_t>(f32_to_bf16(p1 - bf16_to_f32(h1))) << 16);
+            wh[e] = bf16x2_rn(p0, p1);
+            wl[e] = bf16x2_rn(p0 - __uint_as_float(wh[e] << 16), p1 - __uint_as_float(wh[e] & 0xFFFF0000u));
           }
           const int cs = (c ^ (r & 7)) << 4;
           *reinterpret_cast<uint4*>(rowp + cs) = make_uint4(wh[0], wh[1], wh[2], wh[3]);

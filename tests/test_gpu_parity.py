@@ -303,11 +303,11 @@ def test_prompt_attention_matches_oracle(Hq, Hkv, D, T, rows, pos0, spike):
     Kf, Vf = oracle.bf16_bits_to_f64(K), oracle.bf16_bits_to_f64(V)
     ref = np.stack([oracle.attention_row(q[m].reshape(Hq, D).astype(np.float64), Kf, Vf,
                                          pos0 + m + 1).reshape(-1) for m in range(rows)])
-    # queries carry ~2^-16 relative (bf16 hi + lo); each weight enters the
-    # second product as bf16 (2^-9 relative), which moves an output by at
-    # most 2^-9 of its spread of V values
-    assert np.max(np.abs(got - ref)) <= 2.0 ** -8 * np.max(np.abs(Vf[np.isfinite(Vf)]))
-    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2.0 ** -9
+    # queries and weights both enter the products as bf16 hi + lo parts
+    # (about 2^-17 relative each), with fp32 accumulation: measured on GB300
+    # at most 1.9e-5 of max|V| and 6.8e-6 in rel-L2 over these shapes
+    assert np.max(np.abs(got - ref)) <= 2.0 ** -13 * np.max(np.abs(Vf[np.isfinite(Vf)]))
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 2.0 ** -15
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (200, 6144, 2560), (77, 2560, 9728),

@@ -99,6 +99,10 @@ struct GemvParams {
   // HBM keeps streaming across the kernel boundary.
   const uint8_t* pf_w;
   int32_t pf_units, pf_unit, pf_rowbytes, pf_grid, pf_bytes;
+  // QKV GEMV of one sequence (dense caches): after its last weight copy each
+  // CTA also asks L2 for its share of the layer's cached K and V rows
+  // 0..pos-1, which the attention kernel that follows reads.
+  int32_t kv_pf;
   // q/k RMSNorm option: the QKV epilogue stores the q and k pairs as they
   // are (RoPE-pair order, [M][q_dim + kv_dim]) for k_qknorm to finish
   float* qk_raw;

@@ -352,9 +352,14 @@ cudaError_t launch_dg(const AttnParams& p, int M, bool pdl, cudaStream_t s) {
 // and shared-memory footprint only pay off when a CTA's slice is short.
 constexpr int kRowWarps = 8;
 constexpr int kRowUnroll = 4;
+#ifndef TF_ROWS_MINB
+#define TF_ROWS_MINB 2
+#endif
 
+// TF_ROWS_MINB CTAs of 8 warps fit one SM (registers capped to match); the
+// eight-head groups keep more registers.
 template <int D, int G>
-__global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p) {
+__global__ void __launch_bounds__(kRowWarps * 32, G >= 8 ? 2 : TF_ROWS_MINB) k_attn_rows(const AttnParams p) {
   constexpr int DL = D / 32;  // dims per lane
   const int s = blockIdx.x, g = blockIdx.y, m = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -408,9 +413,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p
     const int page = __ldg(p.kv_tbl + (size_t)seq * p.kv_npp + t / kKvPage);
     return (((size_t)page * p.Hkv + g) * kKvPage + t % kKvPage) * D;
   };
-  for (int t0 = k0 + warp * kRowUnroll; t0 < k1; t0 += kRowWarps * kRowUnroll) {
-    // Load up to kRowUnroll rows of K and V (DL bf16 per lane).
-    uint32_t kr[kRowUnroll][DL / 2], vr[kRowUnroll][DL / 2];
+  // Up to kRowUnroll rows of K and V (DL bf16 per lane) from key t0 on.
+  auto load_rows = [&](int t0, uint32_t (&kr)[kRowUnroll][DL / 2], uint32_t (&vr)[kRowUnroll][DL / 2]) {
 #pragma unroll
     for (int u = 0; u < kRowUnroll; ++u) {
       const int t = t0 + u;
@@ -427,6 +431,22 @@ __global__ void __launch_bounds__(kRowWarps * 32) k_attn_rows(const AttnParams p
         }
       }
     }
+  };
+  // The next group of rows is loaded before the current one is used, so two
+  // groups per warp are in flight.
+  uint32_t kn[kRowUnroll][DL / 2], vn[kRowUnroll][DL / 2];
+  int t0 = k0 + warp * kRowUnroll;
+  if (t0 < k1) load_rows(t0, kn, vn);
+  for (; t0 < k1; t0 += kRowWarps * kRowUnroll) {
+    uint32_t kr[kRowUnroll][DL / 2], vr[kRowUnroll][DL / 2];
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u)
+#pragma unroll
+      for (int i = 0; i < DL / 2; ++i) {
+        kr[u][i] = kn[u][i];
+        vr[u][i] = vn[u][i];
+      }
+    if (t0 + kRowWarps * kRowUnroll < k1) load_rows(t0 + kRowWarps * kRowUnroll, kn, vn);
 #pragma unroll
     for (int u = 0; u < kRowUnroll; ++u) {
       if (t0 + u >= k1) break;

@@ -327,6 +327,31 @@ __global__ void __launch_bounds__(kMaxConsumerWarps * 32 + 32, 1) k_gemv(const G
           }
         }
       }
+      // Hint L2 with this CTA's share of the cached K and V rows the
+      // attention after this QKV GEMV reads (they do not depend on it).
+      if (p.kv_pf && !*abort_flag) {
+        const int pos = row_pos(p, 0);
+        if (pos >= 32 && pos <= p.T) {
+          const int hkv = p.kv_dim / p.head_dim;
+          const size_t region = (size_t)pos * p.head_dim * 2;  // one head's cached rows, bytes
+          const size_t total = 2 * (size_t)hkv * region;
+          const size_t b0 = (total * c / G) & ~size_t(255);
+          const size_t b1 = c + 1 == G ? total : (total * (c + 1) / G) & ~size_t(255);
+          const size_t seq_off = (size_t)row_seq(p, 0) * (size_t)p.kv_seq;
+          for (size_t b = b0; b < b1;) {
+            const size_t r = b / region, off = b - r * region;
+            const size_t n = std::min(b1 - b, region - off);
+            const uint16_t* head = (r < (size_t)hkv ? p.Kc : p.Vc) + seq_off +
+                                   (r % hkv) * (size_t)p.T * p.head_dim;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(head) + off;
+            for (size_t o = 0; o < n; o += 32768) {
+              const uint32_t len = static_cast<uint32_t>(std::min<size_t>(32768, n - o));
+              asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + o), "r"(len) : "memory");
+            }
+            b += n;
+          }
+        }
+      }
       // Drain: the last (up to nst) issued copies may still be in flight.
       for (int t = max(0, s - p.nst); t < s; ++t)
         mbar_wait(&full[t % p.nst], (t / p.nst) & 1, p.err);

@@ -45,7 +45,7 @@ constexpr int kMaxBatch = 32;  // sequences per context (fast step 1: 2 rows eac
 constexpr int kIdStride = 16;  // id slots per sequence in the device state
 static_assert(kIdStride == kRepIds, "the repetition ring keeps one frame's id slots");
 #ifndef TF_BATCH_ATTN_CTAS
-#define TF_BATCH_ATTN_CTAS 4
+#define TF_BATCH_ATTN_CTAS 2
 #endif
 constexpr int kBatchAttnCtasPerSm = TF_BATCH_ATTN_CTAS;  // batched attention grid density
 #ifndef TF_BATCH_ATTN_STREAM
@@ -356,6 +356,10 @@ bool uses_select(const tf_sampling* s) { return s->top_k > 0 || s->rep_window > 
 #define TF_GEMV_PREFETCH_BYTES (32 * 1024)
 #endif
 constexpr int kGemvPrefetch = TF_GEMV_PREFETCH_BYTES;  // per CTA, into L2, across a boundary
+#ifndef TF_KV_PREFETCH
+#define TF_KV_PREFETCH 1
+#endif
+constexpr bool kKvPrefetch = TF_KV_PREFETCH;  // QKV GEMVs hint L2 with the cached K / V rows
 
 // The GEMV that follows in the stream (its weight is prefetched into L2).
 struct NextGemv {
@@ -393,6 +397,7 @@ cudaError_t gemv(tf_ctx* c, const Lin& L, int pro, const float* x, const uint16_
       p.kv_tbl = c->kv_tbl;
       p.kv_npp = c->npp;
     }
+    p.kv_pf = kKvPrefetch && epi == EPI_QKV && M == 1 && !layer->paged;
   }
   p.kv_seq = c->kv_seq;
   p.T = c->T;

@@ -313,10 +313,12 @@ cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint
 // the activation rows (bf16 hi / lo parts, [M][K]) on its N side, split over K
 // so that the grid covers the GPU; the last CTA of a weight tile sums the
 // splits' partials in split order (part: skinny_part_floats(), tickets: one
-// per weight tile, zero between launches).
+// per weight tile, zero between launches).  wt = 0: bf16 weights; wt = 1:
+// e4m3 codes (K a multiple of 16) converted to bf16 in shared memory, the
+// fp32 row scale (p.scale) applied in the epilogue.
 int skinny_splits(int N, int K, int num_sms);
 size_t skinny_part_floats(int N, int K, int M, int num_sms);
-cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo,
+cudaError_t launch_gemm_skinny(const GemvParams& p, int wt, const uint16_t* a_hi, const uint16_t* a_lo,
                                int M, float* part, uint32_t* tickets, int num_sms, bool pdl,
                                cudaStream_t s);
 // Rows for a skinny GEMM with a deferred RMSNorm: a = x[m] * w as bf16 hi / lo

@@ -483,38 +483,81 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 constexpr int kSkStages = TF_SKINNY_STAGES;
+#ifndef TF_SKINNY_F8_BSLOTS
+#define TF_SKINNY_F8_BSLOTS 3   // e4m3 weights: bf16 slots the converters fill
+#endif
+#ifndef TF_SKINNY_F8_SLOTS
+#define TF_SKINNY_F8_SLOTS 3    // e4m3 weights: e4m3 + activation slots in flight
+#endif
 constexpr int kSkThreads = 6 * 32;
 
-template <int NB>
+// WT = 0: bf16 weights.  WT = 1: e4m3 weights (fp32 row scale applied in the
+// epilogue), so that HBM only carries the e4m3 bytes: the producer streams
+// each e4m3 slice (8 KB) with its activation parts into a deep ring; the
+// four epilogue warps convert the slice (one row per thread, exactly: every
+// e4m3 value is a bf16 value) into a slot of a shallow ring of bf16 slices,
+// and the MMA reads the bf16 slot and the activation parts where they
+// landed.  Two CTAs per SM for up to 32 rows.
+template <int NB, int WT>
 struct Skinny {
-  static constexpr int kW = 128 * BK * 2;            // weight slice, 16 KB
+  static constexpr int kStages = WT ? TF_SKINNY_F8_BSLOTS : kSkStages;  // WT = 0: weight + activation stages;
+                                                      // WT = 1: bf16 weight slots
+  static constexpr int kW = 128 * BK * 2;            // weight slice (bf16), 16 KB
   static constexpr int kA = NB * BK * 2;             // one activation part
-  static constexpr int kStage = kW + 2 * kA;
+  static constexpr int kW8 = 128 * BK;               // one e4m3 slice
+  static constexpr int kF8 = WT ? TF_SKINNY_F8_SLOTS : 0;  // e4m3 + activation slots
+  static constexpr int kF8Slot = kW8 + 2 * kA;
+  static constexpr int kStage = WT ? kW : kW + 2 * kA;
+  static constexpr size_t kRing = (size_t)kStages * kStage + (size_t)kF8 * kF8Slot;
   static constexpr uint32_t kCols = NB < 32 ? 32u : static_cast<uint32_t>(NB);
   // kind::f16, fp32 accumulate, bf16 A and B, both K-major, M = 128, N = NB.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                      ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   static constexpr size_t kSmem =
-      1024 + (size_t)kSkStages * kStage + (2 * kSkStages + 2) * 8 + 64 + (64 + 4 * NB) * 4;
+      1024 + kRing + (3 * kStages + 2 * kF8 + 2) * 8 + 64 + (64 + 4 * NB) * 4;
   // one split's partial of a tile: [NB][128] fp32
   static constexpr uint32_t kChunk = NB * 128 * 4;
-  static constexpr int kChunksPerRound = (kSkStages * kStage) / kChunk;
+  static constexpr int kChunksPerRound = static_cast<int>(kRing / kChunk);
 };
 
-template <int NB>
+// 8 e4m3 codes (two words) -> 8 bf16 (four words), exactly.
+__device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t a, uint32_t b, uint32_t* o) {
+  const uint32_t w[2] = {a, b};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint16_t pr = static_cast<uint16_t>(w[i] >> (16 * h));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
+      const __half2 hv = *reinterpret_cast<__half2*>(&h2);
+      const float2 f = __half22float2(hv);
+      uint32_t d;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y), "f"(f.x));
+      o[2 * i + h] = d;
+    }
+  }
+}
+
+template <int NB, int WT>
 __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM : 1)
     k_umma_skinny(const __grid_constant__ CUtensorMap map_w,
                   const __grid_constant__ CUtensorMap map_ahi,
                   const __grid_constant__ CUtensorMap map_alo, const GemvParams p, int M, int S,
                   float* part, uint32_t* tickets) {
-  using C = Skinny<NB>;
+  using C = Skinny<NB, WT>;
+  constexpr int kSkStages = C::kStages;
   static_assert(C::kStage % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSkStages * C::kStage);
+  uint8_t* f8 = smem + kSkStages * C::kStage;   // WT = 1: [kF8][e4m3 128 x 64 B | A hi | A lo]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRing);
   uint64_t* empty = full + kSkStages;
-  uint64_t* done = empty + kSkStages;
+  uint64_t* conv = empty + kSkStages;     // WT = 1: the slot's bf16 slice is written
+  uint64_t* f8full = conv + kSkStages;    // WT = 1: an e4m3 slice landed
+  uint64_t* f8empty = f8full + C::kF8;    // WT = 1: the MMA is done with a slot
+  uint64_t* done = f8empty + C::kF8;
   uint64_t* red = done + 1;   // split partials staged into the (idle) ring
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -537,6 +580,11 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
     for (int s = 0; s < kSkStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], 128);
+    }
+    for (int s = 0; s < C::kF8; ++s) {
+      mbar_init(&f8full[s], 1);
+      mbar_init(&f8empty[s], 1);
     }
     mbar_init(done, 1);
     mbar_init(red, 1);
@@ -563,6 +611,47 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       prefetch_tensormap(&map_w);
+      if constexpr (WT == 1) {
+        prefetch_tensormap(&map_ahi);
+        prefetch_tensormap(&map_alo);
+        // e4m3 slices into their ring; the converters load the activations.
+        int issued = 0;
+        for (int i = 0; i < nkb; ++i) {
+          const int s8 = i % C::kF8;
+          if (i >= C::kF8 && !mbar_wait(&f8empty[s8], ((i / C::kF8) & 1) ^ 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          uint8_t* sl = f8 + s8 * C::kF8Slot;
+          mbar_arrive_expect_tx(&f8full[s8], C::kF8Slot);
+          tma_load_2d_hint(sl, &map_w, (kb0 + i) * BK, n0, &f8full[s8], pol);
+          if (i == (nkb < C::kF8 ? nkb : C::kF8) - 1 || i >= C::kF8) {
+            // the activation parts come from the previous kernel: the first
+            // ring's worth of weight slices is issued before waiting for it
+            if (i == (nkb < C::kF8 ? nkb : C::kF8) - 1) {
+              pdl_wait();
+              for (int j = 0; j < i; ++j) {
+                uint8_t* sj = f8 + j * C::kF8Slot;
+                tma_load_2d(sj + C::kW8, &map_ahi, (kb0 + j) * BK, 0, &f8full[j]);
+                tma_load_2d(sj + C::kW8 + C::kA, &map_alo, (kb0 + j) * BK, 0, &f8full[j]);
+              }
+            }
+            tma_load_2d(sl + C::kW8, &map_ahi, (kb0 + i) * BK, 0, &f8full[s8]);
+            tma_load_2d(sl + C::kW8 + C::kA, &map_alo, (kb0 + i) * BK, 0, &f8full[s8]);
+          }
+          issued = i + 1;
+          // L2 requests kSkPrefetch slices beyond the ring's
+          if (i == 0)
+            for (int j = C::kF8; j < nkb && j < C::kF8 + kSkPrefetch; ++j)
+              tma_prefetch_l2(&map_w, (kb0 + j) * BK, n0);
+          else if (i >= C::kF8 && i + kSkPrefetch < nkb)
+            tma_prefetch_l2(&map_w, (kb0 + i + kSkPrefetch) * BK, n0);
+        }
+        // the last fills still in flight land before the CTA leaves (bounded)
+        for (int i = issued > C::kF8 ? issued - C::kF8 : 0; i < issued; ++i)
+          if (!mbar_wait(&f8full[i % C::kF8], (i / C::kF8) & 1, p.err)) break;
+      } else {
       prefetch_tensormap(&map_ahi);
       prefetch_tensormap(&map_alo);
       // The weights do not depend on the previous kernel: fill the ring with
@@ -604,25 +693,32 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
       if (*abort_flag)
         for (int i = from; i < issued; ++i)
           if (!mbar_wait(&full[i % kSkStages], (i / kSkStages) & 1, p.err)) break;
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       for (int i = 0; i < nkb; ++i) {
         const int s = i % kSkStages;
-        if (*abort_flag || !mbar_wait(&full[s], (i / kSkStages) & 1, p.err)) {
+        const int s8 = WT ? i % C::kF8 : 0;
+        if (*abort_flag ||
+            (WT ? (!mbar_wait(&conv[s], (i / kSkStages) & 1, p.err) ||
+                   !mbar_wait(&f8full[s8], (i / C::kF8) & 1, p.err))
+                : !mbar_wait(&full[s], (i / kSkStages) & 1, p.err))) {
           *abort_flag = 1;
           break;
         }
         *consumed = static_cast<uint32_t>(i + 1);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t st = smem_u32(smem + s * C::kStage);
+        // activation parts: behind the weights (WT = 0) or in the e4m3 slot
+        const uint32_t at = WT ? smem_u32(f8 + s8 * C::kF8Slot + C::kW8) : st + C::kW;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
           for (int prt = 0; prt < 2; ++prt) {
             const uint64_t wd = smem_desc_sw128(st + kk * 32);
-            const uint64_t ad = smem_desc_sw128(st + C::kW + prt * C::kA + kk * 32);
+            const uint64_t ad = smem_desc_sw128(at + prt * C::kA + kk * 32);
             const uint32_t acc = (i > 0 || kk > 0 || prt > 0) ? 1u : 0u;
             asm volatile(
                 "{\n\t.reg .pred q;\n\t"
@@ -633,14 +729,47 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
           }
         }
         mma_commit(&empty[s]);
+        if constexpr (WT == 1) mma_commit(&f8empty[s8]);
       }
       mma_commit(done);
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    if constexpr (WT == 1) {
+      // Slot sb of the bf16 ring takes slice i once the MMA is done with it:
+      // the e4m3 slice is converted into the 128-byte swizzle layout
+      // (16-byte chunk c of row r at c ^ (r & 7)).
+      for (int i = 0; i < nkb; ++i) {
+        const int sb = i % kSkStages, s8 = i % C::kF8;
+        bool ok = !*abort_flag;
+        if (ok && i >= kSkStages) ok = mbar_wait(&empty[sb], ((i / kSkStages) & 1) ^ 1, p.err);
+        if (ok) ok = mbar_wait(&f8full[s8], (i / C::kF8) & 1, p.err);
+        if (ok) {
+          // four lanes per 64-byte row, eight rows per warp access (a
+          // contiguous 512 bytes: no bank conflicts); warp w takes rows
+          // 32w .. 32w + 31
+          const int q4 = lane & 3;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = (et >> 5) * 32 + k * 8 + (lane >> 2);
+            const uint4 w = *reinterpret_cast<const uint4*>(f8 + s8 * C::kF8Slot + r * BK + q4 * 16);
+            uint32_t o[8];
+            e4m3x8_to_bf16x8(w.x, w.y, o);
+            e4m3x8_to_bf16x8(w.z, w.w, o + 4);
+            uint8_t* row = smem + sb * C::kStage + r * 128;
+            *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        } else {
+          *abort_flag = 1;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&conv[sb]);
+      }
+    }
     pdl_wait();
     const int q = warp & 3;
-    const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
     const int nl = q * 32 + lane;     // weight row within the tile (TMEM lane)
     const int n = n0 + nl;
     // Everything the epilogue reads from global memory is loaded while the
@@ -1271,27 +1400,41 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NB>
+// uint8 [rows][cols] (e4m3 codes), box of 64 columns x box_rows rows, no
+// swizzle (rows of 64 bytes in shared memory).
+bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NB, int WT>
 cudaError_t launch_skinny_nb(const GemvParams& p, const CUtensorMap& mw, const CUtensorMap& mhi,
                              const CUtensorMap& mlo, int M, int S, float* part, uint32_t* tickets,
                              bool pdl, cudaStream_t s) {
   static DeviceOnce once;
   cudaError_t ea = device_once(once, [] {
-    return cudaFuncSetAttribute(k_umma_skinny<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Skinny<NB>::kSmem);
+    return cudaFuncSetAttribute(k_umma_skinny<NB, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Skinny<NB, WT>::kSmem);
   });
   if (ea) return ea;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((p.N + 127) / 128, S);
   cfg.blockDim = dim3(kSkThreads);
-  cfg.dynamicSmemBytes = Skinny<NB>::kSmem;
+  cfg.dynamicSmemBytes = Skinny<NB, WT>::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_umma_skinny<NB>, mw, mhi, mlo, p, M, S, part, tickets);
+  return cudaLaunchKernelEx(&cfg, k_umma_skinny<NB, WT>, mw, mhi, mlo, p, M, S, part, tickets);
 }
 
 int skinny_nb(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
@@ -1310,24 +1453,34 @@ size_t skinny_part_floats(int N, int K, int M, int num_sms) {
   return S > 1 ? (size_t)S * ((N + 127) / 128) * 128 * skinny_nb(M) : 0;
 }
 
-cudaError_t launch_gemm_skinny(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo,
+cudaError_t launch_gemm_skinny(const GemvParams& p, int wt, const uint16_t* a_hi, const uint16_t* a_lo,
                                int M, float* part, uint32_t* tickets, int num_sms, bool pdl,
                                cudaStream_t s) {
-  if (M < 1 || M > 64 || p.N < 2 || (p.N & 1) || p.K < 8 || (p.K % 8)) return cudaErrorInvalidValue;
+  if (M < 1 || M > 64 || p.N < 2 || (p.N & 1) || p.K < 8 || (p.K % 8) || wt < 0 || wt > 1 ||
+      (wt == 1 && p.K % 16))
+    return cudaErrorInvalidValue;
   const int NB = skinny_nb(M);
   // activation row m is row m * in_rps + in_rps - 1 of the parts
   const int rs = p.in_rps > 1 ? p.in_rps : 1;
   const size_t a0 = (size_t)(rs - 1) * p.K;
   CUtensorMap mw, mhi, mlo;
-  if (!make_map(&mw, p.W, p.N, p.K, 128) || !make_map(&mhi, a_hi + a0, M, p.K, NB, (size_t)rs * p.K) ||
+  if (!(wt ? make_map_u8(&mw, p.W, p.N, p.K, 128) : make_map(&mw, p.W, p.N, p.K, 128)) ||
+      !make_map(&mhi, a_hi + a0, M, p.K, NB, (size_t)rs * p.K) ||
       !make_map(&mlo, a_lo + a0, M, p.K, NB, (size_t)rs * p.K))
     return cudaErrorInvalidValue;
   const int S = skinny_splits(p.N, p.K, num_sms);
   if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
+  if (wt == 1) {
+    switch (NB) {
+      case 16: return launch_skinny_nb<16, 1>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+      case 32: return launch_skinny_nb<32, 1>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+      default: return launch_skinny_nb<64, 1>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+    }
+  }
   switch (NB) {
-    case 16: return launch_skinny_nb<16>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-    case 32: return launch_skinny_nb<32>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-    default: return launch_skinny_nb<64>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+    case 16: return launch_skinny_nb<16, 0>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+    case 32: return launch_skinny_nb<32, 0>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
+    default: return launch_skinny_nb<64, 0>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
   }
 }
 

@@ -54,6 +54,12 @@ constexpr int kBatchAttnCtasPerSm = TF_BATCH_ATTN_CTAS;  // batched attention gr
 // Batched attention kernel: 1 = streaming (keys straight from the cache, small
 // shared-memory footprint), 0 = staged (key chunks bulk-copied to shared memory).
 constexpr bool kBatchAttnStream = TF_BATCH_ATTN_STREAM != 0;
+#ifndef TF_SKINNY_FP8
+#define TF_SKINNY_FP8 1
+#endif
+// Batched steps read e4m3 weights directly (converted in the GEMM's shared
+// memory) instead of through a bf16 copy of each linear.
+constexpr bool kSkinnyFp8 = TF_SKINNY_FP8 != 0;
 thread_local std::string g_create_error;
 // Failure test: the n-th following device allocation is refused (0: off).
 std::atomic<int> g_fail_alloc{0};
@@ -661,15 +667,19 @@ cudaError_t skinny(tf_ctx* c, const Lin& L, int set, int M, int epi, float* out,
   // The GEMM streams its weight slices before it waits for the previous
   // kernel (programmatic dependent launch), which is only right for weights
   // no kernel writes: a converted fp8 weight is launched without the overlap.
+  // e4m3 weights are converted to bf16 inside the GEMM (shared memory only).
   bool pdl = true;
-  if (L.s) {  // quantised: exact bf16 copy of the values; the row scale stays in p.scale
+  int wt = 0;
+  if (L.wt == TF_WEIGHT_FP8 && kSkinnyFp8) {
+    wt = 1;
+  } else if (L.s) {  // exact bf16 copy of the values; the row scale stays in p.scale
     if (cudaError_t e = L.wt == 2 ? launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream)
                                   : launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))
       return e;
     p.W = reinterpret_cast<const uint8_t*>(c->wconv);
     pdl = false;
   }
-  return launch_gemm_skinny(p, c->bh[set], c->bl[set], M, c->sk_part, c->sk_tickets, c->num_sms,
+  return launch_gemm_skinny(p, wt, c->bh[set], c->bl[set], M, c->sk_part, c->sk_tickets, c->num_sms,
                             pdl, c->stream);
 }
 
@@ -2099,9 +2109,12 @@ tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, in
   return r;
 }
 
-tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K,
-                            float* C, void* stream) {
-  if (!A || !W || !C || M < 1 || M > 64 || N < 2 || (N & 1) || K < 8 || (K % 8)) return TF_E_INVAL;
+namespace {
+tf_status skinny_op(const float* A, const void* W, int wt, const float* row_scale, int32_t M, int32_t N,
+                    int32_t K, float* C, void* stream) {
+  if (!A || !W || !C || M < 1 || M > 64 || N < 2 || (N & 1) || K < 8 || (K % 8) ||
+      (wt == 1 && (!row_scale || K % 16)))
+    return TF_E_INVAL;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -2127,6 +2140,7 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
   tf_status r = TF_OK;
   GemvParams p = {};
   p.W = reinterpret_cast<const uint8_t*>(W);
+  p.scale = row_scale;
   p.N = N;
   p.K = K;
   p.epi = EPI_STORE;
@@ -2135,7 +2149,7 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
   p.err = err;
   if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || cudaMemsetAsync(tickets, 0, nt * 4, s) != cudaSuccess ||
       launch_split_bf16(A, hi, lo, n, s) != cudaSuccess ||
-      launch_gemm_skinny(p, hi, lo, M, part, tickets, sms, false, s) != cudaSuccess)
+      launch_gemm_skinny(p, wt, hi, lo, M, part, tickets, sms, false, s) != cudaSuccess)
     r = TF_E_CUDA;
   uint32_t e = 0;
   if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -2148,6 +2162,17 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
   cudaFree(part);
   if (r == TF_OK && (e & ERR_TIMEOUT)) r = TF_E_TIMEOUT;
   return r;
+}
+}  // namespace
+
+tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K,
+                            float* C, void* stream) {
+  return skinny_op(A, W, 0, nullptr, M, N, K, C, stream);
+}
+
+tf_status tf_op_gemm_skinny_fp8(const float* A, const uint8_t* W, const float* row_scale, int32_t M,
+                                int32_t N, int32_t K, float* C, void* stream) {
+  return skinny_op(A, W, 1, row_scale, M, N, K, C, stream);
 }
 
 tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64_t rows,

@@ -397,6 +397,16 @@ tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, in
 tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K,
                             float* C, void* stream);
 
+/* tf_op_gemm_skinny with e4m3 weights (the drbaph s2-pro-fp8 card,
+ * "Quantization Details": e4m3 codes with a float32 scale per output row):
+ * C[m][n] = row_scale[n] * sum_k A[m][k] e4m3(W[n][k]).  The codes stream
+ * from memory as they are and are converted to bf16 (exactly) in shared
+ * memory for the tensor cores.  W: uint8 codes [N][K] device; row_scale:
+ * float32 [N] device.  K a multiple of 16; other arguments and errors as
+ * tf_op_gemm_skinny.  Codes must be finite (tf_load_weights refuses NaN). */
+tf_status tf_op_gemm_skinny_fp8(const float* A, const uint8_t* W, const float* row_scale, int32_t M,
+                                int32_t N, int32_t K, float* C, void* stream);
+
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
  * TF_DTYPE_BF16), e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3), or

@@ -57,6 +57,38 @@ def test_skinny_gemm_matches_oracle(M, N, K):
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-5
 
 
+@pytest.mark.parametrize("M,N,K,all_codes", [(16, 6144, 2560, False), (32, 19456, 2560, False),
+                                             (17, 2560, 9728, False), (3, 200, 208, False),
+                                             (64, 4096, 2560, False), (16, 300, 512, True)])
+def test_skinny_gemm_fp8_matches_oracle(M, N, K, all_codes):
+    """The e4m3 skinny GEMM (codes converted to bf16 in shared memory, row
+    scale in the epilogue) against A @ dequant(W)^T in float64, with the
+    oracle's own quantiser (or every finite code, with random row scales)."""
+    from dual_ar_decode_gb300 import op_gemm_skinny_fp8
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    if all_codes:
+        codes = (np.arange(N * K) % 256).astype(np.uint8).reshape(N, K)
+        codes[(codes & 0x7F) == 0x7F] = 0          # NaN codes are refused at load
+        scale = rng.uniform(0.5, 2.0, N).astype(np.float32) / 448.0
+    else:
+        codes, scale = oracle.fp8_quantize_rows(
+            f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32) * 0.02))
+    Ad = torch.from_numpy(A).to(DEV)
+    Wd = torch.from_numpy(np.ascontiguousarray(codes)).to(DEV)
+    Sd = torch.from_numpy(np.asarray(scale, np.float32)).to(DEV)
+    C = torch.full((M, N), np.nan, dtype=torch.float32, device=DEV)
+    op_gemm_skinny_fp8(Ad.data_ptr(), Wd.data_ptr(), Sd.data_ptr(), M, N, K, C.data_ptr())
+    ref = oracle.linear(oracle.fp8_dequant_rows(codes, scale), A.astype(np.float64))
+    got = C.cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.isfinite(got).all()
+    # the bf16 values of the codes are exact; hi + lo activations and fp32
+    # accumulation as in the bf16 case, the row scale one more rounding
+    assert np.max(np.abs(got - ref)) <= 2e-4 * rms
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-5
+
+
 def test_skinny_gemm_is_deterministic_and_rejects_bad_shapes():
     rng = np.random.default_rng(3)
     M, N, K = 16, 2560, 9728

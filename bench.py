@@ -254,14 +254,15 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--profile-range", action="store_true",
                     help="mark the timed decode frames as the profiler range (ncu --profile-from-start off)")
-    ap.add_argument("--op", default=None, choices=["gemv", "gemm", "skinny", "attn"],
+    ap.add_argument("--op", default=None, choices=["gemv", "gemm", "skinny", "attn", "attn_prompt",
+                                                   "prefill"],
                     help="time one kernel on its own instead of the decode step")
     ap.add_argument("--rows", type=int, default=19456)
     ap.add_argument("--cols", type=int, default=2560)
     ap.add_argument("--fp8", action="store_true")
     ap.add_argument("--nvfp4", action="store_true", help="--op gemv: 4-bit block-scaled rows")
     ap.add_argument("--m", type=int, default=None,
-                    help="--op gemm: prompt rows (1024); --op skinny: activation rows (16)")
+                    help="--op gemm / attn_prompt: prompt rows (1024); --op skinny: activation rows (16)")
     args = ap.parse_args()
     if args.op == "gemv":
         return run_gemv_case(args)
@@ -273,6 +274,11 @@ def main():
         return run_skinny_case(args)
     if args.op == "attn":
         return run_attn_case(args)
+    if args.op == "attn_prompt":
+        args.m = args.m or 1024
+        return run_attn_prompt_case(args)
+    if args.op == "prefill":
+        return run_prefill_case(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -577,6 +583,90 @@ def run_attn_case(args):
                       "us_per_call_incl_host_sync": round(us, 3), "kv_bytes": nbytes,
                       "note": "one query row at position T-1; each call syncs for its error word"}),
           flush=True)
+
+
+def run_attn_prompt_case(args):
+    """Causal prompt attention alone (tf_op_attention_prompt: tcgen05, one
+    CTA per 128 query rows and head): --m rows at positions m..2m-1 of a
+    full-size head layout (32 q / 8 kv heads of 128, T = 2m), so each row
+    attends to m + 1 .. 2m keys.  steps calls after W warm-up calls; each call
+    splits the queries into bf16 parts and allocates its scratch.  Prints one
+    JSON line; tflops count 4 * Hq * D * (keys summed over rows) once."""
+    import torch
+    from dual_ar_decode_gb300 import op_attention_prompt
+    dev = torch.device("cuda", 0)
+    m = args.m
+    T, Hq, Hkv, D = 2 * m, 32, 8, 128
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    q = torch.randn(m, Hq * D, device=dev, generator=g)
+    K = torch.randn(Hkv, T, D, device=dev, generator=g).to(torch.bfloat16)
+    V = torch.randn(Hkv, T, D, device=dev, generator=g).to(torch.bfloat16)
+    out = torch.empty(m, Hq * D, device=dev)
+    call = lambda: op_attention_prompt(q.data_ptr(), K.data_ptr(), V.data_ptr(), T, Hq, Hkv, D, m, m,
+                                       out.data_ptr())
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    keys = sum(m + r + 1 for r in range(m))
+    tflops = 4.0 * Hq * D * keys / (ms / 1e3) / 1e12
+    peaks = measured_peaks()
+    print(json.dumps({"op": "attn_prompt", "rows": m, "T": T, "Hq": Hq, "Hkv": Hkv, "D": D,
+                      "ms_per_call": round(ms, 4), "tflops": round(tflops, 2),
+                      "bf16_peak_tflops": peaks["bf16_tflops"], "frac": round(tflops / peaks["bf16_tflops"], 4),
+                      "note": "per call: query split + allocation + kernel; tensor work ~4x the "
+                              "algorithmic flops (hi + lo parts, whole tiles up to the diagonal)"}),
+          flush=True)
+
+
+def run_prefill_case(args):
+    """tf_prefill alone on the workload's model and prompt (--workload):
+    W warm-up prefills, then `steps` timed ones (CUDA events on the
+    library's stream); with --profile-range the last one is bracketed by the
+    profiler range.  Prints one JSON line (ms, prompt tokens/s)."""
+    import torch
+    from dual_ar_decode_gb300 import Decoder
+    from synth import make_prompt
+    wl = WORKLOADS[args.workload]
+    d = wl.dims
+    dev = torch.device("cuda", 0)
+    tensors = device_weights(d, args.seed, dev)
+    dec = Decoder(d, wl.weight_dtype, max_batch=wl.batch)
+    dec.load_weights(tensors)
+    del tensors
+    torch.cuda.empty_cache()
+    prompt = make_prompt(d, wl.prefill, seed=args.seed, batch=wl.batch)
+    stream = torch.cuda.ExternalStream(dec.stream(), device=dev)
+    for _ in range(args.warmup):
+        dec.prefill(prompt)
+    ts = []
+    for i in range(args.steps):
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        last = args.profile_range and i == args.steps - 1
+        e0.record(stream)
+        if last:
+            torch.cuda.profiler.start()
+        dec.prefill(prompt)
+        if last:
+            torch.cuda.synchronize(dev)
+            torch.cuda.profiler.stop()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    dec.close()
+    ms = float(np.median(ts))
+    print(json.dumps({"op": "prefill", "workload": wl.name, "tokens": wl.prefill * wl.batch,
+                      "ms": round(ms, 3), "tok_s": round(wl.prefill * wl.batch / (ms / 1e3), 1),
+                      "note": "prompt ids from the host, frame 0 back to the host"}), flush=True)
 
 
 def run_reference(args, wl, world, rank):

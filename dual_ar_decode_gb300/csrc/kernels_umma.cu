@@ -45,12 +45,23 @@ namespace tf {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kStages = 4;
 constexpr int kTileA = BM * BK * 2;             // 16 KB (one bf16 part)
-constexpr int kTileW = BN * BK * 2;             // 16 KB
-constexpr int kStageBytes = 2 * kTileA + kTileW;  // A hi, A lo, W
 constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTmemCols = 128;
+
+// Prompt GEMM tile shapes: 128 prompt rows x GBN weight rows.  256-wide tiles
+// (where N allows) halve the activation bytes each weight byte needs, and
+// their MMAs are twice as wide.
+template <int GBN>
+struct GemmCfg {
+  static constexpr int kTileW = GBN * BK * 2;              // 16 or 32 KB
+  static constexpr int kStageBytes = 2 * kTileA + kTileW;  // A hi, A lo, W
+  static constexpr int kStages = GBN == 256 ? 3 : 4;
+  static constexpr uint32_t kTmemCols = GBN;
+  // kind::f16, fp32 accumulate, bf16 A and B, both K-major, M = 128, N = GBN.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GBN >> 3) << 17) |
+                                     ((uint32_t)(BM >> 4) << 24);
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 1) * 8 + 64;
+};
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
@@ -74,18 +85,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
-// K-major, M = 128, N = BN.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
+                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -233,11 +239,15 @@ __device__ __forceinline__ void gemm_epi_chunk(const GemvParams& p, int m, int n
   }
 }
 
+template <int GBN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap map_ahi,
                 const __grid_constant__ CUtensorMap map_alo,
                 const __grid_constant__ CUtensorMap map_w, const GemvParams p, int M, int S,
                 float* part, uint32_t* tickets) {
+  using G = GemmCfg<GBN>;
+  constexpr int BN = GBN, kStages = G::kStages, kStageBytes = G::kStageBytes;
+  constexpr uint32_t kTmemCols = G::kTmemCols;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t w_base = st + 2 * kTileA;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            mma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(w_base + kk * 32),
+            mma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(w_base + kk * 32), G::kIdesc,
                      (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
           }
         }
@@ -1518,11 +1528,17 @@ cudaError_t launch_prompt_attention_tc(const uint16_t* q_hi, const uint16_t* q_l
 
 bool gemm_tc_supported(int N, int K) { return N % BN == 0 && K % BK == 0 && encode_fn() != nullptr; }
 
+// Weight rows per tile: 256 for prompts above 512 rows where N allows (at
+// 512 rows the 256-wide tiles were slower: 216 -> 233 ms for 16 x 512 ids).  Short prompts
+// have few tiles and split K many ways; 256-wide partials would make the
+// last CTA's reduce the bottleneck (measured: 128 ids 8.7 -> 14.7 ms).
+int gemm_tc_bn(int M, int N) { return (N % 256 == 0 && M > 512) ? 256 : 128; }
+
 // K splits of a prompt GEMM: the fewest that fill at least 80% of the last
 // wave of CTAs (one CTA per SM), keeping >= 4 K slices per split; else the
 // best fill found.
 int gemm_tc_splits(int M, int N, int K, int num_sms) {
-  const int tiles = ((M + BM - 1) / BM) * (N / BN);
+  const int tiles = ((M + BM - 1) / BM) * (N / gemm_tc_bn(M, N));
   const int smax = std::max(1, std::min(16, (K / BK) / 4));
   int best = 1;
   double best_fill = 0.0;
@@ -1541,10 +1557,10 @@ int gemm_tc_splits(int M, int N, int K, int num_sms) {
 
 size_t gemm_tc_part_floats(int M, int N, int K, int num_sms) {
   const int S = gemm_tc_splits(M, N, K, num_sms);
-  return S > 1 ? (size_t)S * ((M + BM - 1) / BM) * (N / BN) * BM * BN : 0;
+  return S > 1 ? (size_t)S * ((M + BM - 1) / BM) * (size_t)N * BM : 0;
 }
 
-size_t gemm_tc_smem_bytes() { return 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 64; }
+size_t gemm_tc_smem_bytes() { return GemmCfg<256>::kSmem; }
 
 cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s) {
   const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
@@ -1558,24 +1574,33 @@ cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaS
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
-                           float* part, uint32_t* tickets, int num_sms, cudaStream_t s) {
+template <int GBN>
+cudaError_t launch_gemm_tc_bn(const CUtensorMap& ma_hi, const CUtensorMap& ma_lo, const CUtensorMap& mw,
+                              const GemvParams& p, int M, int S, float* part, uint32_t* tickets,
+                              cudaStream_t s) {
   static DeviceOnce once;
   cudaError_t ea = device_once(once, [] {
-    return cudaFuncSetAttribute(k_umma_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)gemm_tc_smem_bytes());
+    return cudaFuncSetAttribute(k_umma_gemm<GBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)GemmCfg<GBN>::kSmem);
   });
   if (ea) return ea;
+  dim3 grid((M + BM - 1) / BM, p.N / GBN, S);
+  k_umma_gemm<GBN><<<grid, kThreads, GemmCfg<GBN>::kSmem, s>>>(ma_hi, ma_lo, mw, p, M, S, part, tickets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
+                           float* part, uint32_t* tickets, int num_sms, cudaStream_t s) {
   if (!gemm_tc_supported(p.N, p.K) || M < 1) return cudaErrorInvalidValue;
+  const int bn = gemm_tc_bn(M, p.N);
   CUtensorMap ma_hi, ma_lo, mw;
   if (!make_map(&ma_hi, a_hi, M, p.K, BM) || !make_map(&ma_lo, a_lo, M, p.K, BM) ||
-      !make_map(&mw, p.W, p.N, p.K, BN))
+      !make_map(&mw, p.W, p.N, p.K, bn))
     return cudaErrorInvalidValue;
   const int S = gemm_tc_splits(M, p.N, p.K, num_sms);
   if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
-  dim3 grid((M + BM - 1) / BM, p.N / BN, S);
-  k_umma_gemm<<<grid, kThreads, gemm_tc_smem_bytes(), s>>>(ma_hi, ma_lo, mw, p, M, S, part, tickets);
-  return cudaGetLastError();
+  return bn == 256 ? launch_gemm_tc_bn<256>(ma_hi, ma_lo, mw, p, M, S, part, tickets, s)
+                   : launch_gemm_tc_bn<128>(ma_hi, ma_lo, mw, p, M, S, part, tickets, s);
 }
 
 }  // namespace tf

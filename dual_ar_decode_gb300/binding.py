@@ -94,6 +94,9 @@ EXPORTS = {
     "tf_op_gemm_skinny_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                              ctypes.c_void_p, ctypes.c_void_p]),
+    "tf_op_gemm_skinny_nvfp4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
     "tf_op_gemv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                   ctypes.POINTER(ctypes.c_float), ctypes.c_void_p]),
@@ -310,6 +313,10 @@ def op_gemm_skinny(A_dev, W_dev, M, N, K, C_dev, stream=0):
 
 def op_gemm_skinny_fp8(A_dev, W_dev, scale_dev, M, N, K, C_dev, stream=0):
     _check(lib().tf_op_gemm_skinny_fp8(A_dev, W_dev, scale_dev, M, N, K, C_dev, stream))
+
+
+def op_gemm_skinny_nvfp4(A_dev, W_dev, scale_dev, M, N, K, C_dev, stream=0):
+    _check(lib().tf_op_gemm_skinny_nvfp4(A_dev, W_dev, scale_dev, M, N, K, C_dev, stream))
 
 
 def op_gemv(W_dev, dtype, scale_dev, rows, cols, x_dev, y_dev, repeat=1, stream=0):

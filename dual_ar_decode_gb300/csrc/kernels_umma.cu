@@ -514,7 +514,9 @@ struct Skinny {
                                                       // WT = 1: bf16 weight slots
   static constexpr int kW = 128 * BK * 2;            // weight slice (bf16), 16 KB
   static constexpr int kA = NB * BK * 2;             // one activation part
-  static constexpr int kW8 = 128 * BK;               // one e4m3 slice
+  // one quantised slice: e4m3 codes (128 x 64 B), or 4-bit codes (128 x 32 B)
+  // followed by the 16-byte scale box that holds its block scales (128 x 16 B)
+  static constexpr int kW8 = WT == 2 ? 128 * 32 + 128 * 16 : 128 * BK;
   static constexpr int kF8 = WT ? TF_SKINNY_F8_SLOTS : 0;  // e4m3 + activation slots
   static constexpr int kF8Slot = kW8 + 2 * kA;
   static constexpr int kStage = WT ? kW : kW + 2 * kA;
@@ -549,12 +551,38 @@ __device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t a, uint32_t b, uint32_
   }
 }
 
+// 16 4-bit codes (w: 8 bytes, element 2i in the low nibble of byte i) times
+// their block scale (e4m3 bits sb) -> 16 bf16 (eight words), exactly: an
+// e2m1 value times an e4m3 value has at most 6 significant bits.
+__device__ __forceinline__ void e2m1x16_to_bf16(const uint2 w, uint32_t sb, uint32_t* o) {
+  const float sc = __uint_as_float((sb & 0x7Fu) << 20) * 1.329227995784915873e36f;  // e4m3 by bit placement, x 2^120
+  const uint32_t v[2] = {w.x, w.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t h[4];
+    asm("{.reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+        " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+        " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3;}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(v[i]));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
+      uint32_t d;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y * sc), "f"(f.x * sc));
+      o[4 * i + b] = d;
+    }
+  }
+}
+
+// WT = 2: 4-bit rows (K/2 code bytes, then K/16 e4m3 block-scale bytes):
+// map_w takes 32-byte code boxes, map_s the 16-byte scale boxes (4 slices'
+// scales each); the row scale is applied in the epilogue.
 template <int NB, int WT>
 __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM : 1)
     k_umma_skinny(const __grid_constant__ CUtensorMap map_w,
                   const __grid_constant__ CUtensorMap map_ahi,
-                  const __grid_constant__ CUtensorMap map_alo, const GemvParams p, int M, int S,
-                  float* part, uint32_t* tickets) {
+                  const __grid_constant__ CUtensorMap map_alo, const __grid_constant__ CUtensorMap map_s,
+                  const GemvParams p, int M, int S, float* part, uint32_t* tickets) {
   using C = Skinny<NB, WT>;
   constexpr int kSkStages = C::kStages;
   static_assert(C::kStage % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
@@ -621,9 +649,10 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       prefetch_tensormap(&map_w);
-      if constexpr (WT == 1) {
+      if constexpr (WT >= 1) {
         prefetch_tensormap(&map_ahi);
         prefetch_tensormap(&map_alo);
+        if (WT == 2) prefetch_tensormap(&map_s);
         // e4m3 slices into their ring; the converters load the activations.
         int issued = 0;
         for (int i = 0; i < nkb; ++i) {
@@ -635,7 +664,12 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
           if (*abort_flag) break;
           uint8_t* sl = f8 + s8 * C::kF8Slot;
           mbar_arrive_expect_tx(&f8full[s8], C::kF8Slot);
-          tma_load_2d_hint(sl, &map_w, (kb0 + i) * BK, n0, &f8full[s8], pol);
+          if constexpr (WT == 2) {
+            tma_load_2d_hint(sl, &map_w, (kb0 + i) * 32, n0, &f8full[s8], pol);
+            tma_load_2d_hint(sl + 128 * 32, &map_s, p.K / 2 + ((kb0 + i) >> 2) * 16, n0, &f8full[s8], pol);
+          } else {
+            tma_load_2d_hint(sl, &map_w, (kb0 + i) * BK, n0, &f8full[s8], pol);
+          }
           if (i == (nkb < C::kF8 ? nkb : C::kF8) - 1 || i >= C::kF8) {
             // the activation parts come from the previous kernel: the first
             // ring's worth of weight slices is issued before waiting for it
@@ -652,11 +686,12 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
           }
           issued = i + 1;
           // L2 requests kSkPrefetch slices beyond the ring's
+          constexpr int kx = WT == 2 ? 32 : BK;  // x extent of one slice's codes
           if (i == 0)
             for (int j = C::kF8; j < nkb && j < C::kF8 + kSkPrefetch; ++j)
-              tma_prefetch_l2(&map_w, (kb0 + j) * BK, n0);
+              tma_prefetch_l2(&map_w, (kb0 + j) * kx, n0);
           else if (i >= C::kF8 && i + kSkPrefetch < nkb)
-            tma_prefetch_l2(&map_w, (kb0 + i + kSkPrefetch) * BK, n0);
+            tma_prefetch_l2(&map_w, (kb0 + i + kSkPrefetch) * kx, n0);
         }
         // the last fills still in flight land before the CTA leaves (bounded)
         for (int i = issued > C::kF8 ? issued - C::kF8 : 0; i < issued; ++i)
@@ -739,14 +774,14 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
           }
         }
         mma_commit(&empty[s]);
-        if constexpr (WT == 1) mma_commit(&f8empty[s8]);
+        if constexpr (WT >= 1) mma_commit(&f8empty[s8]);
       }
       mma_commit(done);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
-    if constexpr (WT == 1) {
+    if constexpr (WT >= 1) {
       // Slot sb of the bf16 ring takes slice i once the MMA is done with it:
       // the e4m3 slice is converted into the 128-byte swizzle layout
       // (16-byte chunk c of row r at c ^ (r & 7)).
@@ -763,10 +798,18 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int r = (et >> 5) * 32 + k * 8 + (lane >> 2);
-            const uint4 w = *reinterpret_cast<const uint4*>(f8 + s8 * C::kF8Slot + r * BK + q4 * 16);
             uint32_t o[8];
-            e4m3x8_to_bf16x8(w.x, w.y, o);
-            e4m3x8_to_bf16x8(w.z, w.w, o + 4);
+            if constexpr (WT == 2) {
+              // lane q4 takes block q4 of the slice: 8 code bytes, its scale byte
+              const uint8_t* sl = f8 + s8 * C::kF8Slot;
+              const uint2 w = *reinterpret_cast<const uint2*>(sl + r * 32 + q4 * 8);
+              const uint32_t sb = sl[128 * 32 + r * 16 + ((kb0 + i) & 3) * 4 + q4];
+              e2m1x16_to_bf16(w, sb, o);
+            } else {
+              const uint4 w = *reinterpret_cast<const uint4*>(f8 + s8 * C::kF8Slot + r * BK + q4 * 16);
+              e4m3x8_to_bf16x8(w.x, w.y, o);
+              e4m3x8_to_bf16x8(w.z, w.w, o + 4);
+            }
             uint8_t* row = smem + sb * C::kStage + r * 128;
             *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -1410,14 +1453,15 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// uint8 [rows][cols] (e4m3 codes), box of 64 columns x box_rows rows, no
-// swizzle (rows of 64 bytes in shared memory).
-bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// uint8 [rows][cols] (e4m3 codes, or 4-bit rows), box of box_cols bytes x
+// box_rows rows, no swizzle.
+bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols = BK) {
   EncodeTiled fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {BK, box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1426,8 +1470,8 @@ bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 
 template <int NB, int WT>
 cudaError_t launch_skinny_nb(const GemvParams& p, const CUtensorMap& mw, const CUtensorMap& mhi,
-                             const CUtensorMap& mlo, int M, int S, float* part, uint32_t* tickets,
-                             bool pdl, cudaStream_t s) {
+                             const CUtensorMap& mlo, const CUtensorMap& ms, int M, int S, float* part,
+                             uint32_t* tickets, bool pdl, cudaStream_t s) {
   static DeviceOnce once;
   cudaError_t ea = device_once(once, [] {
     return cudaFuncSetAttribute(k_umma_skinny<NB, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1444,7 +1488,7 @@ cudaError_t launch_skinny_nb(const GemvParams& p, const CUtensorMap& mw, const C
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_umma_skinny<NB, WT>, mw, mhi, mlo, p, M, S, part, tickets);
+  return cudaLaunchKernelEx(&cfg, k_umma_skinny<NB, WT>, mw, mhi, mlo, ms, p, M, S, part, tickets);
 }
 
 int skinny_nb(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
@@ -1466,32 +1510,34 @@ size_t skinny_part_floats(int N, int K, int M, int num_sms) {
 cudaError_t launch_gemm_skinny(const GemvParams& p, int wt, const uint16_t* a_hi, const uint16_t* a_lo,
                                int M, float* part, uint32_t* tickets, int num_sms, bool pdl,
                                cudaStream_t s) {
-  if (M < 1 || M > 64 || p.N < 2 || (p.N & 1) || p.K < 8 || (p.K % 8) || wt < 0 || wt > 1 ||
-      (wt == 1 && p.K % 16))
+  if (M < 1 || M > 64 || p.N < 2 || (p.N & 1) || p.K < 8 || (p.K % 8) || wt < 0 || wt > 2 ||
+      (wt == 1 && p.K % 16) || (wt == 2 && p.K % 256))
     return cudaErrorInvalidValue;
   const int NB = skinny_nb(M);
   // activation row m is row m * in_rps + in_rps - 1 of the parts
   const int rs = p.in_rps > 1 ? p.in_rps : 1;
   const size_t a0 = (size_t)(rs - 1) * p.K;
-  CUtensorMap mw, mhi, mlo;
-  if (!(wt ? make_map_u8(&mw, p.W, p.N, p.K, 128) : make_map(&mw, p.W, p.N, p.K, 128)) ||
-      !make_map(&mhi, a_hi + a0, M, p.K, NB, (size_t)rs * p.K) ||
+  CUtensorMap mw, mhi, mlo, ms;
+  const uint64_t qrow = (uint64_t)p.K / 2 + (uint64_t)p.K / 16;  // bytes of one 4-bit row
+  bool ok = wt == 2 ? (make_map_u8(&mw, p.W, p.N, qrow, 128, 32) && make_map_u8(&ms, p.W, p.N, qrow, 128, 16))
+          : wt == 1 ? make_map_u8(&mw, p.W, p.N, p.K, 128)
+                    : make_map(&mw, p.W, p.N, p.K, 128);
+  if (wt != 2) ms = mw;  // unused
+  if (!ok || !make_map(&mhi, a_hi + a0, M, p.K, NB, (size_t)rs * p.K) ||
       !make_map(&mlo, a_lo + a0, M, p.K, NB, (size_t)rs * p.K))
     return cudaErrorInvalidValue;
   const int S = skinny_splits(p.N, p.K, num_sms);
   if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
-  if (wt == 1) {
-    switch (NB) {
-      case 16: return launch_skinny_nb<16, 1>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-      case 32: return launch_skinny_nb<32, 1>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-      default: return launch_skinny_nb<64, 1>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-    }
+#define TF_SKINNY_CASE(WTV)                                                                            \
+  switch (NB) {                                                                                        \
+    case 16: return launch_skinny_nb<16, WTV>(p, mw, mhi, mlo, ms, M, S, part, tickets, pdl, s);      \
+    case 32: return launch_skinny_nb<32, WTV>(p, mw, mhi, mlo, ms, M, S, part, tickets, pdl, s);      \
+    default: return launch_skinny_nb<64, WTV>(p, mw, mhi, mlo, ms, M, S, part, tickets, pdl, s);      \
   }
-  switch (NB) {
-    case 16: return launch_skinny_nb<16, 0>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-    case 32: return launch_skinny_nb<32, 0>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-    default: return launch_skinny_nb<64, 0>(p, mw, mhi, mlo, M, S, part, tickets, pdl, s);
-  }
+  if (wt == 2) TF_SKINNY_CASE(2)
+  if (wt == 1) TF_SKINNY_CASE(1)
+  TF_SKINNY_CASE(0)
+#undef TF_SKINNY_CASE
 }
 
 template <int D>

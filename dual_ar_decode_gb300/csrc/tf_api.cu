@@ -667,11 +667,14 @@ cudaError_t skinny(tf_ctx* c, const Lin& L, int set, int M, int epi, float* out,
   // The GEMM streams its weight slices before it waits for the previous
   // kernel (programmatic dependent launch), which is only right for weights
   // no kernel writes: a converted fp8 weight is launched without the overlap.
-  // e4m3 weights are converted to bf16 inside the GEMM (shared memory only).
+  // e4m3 and 4-bit weights are converted to bf16 inside the GEMM (shared
+  // memory only).
   bool pdl = true;
   int wt = 0;
   if (L.wt == TF_WEIGHT_FP8 && kSkinnyFp8) {
     wt = 1;
+  } else if (L.wt == TF_WEIGHT_NVFP4 && kSkinnyFp8 && L.K % 256 == 0) {
+    wt = 2;
   } else if (L.s) {  // exact bf16 copy of the values; the row scale stays in p.scale
     if (cudaError_t e = L.wt == 2 ? launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream)
                                   : launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))
@@ -2113,7 +2116,7 @@ namespace {
 tf_status skinny_op(const float* A, const void* W, int wt, const float* row_scale, int32_t M, int32_t N,
                     int32_t K, float* C, void* stream) {
   if (!A || !W || !C || M < 1 || M > 64 || N < 2 || (N & 1) || K < 8 || (K % 8) ||
-      (wt == 1 && (!row_scale || K % 16)))
+      (wt >= 1 && !row_scale) || (wt == 1 && K % 16) || (wt == 2 && K % 256))
     return TF_E_INVAL;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -2173,6 +2176,11 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
 tf_status tf_op_gemm_skinny_fp8(const float* A, const uint8_t* W, const float* row_scale, int32_t M,
                                 int32_t N, int32_t K, float* C, void* stream) {
   return skinny_op(A, W, 1, row_scale, M, N, K, C, stream);
+}
+
+tf_status tf_op_gemm_skinny_nvfp4(const float* A, const uint8_t* W, const float* row_scale, int32_t M,
+                                  int32_t N, int32_t K, float* C, void* stream) {
+  return skinny_op(A, W, 2, row_scale, M, N, K, C, stream);
 }
 
 tf_status tf_op_gemv(const void* W, int32_t dtype, const float* row_scale, int64_t rows,

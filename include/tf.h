@@ -407,6 +407,16 @@ tf_status tf_op_gemm_skinny(const float* A, const uint16_t* W, int32_t M, int32_
 tf_status tf_op_gemm_skinny_fp8(const float* A, const uint8_t* W, const float* row_scale, int32_t M,
                                 int32_t N, int32_t K, float* C, void* stream);
 
+/* tf_op_gemm_skinny with block-scaled 4-bit weights in the layout
+ * tf_op_quantize_nvfp4 writes (per row: K/2 bytes of e2m1 codes, the even
+ * element in the low nibble, then K/16 e4m3 block-scale bytes; row_scale
+ * float32 [N]): C[m][n] = row_scale[n] * sum_k A[m][k] w[n][k] with w = e2m1
+ * value x block scale.  The rows stream as they are and are decoded to bf16
+ * (exactly) in shared memory.  K a multiple of 256; other arguments and
+ * errors as tf_op_gemm_skinny. */
+tf_status tf_op_gemm_skinny_nvfp4(const float* A, const uint8_t* W, const float* row_scale, int32_t M,
+                                  int32_t N, int32_t K, float* C, void* stream);
+
 /* Weight-streaming GEMV y[r] = sum_k W[r][k] x[k] (the decode path's matrix
  * kernel, no prologue or epilogue): W bf16 [rows][cols] (dtype
  * TF_DTYPE_BF16), e4m3 codes with row_scale[rows] (TF_DTYPE_FP8_E4M3), or

@@ -122,6 +122,9 @@ WORKLOADS = {
     "full_fp8_batched16": Workload(
         "full-size fp8 per-row, batch 16, prefill 512 + decode 512 (T=4096)",
         FULL.replace(max_seq_len=4096), "fp8", 16, 512, 512),
+    "full_nvfp4_batched16": Workload(
+        "full-size 4-bit block-scaled, batch 16, prefill 512 + decode 512 (T=4096)",
+        FULL.replace(max_seq_len=4096), "nvfp4", 16, 512, 512),
     "full_fp8_long_topk": Workload(
         "full-size fp8 per-row, prefill 3072 + decode 1024 (T=4096), top-k 30",
         FULL.replace(max_seq_len=4096), "fp8", 1, 3072, 1024, top_k=30),

@@ -206,3 +206,10 @@ class ContinuousForced:
         tf.d = self.d
         tf.frames = [(t, slot, rf, rz, gf, gz) for t, slot, rf, rz, gf, gz in self.frames]
         return TeacherForced.check(tf, tol, sampling)
+
+
+def nvfp4_pack(codes, sb):
+    """Oracle codes [rows][blocks][16] and block scales -> the stored rows:
+    two codes per byte (even element in the low nibble), then the scales."""
+    c = codes.reshape(codes.shape[0], -1)
+    return np.concatenate([(c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8), sb], axis=1)

@@ -89,6 +89,42 @@ def test_skinny_gemm_fp8_matches_oracle(M, N, K, all_codes):
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-5
 
 
+@pytest.mark.parametrize("M,N,K,all_codes", [(16, 6144, 2560, False), (32, 19456, 2560, False),
+                                             (17, 2560, 9728, False), (3, 200, 256, False),
+                                             (64, 4096, 2560, False), (16, 130, 512, True)])
+def test_skinny_gemm_nvfp4_matches_oracle(M, N, K, all_codes):
+    """The 4-bit skinny GEMM (e2m1 codes times e4m3 block scales decoded to
+    bf16 in shared memory, row scale in the epilogue) against A @ dequant(W)^T
+    in float64, with the oracle's quantiser, or every code under a range of
+    block scales (2^-9 .. 448) with random row scales."""
+    from dual_ar_decode_gb300 import op_gemm_skinny_nvfp4
+    from gpu_helpers import nvfp4_pack
+    rng = np.random.default_rng(M * 11 + N + K)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    if all_codes:
+        codes = (np.arange(N * K) % 16).astype(np.uint8).reshape(N, K // 16, 16)
+        sb = np.array([0x01, 0x20, 0x38, 0x40, 0x55, 0x7E], np.uint8)[np.arange(N * (K // 16)) % 6]
+        sb = sb.reshape(N, K // 16)
+        sr = rng.uniform(0.5, 2.0, N).astype(np.float32) / 2688.0
+    else:
+        codes, sb, sr = oracle.nvfp4_quantize_rows(
+            f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32) * 0.02))
+    Ad = torch.from_numpy(A).to(DEV)
+    Wd = torch.from_numpy(nvfp4_pack(codes, sb)).to(DEV)
+    Sd = torch.from_numpy(np.asarray(sr, np.float32)).to(DEV)
+    C = torch.full((M, N), np.nan, dtype=torch.float32, device=DEV)
+    op_gemm_skinny_nvfp4(Ad.data_ptr(), Wd.data_ptr(), Sd.data_ptr(), M, N, K, C.data_ptr())
+    ref = oracle.linear(oracle.nvfp4_dequant_rows(codes, sb, sr), A.astype(np.float64))
+    got = C.cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert np.isfinite(got).all()
+    # exact bf16 weights (e2m1 x e4m3 has <= 6 significant bits); hi + lo
+    # activations and fp32 accumulation as in the bf16 case; the row scale
+    # applied once where the oracle rounds each weight
+    assert np.max(np.abs(got - ref)) <= 2e-4 * rms
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-5
+
+
 def test_skinny_gemm_is_deterministic_and_rejects_bad_shapes():
     rng = np.random.default_rng(3)
     M, N, K = 16, 2560, 9728

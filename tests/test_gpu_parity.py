@@ -15,7 +15,7 @@ from dual_ar_decode_gb300 import (Decoder, TfError, op_attention, op_gemm, op_ge
 from dual_ar_decode_gb300.binding import TF_DTYPE_BF16, TF_DTYPE_FP8_E4M3, TF_DTYPE_NVFP4
 from synth import FULL, TINY, make_logits, make_prompt, make_weights, f32_to_bf16_bits
 
-from gpu_helpers import BF16_TOL, FP8_TOL, TeacherForced
+from gpu_helpers import BF16_TOL, FP8_TOL, TeacherForced, nvfp4_pack
 
 pytestmark = pytest.mark.gpu
 
@@ -48,13 +48,6 @@ def test_quantize_fp8_bit_exact(rows, cols):
     rc, rs = oracle.fp8_quantize_rows(w)
     assert np.array_equal(codes.cpu().numpy(), rc)
     assert np.array_equal(scale.cpu().numpy().view(np.uint32), rs.view(np.uint32))
-
-
-def nvfp4_pack(codes, sb):
-    """Oracle codes [rows][blocks][16] and block scales -> the stored rows:
-    two codes per byte (even element in the low nibble), then the scales."""
-    c = codes.reshape(codes.shape[0], -1)
-    return np.concatenate([(c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8), sb], axis=1)
 
 
 @pytest.mark.parametrize("rows,cols", [(37, 2560), (5, 256), (64, 9728), (3, 512)])

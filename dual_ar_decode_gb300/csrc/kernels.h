@@ -159,14 +159,16 @@ struct AttnParams {
 cudaError_t launch_attention(const AttnParams& p, int M, bool pdl, cudaStream_t s);
 // The same attention for prompt rows (many rows, one long key slice each).
 cudaError_t launch_attention_rows(const AttnParams& p, int M, bool pdl, cudaStream_t s);
-// Causal attention of P prompt rows on the tensor cores: row m sits at
-// position pos0 + m and attends to keys 0..pos0 + m of its sequence.  The
-// queries come as bf16 hi / lo parts [P][Hq*D]; Kc / Vc are the sequence's
-// dense cache [Hkv][T][D] (kv_rows = Hkv*T), or with kv_tbl the page pool
+// Causal attention of prompt rows on the tensor cores, nseq sequences of P
+// rows: row m of a sequence sits at position pos0 + m and attends to keys
+// 0..pos0 + m of that sequence.  The queries come as bf16 hi / lo parts
+// [nseq * P][Hq*D]; Kc / Vc are dense caches [slots][Hkv][T][D] (kv_rows =
+// slots*Hkv*T, sequence z in slot seq + z), or with kv_tbl the page pool
 // [pages][Hkv][kKvPage][D] (kv_rows = pages*Hkv*kKvPage).  D = 64 or 128.
 struct PromptAttnArgs {
   int32_t P, pos0, Hq, Hkv, T;
-  int32_t seq;             // the sequence's slot (paged caches)
+  int32_t nseq;            // sequences, P query rows each ([nseq][P] rows of q and out)
+  int32_t seq;             // the first sequence's slot; sequence z is slot seq + z
   const int32_t* kv_tbl;   // paged: block table [slots][npp]; null: dense
   int32_t kv_npp;
   float scale_log2;        // log2(e) / sqrt(D)

@@ -991,10 +991,10 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
 }
 
 // ---------------------------------------------------------------- prompt attention
-// Causal attention of P prompt rows on the tensor cores ("Fish Speech" tour,
+// Causal attention of prompt rows on the tensor cores ("Fish Speech" tour,
 // "Why You Need This": grouped-query attention; the tuna-fish README's
-// prefill tokens/s).  One CTA per (block of 128 query rows, query head); the
-// keys 0..pos of every row are visited in tiles of 128:
+// prefill tokens/s).  One CTA per (block of 128 query rows, query head,
+// sequence); the keys 0..pos of every row are visited in tiles of 128:
 //   * warp 0 loads the block's queries once (bf16 hi and lo parts), the K
 //     tiles of the head's KV group into two stages and the V tiles into one
 //     (TMA, 128-byte swizzle; paged caches: one box per 32-position page);
@@ -1117,6 +1117,8 @@ __global__ void __launch_bounds__(192, 1)
   const int blk = nblk - 1 - static_cast<int>(blockIdx.x);   // longest rows first
   const int h = blockIdx.y;
   const int g = h / (a.Hq / a.Hkv);
+  const int seq = a.seq + static_cast<int>(blockIdx.z);       // this sequence's slot
+  const int qbase = static_cast<int>(blockIdx.z) * a.P;       // its first row in q and out
   const int q0 = blk * 128;                                  // first query row
   const int rows = min(128, a.P - q0);
   const int last_key = a.pos0 + q0 + rows - 1;               // the block's last key
@@ -1160,21 +1162,22 @@ __global__ void __launch_bounds__(192, 1)
       prefetch_tensormap(&map_v);
       mbar_arrive_expect_tx(q_full, 2 * C::kQ);
       for (int b = 0; b < C::kBoxes; ++b) {
-        tma_load_2d(sq + b * 16384, &map_qhi, h * D + b * 64, q0, q_full);
-        tma_load_2d(sq + C::kQ + b * 16384, &map_qlo, h * D + b * 64, q0, q_full);
+        tma_load_2d(sq + b * 16384, &map_qhi, h * D + b * 64, qbase + q0, q_full);
+        tma_load_2d(sq + C::kQ + b * 16384, &map_qlo, h * D + b * 64, qbase + q0, q_full);
       }
       // one tile of K or V rows (128 keys from kbase) into dst
       auto load_tile = [&](const CUtensorMap* map, uint8_t* dst, int kbase, uint64_t* b_) {
         if (a.kv_tbl) {
           for (int pg = 0; pg < 128 / kKvPage; ++pg) {
             const int pi = kbase / kKvPage + pg;
-            const int page = pi < a.kv_npp ? __ldg(a.kv_tbl + (size_t)a.seq * a.kv_npp + pi) : 0;
+            const int page = pi < a.kv_npp ? __ldg(a.kv_tbl + (size_t)seq * a.kv_npp + pi) : 0;
             const int y = (page * a.Hkv + g) * kKvPage;
             for (int b = 0; b < C::kBoxes; ++b)
               tma_load_2d(dst + b * 16384 + pg * (kKvPage * 128), map, b * 64, y, b_);
           }
         } else {
-          for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(dst + b * 16384, map, b * 64, g * a.T + kbase, b_);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_2d(dst + b * 16384, map, b * 64, (seq * a.Hkv + g) * a.T + kbase, b_);
         }
       };
       for (int j = 0; j < nt; ++j) {
@@ -1348,7 +1351,7 @@ __global__ void __launch_bounds__(192, 1)
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const float inv = 1.0f / l;
       const int m = q0 + r;
-      const size_t o = (size_t)m * a.Hq * D + (size_t)h * D;
+      const size_t o = (size_t)(qbase + m) * a.Hq * D + (size_t)h * D;
 #pragma unroll 1
       for (int c = 0; c < D; c += 16) {
         float t[16];
@@ -1549,7 +1552,7 @@ cudaError_t launch_prompt_attn_d(const CUtensorMap& mqh, const CUtensorMap& mql,
                                 (int)PAttn<D>::kSmem);
   });
   if (ea) return ea;
-  const dim3 grid((a.P + 127) / 128, a.Hq);
+  const dim3 grid((a.P + 127) / 128, a.Hq, a.nseq);
   k_umma_attn<D><<<grid, 192, PAttn<D>::kSmem, s>>>(mqh, mql, mk, mv, a);
   return cudaGetLastError();
 }
@@ -1561,11 +1564,13 @@ bool prompt_attention_tc_supported(int D, int Hq, int Hkv) {
 cudaError_t launch_prompt_attention_tc(const uint16_t* q_hi, const uint16_t* q_lo, const uint16_t* Kc,
                                        const uint16_t* Vc, int64_t kv_rows, int D,
                                        const PromptAttnArgs& a, cudaStream_t s) {
-  if (!prompt_attention_tc_supported(D, a.Hq, a.Hkv) || a.P < 1 || a.pos0 < 0 || a.pos0 + a.P > a.T)
+  if (!prompt_attention_tc_supported(D, a.Hq, a.Hkv) || a.P < 1 || a.nseq < 1 || a.pos0 < 0 ||
+      a.pos0 + a.P > a.T)
     return cudaErrorInvalidValue;
   const uint32_t box = a.kv_tbl ? static_cast<uint32_t>(kKvPage) : 128u;
   CUtensorMap mqh, mql, mk, mv;
-  if (!make_map(&mqh, q_hi, a.P, (uint64_t)a.Hq * D, 128) || !make_map(&mql, q_lo, a.P, (uint64_t)a.Hq * D, 128) ||
+  const uint64_t qrows = (uint64_t)a.P * a.nseq;
+  if (!make_map(&mqh, q_hi, qrows, (uint64_t)a.Hq * D, 128) || !make_map(&mql, q_lo, qrows, (uint64_t)a.Hq * D, 128) ||
       !make_map(&mk, Kc, kv_rows, D, box) || !make_map(&mv, Vc, kv_rows, D, box))
     return cudaErrorInvalidValue;
   return D == 64 ? launch_prompt_attn_d<64>(mqh, mql, mk, mv, a, s)

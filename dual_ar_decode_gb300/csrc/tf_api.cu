@@ -903,16 +903,18 @@ cudaError_t enqueue_decode_frame(tf_ctx* c, const tf_sampling* s) {
   return enqueue_tail(c, s, 1, true);
 }
 
-// Prompt pass of one sequence: the P ids at tokens_dev (device) at positions
-// 0..P-1 through the slow decoder into slot `slot`'s KV caches (tensor-core
-// GEMMs with the decode path's epilogues, causal attention over the rows);
-// the last row's residual goes to xs[slot].
-cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
+// Prompt pass of nseq sequences with P ids each (nseq * P <= T rows): the ids
+// at tokens_dev (device, [nseq][P]) at positions 0..P-1 through the slow
+// decoder into slots slot .. slot + nseq - 1 (tensor-core GEMMs over all the
+// rows with the decode path's epilogues, causal attention per sequence); each
+// sequence's last row's residual goes to xs[its slot].
+cudaError_t prompt_pass(tf_ctx* c, int slot, int nseq, const int32_t* tokens_dev, int P) {
   cudaError_t e;
+  const int rows = nseq * P;
   BuildParams b = {};
   b.mode = BUILD_TOKENS;
   b.H = c->H;
-  b.M = P;
+  b.M = rows;
   b.table = c->text_embed;
   b.table_rows = c->Vt;
   b.ids = tokens_dev;
@@ -945,6 +947,7 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
       p.Kc = layer->K;
       p.Vc = layer->V;
       p.seq_base = slot;
+      p.rps = P;  // row m: sequence slot + m / P at position m % P
       p.kv_seq = c->kv_seq;
       if (layer->paged) {
         p.kv_tbl = c->kv_tbl;
@@ -970,18 +973,18 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
         if ((e2 = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e2;
         p.W = reinterpret_cast<const uint8_t*>(c->wconv);
       }
-      return launch_gemm_tc(p, hi, lo, P, c->g_part, c->g_tickets, c->num_sms, c->stream);
+      return launch_gemm_tc(p, hi, lo, rows, c->g_part, c->g_tickets, c->num_sms, c->stream);
     }
-    return launch_gemm_rows(p, wt, P, c->stream);
+    return launch_gemm_rows(p, wt, rows, c->stream);
   };
   auto norm = [&](const uint16_t* w) {
-    return tc ? launch_rmsnorm_split(c->px, w, c->a_hi, c->a_lo, P, c->H, c->cfg.rms_eps, c->stream)
-              : launch_rmsnorm_rows(c->px, w, c->pa, P, c->H, c->cfg.rms_eps, c->stream);
+    return tc ? launch_rmsnorm_split(c->px, w, c->a_hi, c->a_lo, rows, c->H, c->cfg.rms_eps, c->stream)
+              : launch_rmsnorm_rows(c->px, w, c->pa, rows, c->H, c->cfg.rms_eps, c->stream);
   };
   for (const Layer& L : c->slow) {
     if ((e = norm(L.attn_norm))) return e;
     if ((e = gemm(L.qkv, c->pa, c->a_hi, c->a_lo, EPI_QKV, nullptr, 0, &L))) return e;
-    if (L.q_norm && (e = qknorm(c, L, P, nullptr, 0, 0, slot, c->pq, false))) return e;
+    if (L.q_norm && (e = qknorm(c, L, rows, nullptr, 0, P, slot, c->pq, false))) return e;
     AttnParams a = {};
     a.q = c->pq;
     a.Kc = L.K;
@@ -991,6 +994,7 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
     a.Hkv = c->Hkv;
     a.D = c->D;
     a.pos_fixed = 0;
+    a.rps = P;
     a.seq_base = slot;
     a.kv_seq = c->kv_seq;
     if (L.paged) {
@@ -1009,9 +1013,10 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
     if (c->attn_tc) {
       // tensor-core causal attention; the queries as bf16 parts in the
       // (idle) SwiGLU part buffers
-      if ((e = launch_split_bf16(c->pq, c->u_hi, c->u_lo, (size_t)P * c->Q, c->stream))) return e;
+      if ((e = launch_split_bf16(c->pq, c->u_hi, c->u_lo, (size_t)rows * c->Q, c->stream))) return e;
       PromptAttnArgs t = {};
       t.P = P;
+      t.nseq = nseq;
       t.pos0 = 0;
       t.Hq = c->Hq;
       t.Hkv = c->Hkv;
@@ -1022,19 +1027,14 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
       t.out_hi = a.out_hi;
       t.out_lo = a.out_lo;
       t.err = &c->st->err;
-      const uint16_t* Kc = L.K;
-      const uint16_t* Vc = L.V;
-      int64_t rows = (int64_t)c->Hkv * c->T;
+      int64_t kv_rows = (int64_t)c->Bmax * c->Hkv * c->T;  // every slot's dense cache
       if (L.paged) {
         t.kv_tbl = c->kv_tbl;
         t.kv_npp = c->npp;
-        rows = (int64_t)(c->Bmax * c->npp + 1) * c->Hkv * kKvPage;
-      } else {
-        Kc += (size_t)slot * c->kv_seq;
-        Vc += (size_t)slot * c->kv_seq;
+        kv_rows = (int64_t)(c->Bmax * c->npp + 1) * c->Hkv * kKvPage;
       }
-      if ((e = launch_prompt_attention_tc(c->u_hi, c->u_lo, Kc, Vc, rows, c->D, t, c->stream))) return e;
-    } else if ((e = launch_attention_rows(a, P, false, c->stream))) {
+      if ((e = launch_prompt_attention_tc(c->u_hi, c->u_lo, L.K, L.V, kv_rows, c->D, t, c->stream))) return e;
+    } else if ((e = launch_attention_rows(a, rows, false, c->stream))) {
       return e;
     }
     if ((e = gemm(L.o, c->po, c->a_hi, c->a_lo, EPI_RESID, c->px, c->H, nullptr))) return e;
@@ -1042,8 +1042,9 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, const int32_t* tokens_dev, int P) {
     if ((e = gemm(L.w13, c->pa, c->a_hi, c->a_lo, EPI_SWIGLU, c->pu, c->F, nullptr))) return e;
     if ((e = gemm(L.w2, c->pu, c->u_hi, c->u_lo, EPI_RESID, c->px, c->H, nullptr))) return e;
   }
-  return cudaMemcpyAsync(c->xs + (size_t)slot * c->H, c->px + (size_t)(P - 1) * c->H, sizeof(float) * c->H,
-                         cudaMemcpyDeviceToDevice, c->stream);
+  return cudaMemcpy2DAsync(c->xs + (size_t)slot * c->H, sizeof(float) * c->H, c->px + (size_t)(P - 1) * c->H,
+                           sizeof(float) * c->H * P, sizeof(float) * c->H, nseq, cudaMemcpyDeviceToDevice,
+                           c->stream);
 }
 
 bool same_sampling(const tf_sampling& a, const tf_sampling& b) {
@@ -1630,7 +1631,10 @@ tf_status tf_prefill(tf_ctx* c, const int32_t* tokens, int32_t B, int32_t P,
   c->Bc = B;
   c->uniform = true;
   c->prefilled = false;
-  for (int sb = 0; sb < B; ++sb) CK(prompt_pass(c, sb, c->tokens + (size_t)sb * P, P));
+  // as many prompts per pass as the T-row prompt buffers hold
+  const int per_pass = std::max(1, c->T / P);
+  for (int sb = 0; sb < B; sb += per_pass)
+    CK(prompt_pass(c, sb, std::min(per_pass, B - sb), c->tokens + (size_t)sb * P, P));
   if (B > 1) {
     CK(enqueue_tail_batched(c, &s, B, 0, true));
   } else {
@@ -1658,7 +1662,7 @@ tf_status tf_prefill_seq(tf_ctx* c, int32_t slot, const int32_t* tokens, int32_t
   if (P > 1) {  // every prompt id but the last through the prompt pass
     CK(cudaMemcpyAsync(c->tokens, tokens, sizeof(int32_t) * (P - 1), cudaMemcpyHostToDevice, c->stream));
     CK(cudaStreamSynchronize(c->stream));
-    CK(prompt_pass(c, slot, c->tokens, P - 1));
+    CK(prompt_pass(c, slot, 1, c->tokens, P - 1));
   }
   // the last prompt id is fed by the next decode step, which emits frame 0
   c->pos_host[slot] = P - 1;
@@ -2038,6 +2042,7 @@ tf_status tf_op_attention_prompt(const float* q, const uint16_t* K, const uint16
   }
   PromptAttnArgs a = {};
   a.P = rows;
+  a.nseq = 1;
   a.pos0 = pos0;
   a.Hq = Hq;
   a.Hkv = Hkv;

@@ -306,9 +306,12 @@ cudaError_t launch_gemm_rows(const GemvParams& p, int wt, int M, cudaStream_t s)
 // output tile (returned to zero by the launch).
 bool gemm_tc_supported(int N, int K);
 size_t gemm_tc_smem_bytes();
-int gemm_tc_splits(int M, int N, int K, int num_sms);
+// wt = 0: bf16 weights; 1: e4m3 codes (row scale in p.scale); 2: 4-bit rows
+// as k_pack writes them (K a multiple of 256): quantised weights stream as
+// they are and are converted to bf16 in shared memory (128-wide tiles).
+int gemm_tc_splits(int M, int N, int K, int num_sms, int wt = 0);
 size_t gemm_tc_part_floats(int M, int N, int K, int num_sms);
-cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
+cudaError_t launch_gemm_tc(const GemvParams& p, int wt, const uint16_t* a_hi, const uint16_t* a_lo, int M,
                            float* part, uint32_t* tickets, int num_sms, cudaStream_t s);
 // Skinny tensor-core GEMM for batched decode (M <= 64 activation rows):
 // out = epi(A[M][K] * W[N][K]^T), the weight rows on the MMA's 128-row side,

@@ -51,16 +51,20 @@ constexpr int kThreads = 6 * 32;
 // Prompt GEMM tile shapes: 128 prompt rows x GBN weight rows.  256-wide tiles
 // (where N allows) halve the activation bytes each weight byte needs, and
 // their MMAs are twice as wide.
-template <int GBN>
+// WT = 1 / 2: e4m3 or 4-bit weights (128-wide tiles), staged as they are
+// behind the bf16 tile and converted into it by the epilogue warps.
+template <int GBN, int WT = 0>
 struct GemmCfg {
   static constexpr int kTileW = GBN * BK * 2;              // 16 or 32 KB
-  static constexpr int kStageBytes = 2 * kTileA + kTileW;  // A hi, A lo, W
-  static constexpr int kStages = GBN == 256 ? 3 : 4;
+  static constexpr int kTileWq = WT == 1 ? GBN * BK : WT == 2 ? GBN * 48 : 0;
+  static constexpr int kStageBytes = 2 * kTileA + kTileW + kTileWq;  // A hi, A lo, W (, W staged)
+  static constexpr int kStages = (GBN == 256 || WT) ? 3 : 4;
   static constexpr uint32_t kTmemCols = GBN;
   // kind::f16, fp32 accumulate, bf16 A and B, both K-major, M = 128, N = GBN.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GBN >> 3) << 17) |
                                      ((uint32_t)(BM >> 4) << 24);
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 1) * 8 + 64;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (3 * kStages + 1) * 8 + 64;
+  static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 };
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -239,13 +243,82 @@ __device__ __forceinline__ void gemm_epi_chunk(const GemvParams& p, int m, int n
   }
 }
 
-template <int GBN>
+// 8 e4m3 codes (two words) -> 8 bf16 (four words), exactly.
+__device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t a, uint32_t b, uint32_t* o) {
+  const uint32_t w[2] = {a, b};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint16_t pr = static_cast<uint16_t>(w[i] >> (16 * h));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
+      const __half2 hv = *reinterpret_cast<__half2*>(&h2);
+      const float2 f = __half22float2(hv);
+      uint32_t d;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y), "f"(f.x));
+      o[2 * i + h] = d;
+    }
+  }
+}
+
+// 16 4-bit codes (w: 8 bytes, element 2i in the low nibble of byte i) times
+// their block scale (e4m3 bits sb) -> 16 bf16 (eight words), exactly: an
+// e2m1 value times an e4m3 value has at most 6 significant bits.
+__device__ __forceinline__ void e2m1x16_to_bf16(const uint2 w, uint32_t sb, uint32_t* o) {
+  const float sc = __uint_as_float((sb & 0x7Fu) << 20) * 1.329227995784915873e36f;  // e4m3 by bit placement, x 2^120
+  const uint32_t v[2] = {w.x, w.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t h[4];
+    asm("{.reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
+        " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
+        " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3;}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(v[i]));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
+      uint32_t d;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y * sc), "f"(f.x * sc));
+      o[4 * i + b] = d;
+    }
+  }
+}
+
+// One quantised weight slice (128 rows x 64 elements) at q -> bf16 in the
+// 128-byte swizzle layout at w (row r at r * 128, 16-byte chunk c at
+// c ^ (r & 7)), by the 128 threads et: four lanes per row, so that the reads
+// of q are contiguous across a warp.  WT = 1: e4m3 rows of 64 bytes.
+// WT = 2: 4-bit rows of 32 bytes, then the slice's 16-byte scale boxes (the
+// scales of slices kb & ~3 .. kb | 3).
+template <int WT>
+__device__ __forceinline__ void dequant_slice(const uint8_t* q, uint8_t* w, int kb, int et) {
+  const int lane = et & 31, q4 = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = (et >> 5) * 32 + k * 8 + (lane >> 2);
+    uint32_t o[8];
+    if constexpr (WT == 2) {
+      const uint2 c = *reinterpret_cast<const uint2*>(q + r * 32 + q4 * 8);
+      e2m1x16_to_bf16(c, q[128 * 32 + r * 16 + (kb & 3) * 4 + q4], o);
+    } else {
+      const uint4 c = *reinterpret_cast<const uint4*>(q + r * BK + q4 * 16);
+      e4m3x8_to_bf16x8(c.x, c.y, o);
+      e4m3x8_to_bf16x8(c.z, c.w, o + 4);
+    }
+    uint8_t* row = w + r * 128;
+    *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <int GBN, int WT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_umma_gemm(const __grid_constant__ CUtensorMap map_ahi,
                 const __grid_constant__ CUtensorMap map_alo,
-                const __grid_constant__ CUtensorMap map_w, const GemvParams p, int M, int S,
-                float* part, uint32_t* tickets) {
-  using G = GemmCfg<GBN>;
+                const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_s,
+                const GemvParams p, int M, int S, float* part, uint32_t* tickets) {
+  using G = GemmCfg<GBN, WT>;
   constexpr int BN = GBN, kStages = G::kStages, kStageBytes = G::kStageBytes;
   constexpr uint32_t kTmemCols = G::kTmemCols;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -254,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  uint64_t* conv = empty + kStages;  // WT: the stage's bf16 weight tile is written
+  uint64_t* done = conv + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* consumed = tmem_slot + 2;  // K slices the MMA warp took
@@ -272,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], 128);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -301,10 +376,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         uint8_t* st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        mbar_arrive_expect_tx(&full[s], WT ? 2 * kTileA + G::kTileWq : kStageBytes);
         tma_load_2d(st, &map_ahi, (kb0 + k) * BK, m0, &full[s]);
         tma_load_2d(st + kTileA, &map_alo, (kb0 + k) * BK, m0, &full[s]);
-        tma_load_2d(st + 2 * kTileA, &map_w, (kb0 + k) * BK, n0, &full[s]);
+        uint8_t* wq = st + 2 * kTileA + G::kTileW;  // quantised staging
+        if constexpr (WT == 2) {
+          tma_load_2d(wq, &map_w, (kb0 + k) * 32, n0, &full[s]);
+          tma_load_2d(wq + 128 * 32, &map_s, p.K / 2 + ((kb0 + k) >> 2) * 16, n0, &full[s]);
+        } else if constexpr (WT == 1) {
+          tma_load_2d(wq, &map_w, (kb0 + k) * BK, n0, &full[s]);
+        } else {
+          tma_load_2d(st + 2 * kTileA, &map_w, (kb0 + k) * BK, n0, &full[s]);
+        }
         issued = k + 1;
       }
       // After an abort, let the copies still in flight land before the CTA
@@ -318,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int k = 0; k < nk; ++k) {
         const int s = k % kStages;
-        if (*abort_flag || !mbar_wait(&full[s], (k / kStages) & 1, p.err)) {
+        if (*abort_flag || !mbar_wait(&full[s], (k / kStages) & 1, p.err) ||
+            (WT && !mbar_wait(&conv[s], (k / kStages) & 1, p.err))) {
           *abort_flag = 1;
           break;
         }
@@ -341,6 +425,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    if constexpr (WT != 0) {
+      // First the weight conversion of every slice: stage s's staged codes
+      // into its bf16 tile (the MMA of its previous slice is done: the
+      // producer reloaded the stage only after it).
+      const int et = threadIdx.x - 64;
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % kStages;
+        uint8_t* st = smem + s * kStageBytes;
+        if (!*abort_flag && mbar_wait(&full[s], (k / kStages) & 1, p.err))
+          dequant_slice<WT>(st + 2 * kTileA + G::kTileW, st + 2 * kTileA, kb0 + k, et);
+        else
+          *abort_flag = 1;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&conv[s]);
+      }
+    }
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int m = m0 + row;
@@ -531,48 +631,6 @@ struct Skinny {
   static constexpr uint32_t kChunk = NB * 128 * 4;
   static constexpr int kChunksPerRound = static_cast<int>(kRing / kChunk);
 };
-
-// 8 e4m3 codes (two words) -> 8 bf16 (four words), exactly.
-__device__ __forceinline__ void e4m3x8_to_bf16x8(uint32_t a, uint32_t b, uint32_t* o) {
-  const uint32_t w[2] = {a, b};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint16_t pr = static_cast<uint16_t>(w[i] >> (16 * h));
-      uint32_t h2;
-      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
-      const __half2 hv = *reinterpret_cast<__half2*>(&h2);
-      const float2 f = __half22float2(hv);
-      uint32_t d;
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y), "f"(f.x));
-      o[2 * i + h] = d;
-    }
-  }
-}
-
-// 16 4-bit codes (w: 8 bytes, element 2i in the low nibble of byte i) times
-// their block scale (e4m3 bits sb) -> 16 bf16 (eight words), exactly: an
-// e2m1 value times an e4m3 value has at most 6 significant bits.
-__device__ __forceinline__ void e2m1x16_to_bf16(const uint2 w, uint32_t sb, uint32_t* o) {
-  const float sc = __uint_as_float((sb & 0x7Fu) << 20) * 1.329227995784915873e36f;  // e4m3 by bit placement, x 2^120
-  const uint32_t v[2] = {w.x, w.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t h[4];
-    asm("{.reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;"
-        " cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;"
-        " cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3;}"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(v[i]));
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
-      uint32_t d;
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(f.y * sc), "f"(f.x * sc));
-      o[4 * i + b] = d;
-    }
-  }
-}
 
 // WT = 2: 4-bit rows (K/2 code bytes, then K/16 e4m3 block-scale bytes):
 // map_w takes 32-byte code boxes, map_s the 16-byte scale boxes (4 slices'
@@ -791,29 +849,7 @@ __global__ void __launch_bounds__(kSkThreads, NB <= 32 ? TF_SKINNY_CTAS_PER_SM :
         if (ok && i >= kSkStages) ok = mbar_wait(&empty[sb], ((i / kSkStages) & 1) ^ 1, p.err);
         if (ok) ok = mbar_wait(&f8full[s8], (i / C::kF8) & 1, p.err);
         if (ok) {
-          // four lanes per 64-byte row, eight rows per warp access (a
-          // contiguous 512 bytes: no bank conflicts); warp w takes rows
-          // 32w .. 32w + 31
-          const int q4 = lane & 3;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = (et >> 5) * 32 + k * 8 + (lane >> 2);
-            uint32_t o[8];
-            if constexpr (WT == 2) {
-              // lane q4 takes block q4 of the slice: 8 code bytes, its scale byte
-              const uint8_t* sl = f8 + s8 * C::kF8Slot;
-              const uint2 w = *reinterpret_cast<const uint2*>(sl + r * 32 + q4 * 8);
-              const uint32_t sb = sl[128 * 32 + r * 16 + ((kb0 + i) & 3) * 4 + q4];
-              e2m1x16_to_bf16(w, sb, o);
-            } else {
-              const uint4 w = *reinterpret_cast<const uint4*>(f8 + s8 * C::kF8Slot + r * BK + q4 * 16);
-              e4m3x8_to_bf16x8(w.x, w.y, o);
-              e4m3x8_to_bf16x8(w.z, w.w, o + 4);
-            }
-            uint8_t* row = smem + sb * C::kStage + r * 128;
-            *reinterpret_cast<uint4*>(row + (((2 * q4) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(row + (((2 * q4 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+          dequant_slice<WT>(f8 + s8 * C::kF8Slot, smem + sb * C::kStage, kb0 + i, et);
         } else {
           *abort_flag = 1;
         }
@@ -1588,8 +1624,8 @@ int gemm_tc_bn(int M, int N) { return (N % 256 == 0 && M > 512) ? 256 : 128; }
 // K splits of a prompt GEMM: the fewest that fill at least 80% of the last
 // wave of CTAs (one CTA per SM), keeping >= 4 K slices per split; else the
 // best fill found.
-int gemm_tc_splits(int M, int N, int K, int num_sms) {
-  const int tiles = ((M + BM - 1) / BM) * (N / gemm_tc_bn(M, N));
+int gemm_tc_splits(int M, int N, int K, int num_sms, int wt) {
+  const int tiles = ((M + BM - 1) / BM) * (N / (wt ? 128 : gemm_tc_bn(M, N)));
   const int smax = std::max(1, std::min(16, (K / BK) / 4));
   int best = 1;
   double best_fill = 0.0;
@@ -1607,7 +1643,7 @@ int gemm_tc_splits(int M, int N, int K, int num_sms) {
 }
 
 size_t gemm_tc_part_floats(int M, int N, int K, int num_sms) {
-  const int S = gemm_tc_splits(M, N, K, num_sms);
+  const int S = std::max(gemm_tc_splits(M, N, K, num_sms, 0), gemm_tc_splits(M, N, K, num_sms, 1));
   return S > 1 ? (size_t)S * ((M + BM - 1) / BM) * (size_t)N * BM : 0;
 }
 
@@ -1625,33 +1661,41 @@ cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaS
   return cudaGetLastError();
 }
 
-template <int GBN>
+template <int GBN, int WT>
 cudaError_t launch_gemm_tc_bn(const CUtensorMap& ma_hi, const CUtensorMap& ma_lo, const CUtensorMap& mw,
-                              const GemvParams& p, int M, int S, float* part, uint32_t* tickets,
-                              cudaStream_t s) {
+                              const CUtensorMap& ms, const GemvParams& p, int M, int S, float* part,
+                              uint32_t* tickets, cudaStream_t s) {
   static DeviceOnce once;
   cudaError_t ea = device_once(once, [] {
-    return cudaFuncSetAttribute(k_umma_gemm<GBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)GemmCfg<GBN>::kSmem);
+    return cudaFuncSetAttribute(k_umma_gemm<GBN, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)GemmCfg<GBN, WT>::kSmem);
   });
   if (ea) return ea;
   dim3 grid((M + BM - 1) / BM, p.N / GBN, S);
-  k_umma_gemm<GBN><<<grid, kThreads, GemmCfg<GBN>::kSmem, s>>>(ma_hi, ma_lo, mw, p, M, S, part, tickets);
+  k_umma_gemm<GBN, WT><<<grid, kThreads, GemmCfg<GBN, WT>::kSmem, s>>>(ma_hi, ma_lo, mw, ms, p, M, S, part,
+                                                                       tickets);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(const GemvParams& p, const uint16_t* a_hi, const uint16_t* a_lo, int M,
+cudaError_t launch_gemm_tc(const GemvParams& p, int wt, const uint16_t* a_hi, const uint16_t* a_lo, int M,
                            float* part, uint32_t* tickets, int num_sms, cudaStream_t s) {
-  if (!gemm_tc_supported(p.N, p.K) || M < 1) return cudaErrorInvalidValue;
-  const int bn = gemm_tc_bn(M, p.N);
-  CUtensorMap ma_hi, ma_lo, mw;
-  if (!make_map(&ma_hi, a_hi, M, p.K, BM) || !make_map(&ma_lo, a_lo, M, p.K, BM) ||
-      !make_map(&mw, p.W, p.N, p.K, bn))
+  if (!gemm_tc_supported(p.N, p.K) || M < 1 || wt < 0 || wt > 2 || (wt == 2 && p.K % 256))
     return cudaErrorInvalidValue;
-  const int S = gemm_tc_splits(M, p.N, p.K, num_sms);
+  const int bn = wt ? 128 : gemm_tc_bn(M, p.N);
+  CUtensorMap ma_hi, ma_lo, mw, ms;
+  const uint64_t qrow = (uint64_t)p.K / 2 + (uint64_t)p.K / 16;  // bytes of one 4-bit row
+  const bool okw = wt == 2 ? (make_map_u8(&mw, p.W, p.N, qrow, 128, 32) && make_map_u8(&ms, p.W, p.N, qrow, 128, 16))
+                 : wt == 1 ? make_map_u8(&mw, p.W, p.N, p.K, 128)
+                           : make_map(&mw, p.W, p.N, p.K, bn);
+  if (wt != 2) ms = mw;  // unused
+  if (!okw || !make_map(&ma_hi, a_hi, M, p.K, BM) || !make_map(&ma_lo, a_lo, M, p.K, BM))
+    return cudaErrorInvalidValue;
+  const int S = gemm_tc_splits(M, p.N, p.K, num_sms, wt);
   if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
-  return bn == 256 ? launch_gemm_tc_bn<256>(ma_hi, ma_lo, mw, p, M, S, part, tickets, s)
-                   : launch_gemm_tc_bn<128>(ma_hi, ma_lo, mw, p, M, S, part, tickets, s);
+  if (wt == 2) return launch_gemm_tc_bn<128, 2>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s);
+  if (wt == 1) return launch_gemm_tc_bn<128, 1>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s);
+  return bn == 256 ? launch_gemm_tc_bn<256, 0>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s)
+                   : launch_gemm_tc_bn<128, 0>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s);
 }
 
 }  // namespace tf

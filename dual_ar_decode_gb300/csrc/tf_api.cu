@@ -964,16 +964,28 @@ cudaError_t prompt_pass(tf_ctx* c, int slot, int nseq, const int32_t* tokens_dev
     p.rope = c->rope;
     p.err = &c->st->err;
     cudaError_t e2;
-    if (c->wt == TF_WEIGHT_NVFP4) {  // exact bf16 copy of e2m1 x block scale; row scale in p.scale
-      if ((e2 = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e2;
-      p.W = reinterpret_cast<const uint8_t*>(c->wconv);
-    }
     if (tc) {
-      if (c->wt == TF_WEIGHT_FP8) {  // bf16 copy of the e4m3 values; the row scale stays in p.scale
+      // Short prompts: e4m3 and 4-bit weights stream as they are and are
+      // converted in the GEMM's shared memory.  Longer prompts (more than
+      // four row tiles, each converting the weight again) take one exact
+      // bf16 copy per linear and the 256-wide bf16 tiles (measured: 3072
+      // fp8 ids 60.0 ms this way, 75.6 ms converting in the GEMM).  The row
+      // scale stays in p.scale either way.
+      const bool q_in_gemm = rows <= 512;
+      const int gwt = !q_in_gemm ? 0 : c->wt == TF_WEIGHT_FP8 ? 1
+                      : (c->wt == TF_WEIGHT_NVFP4 && L.K % 256 == 0) ? 2 : 0;
+      if (c->wt == TF_WEIGHT_NVFP4 && gwt == 0) {  // exact bf16 copy of e2m1 x block scale
+        if ((e2 = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e2;
+        p.W = reinterpret_cast<const uint8_t*>(c->wconv);
+      } else if (c->wt == TF_WEIGHT_FP8 && gwt == 0) {  // exact bf16 copy of the e4m3 values
         if ((e2 = launch_e4m3_to_bf16(L.w, c->wconv, (size_t)L.N * L.K, c->stream))) return e2;
         p.W = reinterpret_cast<const uint8_t*>(c->wconv);
       }
-      return launch_gemm_tc(p, hi, lo, rows, c->g_part, c->g_tickets, c->num_sms, c->stream);
+      return launch_gemm_tc(p, gwt, hi, lo, rows, c->g_part, c->g_tickets, c->num_sms, c->stream);
+    }
+    if (c->wt == TF_WEIGHT_NVFP4) {  // exact bf16 copy of e2m1 x block scale; row scale in p.scale
+      if ((e2 = launch_nvfp4_to_bf16(L.w, c->wconv, L.N, L.K, c->stream))) return e2;
+      p.W = reinterpret_cast<const uint8_t*>(c->wconv);
     }
     return launch_gemm_rows(p, wt, rows, c->stream);
   };
@@ -1351,7 +1363,7 @@ tf_status tf_create(const tf_config* cfg, int device, tf_ctx** out) {
       for (auto& sh : shapes) {
         const int M = std::min(m, T);
         c->g_part_floats = std::max(c->g_part_floats, gemm_tc_part_floats(M, sh[0], sh[1], c->num_sms));
-        if (gemm_tc_splits(M, sh[0], sh[1], c->num_sms) > 1)
+        if (std::max(gemm_tc_splits(M, sh[0], sh[1], c->num_sms, 0), gemm_tc_splits(M, sh[0], sh[1], c->num_sms, 1)) > 1)
           c->g_tiles = std::max(c->g_tiles, (size_t)((M + 127) / 128) * (sh[0] / 128));
       }
     c->attn_tc = prompt_attention_tc_supported(c->D, c->Hq, c->Hkv) && c->F >= c->Q;
@@ -2102,7 +2114,7 @@ tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, in
   p.err = err;
   if (cudaMemsetAsync(err, 0, 4, s) != cudaSuccess || cudaMemsetAsync(tickets, 0, nt * 4, s) != cudaSuccess ||
       launch_split_bf16(A, hi, lo, n, s) != cudaSuccess ||
-      launch_gemm_tc(p, hi, lo, M, part, tickets, sms, s) != cudaSuccess)
+      launch_gemm_tc(p, 0, hi, lo, M, part, tickets, sms, s) != cudaSuccess)
     r = TF_E_CUDA;
   uint32_t e = 0;
   if (r == TF_OK && (cudaMemcpyAsync(&e, err, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||

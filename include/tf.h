@@ -180,8 +180,9 @@ tf_status tf_load_weights(tf_ctx* ctx, const tf_tensor* t, int32_t n);
 /* Prompt in, frame 0 out.  tokens: host int32 [B][P], ids in [0, text_vocab),
  * 1 <= B <= max_batch: B independent sequences with prompts of one length P.
  * Resets every sequence to position 0, runs the slow decoder over each
- * prompt (positions 0..P-1, the sequence's own KV cache), then selects frame
- * 0 of every sequence from its last row.  The B sequences then decode in
+ * prompt (positions 0..P-1, the sequence's own KV cache; max_seq_len / P
+ * prompts share one pass of the tensor-core GEMMs), then selects frame 0 of
+ * every sequence from its last row.  The B sequences then decode in
  * lockstep: each later decode call advances all B by one frame (B > 1 runs
  * every linear layer as one skinny tensor-core GEMM over the B rows, see
  * tf_op_gemm_skinny).  Sampling draws use the sequence index b as the

@@ -516,14 +516,16 @@ def run_skinny_case(args):
     configuration (tf_profile_kernel 4..7: deferred-RMSNorm input, fused
     epilogue, launches chained with PDL and replayed as a graph) over --m
     activation rows, on a full-width model cut to 8 slow layers (1.6 GB of
-    distinct weights per pass, far above L2).  Prints one JSON line."""
+    distinct bf16 weights per pass, far above L2; --fp8 / --nvfp4: the same
+    linears quantised, read as they are).  Prints one JSON line."""
     import torch
     from dual_ar_decode_gb300 import Decoder
     from synth import FULL
     d = FULL.replace(slow_layers=8, fast_layers=1, max_seq_len=64)
     dev = torch.device("cuda", 0)
     w = device_weights(d, args.seed, dev)
-    dec = Decoder(d, "bf16", max_batch=args.m)
+    fmt = "nvfp4" if getattr(args, "nvfp4", False) else "fp8" if args.fp8 else "bf16"
+    dec = Decoder(d, fmt, max_batch=args.m)
     dec.load_weights(w)
     del w
     peaks = measured_peaks()
@@ -537,7 +539,7 @@ def run_skinny_case(args):
         out[name] = {"us_per_launch": round(ms * 1e3, 3), "bytes_per_launch": nbytes,
                      "achieved_gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
     dec.close()
-    print(json.dumps({"op": "skinny", "rows_m": args.m, "shapes": out, "peak_gbs": peaks["hbm_gbs"],
+    print(json.dumps({"op": "skinny", "rows_m": args.m, "weights": fmt, "shapes": out, "peak_gbs": peaks["hbm_gbs"],
                       "peak_source": peaks["source"]}), flush=True)
 
 

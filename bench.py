@@ -632,7 +632,8 @@ def run_prefill_case(args):
     """tf_prefill alone on the workload's model and prompt (--workload):
     W warm-up prefills, then `steps` timed ones (CUDA events on the
     library's stream); with --profile-range the last one is bracketed by the
-    profiler range.  Prints one JSON line (ms, prompt tokens/s)."""
+    profiler range.  Prints one JSON line (ms, prompt tokens/s, algorithmic
+    TFLOP/s and their fraction of the measured bf16 burst peak)."""
     import torch
     from dual_ar_decode_gb300 import Decoder
     from synth import make_prompt
@@ -666,9 +667,14 @@ def run_prefill_case(args):
         ts.append(e0.elapsed_time(e1))
     dec.close()
     ms = float(np.median(ts))
+    peaks = measured_peaks()
+    tflops = wl.batch * prefill_flops(d, wl.prefill) / (ms / 1e3) / 1e12
     print(json.dumps({"op": "prefill", "workload": wl.name, "tokens": wl.prefill * wl.batch,
                       "ms": round(ms, 3), "tok_s": round(wl.prefill * wl.batch / (ms / 1e3), 1),
-                      "note": "prompt ids from the host, frame 0 back to the host"}), flush=True)
+                      "tflops": round(tflops, 1), "bf16_peak_tflops": peaks["bf16_tflops"],
+                      "frac": round(tflops / peaks["bf16_tflops"], 4), "peak_source": peaks["source"],
+                      "note": "prompt ids from the host, frame 0 back to the host; flops: the slow "
+                              "decoder's linears and causal attention over the prompt rows"}), flush=True)
 
 
 def run_reference(args, wl, world, rank):

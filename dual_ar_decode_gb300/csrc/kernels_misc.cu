@@ -582,22 +582,58 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* x, const uint
 }
 
 // RMSNorm rows straight into the bf16 hi / lo parts a tensor-core prompt GEMM
-// reads: a = x * rstd * w (the same float operations as k_rmsnorm_rows), hi =
-// bf16(a), lo = bf16(a - hi); one CTA per row.
+// reads: a = x * rstd * w (per element the same float operations as
+// k_rmsnorm_rows), hi = bf16(a), lo = bf16(a - hi); one CTA per row.  Rows of
+// a multiple of 4 elements move as 16-byte loads and 8-byte stores.
+__device__ __forceinline__ uint32_t split_pair(float a0, float a1, uint32_t* lo) {
+  const uint16_t h0 = f32_to_bf16(a0), h1 = f32_to_bf16(a1);
+  const uint16_t l0 = f32_to_bf16(a0 - bf16_to_f32(h0)), l1 = f32_to_bf16(a1 - bf16_to_f32(h1));
+  *lo = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+  return static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+}
+
 __global__ void __launch_bounds__(256) k_rmsnorm_split(const float* x, const uint16_t* w,
                                                        uint16_t* hi, uint16_t* lo, int H, float eps) {
   __shared__ float red[32];
   const int m = blockIdx.x;
   const float* xm = x + (size_t)m * H;
+  const bool v4 = (H & 3) == 0;
   float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
+  if (v4) {
+    const float4* x4 = reinterpret_cast<const float4*>(xm);
+    for (int k = threadIdx.x; k < (H >> 2); k += blockDim.x) {
+      const float4 v = x4[k];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+  } else {
+    for (int k = threadIdx.x; k < H; k += blockDim.x) ss = fmaf(xm[k], xm[k], ss);
+  }
   ss = block_sum_256(ss, red);
   const float rstd = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    const float a = xm[k] * rstd * bf16_to_f32(w[k]);
-    const uint16_t h = f32_to_bf16(a);
-    hi[(size_t)m * H + k] = h;
-    lo[(size_t)m * H + k] = f32_to_bf16(a - bf16_to_f32(h));
+  if (v4) {
+    const float4* x4 = reinterpret_cast<const float4*>(xm);
+    const uint2* w4 = reinterpret_cast<const uint2*>(w);
+    uint2* h4 = reinterpret_cast<uint2*>(hi + (size_t)m * H);
+    uint2* l4 = reinterpret_cast<uint2*>(lo + (size_t)m * H);
+    for (int k = threadIdx.x; k < (H >> 2); k += blockDim.x) {
+      const float4 v = x4[k];
+      const uint2 wk = w4[k];
+      uint2 hv, lv;
+      hv.x = split_pair(v.x * rstd * bf16_lo(wk.x), v.y * rstd * bf16_hi(wk.x), &lv.x);
+      hv.y = split_pair(v.z * rstd * bf16_lo(wk.y), v.w * rstd * bf16_hi(wk.y), &lv.y);
+      h4[k] = hv;
+      l4[k] = lv;
+    }
+  } else {
+    for (int k = threadIdx.x; k < H; k += blockDim.x) {
+      const float a = xm[k] * rstd * bf16_to_f32(w[k]);
+      const uint16_t h = f32_to_bf16(a);
+      hi[(size_t)m * H + k] = h;
+      lo[(size_t)m * H + k] = f32_to_bf16(a - bf16_to_f32(h));
+    }
   }
 }
 

@@ -45,6 +45,9 @@ namespace tf {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 64;
+#ifndef TF_GEMM_PERSISTENT
+#define TF_GEMM_PERSISTENT 1  // bf16 prompt GEMM: one CTA per SM over all units
+#endif
 constexpr int kTileA = BM * BK * 2;             // 16 KB (one bf16 part)
 constexpr int kThreads = 6 * 32;
 
@@ -59,11 +62,10 @@ struct GemmCfg {
   static constexpr int kTileWq = WT == 1 ? GBN * BK : WT == 2 ? GBN * 48 : 0;
   static constexpr int kStageBytes = 2 * kTileA + kTileW + kTileWq;  // A hi, A lo, W (, W staged)
   static constexpr int kStages = (GBN == 256 || WT) ? 3 : 4;
-  static constexpr uint32_t kTmemCols = GBN;
   // kind::f16, fp32 accumulate, bf16 A and B, both K-major, M = 128, N = GBN.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(GBN >> 3) << 17) |
                                      ((uint32_t)(BM >> 4) << 24);
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (3 * kStages + 1) * 8 + 64;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (3 * kStages + 5) * 8 + 64;
   static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 };
 
@@ -320,27 +322,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const GemvParams p, int M, int S, float* part, uint32_t* tickets) {
   using G = GemmCfg<GBN, WT>;
   constexpr int BN = GBN, kStages = G::kStages, kStageBytes = G::kStageBytes;
-  constexpr uint32_t kTmemCols = G::kTmemCols;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* conv = empty + kStages;  // WT: the stage's bf16 weight tile is written
-  uint64_t* done = conv + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* conv = empty + kStages;      // WT: the stage's bf16 weight tile is written
+  uint64_t* acc_full = conv + kStages;   // [2] accumulator b holds a finished unit
+  uint64_t* acc_empty = acc_full + 2;    // [2] accumulator b was read out
+  uint64_t* drain = acc_empty + 2;       // the MMA warp's last MMAs are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* consumed = tmem_slot + 2;  // K slices the MMA warp took
   volatile uint32_t* okv = tmem_slot + 4;       // [4] epilogue warps' wait outcomes
   volatile uint32_t* last_flag = tmem_slot + 8;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-  const int split = blockIdx.z;
+  // Work units: (128-row tile, GBN-column tile, K split), row tiles fastest.
+  // CTA c takes units c, c + gridDim.x, ...; with more units than CTAs the
+  // two accumulators alternate, so one unit's epilogue overlaps the next
+  // unit's MMAs and the producer runs ahead across units.
+  const int mt = (M + BM - 1) / BM, nt = p.N / BN;
+  const int tiles = mt * nt, units = tiles * S;
   const int nkt = p.K / BK;
-  const int kb0 = static_cast<int>((int64_t)split * nkt / S);
-  const int nk = static_cast<int>((int64_t)(split + 1) * nkt / S) - kb0;
+  const bool two = static_cast<int>(gridDim.x) < units;
+  const uint32_t tcols = two ? 2u * BN : static_cast<uint32_t>(BN);
+  struct Unit {
+    int m0, n0, split, tile, kb0, nk;
+  };
+  auto unit = [&](int u) {
+    Unit w;
+    const int mi = u % mt, rest = u / mt;
+    const int ni = rest % nt;
+    w.split = rest / nt;
+    w.m0 = mi * BM;
+    w.n0 = ni * BN;
+    w.tile = mi * nt + ni;
+    w.kb0 = static_cast<int>((int64_t)w.split * nkt / S);
+    w.nk = static_cast<int>((int64_t)(w.split + 1) * nkt / S) - w.kb0;
+    return w;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -348,7 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
       mbar_init(&conv[s], 128);
     }
-    mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     *consumed = 0;
     fence_mbar_init();
@@ -356,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(tcols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -368,27 +394,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int k = 0; k < nk; ++k) {
-        const int s = k % kStages;
-        if (k >= kStages && !mbar_wait(&empty[s], ((k / kStages) & 1) ^ 1, p.err)) {
-          *abort_flag = 1;
-          break;
+      int kc = 0, issued = 0;  // K slices over all of this CTA's units
+      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+        const Unit w = unit(u);
+        for (int k = 0; k < w.nk; ++k, ++kc) {
+          const int s = kc % kStages;
+          if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) & 1) ^ 1, p.err)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* st = smem + s * kStageBytes;
+          const int kx = (w.kb0 + k) * BK;
+          mbar_arrive_expect_tx(&full[s], WT ? 2 * kTileA + G::kTileWq : kStageBytes);
+          tma_load_2d(st, &map_ahi, kx, w.m0, &full[s]);
+          tma_load_2d(st + kTileA, &map_alo, kx, w.m0, &full[s]);
+          uint8_t* wq = st + 2 * kTileA + G::kTileW;  // quantised staging
+          if constexpr (WT == 2) {
+            tma_load_2d(wq, &map_w, (w.kb0 + k) * 32, w.n0, &full[s]);
+            tma_load_2d(wq + 128 * 32, &map_s, p.K / 2 + ((w.kb0 + k) >> 2) * 16, w.n0, &full[s]);
+          } else if constexpr (WT == 1) {
+            tma_load_2d(wq, &map_w, kx, w.n0, &full[s]);
+          } else {
+            tma_load_2d(st + 2 * kTileA, &map_w, kx, w.n0, &full[s]);
+          }
+          issued = kc + 1;
         }
-        uint8_t* st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&full[s], WT ? 2 * kTileA + G::kTileWq : kStageBytes);
-        tma_load_2d(st, &map_ahi, (kb0 + k) * BK, m0, &full[s]);
-        tma_load_2d(st + kTileA, &map_alo, (kb0 + k) * BK, m0, &full[s]);
-        uint8_t* wq = st + 2 * kTileA + G::kTileW;  // quantised staging
-        if constexpr (WT == 2) {
-          tma_load_2d(wq, &map_w, (kb0 + k) * 32, n0, &full[s]);
-          tma_load_2d(wq + 128 * 32, &map_s, p.K / 2 + ((kb0 + k) >> 2) * 16, n0, &full[s]);
-        } else if constexpr (WT == 1) {
-          tma_load_2d(wq, &map_w, (kb0 + k) * BK, n0, &full[s]);
-        } else {
-          tma_load_2d(st + 2 * kTileA, &map_w, (kb0 + k) * BK, n0, &full[s]);
-        }
-        issued = k + 1;
       }
       // After an abort, let the copies still in flight land before the CTA
       // leaves (bounded).
@@ -399,144 +429,172 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int k = 0; k < nk; ++k) {
-        const int s = k % kStages;
-        if (*abort_flag || !mbar_wait(&full[s], (k / kStages) & 1, p.err) ||
-            (WT && !mbar_wait(&conv[s], (k / kStages) & 1, p.err))) {
-          *abort_flag = 1;
-          break;
-        }
-        *consumed = static_cast<uint32_t>(k + 1);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t st = smem_u32(smem + s * kStageBytes);
+      int kc = 0, li = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++li) {
+        const Unit w = unit(u);
+        const int b = two ? (li & 1) : 0;
+        bool ok = !*abort_flag;
+        // accumulator b is free once the epilogue has read out unit li - 2
+        if (ok && two && li >= 2 && !mbar_wait(&acc_empty[b], ((li >> 1) & 1) ^ 1, p.err)) ok = false;
+        if (ok) {
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t acc = tmem + static_cast<uint32_t>(b * BN);
+          for (int k = 0; k < w.nk; ++k, ++kc) {
+            const int s = kc % kStages;
+            if (*abort_flag || !mbar_wait(&full[s], (kc / kStages) & 1, p.err) ||
+                (WT && !mbar_wait(&conv[s], (kc / kStages) & 1, p.err))) {
+              ok = false;
+              break;
+            }
+            *consumed = static_cast<uint32_t>(kc + 1);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t st = smem_u32(smem + s * kStageBytes);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t a_base = st + part * kTileA;
-          const uint32_t w_base = st + 2 * kTileA;
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t a_base = st + part * kTileA;
+              const uint32_t w_base = st + 2 * kTileA;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            mma_bf16(tmem, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(w_base + kk * 32), G::kIdesc,
-                     (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                mma_bf16(acc, smem_desc_sw128(a_base + kk * 32), smem_desc_sw128(w_base + kk * 32), G::kIdesc,
+                         (k > 0 || part > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&empty[s]);  // frees the stage when these MMAs are done
           }
         }
-        mma_commit(&empty[s]);  // frees the stage when these MMAs are done
+        if (!ok) *abort_flag = 1;
+        mma_commit(&acc_full[b]);  // unit complete (or abandoned)
+        if (!ok) break;
       }
-      mma_commit(done);         // accumulator complete (or abandoned)
+      // no MMA of this thread is in flight when the TMEM is released
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.err);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    if constexpr (WT != 0) {
-      // First the weight conversion of every slice: stage s's staged codes
-      // into its bf16 tile (the MMA of its previous slice is done: the
-      // producer reloaded the stage only after it).
-      const int et = threadIdx.x - 64;
-      for (int k = 0; k < nk; ++k) {
-        const int s = k % kStages;
-        uint8_t* st = smem + s * kStageBytes;
-        if (!*abort_flag && mbar_wait(&full[s], (k / kStages) & 1, p.err))
-          dequant_slice<WT>(st + 2 * kTileA + G::kTileW, st + 2 * kTileA, kb0 + k, et);
-        else
-          *abort_flag = 1;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&conv[s]);
-      }
-    }
-    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    const int m = m0 + row;
-    // the first chunk's residual is loaded while the MMAs run
-    const bool resid = p.epi == EPI_RESID && m < M;
-    const float* xrow = p.out + (size_t)m * p.ldo + n0;
-    float xr[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) xr[i] = 0.f;
-    if (resid) {
-#pragma unroll
-      for (int i = 0; i < 16; i += 4) {
-        const float4 t = *reinterpret_cast<const float4*>(xrow + i);
-        xr[i] = t.x;
-        xr[i + 1] = t.y;
-        xr[i + 2] = t.z;
-        xr[i + 3] = t.w;
+    const size_t tile_stride = (size_t)tiles * (BM * BN);
+    [[maybe_unused]] int kc = 0;  // K slices converted (staged weights)
+    int li = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++li) {
+      const Unit w = unit(u);
+      const int b = two ? (li & 1) : 0;
+      if constexpr (WT != 0) {
+        // First the weight conversion of every slice: stage s's staged codes
+        // into its bf16 tile (the MMA of its previous slice is done: the
+        // producer reloaded the stage only after it).
+        const int et = threadIdx.x - 64;
+        for (int k = 0; k < w.nk; ++k, ++kc) {
+          const int s = kc % kStages;
+          uint8_t* st = smem + s * kStageBytes;
+          if (!*abort_flag && mbar_wait(&full[s], (kc / kStages) & 1, p.err))
+            dequant_slice<WT>(st + 2 * kTileA + G::kTileW, st + 2 * kTileA, w.kb0 + k, et);
+          else
+            *abort_flag = 1;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&conv[s]);
+        }
       }
-    }
-    const bool wok = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, p.err) ? 1 : 0) && !*abort_flag;
-    if (lane == 0) okv[q] = wok ? 1u : 0u;
-    epi_bar_sync();
-    const bool ok = okv[0] && okv[1] && okv[2] && okv[3];  // CTA-uniform
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    bool run = ok;
-    const size_t tile_id = (size_t)blockIdx.x * gridDim.y + blockIdx.y;
-    const size_t tile_stride = (size_t)gridDim.x * gridDim.y * (BM * BN);
-    if (S > 1) {
-      // this split's partial tile [128 rows][128 columns], then a ticket
-      float* mine = part + split * tile_stride + tile_id * (BM * BN) + (size_t)row * BN;
-      if (ok) {
+      const int m = w.m0 + row;
+      // the first chunk's residual is loaded while the MMAs run
+      const bool resid = p.epi == EPI_RESID && m < M;
+      const float* xrow = p.out + (size_t)m * p.ldo + w.n0;
+      float xr[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xr[i] = 0.f;
+      if (resid) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 t = *reinterpret_cast<const float4*>(xrow + i);
+          xr[i] = t.x;
+          xr[i + 1] = t.y;
+          xr[i + 2] = t.z;
+          xr[i + 3] = t.w;
+        }
+      }
+      const bool wok =
+          __all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[b], (li >> 1) & 1, p.err) ? 1 : 0) && !*abort_flag;
+      if (lane == 0) okv[q] = wok ? 1u : 0u;
+      epi_bar_sync();
+      const bool ok = okv[0] && okv[1] && okv[2] && okv[3];  // uniform over the four warps
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+      bool run = true;
+      if (S > 1) {
+        // this split's partial tile [128 rows][BN columns], then a ticket
+        float* mine = part + w.split * tile_stride + (size_t)w.tile * (BM * BN) + (size_t)row * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+          tmem_ld16(acc + c, v);
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
             __stcg(reinterpret_cast<float4*>(mine + c + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
         }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(&acc_empty[b]);  // the accumulator is free for unit li + 2
+        epi_bar_sync();
+        if (threadIdx.x == 64) {
+          const uint32_t t = ticket_acq_rel(&tickets[w.tile]);
+          *last_flag = (t == static_cast<uint32_t>(S) - 1u) ? 1u : 0u;
+        }
+        epi_bar_sync();
+        run = *last_flag != 0;
       }
-      epi_bar_sync();
-      if (threadIdx.x == 64) {
-        const uint32_t t = ticket_acq_rel(&tickets[tile_id]);
-        *last_flag = (t == static_cast<uint32_t>(S) - 1u) ? 1u : 0u;
-      }
-      epi_bar_sync();
-      run = ok && *last_flag != 0;
-    }
-    if (run) {
+      if (run) {
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        float v[16];
-        if (S > 1) {
-          // the splits' partials, added in split order
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          if (S > 1) {
+            // the splits' partials, added in split order
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
-          const float* src = part + tile_id * (BM * BN) + (size_t)row * BN + c;
-          for (int j = 0; j < S; ++j, src += tile_stride) {
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            const float* src = part + (size_t)w.tile * (BM * BN) + (size_t)row * BN + c;
+            for (int j = 0; j < S; ++j, src += tile_stride) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 t = __ldcg(reinterpret_cast<const float4*>(src + i));
+                v[i] += t.x;
+                v[i + 1] += t.y;
+                v[i + 2] += t.z;
+                v[i + 3] += t.w;
+              }
+            }
+          } else {
+            tmem_ld16(acc + c, v);
+          }
+          if (m >= M) continue;
+          float xc[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xc[i] = xr[i];
+          if (resid && c + 16 < BN) {  // the next chunk's residual, ahead of this chunk's stores
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
-              const float4 t = __ldcg(reinterpret_cast<const float4*>(src + i));
-              v[i] += t.x;
-              v[i + 1] += t.y;
-              v[i + 2] += t.z;
-              v[i + 3] += t.w;
+              const float4 t = *reinterpret_cast<const float4*>(xrow + c + 16 + i);
+              xr[i] = t.x;
+              xr[i + 1] = t.y;
+              xr[i + 2] = t.z;
+              xr[i + 3] = t.w;
             }
           }
-        } else {
-          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+          gemm_epi_chunk(p, m, w.n0 + c, v, xc);
         }
-        if (m >= M) continue;
-        float xc[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) xc[i] = xr[i];
-        if (resid && c + 16 < BN) {  // the next chunk's residual, ahead of this chunk's stores
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(xrow + c + 16 + i);
-            xr[i] = t.x;
-            xr[i + 1] = t.y;
-            xr[i + 2] = t.z;
-            xr[i + 3] = t.w;
-          }
-        }
-        gemm_epi_chunk(p, m, n0 + c, v, xc);
+        if (S > 1 && threadIdx.x == 64) tickets[w.tile] = 0u;
       }
-      if (S > 1 && threadIdx.x == 64) tickets[tile_id] = 0u;
+      if (S == 1) {
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        mbar_arrive(&acc_empty[b]);
+      }
+      epi_bar_sync();  // okv and last_flag are written again for the next unit
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tcols) : "memory");
   }
 }
 
@@ -1456,6 +1514,26 @@ __global__ void k_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t 
   }
 }
 
+// The same, four elements per step: 16-byte loads, 8-byte stores.
+__global__ void k_split_bf16_x4(const float4* a, uint2* hi, uint2* lo, size_t n4) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 x = a[i];
+    const float v[4] = {x.x, x.y, x.z, x.w};
+    uint32_t h[2], l[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint16_t h0 = f32_to_bf16(v[2 * j]), h1 = f32_to_bf16(v[2 * j + 1]);
+      const uint16_t l0 = f32_to_bf16(v[2 * j] - bf16_to_f32(h0));
+      const uint16_t l1 = f32_to_bf16(v[2 * j + 1] - bf16_to_f32(h1));
+      h[j] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+      l[j] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+    }
+    hi[i] = make_uint2(h[0], h[1]);
+    lo[i] = make_uint2(l[0], l[1]);
+  }
+}
+
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1650,8 +1728,17 @@ size_t gemm_tc_part_floats(int M, int N, int K, int num_sms) {
 size_t gemm_tc_smem_bytes() { return GemmCfg<256>::kSmem; }
 
 cudaError_t launch_split_bf16(const float* a, uint16_t* hi, uint16_t* lo, size_t n, cudaStream_t s) {
-  const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
-  k_split_bf16<<<grid, 256, 0, s>>>(a, hi, lo, n);
+  if (n == 0) return cudaSuccess;
+  const bool v4 = n % 4 == 0 && reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(hi) % 8 == 0 && reinterpret_cast<uintptr_t>(lo) % 8 == 0;
+  if (v4) {
+    const int grid = static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096));
+    k_split_bf16_x4<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(a), reinterpret_cast<uint2*>(hi),
+                                         reinterpret_cast<uint2*>(lo), n / 4);
+  } else {
+    const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
+    k_split_bf16<<<grid, 256, 0, s>>>(a, hi, lo, n);
+  }
   return cudaGetLastError();
 }
 
@@ -1664,14 +1751,18 @@ cudaError_t launch_e4m3_to_bf16(const uint8_t* q, uint16_t* out, size_t n, cudaS
 template <int GBN, int WT>
 cudaError_t launch_gemm_tc_bn(const CUtensorMap& ma_hi, const CUtensorMap& ma_lo, const CUtensorMap& mw,
                               const CUtensorMap& ms, const GemvParams& p, int M, int S, float* part,
-                              uint32_t* tickets, cudaStream_t s) {
+                              uint32_t* tickets, int num_sms, cudaStream_t s) {
   static DeviceOnce once;
   cudaError_t ea = device_once(once, [] {
     return cudaFuncSetAttribute(k_umma_gemm<GBN, WT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)GemmCfg<GBN, WT>::kSmem);
   });
   if (ea) return ea;
-  dim3 grid((M + BM - 1) / BM, p.N / GBN, S);
+  // bf16 weights: one CTA per SM working through the units (two TMEM
+  // accumulators); staged quantised weights: one CTA per unit, because their
+  // epilogue warps are also the converters of the unit's weight slices.
+  const int units = ((M + BM - 1) / BM) * (p.N / GBN) * S;
+  const int grid = (WT == 0 && TF_GEMM_PERSISTENT) ? std::min(units, std::max(1, num_sms)) : units;
   k_umma_gemm<GBN, WT><<<grid, kThreads, GemmCfg<GBN, WT>::kSmem, s>>>(ma_hi, ma_lo, mw, ms, p, M, S, part,
                                                                        tickets);
   return cudaGetLastError();
@@ -1692,10 +1783,10 @@ cudaError_t launch_gemm_tc(const GemvParams& p, int wt, const uint16_t* a_hi, co
     return cudaErrorInvalidValue;
   const int S = gemm_tc_splits(M, p.N, p.K, num_sms, wt);
   if (S > 1 && (!part || !tickets)) return cudaErrorInvalidValue;
-  if (wt == 2) return launch_gemm_tc_bn<128, 2>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s);
-  if (wt == 1) return launch_gemm_tc_bn<128, 1>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s);
-  return bn == 256 ? launch_gemm_tc_bn<256, 0>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s)
-                   : launch_gemm_tc_bn<128, 0>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, s);
+  if (wt == 2) return launch_gemm_tc_bn<128, 2>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, num_sms, s);
+  if (wt == 1) return launch_gemm_tc_bn<128, 1>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, num_sms, s);
+  return bn == 256 ? launch_gemm_tc_bn<256, 0>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, num_sms, s)
+                   : launch_gemm_tc_bn<128, 0>(ma_hi, ma_lo, mw, ms, p, M, S, part, tickets, num_sms, s);
 }
 
 }  // namespace tf

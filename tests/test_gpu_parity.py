@@ -305,7 +305,7 @@ def test_prompt_attention_matches_oracle(Hq, Hkv, D, T, rows, pos0, spike):
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (200, 6144, 2560), (77, 2560, 9728),
                                    (1, 256, 128), (300, 19456, 2560), (129, 2560, 4096),
-                                   (1024, 2560, 9728), (700, 6144, 2560)])
+                                   (1024, 2560, 9728), (700, 6144, 2560), (1500, 4096, 2560)])
 def test_tensor_core_gemm_matches_oracle(M, N, K):
     """The prompt GEMM (tcgen05 / TMEM) against A @ W^T in float64."""
     rng = np.random.default_rng(M * 7 + N + K)

@@ -4,25 +4,30 @@
 // "Inference speedtest": prefill is reported separately in tokens/s); its
 // linear layers are dense contractions C[m][n] = sum_k A[m][k] W[n][k] with
 // m over prompt tokens, so they belong on the 5th-generation tensor cores:
-//   * one CTA per 128 x 128 output tile and slice of K; warp 0 streams
-//     64-wide K slices of the activation tile and the weight tile into a
-//     4-stage shared-memory ring with TMA tensor copies (128-byte swizzle),
+//   * the work is split into units (a 128-row x GBN-column output tile,
+//     GBN = 128 or 256, and a slice of K); warp 0 streams 64-wide K slices
+//     of the activation tile and the weight tile into a 3- or 4-stage
+//     shared-memory ring with TMA tensor copies (128-byte swizzle),
 //     completion counted on mbarriers;
-//   * warp 1 owns 128 TMEM columns (the fp32 accumulator) and issues
-//     tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), four K=16 steps per slice;
-//     tcgen05.commit frees a stage once the MMAs reading it are done;
+//   * warp 1 owns the TMEM accumulator(s) (fp32, GBN columns each) and
+//     issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32), four K=16 steps
+//     per slice; tcgen05.commit frees a stage once the MMAs reading it are
+//     done, and marks a unit's accumulator full after its last slice;
 //   * the activations enter as two bf16 parts (hi = bf16(a), lo = bf16(a -
 //     hi)) multiplied by the same weight slice, so the products keep about 16
 //     significant bits of the fp32 activations instead of 8;
-//   * warps 2-5 wait for the final commit, read the accumulator with
-//     tcgen05.ld (each warp its 32-lane quarter, one row per thread) and run
+//   * warps 2-5 wait for a full accumulator, read it with tcgen05.ld (each
+//     warp its 32-lane quarter, one row per thread), hand it back, and run
 //     the decode path's fused epilogues (RoPE + KV append, residual add,
 //     SwiGLU, store);
+//   * with bf16 weights one CTA per SM works through all units, and two
+//     accumulators alternate: one unit's epilogue runs while the MMAs of the
+//     next fill the other, and the producer runs ahead across units;
 //   * few tiles (short prompts, or the 2560-wide O and down projections)
-//     would leave most SMs idle, so K is split until the grid fills whole
+//     would leave most SMs idle, so K is split until the units fill whole
 //     waves: each split stores its partial tile and takes a ticket, and the
-//     tile's last CTA adds the partials in split order (deterministic) before
-//     the epilogue.
+//     tile's last split adds the partials in split order (deterministic)
+//     before the epilogue.
 // Every wait is bounded; the TMEM columns are always released.
 //
 // Batched decode (several sequences in lockstep, one row each per step) turns

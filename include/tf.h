@@ -376,10 +376,12 @@ tf_status tf_op_attention_prompt(const float* q, const uint16_t* K, const uint16
  * rows m.  A: float32 [M][K] device; W: bf16 bits [N][K] device; C: float32
  * [M][N] device.  A is split into bf16 hi and lo parts that are both
  * multiplied with W, so the result carries about 16 significant bits of A.
- * N must be a multiple of 128 and K of 64.  When the 128 x 128 output tiles
+ * N must be a multiple of 128 and K of 64.  Output tiles are 128 rows by 128
+ * columns (by 256 when M > 512 and N is a multiple of 256).  When the tiles
  * would not fill the GPU, K is split and the splits' partials are added in
- * split order (results do not depend on timing).  Allocates and frees its
- * scratch.  Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA, TF_E_TIMEOUT. */
+ * split order (results do not depend on timing).  One CTA per SM works
+ * through the (tile, split) units.  Allocates and frees its scratch.
+ * Errors: TF_E_INVAL, TF_E_NOMEM, TF_E_CUDA, TF_E_TIMEOUT. */
 tf_status tf_op_gemm(const float* A, const uint16_t* W, int32_t M, int32_t N, int32_t K, float* C,
                      void* stream);
 

@@ -142,3 +142,16 @@ def test_reference_arm_times_what_it_prints(capsys):
     assert line["steps"] == 3 and line["warmup"] == 3
     assert line["ms_per_step"] == pytest.approx(1e3 / line["value"], rel=1e-3)
     assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]
+
+
+@pytest.mark.parametrize("d", [TINY, FULL])
+@pytest.mark.parametrize("P", [1, 128, 1024])
+def test_prefill_flops_from_the_tensor_list(d, P):
+    """The prefill TFLOP/s that `--op prefill` prints: 2 flops per slow-layer
+    linear weight element and prompt row (summed from the tensor list, the
+    slow head excluded: only the last row reaches it), plus causal attention,
+    2 * 2 * head_dim flops per (query, key <= query) pair and query head."""
+    lin = sum(int(np.prod(shape)) for name, shape, kind in tensor_specs(d)
+              if kind == "linear" and name.startswith("slow.") and name.split(".")[1].isdigit())
+    attn = d.slow_layers * d.n_heads * 4 * d.head_dim * (P * (P + 1) // 2)
+    assert bench.prefill_flops(d, P) == pytest.approx(2 * P * lin + attn, rel=1e-12)
